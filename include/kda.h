@@ -1,0 +1,169 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) chunked KDA prefill and decode library.
+ *
+ * KDA is the gated delta rule with a per-channel (per key channel) decay gate.
+ * Per v-head, token by token:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * The prefill evaluates this in chunks of 64 tokens (intra-chunk work in
+ * parallel, one sequential state pass across chunks), which is the pipeline of
+ * the sglang PR 27488 digest "KDA SM100 CuteDSL prefill" (sections 实现拆解 /
+ * implementation breakdown and 关键文件 / key files: gate prologue, KKT inverse
+ * and U/W, h (state) kernel, output kernel).  The state pool I/O follows the
+ * sglang PR 30169 digest "pool state I/O fused into the h kernel" (实现拆解
+ * items 1-3).  The decode grid rule follows the sglang PR 37317 digest "FLA/MoE
+ * grid split" (实现拆解 item 1: sequences and heads on separate grid axes).
+ *
+ * General rules for every entry point
+ * -----------------------------------
+ *  - All tensor pointers are DEVICE pointers, owned by the caller; tensors are
+ *    packed, contiguous and row-major with the shapes given below.
+ *  - Calls are asynchronous on `stream`.  They never allocate device memory and
+ *    never synchronise the host (the pages measured both as the dominant host
+ *    cost: a ~200 MB re-allocation per call and a device->host `.item()` in the
+ *    metadata step -- PR 27488 digest, 功能与动机 and 关键源码片段).
+ *  - Host-checkable errors return synchronously and nothing is enqueued.
+ *  - Errors found in device data (a slot index out of range, a non-monotone or
+ *    out-of-range cu_seqlens) set bits in a status word kept in the workspace;
+ *    the offending sequence is skipped (its outputs and state rows are left
+ *    untouched) and every other sequence is computed normally.  Read the word
+ *    with kda_read_device_status().  Kernels never trap.
+ *  - Thread safety: calls that share a workspace must be ordered on one stream.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1,   /* bad pointer, shape or mode combination      */
+    KDA_ERR_UNSUPPORTED = 2,        /* valid but not implemented (dtype, head dims) */
+    KDA_ERR_WORKSPACE_TOO_SMALL = 3,
+    KDA_ERR_CUDA = 4,               /* a CUDA launch or copy failed                */
+    KDA_ERR_DEVICE_DATA = 5         /* kda_read_device_status: device data invalid */
+} kda_status_t;
+
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
+
+/* Device status bits (kda_read_device_status). */
+#define KDA_DEVICE_BAD_SLOT      0x1u  /* state index < -1 or >= num_slots          */
+#define KDA_DEVICE_BAD_SEQLENS   0x2u  /* cu_seqlens not monotone / outside [0, T]  */
+#define KDA_DEVICE_PIPE_TIMEOUT  0x4u  /* an internal pipeline wait gave up         */
+
+/* Problem descriptor shared by prefill and decode. */
+typedef struct {
+    int32_t num_seqs;          /* N (prefill: packed sequences; decode: rows)          */
+    int64_t total_tokens;      /* T: rows of q/k/v/o.  Authoritative: g and beta may be
+                                  longer (CUDA-graph padding); only T rows are read
+                                  (PR 27488 digest, 实现拆解 item 3).  Decode: T == N. */
+    int32_t num_k_heads;       /* Hk (q and k heads)                                    */
+    int32_t num_v_heads;       /* Hv; Hv % Hk == 0; v-head h reads k/q head h/(Hv/Hk)   */
+    int32_t head_k_dim;        /* K in {64, 128}                                        */
+    int32_t head_v_dim;        /* V in {64, 128}                                        */
+    kda_dtype_t qkv_dtype;     /* dtype of q, k, v and o                                */
+    kda_dtype_t state_dtype;   /* dtype of the state / pool (math is fp32 inside)       */
+    float scale;               /* output scale; <= 0 selects K^-0.5                     */
+    int32_t chunk_size;        /* must be 64                                            */
+    int64_t num_slots;         /* pool mode: rows of the pool; slot num_slots-1 is the
+                                  sentinel that index -1 maps to                        */
+    int64_t slot_stride_elems; /* pool: elements between consecutive slots; 0 means
+                                  Hv*K*V.  Must be >= Hv*K*V.  (The pitch is passed, not
+                                  inferred from a shape: PR 37317 digest, 实现拆解 item 2.) */
+    uint32_t flags;            /* reserved, must be 0                                   */
+} kda_desc_t;
+
+/* Bytes of workspace kda_chunk_prefill() needs for this descriptor (0 on an
+ * invalid descriptor).  The workspace is caller-owned device memory, aligned to
+ * 256 bytes, reusable across calls on the same stream; its contents need no
+ * initialisation. */
+size_t kda_chunk_prefill_workspace_size(const kda_desc_t *desc);
+
+/* Bytes of workspace kda_decode() needs (status word only). */
+size_t kda_decode_workspace_size(const kda_desc_t *desc);
+
+/*
+ * Chunked KDA prefill over packed variable-length sequences.
+ *
+ *   q, k         [T, Hk, K]  qkv_dtype.  Expected L2-normalised per head (the
+ *                            caller normalises, as on the pages: PR 27488 digest,
+ *                            CuteDSLKDAKernel.extend); not re-normalised here.
+ *   v            [T, Hv, V]  qkv_dtype
+ *   g            [>=T, Hv, K] fp32 natural-log decay per key channel (g <= 0)
+ *   beta         [>=T, Hv]    fp32
+ *   cu_seqlens   [N+1] int32, cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N] <= T.
+ *                Chunks start at each sequence's first token; the last chunk of a
+ *                sequence may be partial.
+ *   state        pool mode (state_indices != NULL): the pool, num_slots rows of
+ *                [Hv, K, V] (row pitch slot_stride_elems), read and written IN
+ *                PLACE: sequence n starts from slot s_n and its final state is
+ *                written back to slot s_n, where s_n = state_indices[n] if >= 0,
+ *                else num_slots-1 (PR 30169 digest, 实现拆解 items 1-3).  Rows not
+ *                named are not touched.  Indices should be distinct (a repeated
+ *                slot, e.g. the sentinel, gets an unspecified one of the results).
+ *                dense mode (state_indices == NULL): initial states [N, Hv, K, V],
+ *                or NULL for zero initial states.
+ *   state_indices  [N] int32 or NULL (selects the mode)
+ *   final_state  pool mode: must be NULL or equal to `state`.
+ *                dense mode: [N, Hv, K, V] state_dtype, or NULL to skip; may
+ *                equal `state` (in-place update).
+ *   o            [T, Hv, V] qkv_dtype, fully overwritten for every valid token.
+ *   workspace    kda_chunk_prefill_workspace_size(desc) bytes, 256-byte aligned.
+ *
+ * State layout: S[k][v] row-major per (slot or sequence, v-head).
+ * Pool mode and dense mode run the same kernels and the same arithmetic; only
+ * the addresses differ, so o and the written state rows are bit-identical
+ * between the two modes (PR 30169 digest, 实现拆解 item 4).
+ * Run to run, results are bit-identical (no atomics in any reduction).
+ */
+kda_status_t kda_chunk_prefill(const kda_desc_t *desc, const void *q, const void *k,
+                               const void *v, const float *g, const float *beta,
+                               const int32_t *cu_seqlens, void *state,
+                               const int32_t *state_indices, void *final_state, void *o,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * One-token-per-row KDA decode, updating a state pool in place.
+ *
+ *   q, k   [N, Hk, K]   v [N, Hv, V]   g [>=N, Hv, K] fp32   beta [>=N, Hv] fp32
+ *   state_pool     num_slots rows of [Hv, K, V] (pitch slot_stride_elems)
+ *   state_indices  [N] int32; -1 (padding) maps to the sentinel slot num_slots-1;
+ *                  NULL means row n uses slot n.  Rows that share a slot (padding
+ *                  rows on the sentinel) race: their outputs and that slot's final
+ *                  contents are unspecified.
+ *   o      [N, Hv, V] qkv_dtype
+ * The grid keeps rows and heads on separate axes with rows on grid.x, so any
+ * N < 2^31 launches (PR 37317 digest, 实现拆解 item 1 and 风险与影响 item 5:
+ * folding N*Hv into one 65535-limited axis made large decode batches fail).
+ */
+kda_status_t kda_decode(const kda_desc_t *desc, const void *q, const void *k, const void *v,
+                        const float *g, const float *beta, void *state_pool,
+                        const int32_t *state_indices, void *o, void *workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads the device status word left in `workspace`
+ * by the last prefill or decode call that used it.  Returns KDA_OK or
+ * KDA_ERR_DEVICE_DATA (raw bits in *bits_out if bits_out != NULL), or
+ * KDA_ERR_CUDA if the synchronisation or copy failed. */
+kda_status_t kda_read_device_status(const void *workspace, uint32_t *bits_out,
+                                    cudaStream_t stream);
+
+/* Which prefill kernel path a descriptor selects: 1 = fused tensor-core
+ * (tcgen05) path, 0 = CUDA-core (fp32 FFMA) path, -1 = invalid descriptor. */
+int kda_chunk_prefill_path(const kda_desc_t *desc);
+
+/* Human-readable name of a status code (static storage). */
+const char *kda_status_string(kda_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_GB300_H */

@@ -1,0 +1,240 @@
+"""Thin Python binding of ``libkda_gb300.so`` (argument marshalling only).
+
+Every step of the prefill and decode runs in the library's CUDA kernels; this
+module only checks tensors, builds the ``kda_desc_t`` descriptor, allocates the
+workspace and outputs with ``torch.empty`` and passes raw device pointers and
+the current CUDA stream.  There is no CPU fallback: if the library cannot be
+loaded the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+KDA_BF16, KDA_F32 = 0, 1
+KDA_DEVICE_BAD_SLOT, KDA_DEVICE_BAD_SEQLENS, KDA_DEVICE_PIPE_TIMEOUT = 0x1, 0x2, 0x4
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
+           3: "workspace too small", 4: "CUDA error", 5: "invalid device data"}
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code, what=""):
+        self.code = code
+        super().__init__(f"{what}: {_STATUS.get(code, code)} (status {code})")
+
+
+class KdaDesc(ctypes.Structure):
+    """Mirror of ``kda_desc_t`` in include/kda.h."""
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32),
+        ("total_tokens", ctypes.c_int64),
+        ("num_k_heads", ctypes.c_int32),
+        ("num_v_heads", ctypes.c_int32),
+        ("head_k_dim", ctypes.c_int32),
+        ("head_v_dim", ctypes.c_int32),
+        ("qkv_dtype", ctypes.c_int),
+        ("state_dtype", ctypes.c_int),
+        ("scale", ctypes.c_float),
+        ("chunk_size", ctypes.c_int32),
+        ("num_slots", ctypes.c_int64),
+        ("slot_stride_elems", ctypes.c_int64),
+        ("flags", ctypes.c_uint32),
+    ]
+
+
+EXPORTS = ("kda_chunk_prefill_workspace_size", "kda_decode_workspace_size", "kda_chunk_prefill",
+           "kda_decode", "kda_read_device_status", "kda_chunk_prefill_path", "kda_status_string")
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load (building first if needed) the CUDA library and declare its prototypes."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB) and not build_if_missing:
+        raise RuntimeError(f"{_build.LIB} is missing; run __graft_entry__.build()")
+    if build_if_missing:
+        _build.build()  # no-op unless a source is newer than the library
+    lib = ctypes.CDLL(_build.LIB)
+    P = ctypes.c_void_p
+    D = ctypes.POINTER(KdaDesc)
+    lib.kda_chunk_prefill_workspace_size.argtypes = [D]
+    lib.kda_chunk_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.kda_decode_workspace_size.argtypes = [D]
+    lib.kda_decode_workspace_size.restype = ctypes.c_size_t
+    lib.kda_chunk_prefill.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.kda_chunk_prefill.restype = ctypes.c_int
+    lib.kda_decode.argtypes = [D, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.kda_decode.restype = ctypes.c_int
+    lib.kda_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
+    lib.kda_read_device_status.restype = ctypes.c_int
+    lib.kda_chunk_prefill_path.argtypes = [D]
+    lib.kda_chunk_prefill_path.restype = ctypes.c_int
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _dt(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return KDA_BF16
+    if t == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported dtype {t}; use bfloat16 or float32")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype=None, cuda=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def make_desc(*, num_seqs, total_tokens, Hk, Hv, K, V, qkv_dtype, state_dtype=torch.float32,
+              scale=None, num_slots=0, slot_stride=0) -> KdaDesc:
+    d = KdaDesc()
+    d.num_seqs = num_seqs
+    d.total_tokens = total_tokens
+    d.num_k_heads, d.num_v_heads, d.head_k_dim, d.head_v_dim = Hk, Hv, K, V
+    d.qkv_dtype = _dt(qkv_dtype)
+    d.state_dtype = _dt(state_dtype)
+    d.scale = 0.0 if scale is None else float(scale)
+    d.chunk_size = 64
+    d.num_slots = num_slots
+    d.slot_stride_elems = slot_stride
+    d.flags = 0
+    return d
+
+
+def prefill_workspace_size(desc: KdaDesc) -> int:
+    return int(load().kda_chunk_prefill_workspace_size(ctypes.byref(desc)))
+
+
+def prefill_path(desc: KdaDesc) -> int:
+    """1 = fused tensor-core path, 0 = CUDA-core path, -1 = invalid descriptor."""
+    return int(load().kda_chunk_prefill_path(ctypes.byref(desc)))
+
+
+def read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return the device status bits of the last call."""
+    bits = ctypes.c_uint32(0)
+    rc = load().kda_read_device_status(_ptr(workspace), ctypes.byref(bits), _stream(stream))
+    if rc not in (0, 5):
+        raise KdaError(rc, "kda_read_device_status")
+    return int(bits.value)
+
+
+def chunk_prefill(q, k, v, g, beta, cu_seqlens, *, state=None, state_indices=None,
+                  final_state=None, output_final_state=True, scale=None, slot_stride=0,
+                  out=None, workspace=None, stream=None):
+    """Chunked KDA prefill.  Returns ``(o, final)``.
+
+    q, k [T, Hk, K]; v [T, Hv, V] (bf16 or fp32, same dtype); g [>=T, Hv, K] fp32;
+    beta [>=T, Hv] fp32; cu_seqlens [N+1] int32.
+    Pool mode (``state_indices`` [N] int32 given): ``state`` is the pool
+    [num_slots, Hv, K, V], updated in place and returned as ``final``.
+    Dense mode: ``state`` is h0 [N, Hv, K, V] or None; ``final`` is a new
+    [N, Hv, K, V] tensor (or ``final_state`` if given, may be ``state``) or None
+    when ``output_final_state`` is False.
+    """
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name)
+    _need(g, "g", torch.float32)
+    _need(beta, "beta", torch.float32)
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    T, Hk, K = q.shape
+    Hv, V = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    pool = state_indices is not None
+    sdt = state.dtype if state is not None else (final_state.dtype if final_state is not None
+                                                 else torch.float32)
+    num_slots = 0
+    if pool:
+        _need(state_indices, "state_indices", torch.int32)
+        if state is None:
+            raise ValueError("pool mode needs the pool in `state`")
+        num_slots = state.shape[0]
+        final_state = state
+    else:
+        if state is not None:
+            _need(state, "state")
+        if final_state is None and output_final_state:
+            final_state = torch.empty((N, Hv, K, V), dtype=sdt, device=q.device)
+    if state is not None and not pool:
+        _need(state, "state")
+    d = make_desc(num_seqs=N, total_tokens=T, Hk=Hk, Hv=Hv, K=K, V=V, qkv_dtype=q.dtype,
+                  state_dtype=sdt, scale=scale, num_slots=num_slots, slot_stride=slot_stride)
+    if out is None:
+        out = torch.empty((T, Hv, V), dtype=q.dtype, device=q.device)
+    ws_size = lib.kda_chunk_prefill_workspace_size(ctypes.byref(d))
+    if ws_size == 0:
+        raise KdaError(1, "kda_chunk_prefill_workspace_size")
+    if workspace is None or workspace.numel() < ws_size:
+        workspace = torch.empty(ws_size, dtype=torch.uint8, device=q.device)
+    rc = lib.kda_chunk_prefill(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                               _ptr(cu_seqlens), _ptr(state), _ptr(state_indices),
+                               _ptr(final_state), _ptr(out), _ptr(workspace),
+                               workspace.numel(), _stream(stream))
+    if rc != 0:
+        raise KdaError(rc, "kda_chunk_prefill")
+    chunk_prefill.last_workspace = workspace
+    return out, final_state
+
+
+def decode(q, k, v, g, beta, pool, state_indices=None, *, scale=None, slot_stride=0, out=None,
+           workspace=None, stream=None):
+    """One-token-per-row decode, updating ``pool`` [num_slots, Hv, K, V] in place.  Returns o."""
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("pool", pool)):
+        _need(t, name)
+    _need(g, "g", torch.float32)
+    _need(beta, "beta", torch.float32)
+    if state_indices is not None:
+        _need(state_indices, "state_indices", torch.int32)
+    N, Hk, K = q.shape
+    Hv, V = v.shape[1], v.shape[2]
+    d = make_desc(num_seqs=N, total_tokens=N, Hk=Hk, Hv=Hv, K=K, V=V, qkv_dtype=q.dtype,
+                  state_dtype=pool.dtype, scale=scale, num_slots=pool.shape[0],
+                  slot_stride=slot_stride)
+    if out is None:
+        out = torch.empty((N, Hv, V), dtype=q.dtype, device=q.device)
+    ws_size = lib.kda_decode_workspace_size(ctypes.byref(d))
+    if ws_size == 0:
+        raise KdaError(1, "kda_decode_workspace_size")
+    if workspace is None or workspace.numel() < ws_size:
+        workspace = torch.empty(ws_size, dtype=torch.uint8, device=q.device)
+    rc = lib.kda_decode(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                        _ptr(pool), _ptr(state_indices), _ptr(out), _ptr(workspace),
+                        workspace.numel(), _stream(stream))
+    if rc != 0:
+        raise KdaError(rc, "kda_decode")
+    decode.last_workspace = workspace
+    return out

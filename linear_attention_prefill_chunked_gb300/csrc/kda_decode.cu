@@ -1,0 +1,181 @@
+// kda_decode.cu -- one-token-per-row KDA decode on a state pool, in place.
+//
+// Per row n and v-head h (slot s = idx[n], -1 -> sentinel num_slots-1):
+//   S <- Diag(exp g) S;  u = beta (v - S^T k);  S <- S + k u^T;  o = scale S^T q
+// which is one step of the recurrence the prefill evaluates in chunks.
+//
+// Grid (N, Hv, V / VT): rows on grid.x (limit 2^31-1), heads on grid.y, value
+// tiles on grid.z -- rows and heads are never folded into one axis, the rule of
+// the sglang PR 37317 digest "FLA/MoE grid split" (实现拆解 item 1, 风险与影响
+// item 5), which fixed launches failing once N*Hv exceeded 65535.
+//
+// The kernel is bound by HBM: it streams each state tile (K x VT fp32) in and
+// out exactly once.  A CTA of 256 threads holds the tile in registers: 32 (or
+// VT/4) threads cover one row with 16-byte vector accesses, the 8 row groups
+// split the K rows, and the two channel reductions (S^T k and S^T q) go through
+// shared memory.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kDecThreads = 256;
+
+template <typename ST> struct Vec4;
+template <> struct Vec4<float> {
+  __device__ static void load(const float* p, float r[4]) {
+    const float4 x = *reinterpret_cast<const float4*>(p);
+    r[0] = x.x; r[1] = x.y; r[2] = x.z; r[3] = x.w;
+  }
+  __device__ static void store(float* p, const float r[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(r[0], r[1], r[2], r[3]);
+  }
+};
+template <> struct Vec4<__nv_bfloat16> {
+  __device__ static void load(const __nv_bfloat16* p, float r[4]) {
+    const uint2 x = *reinterpret_cast<const uint2*>(p);
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&x.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&x.y);
+    r[0] = __low2float(a); r[1] = __high2float(a); r[2] = __low2float(b); r[3] = __high2float(b);
+  }
+  __device__ static void store(__nv_bfloat16* p, const float r[4]) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(r[0], r[1]);
+    __nv_bfloat162 b = __floats2bfloat162_rn(r[2], r[3]);
+    uint2 x;
+    x.x = *reinterpret_cast<uint32_t*>(&a);
+    x.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = x;
+  }
+};
+
+template <typename QT, typename ST, int K, int VT>
+__global__ void __launch_bounds__(kDecThreads)
+kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* __restrict__ v,
+                  const float* __restrict__ g, const float* __restrict__ beta,
+                  ST* __restrict__ pool, const int32_t* __restrict__ idx, QT* __restrict__ o,
+                  uint32_t* __restrict__ status, int Hk, int Hv, int V, int64_t num_slots,
+                  int64_t slot_stride, float scale) {
+  constexpr int TPR = VT / 4;               // threads per row
+  constexpr int RG = kDecThreads / TPR;     // row groups
+  constexpr int RPT = K / RG;               // rows per thread
+  static_assert(K % RG == 0, "K must split over the row groups");
+
+  const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * VT;
+  const int tid = threadIdx.x, rg = tid / TPR, col = (tid % TPR) * 4;
+
+  int64_t slot = n;
+  if (idx != nullptr) {
+    slot = resolve_slot(idx, n, num_slots);
+    if (slot < 0) {
+      if (tid == 0 && blockIdx.z == 0) raise_status(status, KDA_DEVICE_BAD_SLOT);
+      return;
+    }
+  } else if (slot >= num_slots) {
+    if (tid == 0 && blockIdx.z == 0) raise_status(status, KDA_DEVICE_BAD_SLOT);
+    return;
+  }
+
+  __shared__ float red_w[RG][VT];
+  __shared__ float red_o[RG][VT];
+
+  const int kh = h / (Hv / Hk);
+  const QT* qn = q + ((size_t)n * Hk + kh) * K;
+  const QT* kn = k + ((size_t)n * Hk + kh) * K;
+  const float* gn = g + ((size_t)n * Hv + h) * K;
+  ST* S = pool + slot * slot_stride + (size_t)h * K * V + v0 + col;
+
+  float s[RPT][4], kr[RPT], qr[RPT];
+  // Issue every state load first (the tile is the whole cost of the kernel).
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) Vec4<ST>::load(S + (size_t)(rg + j * RG) * V, s[j]);
+  float w[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) {
+    const int c = rg + j * RG;
+    const float e = expf(gn[c]);
+    kr[j] = to_f32(kn[c]);
+    qr[j] = to_f32(qn[c]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      s[j][i] *= e;                    // decay first
+      w[i] = fmaf(kr[j], s[j][i], w[i]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) red_w[rg][col + i] = w[i];
+  __syncthreads();
+  const float b = beta[(size_t)n * Hv + h];
+  float u[4];
+  {
+    float vin[4];
+    const QT* vn = v + ((size_t)n * Hv + h) * V + v0 + col;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) vin[i] = to_f32(vn[i]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int r = 0; r < RG; ++r) acc += red_w[r][col + i];
+      u[i] = b * (vin[i] - acc);
+    }
+  }
+  float ov[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      s[j][i] = fmaf(kr[j], u[i], s[j][i]);
+      ov[i] = fmaf(qr[j], s[j][i], ov[i]);
+    }
+    Vec4<ST>::store(S + (size_t)(rg + j * RG) * V, s[j]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) red_o[rg][col + i] = ov[i];
+  __syncthreads();
+  if (rg == 0) {
+    QT* on = o + ((size_t)n * Hv + h) * V + v0 + col;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int r = 0; r < RG; ++r) acc += red_o[r][col + i];
+      on[i] = from_f32<QT>(scale * acc);
+    }
+  }
+}
+
+template <typename QT, typename ST, int K>
+cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
+  const int V = a.d.head_v_dim;
+  const int VT = V >= 128 ? 128 : 64;
+  dim3 grid((unsigned)a.d.num_seqs, (unsigned)a.d.num_v_heads, (unsigned)(V / VT));
+  if (VT == 128)
+    kda_decode_kernel<QT, ST, K, 128><<<grid, kDecThreads, 0, st>>>(
+        (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, (ST*)a.pool, a.idx,
+        (QT*)a.o, a.status, a.d.num_k_heads, a.d.num_v_heads, V, a.d.num_slots, a.slot_stride,
+        a.scale);
+  else
+    kda_decode_kernel<QT, ST, K, 64><<<grid, kDecThreads, 0, st>>>(
+        (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, (ST*)a.pool, a.idx,
+        (QT*)a.o, a.status, a.d.num_k_heads, a.d.num_v_heads, V, a.d.num_slots, a.slot_stride,
+        a.scale);
+  return cudaGetLastError();
+}
+
+template <typename QT, typename ST>
+cudaError_t launch_k(const DecodeArgs& a, cudaStream_t st) {
+  return a.d.head_k_dim == 128 ? launch_typed<QT, ST, 128>(a, st) : launch_typed<QT, ST, 64>(a, st);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
+  if (a.d.num_seqs == 0) return cudaSuccess;
+  const bool qb = a.d.qkv_dtype == KDA_BF16, sb = a.d.state_dtype == KDA_BF16;
+  if (qb && sb) return launch_k<__nv_bfloat16, __nv_bfloat16>(a, st);
+  if (qb) return launch_k<__nv_bfloat16, float>(a, st);
+  if (sb) return launch_k<float, __nv_bfloat16>(a, st);
+  return launch_k<float, float>(a, st);
+}
+
+}  // namespace kda

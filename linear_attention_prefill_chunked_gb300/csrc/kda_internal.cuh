@@ -1,0 +1,90 @@
+// kda_internal.cuh -- shared device/host helpers of the KDA CUDA library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Workspace header: the device status word and scheduler counters live in the
+// first 256 bytes; per-path scratch follows at kWsPayload.
+struct WsHeader {
+  uint32_t status;        // KDA_DEVICE_* bits
+  uint32_t next_item;     // dynamic work counter of the persistent prefill
+  uint32_t reserved[62];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+constexpr size_t kWsPayload = 256;
+
+__device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {
+  atomicOr(status, bit);
+}
+
+// ---- element conversions ----------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);  // round to nearest even
+}
+
+// Resolved per-sequence state slot: index -1 -> sentinel (num_slots - 1);
+// returns -1 for an index outside [-1, num_slots).
+__device__ __forceinline__ int64_t resolve_slot(const int32_t* idx, int n, int64_t num_slots) {
+  const int32_t s = idx[n];
+  if (s < -1 || (int64_t)s >= num_slots) return -1;
+  return s < 0 ? num_slots - 1 : (int64_t)s;
+}
+
+// Sequence bounds with validation against [0, T]; returns false if invalid.
+__device__ __forceinline__ bool seq_bounds(const int32_t* cu, int n, int64_t T, int64_t* bos,
+                                           int64_t* eos) {
+  const int64_t a = cu[n], b = cu[n + 1];
+  if (a < 0 || b < a || b > T) return false;
+  *bos = a;
+  *eos = b;
+  return true;
+}
+
+}  // namespace kda
+
+// Internal launchers (C++ linkage, defined in the .cu files).
+namespace kda {
+struct PrefillArgs {
+  kda_desc_t d;
+  float scale;
+  int64_t slot_stride;
+  const void *q, *k, *v;
+  const float *g, *beta;
+  const int32_t* cu;
+  const void* state_in;      // pool, dense h0 or null
+  const int32_t* idx;        // null in dense mode
+  void* state_out;           // pool (== state_in), dense ht, or null
+  void* o;
+  uint32_t* status;
+  uint8_t* ws;               // workspace base
+  size_t ws_bytes;
+};
+cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t st);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st);
+size_t prefill_tc_workspace(const kda_desc_t& d);
+bool prefill_tc_supported(const kda_desc_t& d);
+
+struct DecodeArgs {
+  kda_desc_t d;
+  float scale;
+  int64_t slot_stride;
+  const void *q, *k, *v;
+  const float *g, *beta;
+  void* pool;
+  const int32_t* idx;
+  void* o;
+  uint32_t* status;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+}  // namespace kda

@@ -1,0 +1,94 @@
+"""GPU parity of the one-token decode against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_prefill_chunked_gb300 as kda
+from linear_attention_prefill_chunked_gb300 import synthetic
+from oracle import kda_oracle
+from tests._util import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_rows(w, rows, pool_rows_before):
+    """Oracle o and final state for the given rows (each with its own slot)."""
+    o_all, s_all = [], []
+    for j, n in enumerate(rows):
+        o, fin = kda_oracle.recurrence(
+            w.q[n:n + 1], w.k[n:n + 1], w.v[n:n + 1], w.g[n:n + 1], w.beta[n:n + 1], [0, 1],
+            scale=w.scale, state=pool_rows_before[j:j + 1])
+        o_all.append(o[0])
+        s_all.append(fin[0])
+    return np.stack(o_all), np.stack(s_all)
+
+
+def test_decode_large_batch_sampled():
+    """4096 rows x 32 heads (N*Hv = 131072 > 65535), 8192-slot fp32 pool, 64 pad rows."""
+    w = synthetic.decode_batch(pool_device="cuda")
+    pool = w.state
+    q, k, v, g, beta = (t.cuda() for t in (w.q, w.k, w.v, w.g, w.beta))
+    idx = w.state_indices.cuda()
+    rng = np.random.default_rng(0)
+    real = np.sort(rng.choice(4032, size=48, replace=False))
+    slots = w.state_indices[real].long()
+    before = pool[slots.cuda()].cpu()
+    used = set(w.state_indices[:4032].tolist()) | {pool.shape[0] - 1}
+    free = np.array([s for s in range(pool.shape[0]) if s not in used])
+    untouched = torch.from_numpy(rng.choice(free, size=32, replace=False)).cuda()
+    untouched_before = pool[untouched].clone()
+    o = kda.decode(q, k, v, g, beta, pool, idx, scale=w.scale)
+    torch.cuda.synchronize()
+    assert kda.read_device_status(kda.decode.last_workspace) == 0
+    assert torch.isfinite(o[:4032]).all()
+    o_ref, s_ref = _oracle_rows(w, real, before)
+    assert_close(o[real], o_ref, torch.bfloat16, "o")
+    assert_close(pool[slots.cuda()], s_ref, torch.float32, "pool rows")
+    assert torch.equal(pool[untouched], untouched_before)
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+def test_decode_equals_prefill_with_unit_lengths(state_dtype):
+    w = synthetic.make([1] * 300, Hk=4, Hv=8, K=128, V=128, dtype=torch.bfloat16, seed=2,
+                       state="pool", num_slots=512, state_dtype=state_dtype)
+    q, k, v, g, beta = (t.cuda() for t in (w.q, w.k, w.v, w.g, w.beta))
+    idx = w.state_indices.cuda()
+    pool_d = w.state.cuda()
+    pool_p = pool_d.clone()
+    o_d = kda.decode(q, k, v, g, beta, pool_d, idx)
+    o_p, _ = kda.chunk_prefill(q, k, v, g, beta, w.cu_seqlens.cuda(), state=pool_p,
+                               state_indices=idx)
+    o_ref, pool_ref = kda_oracle.recurrence(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens,
+                                            state=w.state, state_indices=w.state_indices)
+    assert_close(o_d, o_ref, torch.bfloat16, "decode o")
+    assert_close(o_p, o_ref, torch.bfloat16, "prefill o")
+    tol_dtype = torch.bfloat16
+    assert_close(pool_d, pool_ref, tol_dtype, "decode pool")
+    assert_close(pool_p, pool_ref, tol_dtype, "prefill pool")
+
+
+def test_decode_fp32_inputs_and_shuffled_padding():
+    w = synthetic.make([1] * 200, Hk=2, Hv=4, K=64, V=128, dtype=torch.float32, seed=4,
+                       state="pool", num_slots=300)
+    idx = w.state_indices.clone()
+    perm = torch.randperm(200, generator=torch.Generator().manual_seed(1))
+    idx[perm[:7]] = -1  # padding rows spread through the batch
+    q, k, v, g, beta = (t.cuda() for t in (w.q, w.k, w.v, w.g, w.beta))
+    pool = w.state.cuda()
+    o = kda.decode(q, k, v, g, beta, pool, idx.cuda())
+    real = np.array(sorted(set(range(200)) - set(perm[:7].tolist())))
+    before = w.state[idx[real].long()]
+    o_ref, s_ref = _oracle_rows(w, real, before)
+    assert_close(o[real], o_ref, torch.float32, "o")
+    assert_close(pool[idx[real].long().cuda()], s_ref, torch.float32, "pool rows")
+
+
+def test_decode_bad_slot_sets_status():
+    w = synthetic.make([1] * 10, Hk=1, Hv=2, K=128, V=128, dtype=torch.bfloat16, seed=6,
+                       state="pool", num_slots=16)
+    idx = w.state_indices.clone()
+    idx[3] = 16
+    q, k, v, g, beta = (t.cuda() for t in (w.q, w.k, w.v, w.g, w.beta))
+    pool = w.state.cuda()
+    kda.decode(q, k, v, g, beta, pool, idx.cuda())
+    assert kda.read_device_status(kda.decode.last_workspace) & kda.api.KDA_DEVICE_BAD_SLOT

@@ -1,0 +1,211 @@
+"""GPU parity of the chunked prefill against the fp64 oracle, through the C ABI.
+
+Tolerances (relative L2 over the tensor): 1e-2 with bf16 inputs, 1e-4 with fp32
+inputs; every output finite; pool mode bit-identical to dense gather/scatter
+(sglang PR 30169 digest, 关键源码片段 test_gdn_chunk_cutedsl_pool_mode_matches_dense).
+"""
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_prefill_chunked_gb300 as kda
+from linear_attention_prefill_chunked_gb300 import synthetic
+from oracle import kda_oracle
+from tests._util import assert_close, oracle_sampled, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_oracle(w, state=None, pool_mode=True):
+    st = w.state if state is None else state
+    return kda_oracle.recurrence(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, scale=w.scale,
+                                 state=st, state_indices=w.state_indices if pool_mode else None)
+
+
+def test_tiny_varlen_fp32_dense():
+    w = synthetic.tiny_varlen()
+    d = to_dev(w)
+    o, ht = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                              state=d["state"], scale=w.scale)
+    o_ref, ht_ref = _full_oracle(w, pool_mode=False)
+    assert_close(o, o_ref, torch.float32, "o")
+    assert_close(ht, ht_ref, torch.float32, "ht")
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+def test_pool_mode_matches_dense_bitwise_and_oracle(state_dtype):
+    w = synthetic.pool_varlen(state_dtype=state_dtype)
+    d = to_dev(w)
+    pool = d["state"]
+    slots = torch.where(d["state_indices"] >= 0, d["state_indices"],
+                        torch.full_like(d["state_indices"], pool.shape[0] - 1)).long()
+    h0_dense = pool[slots].clone()
+    pool_before = pool.clone()
+    o_dense, ht_dense = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                          d["cu_seqlens"], state=h0_dense.clone())
+    o_pool, ht_pool = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                        d["cu_seqlens"], state=pool,
+                                        state_indices=d["state_indices"])
+    torch.cuda.synchronize()
+    assert ht_pool is pool
+    assert torch.equal(o_pool, o_dense)
+    assert torch.equal(pool[slots], ht_dense)
+    untouched = torch.ones(pool.shape[0], dtype=torch.bool, device=pool.device)
+    untouched[slots] = False
+    assert torch.equal(pool[untouched], pool_before[untouched])
+    # against the oracle (the -1 sequence lands in the sentinel slot 15)
+    o_ref, pool_ref = _full_oracle(w)
+    assert_close(o_pool, o_ref, torch.bfloat16, "o")
+    assert_close(pool[slots], pool_ref[slots.cpu().numpy()], torch.bfloat16, "pool rows")
+    assert int(slots[-1]) == pool.shape[0] - 1
+
+
+def test_large_decay_finite_and_close():
+    w = synthetic.large_decay()
+    d = to_dev(w)
+    pool_before = w.state.clone()
+    o, _ = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                             state=d["state"], state_indices=d["state_indices"])
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all()
+    assert torch.isfinite(d["state"]).all()
+    pairs = [(0, 0), (3, 7), (5, 19), (7, 31), (2, int(torch.argmax(w.g.mean((0, 2)))))]
+    ref = oracle_sampled(w, pairs, state_before=pool_before)
+    cu = w.cu_seqlens.tolist()
+    slots = w.state_indices.tolist()
+    for (n, h), (o_ref, s_ref) in ref.items():
+        assert_close(o[cu[n]:cu[n + 1], h], o_ref, torch.bfloat16, f"o seq {n} head {h}")
+        assert_close(d["state"][slots[n], h], s_ref, torch.bfloat16, f"state seq {n} head {h}")
+
+
+def test_throughput_workload_sampled():
+    w = synthetic.throughput()
+    d = to_dev(w)
+    pool_before = w.state.clone()
+    o, _ = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                             state=d["state"], state_indices=d["state_indices"])
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all()
+    lens = w.lens
+    longest = int(np.argmax(lens))
+    pairs = [(longest, 0), (longest, 31), (int(np.argmin(lens)), 5), (3, 17), (9, 8)]
+    ref = oracle_sampled(w, pairs, state_before=pool_before)
+    cu = w.cu_seqlens.tolist()
+    slots = w.state_indices.tolist()
+    for (n, h), (o_ref, s_ref) in ref.items():
+        assert_close(o[cu[n]:cu[n + 1], h], o_ref, torch.bfloat16, f"o seq {n} head {h}")
+        assert_close(d["state"][slots[n], h], s_ref, torch.bfloat16, f"state seq {n} head {h}")
+
+
+@pytest.mark.parametrize("K,V,dtype", [(64, 128, torch.float32), (128, 64, torch.bfloat16),
+                                       (64, 64, torch.bfloat16), (128, 128, torch.float32)])
+def test_head_dims_and_dtypes(K, V, dtype):
+    w = synthetic.make([3, 64, 129, 1, 200], Hk=2, Hv=4, K=K, V=V, dtype=dtype, seed=K + V,
+                       state="pool", num_slots=8)
+    d = to_dev(w)
+    o, pool = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                state=d["state"], state_indices=d["state_indices"])
+    o_ref, pool_ref = _full_oracle(w)
+    assert_close(o, o_ref, dtype, "o")
+    assert_close(pool, pool_ref, dtype, "pool")
+
+
+@pytest.mark.parametrize("p", [1, 37, 63, 64, 65, 130])
+def test_split_invariance_through_pool(p):
+    w = synthetic.make([200], Hk=4, Hv=8, K=128, V=128, dtype=torch.bfloat16, seed=p,
+                       state="pool", num_slots=4)
+    d = to_dev(w)
+    pool_a = d["state"].clone()
+    o_full, _ = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                  state=pool_a, state_indices=d["state_indices"])
+    pool_b = d["state"].clone()
+    cu1 = torch.tensor([0, p], dtype=torch.int32, device="cuda")
+    cu2 = torch.tensor([0, 200 - p], dtype=torch.int32, device="cuda")
+    o1, _ = kda.chunk_prefill(d["q"][:p].contiguous(), d["k"][:p].contiguous(),
+                              d["v"][:p].contiguous(), d["g"][:p].contiguous(),
+                              d["beta"][:p].contiguous(), cu1, state=pool_b,
+                              state_indices=d["state_indices"])
+    o2, _ = kda.chunk_prefill(d["q"][p:].contiguous(), d["k"][p:].contiguous(),
+                              d["v"][p:].contiguous(), d["g"][p:].contiguous(),
+                              d["beta"][p:].contiguous(), cu2, state=pool_b,
+                              state_indices=d["state_indices"])
+    o_ref, pool_ref = _full_oracle(w)
+    assert_close(torch.cat([o1, o2]), o_ref, torch.bfloat16, "split o")
+    assert_close(pool_b, pool_ref, torch.bfloat16, "split pool")
+    assert_close(o_full, o_ref, torch.bfloat16, "whole o")
+
+
+def test_run_to_run_bit_identical():
+    w = synthetic.pool_varlen()
+    d = to_dev(w)
+    outs = []
+    for _ in range(2):
+        pool = d["state"].clone()
+        o, _ = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                 state=pool, state_indices=d["state_indices"])
+        outs.append((o, pool))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_zero_length_sequences_and_empty_batch():
+    w = synthetic.make([0, 70, 0, 5], Hk=1, Hv=2, K=128, V=128, dtype=torch.bfloat16, seed=3,
+                       state="dense")
+    d = to_dev(w)
+    o, ht = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                              state=d["state"])
+    o_ref, ht_ref = _full_oracle(w, pool_mode=False)
+    assert_close(o, o_ref, torch.bfloat16, "o")
+    assert torch.equal(ht[0], d["state"][0]) and torch.equal(ht[2], d["state"][2])
+    assert_close(ht, ht_ref, torch.bfloat16, "ht")
+    # N = 0, T = 0
+    e = torch.empty((0, 1, 128), dtype=torch.bfloat16, device="cuda")
+    o0, h0 = kda.chunk_prefill(e, e, torch.empty((0, 2, 128), dtype=torch.bfloat16, device="cuda"),
+                               torch.empty((0, 2, 128), device="cuda"),
+                               torch.empty((0, 2), device="cuda"),
+                               torch.zeros(1, dtype=torch.int32, device="cuda"))
+    assert o0.shape == (0, 2, 128) and h0.shape == (0, 2, 128, 128)
+
+
+def test_zero_initial_state_and_padded_gate_rows():
+    w = synthetic.make([90, 33], Hk=2, Hv=2, K=128, V=128, dtype=torch.bfloat16, seed=5,
+                       state=None, g_pad_rows=17)
+    d = to_dev(w)
+    d["g"][-17:] = float("nan")      # padding rows past T must never be read
+    d["beta"][-17:] = float("nan")
+    o, ht = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"])
+    T = w.T
+    o_ref, ht_ref = kda_oracle.recurrence(w.q, w.k, w.v, w.g[:T], w.beta[:T], w.cu_seqlens,
+                                          scale=w.scale)
+    assert_close(o, o_ref, torch.bfloat16, "o")
+    assert_close(ht, ht_ref, torch.bfloat16, "ht")
+
+
+def test_bad_slot_and_bad_seqlens_set_device_status():
+    w = synthetic.make([20, 30, 40], Hk=1, Hv=2, K=128, V=128, dtype=torch.bfloat16, seed=9,
+                       state="pool", num_slots=6)
+    d = to_dev(w)
+    idx = d["state_indices"].clone()
+    idx[1] = 6  # out of range
+    pool = d["state"].clone()
+    o = torch.zeros((w.T, 2, 128), dtype=torch.bfloat16, device="cuda")
+    kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], state=pool,
+                      state_indices=idx, out=o)
+    bits = kda.read_device_status(kda.chunk_prefill.last_workspace)
+    assert bits & kda.api.KDA_DEVICE_BAD_SLOT
+    o_ref, pool_ref = _full_oracle(w)
+    cu = w.cu_seqlens.tolist()
+    assert torch.count_nonzero(o[cu[1]:cu[2]]) == 0          # skipped sequence untouched
+    for n in (0, 2):
+        s = int(w.state_indices[n])
+        assert_close(o[cu[n]:cu[n + 1]], o_ref[cu[n]:cu[n + 1]], torch.bfloat16, f"o seq {n}")
+        assert_close(pool[s], pool_ref[s], torch.bfloat16, f"slot {s}")
+    # a clean call clears the word
+    kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                      state=d["state"].clone(), state_indices=d["state_indices"])
+    assert kda.read_device_status(kda.chunk_prefill.last_workspace) == 0
+    # non-monotone cu_seqlens
+    cu_bad = d["cu_seqlens"].clone()
+    cu_bad[2] = 10
+    kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_bad,
+                      state=d["state"].clone(), state_indices=d["state_indices"])
+    assert kda.read_device_status(kda.chunk_prefill.last_workspace) & kda.api.KDA_DEVICE_BAD_SEQLENS
