@@ -1,0 +1,310 @@
+"""Benchmark of the chunked KDA prefill (tokens/s) on the throughput workload.
+
+Workload: 32768 packed tokens in 16 sequences (lengths log-uniform in [64, 8192],
+rescaled), Hk = Hv = 32, K = V = 128, bf16 q/k/v, fp32 g/beta, fp32 state pool of
+256 slots updated in place.  One step = one kda_chunk_prefill call over the whole
+batch.  Inputs (1.68 GB per step) are larger than L2, so no flush is needed.
+
+Prints one JSON line.  --impl reference times the fp64 CPU oracle instead.
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU
+(replicas, no collective on the data path); value = tokens of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "KDA prefill tokens/s at Hv=32,K=V=128 (1 GB300); % of HBM/tensor roofline"
+SAMPLE_HEADS = 4      # CPU baseline: every sequence, v-heads 0..3 (1/8 of the work)
+SAMPLE_HEADS_REF = 1  # reference arm, per step: every sequence, v-head 0 (1/32 of the work)
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic_bytes(w):
+    """Bytes the path must move once: q, k, v, g, beta in; o out; pool rows in and out."""
+    T, Hk, K = w.q.shape
+    Hv, V = w.v.shape[1], w.v.shape[2]
+    e = w.q.element_size()
+    se = w.state.element_size() if w.state is not None else 4
+    return (T * Hk * K * e * 2 + T * Hv * V * e + T * Hv * K * 4 + T * Hv * 4 + T * Hv * V * e
+            + w.N * Hv * K * V * se * 2)
+
+
+def algorithmic_flops(w):
+    """MMA FLOPs of the chunked form, counting triangles, exact for partial chunks."""
+    K, V, Hv = w.q.shape[2], w.v.shape[2], w.v.shape[1]
+    tot = 0
+    for L in w.lens:
+        for c0 in range(0, L, 64):
+            c = min(64, L - c0)
+            tri_s, tri = c * (c - 1) // 2, c * (c + 1) // 2
+            tot += (2 * tri_s * K + 2 * tri * (K + V + K + V) + c ** 3 // 3 + 3 * 2 * c * K * V)
+    return tot * Hv
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, ws, rank, local
+    return None, 1, 0, local
+
+
+def cpu_baseline(w, num_threads=0, heads=SAMPLE_HEADS):
+    """Time the fp64 oracle on a bounded sample: all sequences, v-heads 0..heads-1."""
+    from oracle import kda_oracle
+    H = heads
+    hk = max(1, H * w.q.shape[1] // w.v.shape[1])
+    kda_oracle.build()
+    args = (w.q[:, :hk].contiguous(), w.k[:, :hk].contiguous(), w.v[:, :H].contiguous(),
+            w.g[:, :H].contiguous(), w.beta[:, :H].contiguous(), w.cu_seqlens)
+    t0 = time.perf_counter()
+    kda_oracle.recurrence(*args, scale=w.scale, state=w.state[:, :H].contiguous(),
+                          state_indices=w.state_indices, num_threads=num_threads)
+    dt = time.perf_counter() - t0
+    cores = num_threads if num_threads > 0 else (os.cpu_count() or 1)
+    frac = H / w.v.shape[1]
+    return {"value": w.T * frac / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"all {w.N} sequences ({w.T} tokens), v-heads 0-{H - 1} of {w.v.shape[1]} "
+                      f"({frac:.3f} of the work), fp64 token-by-token, {dt:.2f} s; value scaled "
+                      f"to full-width tokens"}
+
+
+def run_reference(args, dist, ws, rank):
+    from linear_attention_prefill_chunked_gb300 import synthetic
+    if rank != 0:
+        return
+    w = synthetic.throughput()
+    times = []
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(w, heads=SAMPLE_HEADS_REF)
+        if i >= args.warmup:
+            times.append(cb)
+    val = statistics.median(t["value"] for t in times)
+    ms = w.T / val * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "tokens": w.T, "num_seqs": w.N, "Hk": 32, "Hv": 32,
+                       "K": 128, "V": 128, "parallelism": "host threads over (sequence, head)"},
+            "cpu_baseline": {k: times[-1][k] for k in ("kind", "cores", "sample")} | {"value": val,
+                                                                                      "unit": "tokens/s"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, dist, ws, rank, local):
+    import linear_attention_prefill_chunked_gb300 as kda
+    from linear_attention_prefill_chunked_gb300 import synthetic
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kda.load()
+    w = synthetic.throughput()
+    t = lambda x: x.to(dev).contiguous()
+    q, k, v, g, beta, cu, idx = (t(x) for x in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens,
+                                                 w.state_indices))
+    pool = t(w.state)
+    out = torch.empty((w.T, 32, 128), dtype=torch.bfloat16, device=dev)
+    desc = kda.make_desc(num_seqs=w.N, total_tokens=w.T, Hk=32, Hv=32, K=128, V=128,
+                         qkv_dtype=torch.bfloat16, num_slots=pool.shape[0])
+    path = kda.prefill_path(desc)
+    ws_t = torch.empty(kda.prefill_workspace_size(desc), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.chunk_prefill(q, k, v, g, beta, cu, state=pool, state_indices=idx, out=out,
+                          workspace=ws_t, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    per = [a.elapsed_time(b) for a, b in ev]  # ms, one launch sequence each
+    total_ms = sum(per)
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+        dist.barrier()
+    bits = kda.read_device_status(ws_t)
+
+    # End to end through the public API from pinned host buffers (copies inside).
+    hq, hk, hv, hg, hb, hcu, hidx = (x.contiguous().pin_memory() for x in
+                                     (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.state_indices))
+    h_out = torch.empty((w.T, 32, 128), dtype=torch.bfloat16).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hg, hb, hcu, hidx))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        dq, dk, dv, dg, db, dcu, didx = (x.to(dev, non_blocking=True) for x in
+                                         (hq, hk, hv, hg, hb, hcu, hidx))
+        o, _ = kda.chunk_prefill(dq, dk, dv, dg, db, dcu, state=pool, state_indices=didx,
+                                 workspace=ws_t, stream=stream)
+        h_out.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(2, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    if rank != 0:
+        return
+    hbm, bf16, src = _peaks()
+    ms = total_ms / args.steps
+    value = ws * w.T / (ms * 1e-3)
+    nbytes = algorithmic_bytes(w)
+    flops = algorithmic_flops(w)
+    kern_ms = statistics.median(per)
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    t_roof = max(nbytes / (hbm * 1e9), flops / (bf16 * 1e12))
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    traffic = None
+    if os.path.exists(prof):
+        with open(prof) as f:
+            tr = json.load(f)
+        if tr.get("path") == path:
+            traffic = tr.get("bytes_per_launch")
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.T, "num_seqs": w.N, "Hk": 32, "Hv": 32,
+                   "K": 128, "V": 128, "chunk": 64, "state_pool": "fp32, 256 slots, in place",
+                   "kernel_path": "tcgen05 fused" if path == 1 else "CUDA-core fp32",
+                   "l2": "inputs larger than L2 (1.68 GB per step), no flush",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else src,
+                     "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
+                     "roofline_time_ms": t_roof * 1e3, "frac_of_roofline_time": t_roof * 1e3 / kern_ms},
+        "clocks": clk.summary(),
+        "e2e": {"value": w.T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "note": "pinned host q/k/v/g/beta/cu_seqlens/indices copied in, o copied out each "
+                        "step; the state pool stays resident on the device"},
+        "gpu_launches": args.steps * (2 if path == 1 else 1),
+        "device_status": bits, "wall_s": wall,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    dist, ws, rank, local = _dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist, ws, rank)
+        else:
+            run_ours(args, dist, ws, rank, local)
+    finally:
+        if dist:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -59,6 +59,10 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
 #define KDA_DEVICE_BAD_SEQLENS   0x2u  /* cu_seqlens not monotone / outside [0, T]  */
 #define KDA_DEVICE_PIPE_TIMEOUT  0x4u  /* an internal pipeline wait gave up         */
 
+/* Descriptor flags. */
+#define KDA_FLAG_CUDA_CORE_PATH  0x1u  /* prefill: run the fp32 CUDA-core kernel even where
+                                          the tensor-core kernel applies (cross-checks) */
+
 /* Problem descriptor shared by prefill and decode. */
 typedef struct {
     int32_t num_seqs;          /* N (prefill: packed sequences; decode: rows)          */
@@ -78,7 +82,7 @@ typedef struct {
     int64_t slot_stride_elems; /* pool: elements between consecutive slots; 0 means
                                   Hv*K*V.  Must be >= Hv*K*V.  (The pitch is passed, not
                                   inferred from a shape: PR 37317 digest, 实现拆解 item 2.) */
-    uint32_t flags;            /* reserved, must be 0                                   */
+    uint32_t flags;            /* KDA_FLAG_* bits; every other bit must be 0           */
 } kda_desc_t;
 
 /* Bytes of workspace kda_chunk_prefill() needs for this descriptor (0 on an

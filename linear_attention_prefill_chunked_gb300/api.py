@@ -17,6 +17,7 @@ import torch
 from . import build as _build
 
 KDA_BF16, KDA_F32 = 0, 1
+KDA_FLAG_CUDA_CORE_PATH = 0x1
 KDA_DEVICE_BAD_SLOT, KDA_DEVICE_BAD_SEQLENS, KDA_DEVICE_PIPE_TIMEOUT = 0x1, 0x2, 0x4
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
            3: "workspace too small", 4: "CUDA error", 5: "invalid device data"}
@@ -116,7 +117,7 @@ def _need(t, name, dtype=None, cuda=True):
 
 
 def make_desc(*, num_seqs, total_tokens, Hk, Hv, K, V, qkv_dtype, state_dtype=torch.float32,
-              scale=None, num_slots=0, slot_stride=0) -> KdaDesc:
+              scale=None, num_slots=0, slot_stride=0, flags=0) -> KdaDesc:
     d = KdaDesc()
     d.num_seqs = num_seqs
     d.total_tokens = total_tokens
@@ -127,7 +128,7 @@ def make_desc(*, num_seqs, total_tokens, Hk, Hv, K, V, qkv_dtype, state_dtype=to
     d.chunk_size = 64
     d.num_slots = num_slots
     d.slot_stride_elems = slot_stride
-    d.flags = 0
+    d.flags = flags
     return d
 
 
@@ -151,7 +152,7 @@ def read_device_status(workspace: torch.Tensor, stream=None) -> int:
 
 def chunk_prefill(q, k, v, g, beta, cu_seqlens, *, state=None, state_indices=None,
                   final_state=None, output_final_state=True, scale=None, slot_stride=0,
-                  out=None, workspace=None, stream=None):
+                  out=None, workspace=None, stream=None, cuda_core_path=False):
     """Chunked KDA prefill.  Returns ``(o, final)``.
 
     q, k [T, Hk, K]; v [T, Hv, V] (bf16 or fp32, same dtype); g [>=T, Hv, K] fp32;
@@ -191,7 +192,8 @@ def chunk_prefill(q, k, v, g, beta, cu_seqlens, *, state=None, state_indices=Non
     if state is not None and not pool:
         _need(state, "state")
     d = make_desc(num_seqs=N, total_tokens=T, Hk=Hk, Hv=Hv, K=K, V=V, qkv_dtype=q.dtype,
-                  state_dtype=sdt, scale=scale, num_slots=num_slots, slot_stride=slot_stride)
+                  state_dtype=sdt, scale=scale, num_slots=num_slots, slot_stride=slot_stride,
+                  flags=KDA_FLAG_CUDA_CORE_PATH if cuda_core_path else 0)
     if out is None:
         out = torch.empty((T, Hv, V), dtype=q.dtype, device=q.device)
     ws_size = lib.kda_chunk_prefill_workspace_size(ctypes.byref(d))

@@ -14,7 +14,7 @@ bool dims_ok(const kda_desc_t* d) {
   if (d->num_k_heads <= 0 || d->num_v_heads <= 0) return false;
   if (d->num_v_heads % d->num_k_heads != 0) return false;
   if (d->chunk_size != 64) return false;
-  if (d->flags != 0) return false;
+  if ((d->flags & ~KDA_FLAG_CUDA_CORE_PATH) != 0) return false;
   if (!(d->qkv_dtype == KDA_BF16 || d->qkv_dtype == KDA_F32)) return false;
   if (!(d->state_dtype == KDA_BF16 || d->state_dtype == KDA_F32)) return false;
   if (!std::isfinite(d->scale)) return false;

@@ -72,12 +72,17 @@ def test_workspace_queries_and_path_selection():
     d.chunk_size = 32
     bad.append(d)
     d = _desc()
-    d.flags = 1
+    d.flags = 2
     bad.append(d)
     for b in bad:
         assert kda.prefill_workspace_size(b) == 0
         assert kda.prefill_path(b) == -1
     assert kda.prefill_path(_desc(qkv_dtype=torch.float32)) == 0
+    assert kda.prefill_path(_desc()) == 1                    # bf16, 128x128 heads
+    d = _desc()
+    d.flags = 1                                              # KDA_FLAG_CUDA_CORE_PATH
+    assert kda.prefill_path(d) == 0
+    assert kda.prefill_path(_desc(K=64)) == 0
 
 
 def test_host_checked_errors_return_before_any_launch():

@@ -209,3 +209,27 @@ def test_bad_slot_and_bad_seqlens_set_device_status():
     kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_bad,
                       state=d["state"].clone(), state_indices=d["state_indices"])
     assert kda.read_device_status(kda.chunk_prefill.last_workspace) & kda.api.KDA_DEVICE_BAD_SEQLENS
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+def test_tensor_core_path_matches_cuda_core_path_and_oracle(state_dtype):
+    """The fused tcgen05 kernel and the fp32 CUDA-core kernel on identical inputs."""
+    w = synthetic.make([1, 63, 64, 65, 200, 130, 17], Hk=2, Hv=4, K=128, V=128,
+                       dtype=torch.bfloat16, seed=21, state="pool", num_slots=12,
+                       state_dtype=state_dtype, last_index_pad=True)
+    d = to_dev(w)
+    desc = kda.make_desc(num_seqs=w.N, total_tokens=w.T, Hk=2, Hv=4, K=128, V=128,
+                         qkv_dtype=torch.bfloat16, num_slots=12)
+    assert kda.prefill_path(desc) == 1
+    pool_tc, pool_cc = d["state"].clone(), d["state"].clone()
+    o_tc, _ = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                state=pool_tc, state_indices=d["state_indices"])
+    assert kda.read_device_status(kda.chunk_prefill.last_workspace) == 0
+    o_cc, _ = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                state=pool_cc, state_indices=d["state_indices"],
+                                cuda_core_path=True)
+    o_ref, pool_ref = _full_oracle(w)
+    assert_close(o_tc, o_ref, torch.bfloat16, "tensor-core o")
+    assert_close(pool_tc, pool_ref, torch.bfloat16, "tensor-core pool")
+    assert_close(o_cc, o_ref, torch.bfloat16, "cuda-core o")
+    assert_close(o_tc, o_cc.double().cpu().numpy(), torch.bfloat16, "tc vs cuda-core o")
