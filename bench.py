@@ -176,7 +176,11 @@ def run_ours(args, dist, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     kda.load()
-    w = synthetic.throughput()
+    if args.workload == "profile":
+        w = synthetic.make([1024] * 8, Hk=32, Hv=32, K=128, V=128, seed=5, state="pool",
+                           num_slots=16, name="profile_8x1024_Hv32_K128")
+    else:
+        w = synthetic.throughput()
     t = lambda x: x.to(dev).contiguous()
     q, k, v, g, beta, cu, idx = (t(x) for x in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens,
                                                  w.state_indices))
@@ -218,30 +222,33 @@ def run_ours(args, dist, ws, rank, local):
     bits = kda.read_device_status(ws_t)
 
     # End to end through the public API from pinned host buffers (copies inside).
-    hq, hk, hv, hg, hb, hcu, hidx = (x.contiguous().pin_memory() for x in
-                                     (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.state_indices))
-    h_out = torch.empty((w.T, 32, 128), dtype=torch.bfloat16).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hg, hb, hcu, hidx))
-    d2h = h_out.numel() * h_out.element_size()
+    e2e_ms, h2d, d2h = None, 0, 0
+    if not args.no_e2e:
+        hq, hk, hv, hg, hb, hcu, hidx = (x.contiguous().pin_memory() for x in
+                                         (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens,
+                                          w.state_indices))
+        h_out = torch.empty((w.T, 32, 128), dtype=torch.bfloat16).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hg, hb, hcu, hidx))
+        d2h = h_out.numel() * h_out.element_size()
 
-    def e2e_step():
-        dq, dk, dv, dg, db, dcu, didx = (x.to(dev, non_blocking=True) for x in
-                                         (hq, hk, hv, hg, hb, hcu, hidx))
-        o, _ = kda.chunk_prefill(dq, dk, dv, dg, db, dcu, state=pool, state_indices=didx,
-                                 workspace=ws_t, stream=stream)
-        h_out.copy_(o, non_blocking=True)
+        def e2e_step():
+            dq, dk, dv, dg, db, dcu, didx = (x.to(dev, non_blocking=True) for x in
+                                             (hq, hk, hv, hg, hb, hcu, hidx))
+            o, _ = kda.chunk_prefill(dq, dk, dv, dg, db, dcu, state=pool, state_indices=didx,
+                                     workspace=ws_t, stream=stream)
+            h_out.copy_(o, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_steps = max(2, min(args.steps, 5))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_steps = max(2, min(args.steps, 5))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     if rank != 0:
         return
@@ -275,7 +282,8 @@ def run_ours(args, dist, ws, rank, local):
                      "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
                      "roofline_time_ms": t_roof * 1e3, "frac_of_roofline_time": t_roof * 1e3 / kern_ms},
         "clocks": clk.summary(),
-        "e2e": {"value": w.T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": (w.T / (e2e_ms * 1e-3)) if e2e_ms else None, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "note": "pinned host q/k/v/g/beta/cu_seqlens/indices copied in, o copied out each "
                         "step; the state pool stays resident on the device"},
@@ -294,6 +302,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default="throughput", choices=["throughput", "profile"],
+                    help="profile: 8 x 1024 tokens, Hv=32 (a smaller case for ncu captures)")
     args = ap.parse_args()
     dist, ws, rank, local = _dist()
     try:
