@@ -23,18 +23,20 @@
 //     block 2: k kap / pi_s = k / rho (diagonal sub-chunks) on channels whose
 //              sub-chunk product pi_s >= 2^-64; the remaining ("unsafe")
 //              channels get their diagonal terms from an exact pairwise loop.
-//   Tm = (I + A)^-1 Diag(beta)   (fp32 blocked inverse on CUDA cores)
+//   Tm = (I + A)^-1 Diag(beta): 16x16 diagonal blocks by fp32 forward
+//   substitution, off-diagonal blocks by block forward substitution with tf32
+//   warp MMAs (tiny, latency-bound 16x16 products)
 //   U~^T = V^T Tm^T,  W^T = KG^T Tm^T                     (MMA, KG = k rho E)
 //   per chunk, sequentially (state S^T fp32 in TMEM, lanes = value channel):
 //     U^T = U~^T - S^T W^T          (MMA accumulating onto U~)
 //     O^T = S^T QG^T + U^T B^T      (QG = scale q rho E)
 //     S^T = S^T Diag(gamma) + U^T KR   (KR = k kap F, gamma = prod e)
 //
-// CTA = 9 warps, one CTA per SM, persistent over (sequence, head) items sorted
+// CTA = 12 warps, one CTA per SM, persistent over (sequence, head) items sorted
 // longest first and fetched from a global counter:
-//   warp 0     producer: item scheduling, TMA loads of q/k/v, L2 prefetch
-//   warps 1-4  intra group (S-independent work of chunk c+1)
-//   warps 5-8  recurrence group (state update and output of chunk c)
+//   warps 0-7   intra group (S-independent work of chunk c+1); its thread 0 also
+//               fetches items and issues the TMA loads of q, k, v and g
+//   warps 8-11  recurrence group (state update and output of chunk c)
 // Pool I/O (sglang PR 30169 digest, 实现拆解 items 1-3) is fused: the
 // recurrence group reads h0 from pool[state_indices[n]] (-1 -> last slot) and
 // writes the final state back to the same row.
@@ -51,7 +53,7 @@ using namespace tc;
 constexpr int kC = 64;
 constexpr int kK = 128;
 constexpr int kV = 128;
-constexpr int kThreads = 288;
+constexpr int kThreads = 384;
 constexpr int kRing = 4;
 constexpr float kSafeMin = 5.421010862427522e-20f;  // 2^-64
 
@@ -68,9 +70,12 @@ constexpr uint32_t OFF_KR = 163840;   // [128 ch][64 tokens]  KR              (K
 constexpr uint32_t OFF_ST = 180224;   // [2 K-atoms][128 v][128 B]  S^T bf16   (K-major A)
 constexpr uint32_t OFF_UT = 212992;   // [128 v][64 tokens]   U^T bf16        (K-major A)
 constexpr uint32_t OFF_SMALL = 229376;
-// fp32 scratch of the inverse, aliased on CB blocks 1 and 2 (dead after MMA-AB)
-constexpr uint32_t OFF_AS = OFF_CB + 16384;  // A (and B before it is packed), 64x64 fp32
-constexpr uint32_t OFF_XS = OFF_CB + 32768;  // B rows, then X = (I + A)^-1, 64x64 fp32
+// CB blocks 1 and 2 are dead from MMA-AB completion to the next prologue's
+// writes; they hold, in turn: the fp32 A and B rows and X = (I + A)^-1 of the
+// inverse (AS, XS), then the TMA-staged gate g of the next chunk ([64][128] fp32).
+constexpr uint32_t OFF_AS = OFF_CB + 16384;
+constexpr uint32_t OFF_XS = OFF_CB + 32768;
+constexpr uint32_t OFF_G = OFF_CB + 16384;
 
 // ---- TMEM columns ------------------------------------------------------------------
 constexpr uint32_t TM_U = 0;     // U~ -> U (64)
@@ -78,9 +83,13 @@ constexpr uint32_t TM_O = 64;    // O double buffer (2 x 64)
 constexpr uint32_t TM_S = 192;   // S^T fp32 (128)
 constexpr uint32_t TM_AB = 320;  // A/B result (192), later W^T (64)
 
+constexpr int kIG = 256;  // intra-group threads (warps 0-7)
+constexpr int kRG = 128;  // recurrence-group threads (warps 8-11)
+constexpr uint32_t BAR_IG = 1, BAR_RG = 2;
+
 enum Bar {
-  B_QK_FULL, B_V_FULL, B_QK_FREE, B_VB_FREE, B_AB_DONE, B_UW_DONE, B_GAMMA0, B_GAMMA1,
-  B_REC_READY, B_M1A, B_M1B, B_M3A, B_M3B, B_E1, B_DRAIN_IG, B_DRAIN_RG,
+  B_QK_FULL, B_V_FULL, B_G_FULL, B_AB_DONE, B_UW_DONE, B_GAMMA0, B_GAMMA1, B_REC_READY,
+  B_M1A, B_M1B, B_M3A, B_M3B, B_E1, B_DRAIN_IG, B_DRAIN_RG,
   B_ITEM_FULL, B_ITEM_EMPTY = B_ITEM_FULL + kRing, B_COUNT = B_ITEM_EMPTY + kRing
 };
 
@@ -95,7 +104,7 @@ struct Small {
   ItemInfo ring[kRing];
   float beta[kC];
   float gamma[2][kK];
-  uint32_t unsafe[4][4];  // [sub-chunk][channel word]
+  uint16_t unsafe[4][8];  // [sub-chunk][16-channel group] bitmask
   uint32_t tmem_base;
   uint32_t abort;
 };
@@ -130,6 +139,7 @@ __device__ __forceinline__ void st_chunk(uint8_t* sm, uint32_t off, uint32_t a, 
                                          uint32_t c, uint32_t d) {
   *reinterpret_cast<uint4*>(sm + off) = make_uint4(a, b, c, d);
 }
+// fp32 64x64 scratch index with an XOR swizzle (conflict-free row and fragment reads)
 __device__ __forceinline__ int sidx(int r, int i) { return r * 64 + (i ^ ((r & 7) << 2)); }
 
 __device__ __forceinline__ void fail(const TcParams& p, Small* s) {
@@ -154,242 +164,319 @@ __device__ __forceinline__ bool wait_bar(const TcParams& p, Small* s, int b, uin
   }
 }
 
-// ======================================================================================
-// Producer (warp 0, lane 0): items and TMA loads.
-// ======================================================================================
-__device__ void run_producer(const TcParams& p, uint8_t* sm, Small* s) {
-  uint32_t gc = 0, n_qk = 0, n_v = 0;
-  for (int k = 0;; ++k) {
-    const int slot = k % kRing;
-    if (k >= kRing && !wait_bar(p, s, B_ITEM_EMPTY + slot, ((k / kRing) - 1) & 1)) break;
-    ItemInfo info{};
-    // fetch the next valid item
-    for (;;) {
-      const uint32_t it = aborted(s) ? (uint32_t)p.num_items : atomicAdd(p.next_item, 1u);
-      if (it >= (uint32_t)p.num_items) { info.done = 1; break; }
-      const int n = p.order[it / p.Hv], h = it % p.Hv;
-      int64_t bos, eos;
-      if (!seq_bounds(p.cu, n, p.T, &bos, &eos)) { raise_status(p.status, KDA_DEVICE_BAD_SEQLENS); continue; }
-      int64_t sl = -1;
-      if (p.idx) {
-        sl = resolve_slot(p.idx, n, p.num_slots);
-        if (sl < 0) { raise_status(p.status, KDA_DEVICE_BAD_SLOT); continue; }
-      }
-      info.n = n; info.h = h; info.kh = h / (p.Hv / p.Hk);
-      info.bos = bos; info.eos = eos; info.slot = sl;
-      info.nchunks = (int)((eos - bos + kC - 1) / kC);
-      info.done = 0;
-      break;
+// Fetches the next valid (sequence, head) item from the global counter.
+__device__ ItemInfo fetch_item(const TcParams& p, Small* s) {
+  ItemInfo info{};
+  for (;;) {
+    const uint32_t it = aborted(s) ? (uint32_t)p.num_items : atomicAdd(p.next_item, 1u);
+    if (it >= (uint32_t)p.num_items) { info.done = 1; return info; }
+    const int n = p.order[it / p.Hv], h = it % p.Hv;
+    int64_t bos, eos;
+    if (!seq_bounds(p.cu, n, p.T, &bos, &eos)) { raise_status(p.status, KDA_DEVICE_BAD_SEQLENS); continue; }
+    int64_t sl = -1;
+    if (p.idx) {
+      sl = resolve_slot(p.idx, n, p.num_slots);
+      if (sl < 0) { raise_status(p.status, KDA_DEVICE_BAD_SLOT); continue; }
     }
-    s->ring[slot] = info;
-    mbar_arrive(&s->bar[B_ITEM_FULL + slot]);
-    if (info.done) break;
-    bool stop = false;
-    for (int lc = 0; lc < info.nchunks; ++lc, ++gc) {
-      const int t0 = (int)(info.bos + (int64_t)lc * kC);
-      if (gc > 0 && !wait_bar(p, s, B_QK_FREE, (gc - 1) & 1)) { stop = true; break; }
-      mbar_expect_tx(&s->bar[B_QK_FULL], 32768);
-      ++n_qk;
-      tma_load_3d(sm + OFF_QK + 0, &p.tm_k, &s->bar[B_QK_FULL], 0, info.kh, t0);
-      tma_load_3d(sm + OFF_QK + 16384, &p.tm_k, &s->bar[B_QK_FULL], 64, info.kh, t0);
-      tma_load_3d(sm + OFF_QK + 8192, &p.tm_q, &s->bar[B_QK_FULL], 0, info.kh, t0);
-      tma_load_3d(sm + OFF_QK + 24576, &p.tm_q, &s->bar[B_QK_FULL], 64, info.kh, t0);
-      tma_prefetch_3d(&p.tm_g, 0, info.h, t0);
-      if (lc + 1 < info.nchunks) {
-        tma_prefetch_3d(&p.tm_k, 0, info.kh, t0 + kC);
-        tma_prefetch_3d(&p.tm_k, 64, info.kh, t0 + kC);
-        tma_prefetch_3d(&p.tm_q, 0, info.kh, t0 + kC);
-        tma_prefetch_3d(&p.tm_q, 64, info.kh, t0 + kC);
-        tma_prefetch_3d(&p.tm_g, 0, info.h, t0 + kC);
-      }
-      if (gc > 0 && !wait_bar(p, s, B_VB_FREE, (gc - 1) & 1)) { stop = true; break; }
-      mbar_expect_tx(&s->bar[B_V_FULL], 16384);
-      ++n_v;
-      tma_load_3d(sm + OFF_VB + 0, &p.tm_v, &s->bar[B_V_FULL], 0, info.h, t0);
-      tma_load_3d(sm + OFF_VB + 8192, &p.tm_v, &s->bar[B_V_FULL], 64, info.h, t0);
-      if (lc + 1 < info.nchunks) {
-        tma_prefetch_3d(&p.tm_v, 0, info.h, t0 + kC);
-        tma_prefetch_3d(&p.tm_v, 64, info.h, t0 + kC);
-      }
-    }
-    if (stop) break;
+    info.n = n; info.h = h; info.kh = h / (p.Hv / p.Hk);
+    info.bos = bos; info.eos = eos; info.slot = sl;
+    info.nchunks = (int)((eos - bos + kC - 1) / kC);
+    info.done = 0;
+    return info;
   }
-  // Let the last loads land before the CTA can exit (bounded, ignores abort).
-  if (n_qk > 0) mbar_wait(&s->bar[B_QK_FULL], (n_qk - 1) & 1);
-  if (n_v > 0) mbar_wait(&s->bar[B_V_FULL], (n_v - 1) & 1);
 }
 
-// Reads the next item descriptor (whole group); returns it.  The group leader
-// releases the ring slot once every thread of the group has read it.
+// Reads ring entry k (whole group) and releases it; `done` is uniform.
 __device__ __forceinline__ ItemInfo next_item(const TcParams& p, Small* s, int k, bool leader,
-                                              uint32_t bar_id, bool& ok) {
+                                              uint32_t bar_id, uint32_t nthreads) {
   const int slot = k % kRing;
-  ok = wait_bar(p, s, B_ITEM_FULL + slot, (k / kRing) & 1);
+  const bool ok = wait_bar(p, s, B_ITEM_FULL + slot, (k / kRing) & 1);
   ItemInfo info = s->ring[slot];
-  const bool stop = named_bar_any(bar_id, 128, !ok || info.done != 0 || aborted(s));
+  const bool stop = named_bar_any(bar_id, nthreads, !ok || info.done != 0 || aborted(s));
   if (leader && ok) mbar_arrive(&s->bar[B_ITEM_EMPTY + slot]);
   info.done = stop ? 1 : 0;
   return info;
 }
 
+// ---- warp-level 16x16x16 products on the legacy tensor path (tf32) ------------------
+// acc[nt] (16 x 8 tile nt of a 16x16 result) += M1[r1.., c1..] * M2[r2.., c2..]
+__device__ __forceinline__ void blk_mma(float acc[2][4], const float* M1, int r1, int c1,
+                                        const float* M2, int r2, int c2, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    uint32_t a[4];
+    a[0] = to_tf32(M1[sidx(r1 + g, c1 + 8 * ks + t)]);
+    a[1] = to_tf32(M1[sidx(r1 + g + 8, c1 + 8 * ks + t)]);
+    a[2] = to_tf32(M1[sidx(r1 + g, c1 + 8 * ks + t + 4)]);
+    a[3] = to_tf32(M1[sidx(r1 + g + 8, c1 + 8 * ks + t + 4)]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      uint32_t b[2];
+      b[0] = to_tf32(M2[sidx(r2 + 8 * ks + t, c2 + 8 * nt + g)]);
+      b[1] = to_tf32(M2[sidx(r2 + 8 * ks + t + 4, c2 + 8 * nt + g)]);
+      mma_tf32_16x8x8(acc[nt], a, b);
+    }
+  }
+}
+__device__ __forceinline__ void blk_store(float* M, int r, int c, const float acc[2][4], float sgn,
+                                          int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    M[sidx(r + g, c + 8 * nt + 2 * t)] = sgn * acc[nt][0];
+    M[sidx(r + g, c + 8 * nt + 2 * t + 1)] = sgn * acc[nt][1];
+    M[sidx(r + g + 8, c + 8 * nt + 2 * t)] = sgn * acc[nt][2];
+    M[sidx(r + g + 8, c + 8 * nt + 2 * t + 1)] = sgn * acc[nt][3];
+  }
+}
+
 // ======================================================================================
-// Intra group (warps 1-4): S-independent work of each chunk.
+// Intra group (warps 0-7, 256 threads): S-independent work of each chunk.  Its
+// thread 0 also schedules items and issues every TMA load, at points where the
+// group already knows the target buffer is free.
 // ======================================================================================
+struct Loader {  // state of thread 0 only
+  ItemInfo lq[kRing];
+  int pushed = 0;
+  bool fetched_done = false;
+  uint32_t n_qk = 0, n_g = 0, n_v = 0;  // chunks whose loads were issued
+
+  __device__ void push_one(const TcParams& p, Small* s) {
+    if (fetched_done) return;
+    const int slot = pushed % kRing;
+    if (pushed >= kRing) wait_bar(p, s, B_ITEM_EMPTY + slot, ((pushed / kRing) - 1) & 1);
+    const ItemInfo info = fetch_item(p, s);
+    s->ring[slot] = info;
+    lq[slot] = info;
+    mbar_arrive(&s->bar[B_ITEM_FULL + slot]);
+    ++pushed;
+    if (info.done) fetched_done = true;
+  }
+  __device__ void load_qk(const TcParams& p, uint8_t* sm, Small* s, int kh, int t0) {
+    mbar_expect_tx(&s->bar[B_QK_FULL], 32768);
+    tma_load_3d(sm + OFF_QK + 0, &p.tm_k, &s->bar[B_QK_FULL], 0, kh, t0);
+    tma_load_3d(sm + OFF_QK + 16384, &p.tm_k, &s->bar[B_QK_FULL], 64, kh, t0);
+    tma_load_3d(sm + OFF_QK + 8192, &p.tm_q, &s->bar[B_QK_FULL], 0, kh, t0);
+    tma_load_3d(sm + OFF_QK + 24576, &p.tm_q, &s->bar[B_QK_FULL], 64, kh, t0);
+    ++n_qk;
+  }
+  __device__ void load_g(const TcParams& p, uint8_t* sm, Small* s, int h, int t0) {
+    mbar_expect_tx(&s->bar[B_G_FULL], 32768);
+    tma_load_3d(sm + OFF_G, &p.tm_g, &s->bar[B_G_FULL], 0, h, t0);
+    ++n_g;
+  }
+  __device__ void load_v(const TcParams& p, uint8_t* sm, Small* s, int h, int t0) {
+    mbar_expect_tx(&s->bar[B_V_FULL], 16384);
+    tma_load_3d(sm + OFF_VB + 0, &p.tm_v, &s->bar[B_V_FULL], 0, h, t0);
+    tma_load_3d(sm + OFF_VB + 8192, &p.tm_v, &s->bar[B_V_FULL], 64, h, t0);
+    ++n_v;
+  }
+  // Chunk after (item k, local chunk lc), if already known without blocking.
+  __device__ bool next_chunk(int k, int lc, int& kh, int& h, int& t0) const {
+    const ItemInfo& cur = lq[k % kRing];
+    if (lc + 1 < cur.nchunks) {
+      kh = cur.kh; h = cur.h; t0 = (int)(cur.bos + (int64_t)(lc + 1) * kC);
+      return true;
+    }
+    if (pushed > k + 1) {
+      const ItemInfo& nx = lq[(k + 1) % kRing];
+      if (!nx.done && nx.nchunks > 0) {
+        kh = nx.kh; h = nx.h; t0 = (int)nx.bos;
+        return true;
+      }
+    }
+    return false;
+  }
+  __device__ void prefetch_l2(const TcParams& p, int kh, int h, int t0) {
+    tma_prefetch_3d(&p.tm_k, 0, kh, t0);
+    tma_prefetch_3d(&p.tm_k, 64, kh, t0);
+    tma_prefetch_3d(&p.tm_q, 0, kh, t0);
+    tma_prefetch_3d(&p.tm_q, 64, kh, t0);
+    tma_prefetch_3d(&p.tm_g, 0, h, t0);
+    tma_prefetch_3d(&p.tm_v, 0, h, t0);
+    tma_prefetch_3d(&p.tm_v, 64, h, t0);
+  }
+};
+
 __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tbase) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int quad = warp & 3;
-  const int tl = quad * 32 + lane;  // TMEM lane of this thread / channel of the prologue
-  const int it = threadIdx.x - 32;  // 0..127 within the group
-  const bool leader_warp = (warp == 1);
+  const int t = threadIdx.x;  // 0..255
+  const int warp = t >> 5, lane = t & 31;
+  const int quad = warp & 3, hx = warp >> 2;
+  const int L = quad * 32 + lane;  // TMEM lane of this thread
   const uint32_t taddr_q = tbase + ((uint32_t)(quad * 32) << 16);
   const uint32_t sbase = smem_u32(sm);
   float* As = reinterpret_cast<float*>(sm + OFF_AS);
   float* Xs = reinterpret_cast<float*>(sm + OFF_XS);
+  const float* Gs = reinterpret_cast<const float*>(sm + OFF_G);
+  Loader ld;
   uint32_t gc = 0;
 
   for (int k = 0;; ++k) {
-    bool ok;
-    const ItemInfo info = next_item(p, s, k, it == 0, 1, ok);
+    if (t == 0) {
+      while (ld.pushed <= k + 1 && !ld.fetched_done) ld.push_one(p, s);
+    }
+    __syncwarp();
+    const ItemInfo info = next_item(p, s, k, t == 0, BAR_IG, kIG);
     if (info.done) break;
     const int h = info.h, kh = info.kh;
     bool stop = false;
     for (int lc = 0; lc < info.nchunks; ++lc, ++gc) {
-      if (named_bar_any(1, 128, aborted(s))) { stop = true; break; }
+      if (named_bar_any(BAR_IG, kIG, aborted(s))) { stop = true; break; }
       const int64_t t0 = info.bos + (int64_t)lc * kC;
       const int cv = (int)min((int64_t)kC, info.eos - t0);
+      int nkh = 0, nh = 0, nt0 = 0;
+      bool have_next = false;
+      if (t == 0) {
+        if (ld.n_qk == gc) ld.load_qk(p, sm, s, kh, (int)t0);
+        if (ld.n_g == gc) ld.load_g(p, sm, s, h, (int)t0);
+        if (ld.n_v == gc) ld.load_v(p, sm, s, h, (int)t0);
+        have_next = ld.next_chunk(k, lc, nkh, nh, nt0);
+        if (have_next) ld.prefetch_l2(p, nkh, nh, nt0);
+      }
+      __syncwarp();
       // ------------------------------------------------------------- prologue
-      const int ch = tl;
-      float e[kC];
-      {
-        const float* gp = p.g + ((size_t)t0 * p.Hv + h) * kK + ch;
+      // thread = (channel ch, token half): tokens 32*half .. 32*half+31
+      const int ch = t >> 1, half = t & 1;
+      wait_bar(p, s, B_G_FULL, gc & 1);
+      float e[32];
 #pragma unroll
-        for (int r = 0; r < kC; ++r) e[r] = (r < cv) ? gp[(size_t)r * p.Hv * kK] : 0.f;
-#pragma unroll
-        for (int r = 0; r < kC; ++r) e[r] = __expf(e[r]);  // g = 0 on padded rows -> 1
+      for (int j = 0; j < 32; ++j) {
+        const int r = half * 32 + j;
+        e[j] = (r < cv) ? __expf(Gs[r * kK + ch]) : 1.f;
       }
-      if (tl < kC) s->beta[tl] = (tl < cv) ? p.beta[(size_t)(t0 + tl) * p.Hv + h] : 0.f;
+      if (t < kC) s->beta[t] = (t < cv) ? p.beta[(size_t)(t0 + t) * p.Hv + h] : 0.f;
+      float pa = 1.f, pb = 1.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) { pa *= e[j]; pb *= e[16 + j]; }
+      const float oa = __shfl_xor_sync(0xffffffffu, pa, 1), ob = __shfl_xor_sync(0xffffffffu, pb, 1);
       float pi[4];
-#pragma unroll
-      for (int sc = 0; sc < 4; ++sc) {
-        float a = 1.f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) a *= e[sc * 16 + j];
-        pi[sc] = a;
-      }
-      const float E1v = pi[0], E2v = pi[0] * pi[1], E3v = pi[0] * pi[1] * pi[2];
-      const float Es[4] = {1.f, E1v, E2v, E3v};
+      pi[0] = half ? oa : pa;
+      pi[1] = half ? ob : pb;
+      pi[2] = half ? pa : oa;
+      pi[3] = half ? pb : ob;
+      const float Es[4] = {1.f, pi[0], pi[0] * pi[1], pi[0] * pi[1] * pi[2]};
       const float Fs[4] = {pi[1] * pi[2] * pi[3], pi[2] * pi[3], pi[3], 1.f};
-      bool safe[4];
+      const float gam = Es[3] * pi[3];
 #pragma unroll
       for (int sc = 0; sc < 4; ++sc) {
-        safe[sc] = pi[sc] >= kSafeMin;
-        const uint32_t m = __ballot_sync(0xffffffffu, !safe[sc]);
-        if (lane == 0) s->unsafe[sc][quad] = m;
+        const uint32_t m = __ballot_sync(0xffffffffu, !(pi[sc] >= kSafeMin));
+        uint32_t comp = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) comp |= ((m >> (2 * j)) & 1u) << j;
+        if (lane == 0) s->unsafe[sc][warp] = (uint16_t)comp;
       }
       wait_bar(p, s, B_QK_FULL, gc & 1);
       // QG buffer and this gamma buffer are free once MMA-1b of the previous chunk ran
       if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
-      s->gamma[gc & 1][ch] = E3v * pi[3];
+      if (half == 0) s->gamma[gc & 1][ch] = gam;
+      named_bar(BAR_IG, kIG);  // every thread has read g: CB blocks 1-2 may be overwritten
 #pragma unroll
-      for (int sc = 0; sc < 4; ++sc) {
+      for (int u2 = 0; u2 < 2; ++u2) {
+        const int sc = half * 2 + u2;  // sub-chunk
         float kap[16];
         {
           float a = 1.f;
 #pragma unroll
-          for (int j = 15; j >= 0; --j) { kap[j] = a; a *= e[sc * 16 + j]; }
+          for (int j = 15; j >= 0; --j) { kap[j] = a; a *= e[u2 * 16 + j]; }
         }
-        const float inv_pi = safe[sc] ? 1.f / pi[sc] : 0.f;
-        uint32_t w_cb0[8], w_dg[8], w_kg[8], w_qg[8], w_m1[8], w_m12[8], w_m2[8];
+        const bool safe = pi[sc] >= kSafeMin;
+        const float inv_pi = safe ? 1.f / pi[sc] : 0.f;
+        const float kgs = Es[sc], qgs = p.scale * Es[sc];
         float rho = 1.f;
-        const float qscale = p.scale * Es[sc];
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          float kk[2], dg[2], kg[2], qg[2], m1[2], m12[2], m2[2];
+        for (int jh = 0; jh < 2; ++jh) {
+          float kv[8], qv[8];
+          uint16_t* kp[8];
+          uint16_t* qp[8];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int r = sc * 16 + j + u;
-            rho *= e[r];
-            const uint32_t ka = kmaj_elem(r, ch, 128), qa = kmaj_elem(64 + r, ch, 128);
-            uint16_t* kp = reinterpret_cast<uint16_t*>(sm + OFF_QK + ka);
-            uint16_t* qp = reinterpret_cast<uint16_t*>(sm + OFF_QK + qa);
-            const float kv = (r < cv) ? bf_bits(*kp) : 0.f;
-            const float qv = (r < cv) ? bf_bits(*qp) : 0.f;
-            *kp = to_bf_bits(kv * rho);
-            *qp = to_bf_bits(qv * rho);
-            kk[u] = kv * kap[j + u];
-            dg[u] = kk[u] * inv_pi;
-            kg[u] = kv * rho * Es[sc];
-            qg[u] = qv * rho * qscale;
-            m1[u] = kk[u] * pi[1];
-            m12[u] = kk[u] * pi[1] * pi[2];
-            m2[u] = kk[u] * pi[2];
+          for (int u = 0; u < 8; ++u) {
+            const int r = sc * 16 + jh * 8 + u;
+            kp[u] = reinterpret_cast<uint16_t*>(sm + OFF_QK + kmaj_elem(r, ch, 128));
+            qp[u] = reinterpret_cast<uint16_t*>(sm + OFF_QK + kmaj_elem(64 + r, ch, 128));
+            kv[u] = (r < cv) ? bf_bits(*kp[u]) : 0.f;
+            qv[u] = (r < cv) ? bf_bits(*qp[u]) : 0.f;
           }
-          w_cb0[j / 2] = pack_bf16x2(kk[0], kk[1]);
-          w_dg[j / 2] = pack_bf16x2(dg[0], dg[1]);
-          w_kg[j / 2] = pack_bf16x2(kg[0], kg[1]);
-          w_qg[j / 2] = pack_bf16x2(qg[0], qg[1]);
-          w_m1[j / 2] = pack_bf16x2(m1[0], m1[1]);
-          w_m12[j / 2] = pack_bf16x2(m12[0], m12[1]);
-          w_m2[j / 2] = pack_bf16x2(m2[0], m2[1]);
-        }
+          uint32_t w_cb0[4], w_dg[4], w_kg[4], w_qg[4], w_m1[4], w_m12[4], w_m2[4];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t cj = sc * 2 + hh, o = hh * 4;
-          st_chunk(sm, OFF_CB + 0 + sw128_off(ch, cj), w_cb0[o], w_cb0[o + 1], w_cb0[o + 2], w_cb0[o + 3]);
-          st_chunk(sm, OFF_CB + 32768 + sw128_off(ch, cj), w_dg[o], w_dg[o + 1], w_dg[o + 2], w_dg[o + 3]);
-          st_chunk(sm, OFF_KG + sw128_off(ch, cj), w_kg[o], w_kg[o + 1], w_kg[o + 2], w_kg[o + 3]);
-          st_chunk(sm, OFF_QG + sw128_off(ch, cj), w_qg[o], w_qg[o + 1], w_qg[o + 2], w_qg[o + 3]);
+          for (int u = 0; u < 8; u += 2) {
+            float kk[2], dg[2], kg[2], qg[2], m1[2], m12[2], m2[2];
+#pragma unroll
+            for (int v2 = 0; v2 < 2; ++v2) {
+              const int j = jh * 8 + u + v2;
+              rho *= e[u2 * 16 + j];
+              const float kr = kv[u + v2] * rho, qr = qv[u + v2] * rho;
+              *kp[u + v2] = to_bf_bits(kr);
+              *qp[u + v2] = to_bf_bits(qr);
+              kk[v2] = kv[u + v2] * kap[j];
+              dg[v2] = kk[v2] * inv_pi;
+              kg[v2] = kr * kgs;
+              qg[v2] = qr * qgs;
+              m1[v2] = kk[v2] * pi[1];
+              m12[v2] = m1[v2] * pi[2];
+              m2[v2] = kk[v2] * pi[2];
+            }
+            w_cb0[u / 2] = pack_bf16x2(kk[0], kk[1]);
+            w_dg[u / 2] = pack_bf16x2(dg[0], dg[1]);
+            w_kg[u / 2] = pack_bf16x2(kg[0], kg[1]);
+            w_qg[u / 2] = pack_bf16x2(qg[0], qg[1]);
+            w_m1[u / 2] = pack_bf16x2(m1[0], m1[1]);
+            w_m12[u / 2] = pack_bf16x2(m12[0], m12[1]);
+            w_m2[u / 2] = pack_bf16x2(m2[0], m2[1]);
+          }
+          const uint32_t cj = sc * 2 + jh;
+          st_chunk(sm, OFF_CB + sw128_off(ch, cj), w_cb0[0], w_cb0[1], w_cb0[2], w_cb0[3]);
+          st_chunk(sm, OFF_CB + 32768 + sw128_off(ch, cj), w_dg[0], w_dg[1], w_dg[2], w_dg[3]);
+          st_chunk(sm, OFF_KG + sw128_off(ch, cj), w_kg[0], w_kg[1], w_kg[2], w_kg[3]);
+          st_chunk(sm, OFF_QG + sw128_off(ch, cj), w_qg[0], w_qg[1], w_qg[2], w_qg[3]);
           if (sc == 0) {
-            st_chunk(sm, OFF_CB + 16384 + sw128_off(ch, 0 + hh), w_m1[o], w_m1[o + 1], w_m1[o + 2], w_m1[o + 3]);
-            st_chunk(sm, OFF_CB + 16384 + sw128_off(ch, 2 + hh), w_m12[o], w_m12[o + 1], w_m12[o + 2], w_m12[o + 3]);
+            st_chunk(sm, OFF_CB + 16384 + sw128_off(ch, 0 + jh), w_m1[0], w_m1[1], w_m1[2], w_m1[3]);
+            st_chunk(sm, OFF_CB + 16384 + sw128_off(ch, 2 + jh), w_m12[0], w_m12[1], w_m12[2], w_m12[3]);
           } else if (sc == 1) {
-            st_chunk(sm, OFF_CB + 16384 + sw128_off(ch, 4 + hh), w_m2[o], w_m2[o + 1], w_m2[o + 2], w_m2[o + 3]);
+            st_chunk(sm, OFF_CB + 16384 + sw128_off(ch, 4 + jh), w_m2[0], w_m2[1], w_m2[2], w_m2[3]);
           } else if (sc == 3) {
-            st_chunk(sm, OFF_CB + 16384 + sw128_off(ch, 6 + hh), 0u, 0u, 0u, 0u);
+            st_chunk(sm, OFF_CB + 16384 + sw128_off(ch, 6 + jh), 0u, 0u, 0u, 0u);
           }
         }
       }
       fence_async_smem();
-      named_bar(1, 128);
-      if (it == 0) mbar_arrive(&s->bar[B_GAMMA0 + (gc & 1)]);
-      if (leader_warp) {
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t idesc = idesc_bf16(128, 192, 0, 1);
+      named_bar(BAR_IG, kIG);
+      if (t == 0) {
+        mbar_arrive(&s->bar[B_GAMMA0 + (gc & 1)]);
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16(128, 192, 0, 1);
 #pragma unroll
-          for (int st = 0; st < 8; ++st) {
-            const uint64_t a = sdesc_sw128(sbase + OFF_QK + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
-            const uint64_t b = sdesc_sw128(sbase + OFF_CB + st * 2048, 16384, 1024);
-            mma_bf16(tbase + TM_AB, a, b, idesc, st > 0 ? 1u : 0u);
-          }
-          mma_commit(&s->bar[B_AB_DONE]);
-          mma_commit(&s->bar[B_QK_FREE]);
+        for (int st = 0; st < 8; ++st) {
+          const uint64_t a = sdesc_sw128(sbase + OFF_QK + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(sbase + OFF_CB + st * 2048, 16384, 1024);
+          mma_bf16(tbase + TM_AB, a, b, idesc, st > 0 ? 1u : 0u);
         }
-        __syncwarp();
+        mma_commit(&s->bar[B_AB_DONE]);
       }
+      __syncwarp();
       // ------------------------------------------------------------- A / B rows
       wait_bar(p, s, B_AB_DONE, gc & 1);
       tc_fence_after();
+      if (t == 0 && have_next && ld.n_qk == gc + 1) ld.load_qk(p, sm, s, nkh, nt0);  // QK free
+      __syncwarp();
       {
-        const int L = tl, r = L & 63, a = r >> 4;
+        const int r = L & 63, a = r >> 4;
         const bool isB = L >= 64;
-        const int a0 = (r >> 5) * 2;  // the two sub-chunks of this warp: a0, a0 + 1
-        float x[kC];
+        const int a0 = (L & 32) ? 2 : 0;  // sub-chunks a0, a0+1 live in this warp
+        float x[32];
 #pragma unroll
-        for (int i = 0; i < kC; ++i) x[i] = 0.f;
-        // column of TMEM (relative to TM_AB) holding block (row sub-chunk aa, column block b)
-        auto colof = [](int aa, int b) -> int {
-          if (b == aa) return 128 + 16 * aa;
-          if (b == aa - 1) return 16 * b;
-          if (b == aa - 2) return aa == 2 ? 64 : 96;
-          if (b == aa - 3) return 80;
-          return -1;
-        };
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          float v0[16], v1[16];
+        for (int bb = 0; bb < 2; ++bb) {
+          const int b = hx * 2 + bb;
+          auto colof = [](int aa, int b_) -> int {
+            if (b_ == aa) return 128 + 16 * aa;
+            if (b_ == aa - 1) return 16 * b_;
+            if (b_ == aa - 2) return aa == 2 ? 64 : 96;
+            if (b_ == aa - 3) return 80;
+            return -1;
+          };
           const int c0 = (b <= a0) ? colof(a0, b) : -1;
           const int c1 = (b <= a0 + 1) ? colof(a0 + 1, b) : -1;
+          float v0[16], v1[16];
           if (c0 >= 0) tmem_ld16(taddr_q + TM_AB + c0, v0);
           if (c1 >= 0) tmem_ld16(taddr_q + TM_AB + c1, v1);
           tmem_ld_wait();
@@ -398,29 +485,29 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             float val = 0.f;
             if (a == a0 && c0 >= 0) val = v0[j];
             if (a == a0 + 1 && c1 >= 0) val = v1[j];
-            x[16 * b + j] = val;
+            x[bb * 16 + j] = val;
           }
         }
         tc_fence_before();
-        float* row = (isB ? Xs : As);
+        float* row = isB ? Xs : As;
 #pragma unroll
-        for (int i = 0; i < kC; ++i) row[sidx(r, i)] = x[i];
+        for (int j = 0; j < 32; ++j) row[sidx(r, hx * 32 + j)] = x[j];
       }
-      named_bar(1, 128);
+      named_bar(BAR_IG, kIG);
       // exact pairwise terms of the diagonal sub-chunk blocks on "unsafe" channels
-      {
-        const int L = tl, r = L & 63, a = r >> 4;
+      if (hx == 0) {
+        const int r = L & 63, a = r >> 4;
         const bool isB = L >= 64;
         uint32_t any = 0;
 #pragma unroll
-        for (int wd = 0; wd < 4; ++wd) any |= s->unsafe[a][wd];
+        for (int wd = 0; wd < 8; ++wd) any |= s->unsafe[a][wd];
         if (any != 0u && r < cv) {
-          float* row = (isB ? Xs : As);
+          float* row = isB ? Xs : As;
           const __nv_bfloat16* xsrc = isB ? p.q : p.k;
-          for (int wd = 0; wd < 4; ++wd) {
+          for (int wd = 0; wd < 8; ++wd) {
             uint32_t m = s->unsafe[a][wd];
             while (m) {
-              const int c = wd * 32 + (__ffs(m) - 1);
+              const int c = wd * 16 + (__ffs(m) - 1);
               m &= m - 1;
               const float xr = __bfloat162float(xsrc[((size_t)(t0 + r) * p.Hk + kh) * kK + c]);
               float pr = 1.f;
@@ -434,38 +521,40 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           }
         }
       }
-      named_bar(1, 128);
-      // A: mask + beta_r (in place); B: mask + scale -> bf16 -> BB
+      named_bar(BAR_IG, kIG);
+      // A: mask + beta_r (in place, fp32); B: mask + scale -> bf16 -> BB
       {
-        const int L = tl, r = L & 63;
+        const int r = L & 63;
         if (L < 64) {
           const float br = s->beta[r];
 #pragma unroll
-          for (int i = 0; i < kC; ++i) {
+          for (int j = 0; j < 32; ++j) {
+            const int i = hx * 32 + j;
             const float v = As[sidx(r, i)];
             As[sidx(r, i)] = (i < r) ? br * v : 0.f;
           }
         } else {
           if (gc > 0) wait_bar(p, s, B_M3A, (gc - 1) & 1);  // BB free
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int jc = 0; jc < 4; ++jc) {
             uint32_t w[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const int i0 = j * 8 + u * 2;
+              const int i0 = hx * 32 + jc * 8 + u * 2;
               const float v0 = (i0 <= r) ? p.scale * Xs[sidx(r, i0)] : 0.f;
               const float v1 = (i0 + 1 <= r) ? p.scale * Xs[sidx(r, i0 + 1)] : 0.f;
               w[u] = pack_bf16x2(v0, v1);
             }
-            st_chunk(sm, OFF_BB + sw128_off(r, j), w[0], w[1], w[2], w[3]);
+            st_chunk(sm, OFF_BB + sw128_off(r, hx * 4 + jc), w[0], w[1], w[2], w[3]);
           }
         }
       }
-      named_bar(1, 128);
+      named_bar(BAR_IG, kIG);
       // ------------------------------------------------------------- inverse
-      // (1) 16x16 diagonal blocks by forward substitution: thread (blk, col j)
-      if (it < 64) {
-        const int blk = it >> 4, j = it & 15, o = blk * 16;
+      // X = (I + A)^-1 by 16x16 blocks: diagonal blocks by forward substitution,
+      // then X_ab = -X_aa * sum_{b<=c<a} A_ac X_cb, one block per warp per level.
+      if (warp < 4) {
+        const int o = warp * 16, j = lane & 15;
         float xv[16];
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) xv[rr] = (rr == j) ? 1.f : 0.f;
@@ -476,103 +565,97 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           for (int i = 0; i < rr; ++i) acc = fmaf(As[sidx(o + rr, o + i)], xv[i], acc);
           if (rr > j) xv[rr] = -acc;
         }
+        if (lane < 16) {
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) Xs[sidx(o + rr, o + j)] = xv[rr];
+          for (int rr = 0; rr < 16; ++rr) Xs[sidx(o + rr, o + j)] = xv[rr];
+        }
       } else {
-        // zero the blocks of X above the diagonal blocks' rows that merges do not write
-        const int t2 = it - 64;  // 0..63: clear row t2's strictly-upper 16-blocks
-        const int rb = t2 >> 4;
+        // zero the strictly-upper 16-blocks of X (6 blocks x 256 entries)
+        const int t2 = t - 128;
 #pragma unroll
-        for (int i = 0; i < kC; ++i)
-          if ((i >> 4) > rb) Xs[sidx(t2, i)] = 0.f;
-      }
-      named_bar(1, 128);
-      // (2) level-1 merges: X_{2m+1,2m} = -X_{2m+1,2m+1} (A_{2m+1,2m} X_{2m,2m})
-      {
-        const int m = it >> 6, e2 = it & 63, rr = e2 >> 2, j0 = (e2 & 3) * 4;
-        const int ro = (2 * m + 1) * 16, co = 2 * m * 16;
-        float t[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float av = As[sidx(ro + rr, co + i)];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) t[u] = fmaf(av, Xs[sidx(co + i, co + j0 + u)], t[u]);
+        for (int q2 = 0; q2 < 12; ++q2) {
+          const int e2 = t2 * 12 + q2;  // 0..1535
+          const int blk = e2 >> 8, w2 = e2 & 255;
+          const int ba = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+          const int bbk = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+          Xs[sidx(ba * 16 + (w2 >> 4), bbk * 16 + (w2 & 15))] = 0.f;
         }
-        // temp T in A's unused upper block (rows co..co+15, cols ro..ro+15)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) As[sidx(co + rr, ro + j0 + u)] = t[u];
       }
-      named_bar(1, 128);
-      {
-        const int m = it >> 6, e2 = it & 63, rr = e2 >> 2, j0 = (e2 & 3) * 4;
-        const int ro = (2 * m + 1) * 16, co = 2 * m * 16;
-        float t[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float xv = Xs[sidx(ro + rr, ro + i)];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) t[u] = fmaf(xv, As[sidx(co + i, ro + j0 + u)], t[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) Xs[sidx(ro + rr, co + j0 + u)] = -t[u];
+      named_bar(BAR_IG, kIG);
+      if (warp < 3) {  // X_{a+1,a}
+        const int a = warp;
+        float acc[2][4] = {};
+        blk_mma(acc, As, (a + 1) * 16, a * 16, Xs, a * 16, a * 16, lane);
+        blk_store(As, 0, 16 * (1 + warp), acc, 1.f, lane);  // stage P in A's upper block (0, 1+w)
+        __syncwarp();
+        float acc2[2][4] = {};
+        blk_mma(acc2, Xs, (a + 1) * 16, (a + 1) * 16, As, 0, 16 * (1 + warp), lane);
+        blk_store(Xs, (a + 1) * 16, a * 16, acc2, -1.f, lane);
       }
-      named_bar(1, 128);
-      // (3) level-2 merge: X_21 = -X_22 (A_21 X_11), 32x32 blocks
-      {
-        const int rr = it >> 2, j0 = (it & 3) * 8;
-        float t[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) t[u] = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < 32; ++i) {
-          const float av = As[sidx(32 + rr, i)];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) t[u] = fmaf(av, Xs[sidx(i, j0 + u)], t[u]);
-        }
-        // temp T2 in A's unused upper-right quadrant (rows 0..31, cols 32..63)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) As[sidx(rr, 32 + j0 + u)] = t[u];
+      named_bar(BAR_IG, kIG);
+      if (warp < 2) {  // X_{a+2,a}
+        const int a = warp;
+        float acc[2][4] = {};
+        blk_mma(acc, As, (a + 2) * 16, a * 16, Xs, a * 16, a * 16, lane);
+        blk_mma(acc, As, (a + 2) * 16, (a + 1) * 16, Xs, (a + 1) * 16, a * 16, lane);
+        blk_store(As, 16, 32 + 16 * warp, acc, 1.f, lane);  // stage in (1, 2+w)
+        __syncwarp();
+        float acc2[2][4] = {};
+        blk_mma(acc2, Xs, (a + 2) * 16, (a + 2) * 16, As, 16, 32 + 16 * warp, lane);
+        blk_store(Xs, (a + 2) * 16, a * 16, acc2, -1.f, lane);
       }
-      named_bar(1, 128);
-      {
-        const int rr = it >> 2, j0 = (it & 3) * 8;
-        float t[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) t[u] = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < 32; ++i) {
-          const float xv = Xs[sidx(32 + rr, 32 + i)];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) t[u] = fmaf(xv, As[sidx(i, 32 + j0 + u)], t[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) Xs[sidx(32 + rr, j0 + u)] = -t[u];
+      named_bar(BAR_IG, kIG);
+      if (warp == 0) {  // X_{3,0}
+        float acc[2][4] = {};
+        blk_mma(acc, As, 48, 0, Xs, 0, 0, lane);
+        blk_mma(acc, As, 48, 16, Xs, 16, 0, lane);
+        blk_mma(acc, As, 48, 32, Xs, 32, 0, lane);
+        blk_store(As, 32, 48, acc, 1.f, lane);  // stage in (2, 3)
+        __syncwarp();
+        float acc2[2][4] = {};
+        blk_mma(acc2, Xs, 48, 48, As, 32, 48, lane);
+        blk_store(Xs, 48, 0, acc2, -1.f, lane);
       }
-      named_bar(1, 128);
-      // Tm = X Diag(beta) -> bf16 -> TM (row r, half hh)
+      named_bar(BAR_IG, kIG);
+      // Tm = X Diag(beta) -> bf16 -> TM   (thread: row r, columns 16*qq..)
       {
-        const int rr = it >> 1, hh = it & 1;
+        const int r = t >> 2, qq = t & 3;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = hh * 4 + jj;
+        for (int u2 = 0; u2 < 2; ++u2) {
+          const int j = qq * 2 + u2;
           uint32_t w[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int i0 = j * 8 + u * 2;
-            const float v0 = (i0 <= rr) ? Xs[sidx(rr, i0)] * s->beta[i0] : 0.f;
-            const float v1 = (i0 + 1 <= rr) ? Xs[sidx(rr, i0 + 1)] * s->beta[i0 + 1] : 0.f;
+            const float v0 = (i0 <= r) ? Xs[sidx(r, i0)] * s->beta[i0] : 0.f;
+            const float v1 = (i0 + 1 <= r) ? Xs[sidx(r, i0 + 1)] * s->beta[i0 + 1] : 0.f;
             w[u] = pack_bf16x2(v0, v1);
           }
-          st_chunk(sm, OFF_TM + sw128_off(rr, j), w[0], w[1], w[2], w[3]);
+          st_chunk(sm, OFF_TM + sw128_off(r, j), w[0], w[1], w[2], w[3]);
         }
       }
+      // KR = (k kap) F_s : scaled copy of CB block 0 row `ch` into KR (this half's tokens)
+      if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = half * 4 + jj;
+        const uint4 src = *reinterpret_cast<const uint4*>(sm + OFF_CB + sw128_off(ch, j));
+        const float f = Fs[j >> 1];
+        const uint32_t in[4] = {src.x, src.y, src.z, src.w};
+        uint32_t w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          w[u] = pack_bf16x2(bf_bits(in[u] & 0xFFFFu) * f, bf_bits(in[u] >> 16) * f);
+        st_chunk(sm, OFF_KR + sw128_off(ch, j), w[0], w[1], w[2], w[3]);
+      }
       fence_async_smem();
-      named_bar(1, 128);
+      named_bar(BAR_IG, kIG);
       // ------------------------------------------------------------- U~ and W
-      if (leader_warp) {
-        bool okw = wait_bar(p, s, B_V_FULL, gc & 1);
-        if (okw && gc > 0) okw = wait_bar(p, s, B_E1, (gc - 1) & 1);  // U region read
-        if (okw && lane == 0) {
+      if (t == 0 && have_next && ld.n_g == gc + 1) ld.load_g(p, sm, s, nh, nt0);  // AS/XS dead
+      if (warp == 0) {
+        wait_bar(p, s, B_V_FULL, gc & 1);
+        if (gc > 0) wait_bar(p, s, B_E1, (gc - 1) & 1);  // U region read by the recurrence
+        if (lane == 0) {
           tc_fence_after();
           const uint32_t idu = idesc_bf16(128, 64, 1, 0), idw = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
@@ -584,64 +667,59 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
                      st > 0 ? 1u : 0u);
           }
           mma_commit(&s->bar[B_UW_DONE]);
-          mma_commit(&s->bar[B_VB_FREE]);
         }
         __syncwarp();
       }
       wait_bar(p, s, B_UW_DONE, gc & 1);
       tc_fence_after();
-      // -W^T rows -> WB (row = channel tl)
+      if (t == 0 && have_next && ld.n_v == gc + 1) ld.load_v(p, sm, s, nh, nt0);  // VB free
+      __syncwarp();
+      // -W^T rows -> WB (row = channel L, tokens 32*hx ..)
       if (gc > 0) wait_bar(p, s, B_M1A, (gc - 1) & 1);
 #pragma unroll
-      for (int cq = 0; cq < 4; ++cq) {
+      for (int cq = 0; cq < 2; ++cq) {
         float wv[16];
-        tmem_ld16(taddr_q + TM_AB + cq * 16, wv);
+        tmem_ld16(taddr_q + TM_AB + hx * 32 + cq * 16, wv);
         tmem_ld_wait();
         uint32_t w[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(-wv[2 * u], -wv[2 * u + 1]);
-        st_chunk(sm, OFF_WB + sw128_off(tl, cq * 2), w[0], w[1], w[2], w[3]);
-        st_chunk(sm, OFF_WB + sw128_off(tl, cq * 2 + 1), w[4], w[5], w[6], w[7]);
+        st_chunk(sm, OFF_WB + sw128_off(L, hx * 4 + cq * 2), w[0], w[1], w[2], w[3]);
+        st_chunk(sm, OFF_WB + sw128_off(L, hx * 4 + cq * 2 + 1), w[4], w[5], w[6], w[7]);
       }
       tc_fence_before();
-      // KR = (k kap) F_s : scaled copy of CB block 0 row `ch` into KR
-      if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint4 src = *reinterpret_cast<const uint4*>(sm + OFF_CB + sw128_off(ch, j));
-        const float f = Fs[j >> 1];
-        const uint32_t in[4] = {src.x, src.y, src.z, src.w};
-        uint32_t w[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          w[u] = pack_bf16x2(bf_bits(in[u] & 0xFFFFu) * f, bf_bits(in[u] >> 16) * f);
-        st_chunk(sm, OFF_KR + sw128_off(ch, j), w[0], w[1], w[2], w[3]);
-      }
       fence_async_smem();
-      named_bar(1, 128);
-      if (it == 0) mbar_arrive(&s->bar[B_REC_READY]);
+      named_bar(BAR_IG, kIG);
+      if (t == 0) mbar_arrive(&s->bar[B_REC_READY]);
+      __syncwarp();
     }
     if (stop) break;
   }
-  // drain this group's MMAs before the CTA can release TMEM
-  named_bar(1, 128);
-  if (leader_warp) {
+  // drain: this group's MMAs and the loads it issued, before the CTA releases TMEM
+  named_bar(BAR_IG, kIG);
+  if (warp == 0) {
     if (lane == 0) mma_commit(&s->bar[B_DRAIN_IG]);
     __syncwarp();
     wait_bar(p, s, B_DRAIN_IG, 0);
+    if (lane == 0) {
+      if (ld.n_qk > 0) mbar_wait(&s->bar[B_QK_FULL], (ld.n_qk - 1) & 1);
+      if (ld.n_g > 0) mbar_wait(&s->bar[B_G_FULL], (ld.n_g - 1) & 1);
+      if (ld.n_v > 0) mbar_wait(&s->bar[B_V_FULL], (ld.n_v - 1) & 1);
+    }
+    __syncwarp();
   }
 }
 
 // ======================================================================================
-// Recurrence group (warps 5-8): state update and output, chunk by chunk.
+// Recurrence group (warps 8-11): state update and output, chunk by chunk.
 // ======================================================================================
 template <typename ST>
 __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_t tbase) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
   const int v = quad * 32 + lane;  // TMEM lane = value channel
-  const int rt = threadIdx.x - 160;
-  const bool leader_warp = (warp == 5);
+  const int rt = threadIdx.x - kIG;
+  const bool leader_warp = (warp == kIG / 32);
   const uint32_t taddr_q = tbase + ((uint32_t)(quad * 32) << 16);
   const uint32_t sbase = smem_u32(sm);
   uint32_t gc = 0;
@@ -654,7 +732,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   auto o_epilogue = [&]() {
     if (!pend) return;
     pend = false;
-    if (!wait_bar(p, s, B_M3A, pend_gc & 1)) return;
+    wait_bar(p, s, B_M3A, pend_gc & 1);
     tc_fence_after();
     __nv_bfloat16* op = p.o + ((size_t)pend_t0 * p.Hv + pend_h) * kV + v;
 #pragma unroll
@@ -672,8 +750,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   };
 
   for (int k = 0;; ++k) {
-    bool ok;
-    const ItemInfo info = next_item(p, s, k, rt == 0, 2, ok);
+    const ItemInfo info = next_item(p, s, k, rt == 0, BAR_RG, kRG);
     if (info.done) break;
     const int h = info.h;
     const ST* src = nullptr;
@@ -692,15 +769,15 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       continue;
     }
     // ---- initial state: S^T row v -> ST (bf16) and TMEM S (pre-decayed by gamma of chunk 0)
+    float h0[kK];
+#pragma unroll
+    for (int c = 0; c < kK; ++c) h0[c] = src ? to_f32(src[(size_t)c * kV + v]) : 0.f;
     wait_bar(p, s, B_GAMMA0 + (gc & 1), (gc >> 1) & 1);
 #pragma unroll
     for (int kq = 0; kq < 8; ++kq) {
       float sv[16];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int c = kq * 16 + u;
-        sv[u] = src ? to_f32(src[(size_t)c * kV + v]) : 0.f;
-      }
+      for (int u = 0; u < 16; ++u) sv[u] = h0[kq * 16 + u];
       uint32_t w[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(sv[2 * u], sv[2 * u + 1]);
@@ -714,18 +791,18 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
     tmem_st_wait();
     tc_fence_before();
     fence_async_smem();
-    named_bar(2, 128);
+    named_bar(BAR_RG, kRG);
 
     bool stop = false;
     for (int lc = 0; lc < info.nchunks; ++lc, ++gc) {
-      if (named_bar_any(2, 128, aborted(s))) { stop = true; break; }
+      if (named_bar_any(BAR_RG, kRG, aborted(s))) { stop = true; break; }
       const int64_t t0 = info.bos + (int64_t)lc * kC;
       const int cv = (int)min((int64_t)kC, info.eos - t0);
       const bool last = (lc + 1 == info.nchunks);
       // ---- R1: U~ -= S W^T ; O = S QG^T   (leader warp)
       if (leader_warp) {
-        const bool okr = wait_bar(p, s, B_REC_READY, gc & 1);
-        if (okr && lane == 0) {
+        wait_bar(p, s, B_REC_READY, gc & 1);
+        if (lane == 0) {
           tc_fence_after();
           const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
 #pragma unroll
@@ -761,7 +838,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       }
       tc_fence_before();
       fence_async_smem();
-      named_bar(2, 128);
+      named_bar(BAR_RG, kRG);
       if (rt == 0) {
         mbar_arrive(&s->bar[B_E1]);
         tc_fence_after();
@@ -777,6 +854,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
                    sdesc_sw128(sbase + OFF_BB + st * 32, 16, 1024), id3o, 1u);
         mma_commit(&s->bar[B_M3A]);
       }
+      __syncwarp();
       // ---- E2: S -> ST (bf16) and pre-decay for the next chunk, or the final store
       wait_bar(p, s, B_M3B, gc & 1);
       tc_fence_after();
@@ -805,7 +883,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       tmem_st_wait();
       tc_fence_before();
       fence_async_smem();
-      named_bar(2, 128);
+      named_bar(BAR_RG, kRG);
       pend = true;
       pend_t0 = t0;
       pend_cv = cv;
@@ -815,7 +893,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
     if (stop) break;
   }
   o_epilogue();
-  named_bar(2, 128);
+  named_bar(BAR_RG, kRG);
   if (leader_warp) {
     if (lane == 0) mma_commit(&s->bar[B_DRAIN_RG]);
     __syncwarp();
@@ -845,13 +923,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s->tmem_base;
-  if (warp == 0) {
-    if ((threadIdx.x & 31) == 0) run_producer(p, sm, s);
-  } else if (warp <= 4) {
-    run_intra(p, sm, s, tbase);
-  } else {
-    run_recurrence<ST>(p, sm, s, tbase);
-  }
+  if (threadIdx.x < kIG) run_intra(p, sm, s, tbase);
+  else run_recurrence<ST>(p, sm, s, tbase);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -208,3 +208,22 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t ch
 
 }  // namespace tc
 }  // namespace kda
+
+namespace kda {
+namespace tc {
+// ---- legacy warp-level MMA for tiny latency-bound 16x16 blocks ---------------------------
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+// D = A(16x8, row) * B(8x8, col) + C, tf32 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_tf32_16x8x8(float d[4], const uint32_t a[4], const uint32_t b[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9},"
+      " {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+}  // namespace tc
+}  // namespace kda
