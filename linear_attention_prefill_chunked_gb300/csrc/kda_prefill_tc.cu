@@ -128,9 +128,6 @@ struct TcParams {
 
 // ---- small helpers -----------------------------------------------------------------
 __device__ __forceinline__ float bf_bits(uint32_t b16) { return __uint_as_float(b16 << 16); }
-__device__ __forceinline__ uint16_t to_bf_bits(float x) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
-}
 // Element (row, ch) of a K-major operand with 128 channels in two 64-wide atoms.
 __device__ __forceinline__ uint32_t kmaj_elem(uint32_t row, uint32_t ch, uint32_t rows_per_atom) {
   return (ch >> 6) * rows_per_atom * 128u + sw128_off(row, (ch & 63u) >> 3) + (ch & 7u) * 2u;
@@ -336,109 +333,142 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       }
       __syncwarp();
       // ------------------------------------------------------------- prologue
-      // thread = (channel ch, token half): tokens 32*half .. 32*half+31
-      const int ch = t >> 1, half = t & 1;
+      // thread = (channel pair c0 = 2*cp, c0+1; sub-chunk qt): tokens 16*qt .. 16*qt+15
+      const int cp = t >> 2, qt = t & 3, c0 = 2 * cp;
+      float bt = 0.f;  // beta of token t, needed only after the prologue
+      if (t < kC && t < cv) bt = p.beta[(size_t)(t0 + t) * p.Hv + h];
       wait_bar(p, s, B_G_FULL, gc & 1);
-      float e[32];
+      float e0[16], e1[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int r = half * 32 + j;
-        e[j] = (r < cv) ? __expf(Gs[r * kK + ch]) : 1.f;
+      for (int j = 0; j < 16; ++j) {
+        const int r = qt * 16 + j;
+        const float2 gv = *reinterpret_cast<const float2*>(Gs + r * kK + c0);
+        e0[j] = (r < cv) ? __expf(gv.x) : 1.f;  // padded rows: decay 1
+        e1[j] = (r < cv) ? __expf(gv.y) : 1.f;
       }
-      if (t < kC) s->beta[t] = (t < cv) ? p.beta[(size_t)(t0 + t) * p.Hv + h] : 0.f;
-      float pa = 1.f, pb = 1.f;
+      float pm0 = 1.f, pm1 = 1.f;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) { pa *= e[j]; pb *= e[16 + j]; }
-      const float oa = __shfl_xor_sync(0xffffffffu, pa, 1), ob = __shfl_xor_sync(0xffffffffu, pb, 1);
-      float pi[4];
-      pi[0] = half ? oa : pa;
-      pi[1] = half ? ob : pb;
-      pi[2] = half ? pa : oa;
-      pi[3] = half ? pb : ob;
-      const float Es[4] = {1.f, pi[0], pi[0] * pi[1], pi[0] * pi[1] * pi[2]};
-      const float Fs[4] = {pi[1] * pi[2] * pi[3], pi[2] * pi[3], pi[3], 1.f};
-      const float gam = Es[3] * pi[3];
+      for (int j = 0; j < 16; ++j) { pm0 *= e0[j]; pm1 *= e1[j]; }
+      float pi0[4], pi1[4];
 #pragma unroll
-      for (int sc = 0; sc < 4; ++sc) {
-        const uint32_t m = __ballot_sync(0xffffffffu, !(pi[sc] >= kSafeMin));
+      for (int q2 = 0; q2 < 4; ++q2) {
+        pi0[q2] = __shfl_sync(0xffffffffu, pm0, (lane & ~3) | q2);
+        pi1[q2] = __shfl_sync(0xffffffffu, pm1, (lane & ~3) | q2);
+      }
+      const float E0 = (qt > 0 ? pi0[0] : 1.f) * (qt > 1 ? pi0[1] : 1.f) * (qt > 2 ? pi0[2] : 1.f);
+      const float E1 = (qt > 0 ? pi1[0] : 1.f) * (qt > 1 ? pi1[1] : 1.f) * (qt > 2 ? pi1[2] : 1.f);
+      const float F0 = (qt < 1 ? pi0[1] : 1.f) * (qt < 2 ? pi0[2] : 1.f) * (qt < 3 ? pi0[3] : 1.f);
+      const float F1 = (qt < 1 ? pi1[1] : 1.f) * (qt < 2 ? pi1[2] : 1.f) * (qt < 3 ? pi1[3] : 1.f);
+#pragma unroll
+      for (int q2 = 0; q2 < 4; ++q2) {
+        const uint32_t m0 = __ballot_sync(0xffffffffu, qt == 0 && !(pi0[q2] >= kSafeMin));
+        const uint32_t m1 = __ballot_sync(0xffffffffu, qt == 0 && !(pi1[q2] >= kSafeMin));
         uint32_t comp = 0;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) comp |= ((m >> (2 * j)) & 1u) << j;
-        if (lane == 0) s->unsafe[sc][warp] = (uint16_t)comp;
+        for (int j = 0; j < 8; ++j)
+          comp |= (((m0 >> (4 * j)) & 1u) << (2 * j)) | (((m1 >> (4 * j)) & 1u) << (2 * j + 1));
+        if (lane == 0) s->unsafe[q2][warp] = (uint16_t)comp;
       }
       wait_bar(p, s, B_QK_FULL, gc & 1);
       // QG buffer and this gamma buffer are free once MMA-1b of the previous chunk ran
       if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
-      if (half == 0) s->gamma[gc & 1][ch] = gam;
+      if (qt == 0) {
+        s->gamma[gc & 1][c0] = pi0[0] * pi0[1] * pi0[2] * pi0[3];
+        s->gamma[gc & 1][c0 + 1] = pi1[0] * pi1[1] * pi1[2] * pi1[3];
+      }
       named_bar(BAR_IG, kIG);  // every thread has read g: CB blocks 1-2 may be overwritten
-#pragma unroll
-      for (int u2 = 0; u2 < 2; ++u2) {
-        const int sc = half * 2 + u2;  // sub-chunk
-        float kap[16];
+      {
+        const int sc = qt;
+        float kap0[16], kap1[16];
         {
-          float a = 1.f;
+          float a0 = 1.f, a1 = 1.f;
 #pragma unroll
-          for (int j = 15; j >= 0; --j) { kap[j] = a; a *= e[u2 * 16 + j]; }
+          for (int j = 15; j >= 0; --j) {
+            kap0[j] = a0; a0 *= e0[j];
+            kap1[j] = a1; a1 *= e1[j];
+          }
         }
-        const bool safe = pi[sc] >= kSafeMin;
-        const float inv_pi = safe ? 1.f / pi[sc] : 0.f;
-        const float kgs = Es[sc], qgs = p.scale * Es[sc];
-        float rho = 1.f;
+        const float ip0 = (pm0 >= kSafeMin) ? 1.f / pm0 : 0.f;  // pm = pi of this sub-chunk
+        const float ip1 = (pm1 >= kSafeMin) ? 1.f / pm1 : 0.f;
+        const float qs0 = p.scale * E0, qs1 = p.scale * E1;
+        float rho0 = 1.f, rho1 = 1.f;
 #pragma unroll
         for (int jh = 0; jh < 2; ++jh) {
-          float kv[8], qv[8];
-          uint16_t* kp[8];
-          uint16_t* qp[8];
+          uint32_t kw[8], qw[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int r = sc * 16 + jh * 8 + u;
-            kp[u] = reinterpret_cast<uint16_t*>(sm + OFF_QK + kmaj_elem(r, ch, 128));
-            qp[u] = reinterpret_cast<uint16_t*>(sm + OFF_QK + kmaj_elem(64 + r, ch, 128));
-            kv[u] = (r < cv) ? bf_bits(*kp[u]) : 0.f;
-            qv[u] = (r < cv) ? bf_bits(*qp[u]) : 0.f;
+            const uint32_t* kp = reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128));
+            const uint32_t* qp = reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(64 + r, c0, 128));
+            kw[u] = (r < cv) ? *kp : 0u;
+            qw[u] = (r < cv) ? *qp : 0u;
           }
-          uint32_t w_cb0[4], w_dg[4], w_kg[4], w_qg[4], w_m1[4], w_m12[4], w_m2[4];
+          uint32_t o_cb0[2][4], o_dg[2][4], o_kg[2][4], o_qg[2][4], o_m1[2][4], o_m12[2][4], o_m2[2][4];
 #pragma unroll
           for (int u = 0; u < 8; u += 2) {
-            float kk[2], dg[2], kg[2], qg[2], m1[2], m12[2], m2[2];
+            float kk[2][2], dg[2][2], kg[2][2], qg[2][2], m1[2][2], m12[2][2], m2[2][2];
 #pragma unroll
             for (int v2 = 0; v2 < 2; ++v2) {
               const int j = jh * 8 + u + v2;
-              rho *= e[u2 * 16 + j];
-              const float kr = kv[u + v2] * rho, qr = qv[u + v2] * rho;
-              *kp[u + v2] = to_bf_bits(kr);
-              *qp[u + v2] = to_bf_bits(qr);
-              kk[v2] = kv[u + v2] * kap[j];
-              dg[v2] = kk[v2] * inv_pi;
-              kg[v2] = kr * kgs;
-              qg[v2] = qr * qgs;
-              m1[v2] = kk[v2] * pi[1];
-              m12[v2] = m1[v2] * pi[2];
-              m2[v2] = kk[v2] * pi[2];
+              rho0 *= e0[j];
+              rho1 *= e1[j];
+              const float k0 = bf_bits(kw[u + v2] & 0xFFFFu), k1 = bf_bits(kw[u + v2] >> 16);
+              const float q0 = bf_bits(qw[u + v2] & 0xFFFFu), q1 = bf_bits(qw[u + v2] >> 16);
+              const float kr0 = k0 * rho0, kr1 = k1 * rho1, qr0 = q0 * rho0, qr1 = q1 * rho1;
+              kw[u + v2] = pack_bf16x2(kr0, kr1);
+              qw[u + v2] = pack_bf16x2(qr0, qr1);
+              kk[0][v2] = k0 * kap0[j];
+              kk[1][v2] = k1 * kap1[j];
+              dg[0][v2] = kk[0][v2] * ip0;
+              dg[1][v2] = kk[1][v2] * ip1;
+              kg[0][v2] = kr0 * E0;
+              kg[1][v2] = kr1 * E1;
+              qg[0][v2] = qr0 * qs0;
+              qg[1][v2] = qr1 * qs1;
+              m1[0][v2] = kk[0][v2] * pi0[1];
+              m1[1][v2] = kk[1][v2] * pi1[1];
+              m12[0][v2] = m1[0][v2] * pi0[2];
+              m12[1][v2] = m1[1][v2] * pi1[2];
+              m2[0][v2] = kk[0][v2] * pi0[2];
+              m2[1][v2] = kk[1][v2] * pi1[2];
             }
-            w_cb0[u / 2] = pack_bf16x2(kk[0], kk[1]);
-            w_dg[u / 2] = pack_bf16x2(dg[0], dg[1]);
-            w_kg[u / 2] = pack_bf16x2(kg[0], kg[1]);
-            w_qg[u / 2] = pack_bf16x2(qg[0], qg[1]);
-            w_m1[u / 2] = pack_bf16x2(m1[0], m1[1]);
-            w_m12[u / 2] = pack_bf16x2(m12[0], m12[1]);
-            w_m2[u / 2] = pack_bf16x2(m2[0], m2[1]);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              o_cb0[c][u / 2] = pack_bf16x2(kk[c][0], kk[c][1]);
+              o_dg[c][u / 2] = pack_bf16x2(dg[c][0], dg[c][1]);
+              o_kg[c][u / 2] = pack_bf16x2(kg[c][0], kg[c][1]);
+              o_qg[c][u / 2] = pack_bf16x2(qg[c][0], qg[c][1]);
+              o_m1[c][u / 2] = pack_bf16x2(m1[c][0], m1[c][1]);
+              o_m12[c][u / 2] = pack_bf16x2(m12[c][0], m12[c][1]);
+              o_m2[c][u / 2] = pack_bf16x2(m2[c][0], m2[c][1]);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int r = sc * 16 + jh * 8 + u;
+            *reinterpret_cast<uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128)) = kw[u];
+            *reinterpret_cast<uint32_t*>(sm + OFF_QK + kmaj_elem(64 + r, c0, 128)) = qw[u];
           }
           const uint32_t cj = sc * 2 + jh;
-          st_chunk(sm, OFF_CB + sw128_off(ch, cj), w_cb0[0], w_cb0[1], w_cb0[2], w_cb0[3]);
-          st_chunk(sm, OFF_CB + 32768 + sw128_off(ch, cj), w_dg[0], w_dg[1], w_dg[2], w_dg[3]);
-          st_chunk(sm, OFF_KG + sw128_off(ch, cj), w_kg[0], w_kg[1], w_kg[2], w_kg[3]);
-          st_chunk(sm, OFF_QG + sw128_off(ch, cj), w_qg[0], w_qg[1], w_qg[2], w_qg[3]);
-          if (sc == 0) {
-            st_chunk(sm, OFF_CB + 16384 + sw128_off(ch, 0 + jh), w_m1[0], w_m1[1], w_m1[2], w_m1[3]);
-            st_chunk(sm, OFF_CB + 16384 + sw128_off(ch, 2 + jh), w_m12[0], w_m12[1], w_m12[2], w_m12[3]);
-          } else if (sc == 1) {
-            st_chunk(sm, OFF_CB + 16384 + sw128_off(ch, 4 + jh), w_m2[0], w_m2[1], w_m2[2], w_m2[3]);
-          } else if (sc == 3) {
-            st_chunk(sm, OFF_CB + 16384 + sw128_off(ch, 6 + jh), 0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int row = c0 + c;
+            st_chunk(sm, OFF_CB + sw128_off(row, cj), o_cb0[c][0], o_cb0[c][1], o_cb0[c][2], o_cb0[c][3]);
+            st_chunk(sm, OFF_CB + 32768 + sw128_off(row, cj), o_dg[c][0], o_dg[c][1], o_dg[c][2], o_dg[c][3]);
+            st_chunk(sm, OFF_KG + sw128_off(row, cj), o_kg[c][0], o_kg[c][1], o_kg[c][2], o_kg[c][3]);
+            st_chunk(sm, OFF_QG + sw128_off(row, cj), o_qg[c][0], o_qg[c][1], o_qg[c][2], o_qg[c][3]);
+            if (sc == 0) {
+              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 0 + jh), o_m1[c][0], o_m1[c][1], o_m1[c][2], o_m1[c][3]);
+              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 2 + jh), o_m12[c][0], o_m12[c][1], o_m12[c][2], o_m12[c][3]);
+            } else if (sc == 1) {
+              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 4 + jh), o_m2[c][0], o_m2[c][1], o_m2[c][2], o_m2[c][3]);
+            } else if (sc == 3) {
+              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 6 + jh), 0u, 0u, 0u, 0u);
+            }
           }
         }
       }
+      if (t < kC) s->beta[t] = bt;
       fence_async_smem();
       named_bar(BAR_IG, kIG);
       if (t == 0) {
@@ -459,6 +489,11 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       tc_fence_after();
       if (t == 0 && have_next && ld.n_qk == gc + 1) ld.load_qk(p, sm, s, nkh, nt0);  // QK free
       __syncwarp();
+      uint32_t any_unsafe = 0;
+#pragma unroll
+      for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+        for (int wd = 0; wd < 8; ++wd) any_unsafe |= s->unsafe[q2][wd];
       {
         const int r = L & 63, a = r >> 4;
         const bool isB = L >= 64;
@@ -474,112 +509,136 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             if (b_ == aa - 3) return 80;
             return -1;
           };
-          const int c0 = (b <= a0) ? colof(a0, b) : -1;
-          const int c1 = (b <= a0 + 1) ? colof(a0 + 1, b) : -1;
+          const int cc0 = (b <= a0) ? colof(a0, b) : -1;
+          const int cc1 = (b <= a0 + 1) ? colof(a0 + 1, b) : -1;
           float v0[16], v1[16];
-          if (c0 >= 0) tmem_ld16(taddr_q + TM_AB + c0, v0);
-          if (c1 >= 0) tmem_ld16(taddr_q + TM_AB + c1, v1);
+          if (cc0 >= 0) tmem_ld16(taddr_q + TM_AB + cc0, v0);
+          if (cc1 >= 0) tmem_ld16(taddr_q + TM_AB + cc1, v1);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             float val = 0.f;
-            if (a == a0 && c0 >= 0) val = v0[j];
-            if (a == a0 + 1 && c1 >= 0) val = v1[j];
+            if (a == a0 && cc0 >= 0) val = v0[j];
+            if (a == a0 + 1 && cc1 >= 0) val = v1[j];
             x[bb * 16 + j] = val;
           }
         }
         tc_fence_before();
-        float* row = isB ? Xs : As;
+        if (any_unsafe == 0u) {
+          // fast path: mask and scale straight from TMEM
+          if (!isB) {
+            const float br = s->beta[r];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) row[sidx(r, hx * 32 + j)] = x[j];
+            for (int jc = 0; jc < 8; ++jc) {
+              float4 w4;
+              const int i = hx * 32 + jc * 4;
+              w4.x = (i + 0 < r) ? br * x[jc * 4 + 0] : 0.f;
+              w4.y = (i + 1 < r) ? br * x[jc * 4 + 1] : 0.f;
+              w4.z = (i + 2 < r) ? br * x[jc * 4 + 2] : 0.f;
+              w4.w = (i + 3 < r) ? br * x[jc * 4 + 3] : 0.f;
+              *reinterpret_cast<float4*>(As + sidx(r, i)) = w4;
+            }
+          } else {
+            if (gc > 0) wait_bar(p, s, B_M3A, (gc - 1) & 1);  // BB free
+#pragma unroll
+            for (int jc = 0; jc < 4; ++jc) {
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int i0 = hx * 32 + jc * 8 + u * 2;
+                w[u] = pack_bf16x2((i0 <= r) ? p.scale * x[jc * 8 + u * 2] : 0.f,
+                                   (i0 + 1 <= r) ? p.scale * x[jc * 8 + u * 2 + 1] : 0.f);
+              }
+              st_chunk(sm, OFF_BB + sw128_off(r, hx * 4 + jc), w[0], w[1], w[2], w[3]);
+            }
+          }
+        } else {
+          float* row = isB ? Xs : As;
+#pragma unroll
+          for (int jc = 0; jc < 8; ++jc)
+            *reinterpret_cast<float4*>(row + sidx(r, hx * 32 + jc * 4)) =
+                make_float4(x[jc * 4], x[jc * 4 + 1], x[jc * 4 + 2], x[jc * 4 + 3]);
+        }
       }
       named_bar(BAR_IG, kIG);
-      // exact pairwise terms of the diagonal sub-chunk blocks on "unsafe" channels
-      if (hx == 0) {
-        const int r = L & 63, a = r >> 4;
-        const bool isB = L >= 64;
-        uint32_t any = 0;
+      if (any_unsafe != 0u) {
+        // exact pairwise terms of the diagonal sub-chunk blocks on "unsafe" channels
+        if (hx == 0) {
+          const int r = L & 63, a = r >> 4;
+          const bool isB = L >= 64;
+          uint32_t anya = 0;
 #pragma unroll
-        for (int wd = 0; wd < 8; ++wd) any |= s->unsafe[a][wd];
-        if (any != 0u && r < cv) {
-          float* row = isB ? Xs : As;
-          const __nv_bfloat16* xsrc = isB ? p.q : p.k;
-          for (int wd = 0; wd < 8; ++wd) {
-            uint32_t m = s->unsafe[a][wd];
-            while (m) {
-              const int c = wd * 16 + (__ffs(m) - 1);
-              m &= m - 1;
-              const float xr = __bfloat162float(xsrc[((size_t)(t0 + r) * p.Hk + kh) * kK + c]);
-              float pr = 1.f;
-              for (int i = r; i >= a * 16; --i) {
-                const float ki = __bfloat162float(p.k[((size_t)(t0 + i) * p.Hk + kh) * kK + c]);
-                row[sidx(r, i)] += xr * ki * pr;
-                pr *= __expf(p.g[((size_t)(t0 + i) * p.Hv + h) * kK + c]);
-                if (pr == 0.f) break;
+          for (int wd = 0; wd < 8; ++wd) anya |= s->unsafe[a][wd];
+          if (anya != 0u && r < cv) {
+            float* row = isB ? Xs : As;
+            const __nv_bfloat16* xsrc = isB ? p.q : p.k;
+            for (int wd = 0; wd < 8; ++wd) {
+              uint32_t m = s->unsafe[a][wd];
+              while (m) {
+                const int c = wd * 16 + (__ffs(m) - 1);
+                m &= m - 1;
+                const float xr = __bfloat162float(xsrc[((size_t)(t0 + r) * p.Hk + kh) * kK + c]);
+                float pr = 1.f;
+                for (int i = r; i >= a * 16; --i) {
+                  const float ki = __bfloat162float(p.k[((size_t)(t0 + i) * p.Hk + kh) * kK + c]);
+                  row[sidx(r, i)] += xr * ki * pr;
+                  pr *= __expf(p.g[((size_t)(t0 + i) * p.Hv + h) * kK + c]);
+                  if (pr == 0.f) break;
+                }
               }
             }
           }
         }
-      }
-      named_bar(BAR_IG, kIG);
-      // A: mask + beta_r (in place, fp32); B: mask + scale -> bf16 -> BB
-      {
-        const int r = L & 63;
-        if (L < 64) {
-          const float br = s->beta[r];
+        named_bar(BAR_IG, kIG);
+        // A: mask + beta_r (in place, fp32); B: mask + scale -> bf16 -> BB
+        {
+          const int r = L & 63;
+          if (L < 64) {
+            const float br = s->beta[r];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int i = hx * 32 + j;
-            const float v = As[sidx(r, i)];
-            As[sidx(r, i)] = (i < r) ? br * v : 0.f;
-          }
-        } else {
-          if (gc > 0) wait_bar(p, s, B_M3A, (gc - 1) & 1);  // BB free
-#pragma unroll
-          for (int jc = 0; jc < 4; ++jc) {
-            uint32_t w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int i0 = hx * 32 + jc * 8 + u * 2;
-              const float v0 = (i0 <= r) ? p.scale * Xs[sidx(r, i0)] : 0.f;
-              const float v1 = (i0 + 1 <= r) ? p.scale * Xs[sidx(r, i0 + 1)] : 0.f;
-              w[u] = pack_bf16x2(v0, v1);
+            for (int jc = 0; jc < 8; ++jc) {
+              const int i = hx * 32 + jc * 4;
+              float4 w4 = *reinterpret_cast<const float4*>(As + sidx(r, i));
+              w4.x = (i + 0 < r) ? br * w4.x : 0.f;
+              w4.y = (i + 1 < r) ? br * w4.y : 0.f;
+              w4.z = (i + 2 < r) ? br * w4.z : 0.f;
+              w4.w = (i + 3 < r) ? br * w4.w : 0.f;
+              *reinterpret_cast<float4*>(As + sidx(r, i)) = w4;
             }
-            st_chunk(sm, OFF_BB + sw128_off(r, hx * 4 + jc), w[0], w[1], w[2], w[3]);
+          } else {
+            if (gc > 0) wait_bar(p, s, B_M3A, (gc - 1) & 1);  // BB free
+#pragma unroll
+            for (int jc = 0; jc < 4; ++jc) {
+              const int i = hx * 32 + jc * 8;
+              const float4 lo = *reinterpret_cast<const float4*>(Xs + sidx(r, i));
+              const float4 hi = *reinterpret_cast<const float4*>(Xs + sidx(r, i + 4));
+              const float vv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                w[u] = pack_bf16x2((i + 2 * u <= r) ? p.scale * vv[2 * u] : 0.f,
+                                   (i + 2 * u + 1 <= r) ? p.scale * vv[2 * u + 1] : 0.f);
+              st_chunk(sm, OFF_BB + sw128_off(r, hx * 4 + jc), w[0], w[1], w[2], w[3]);
+            }
           }
         }
+        named_bar(BAR_IG, kIG);
       }
-      named_bar(BAR_IG, kIG);
       // ------------------------------------------------------------- inverse
-      // X = (I + A)^-1 by 16x16 blocks: diagonal blocks by forward substitution,
-      // then X_ab = -X_aa * sum_{b<=c<a} A_ac X_cb, one block per warp per level.
-      if (warp < 4) {
-        const int o = warp * 16, j = lane & 15;
+      // X = (I + A)^-1 by 16x16 blocks: diagonal blocks by forward substitution
+      // (one column per lane, two blocks per warp), then
+      // X_ab = -X_aa * sum_{b<=c<a} A_ac X_cb, one block per warp per level.
+      if (warp < 2) {
+        const int o = (warp * 2 + (lane >> 4)) * 16, j = lane & 15;
         float xv[16];
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) xv[rr] = (rr == j) ? 1.f : 0.f;
 #pragma unroll
-        for (int rr = 1; rr < 16; ++rr) {
-          float acc = 0.f;
+        for (int i = 0; i < 15; ++i)
 #pragma unroll
-          for (int i = 0; i < rr; ++i) acc = fmaf(As[sidx(o + rr, o + i)], xv[i], acc);
-          if (rr > j) xv[rr] = -acc;
-        }
-        if (lane < 16) {
+          for (int rr = i + 1; rr < 16; ++rr) xv[rr] = fmaf(-As[sidx(o + rr, o + i)], xv[i], xv[rr]);
 #pragma unroll
-          for (int rr = 0; rr < 16; ++rr) Xs[sidx(o + rr, o + j)] = xv[rr];
-        }
-      } else {
-        // zero the strictly-upper 16-blocks of X (6 blocks x 256 entries)
-        const int t2 = t - 128;
-#pragma unroll
-        for (int q2 = 0; q2 < 12; ++q2) {
-          const int e2 = t2 * 12 + q2;  // 0..1535
-          const int blk = e2 >> 8, w2 = e2 & 255;
-          const int ba = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-          const int bbk = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-          Xs[sidx(ba * 16 + (w2 >> 4), bbk * 16 + (w2 & 15))] = 0.f;
-        }
+        for (int rr = 0; rr < 16; ++rr) Xs[sidx(o + rr, o + j)] = xv[rr];
       }
       named_bar(BAR_IG, kIG);
       if (warp < 3) {  // X_{a+1,a}
@@ -634,19 +693,22 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           st_chunk(sm, OFF_TM + sw128_off(r, j), w[0], w[1], w[2], w[3]);
         }
       }
-      // KR = (k kap) F_s : scaled copy of CB block 0 row `ch` into KR (this half's tokens)
+      // KR = (k kap) F_s : scaled copy of this thread's CB block-0 chunks into KR
       if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int j = half * 4 + jj;
-        const uint4 src = *reinterpret_cast<const uint4*>(sm + OFF_CB + sw128_off(ch, j));
-        const float f = Fs[j >> 1];
-        const uint32_t in[4] = {src.x, src.y, src.z, src.w};
-        uint32_t w[4];
+      for (int c = 0; c < 2; ++c) {
+        const float f = c ? F1 : F0;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          w[u] = pack_bf16x2(bf_bits(in[u] & 0xFFFFu) * f, bf_bits(in[u] >> 16) * f);
-        st_chunk(sm, OFF_KR + sw128_off(ch, j), w[0], w[1], w[2], w[3]);
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = qt * 2 + jj;
+          const uint4 src = *reinterpret_cast<const uint4*>(sm + OFF_CB + sw128_off(c0 + c, j));
+          const uint32_t in[4] = {src.x, src.y, src.z, src.w};
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            w[u] = pack_bf16x2(bf_bits(in[u] & 0xFFFFu) * f, bf_bits(in[u] >> 16) * f);
+          st_chunk(sm, OFF_KR + sw128_off(c0 + c, j), w[0], w[1], w[2], w[3]);
+        }
       }
       fence_async_smem();
       named_bar(BAR_IG, kIG);
@@ -722,31 +784,41 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   const bool leader_warp = (warp == kIG / 32);
   const uint32_t taddr_q = tbase + ((uint32_t)(quad * 32) << 16);
   const uint32_t sbase = smem_u32(sm);
+  __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + OFF_ST);  // [64][128] staging of O
   uint32_t gc = 0;
-  // deferred output epilogue of the previous chunk
+  // The output epilogue of a chunk is deferred into the next chunk's MMA-3 window,
+  // staged row-major through the S^T buffer (free from MMA-1b until the E2 write).
   bool pend = false;
   int64_t pend_t0 = 0;
   int pend_cv = 0, pend_h = 0;
   uint32_t pend_gc = 0;
 
-  auto o_epilogue = [&]() {
+  auto o_epilogue = [&](bool st_in_use, uint32_t cur_gc) {
     if (!pend) return;
     pend = false;
+    if (st_in_use) wait_bar(p, s, B_M1B, cur_gc & 1);
     wait_bar(p, s, B_M3A, pend_gc & 1);
     tc_fence_after();
-    __nv_bfloat16* op = p.o + ((size_t)pend_t0 * p.Hv + pend_h) * kV + v;
 #pragma unroll
     for (int cq = 0; cq < 4; ++cq) {
       float ov[16];
       tmem_ld16(taddr_q + TM_O + 64 * (pend_gc & 1) + cq * 16, ov);
       tmem_ld_wait();
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int r = cq * 16 + u;
-        if (r < pend_cv) op[(size_t)r * p.Hv * kV] = __float2bfloat16_rn(ov[u]);
-      }
+      for (int u = 0; u < 16; ++u) stage[(cq * 16 + u) * kV + v] = __float2bfloat16_rn(ov[u]);
     }
     tc_fence_before();
+    named_bar(BAR_RG, kRG);
+    {
+      const int r = rt >> 1, hh = rt & 1;
+      if (r < pend_cv) {
+        const uint4* srow = reinterpret_cast<const uint4*>(stage + r * kV + hh * 64);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)(pend_t0 + r) * p.Hv + pend_h) * kV + hh * 64);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) dst[u] = srow[u];
+      }
+    }
+    named_bar(BAR_RG, kRG);  // staging read before S^T is rewritten
   };
 
   for (int k = 0;; ++k) {
@@ -769,29 +841,31 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       continue;
     }
     // ---- initial state: S^T row v -> ST (bf16) and TMEM S (pre-decayed by gamma of chunk 0)
-    float h0[kK];
+    {
+      float h0[kK];
 #pragma unroll
-    for (int c = 0; c < kK; ++c) h0[c] = src ? to_f32(src[(size_t)c * kV + v]) : 0.f;
-    wait_bar(p, s, B_GAMMA0 + (gc & 1), (gc >> 1) & 1);
+      for (int c = 0; c < kK; ++c) h0[c] = src ? to_f32(src[(size_t)c * kV + v]) : 0.f;
+      wait_bar(p, s, B_GAMMA0 + (gc & 1), (gc >> 1) & 1);
 #pragma unroll
-    for (int kq = 0; kq < 8; ++kq) {
-      float sv[16];
+      for (int kq = 0; kq < 8; ++kq) {
+        float sv[16];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) sv[u] = h0[kq * 16 + u];
-      uint32_t w[8];
+        for (int u = 0; u < 16; ++u) sv[u] = h0[kq * 16 + u];
+        uint32_t w[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(sv[2 * u], sv[2 * u + 1]);
-      const uint32_t cj = kq * 2;
-      st_chunk(sm, OFF_ST + (cj >> 3) * 16384 + sw128_off(v, cj & 7), w[0], w[1], w[2], w[3]);
-      st_chunk(sm, OFF_ST + ((cj + 1) >> 3) * 16384 + sw128_off(v, (cj + 1) & 7), w[4], w[5], w[6], w[7]);
+        for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(sv[2 * u], sv[2 * u + 1]);
+        const uint32_t cj = kq * 2;
+        st_chunk(sm, OFF_ST + (cj >> 3) * 16384 + sw128_off(v, cj & 7), w[0], w[1], w[2], w[3]);
+        st_chunk(sm, OFF_ST + ((cj + 1) >> 3) * 16384 + sw128_off(v, (cj + 1) & 7), w[4], w[5], w[6], w[7]);
 #pragma unroll
-      for (int u = 0; u < 16; ++u) sv[u] *= s->gamma[gc & 1][kq * 16 + u];
-      tmem_st16(taddr_q + TM_S + kq * 16, sv);
+        for (int u = 0; u < 16; ++u) sv[u] *= s->gamma[gc & 1][kq * 16 + u];
+        tmem_st16(taddr_q + TM_S + kq * 16, sv);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      fence_async_smem();
+      named_bar(BAR_RG, kRG);
     }
-    tmem_st_wait();
-    tc_fence_before();
-    fence_async_smem();
-    named_bar(BAR_RG, kRG);
 
     bool stop = false;
     for (int lc = 0; lc < info.nchunks; ++lc, ++gc) {
@@ -821,7 +895,21 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         }
         __syncwarp();
       }
-      o_epilogue();
+      // ---- pre-decay S <- Diag(gamma_c) S in TMEM (overlaps MMA-1; MMA-3b accumulates on it)
+      if (lc > 0) {
+        wait_bar(p, s, B_GAMMA0 + (gc & 1), (gc >> 1) & 1);
+        const float* gm = s->gamma[gc & 1];
+#pragma unroll
+        for (int kq = 0; kq < 8; ++kq) {
+          float sv[16];
+          tmem_ld16(taddr_q + TM_S + kq * 16, sv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 16; ++u) sv[u] *= gm[kq * 16 + u];
+          tmem_st16(taddr_q + TM_S + kq * 16, sv);
+        }
+        tmem_st_wait();
+      }
       // ---- E1: U^T row v -> UT (bf16)
       wait_bar(p, s, B_M1A, gc & 1);
       tc_fence_after();
@@ -855,10 +943,11 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         mma_commit(&s->bar[B_M3A]);
       }
       __syncwarp();
-      // ---- E2: S -> ST (bf16) and pre-decay for the next chunk, or the final store
+      // ---- output of the previous chunk, inside this chunk's MMA-3 window
+      o_epilogue(true, gc);
+      // ---- E2: S -> ST (bf16), or the final state store on the last chunk
       wait_bar(p, s, B_M3B, gc & 1);
       tc_fence_after();
-      if (!last) wait_bar(p, s, B_GAMMA0 + ((gc + 1) & 1), ((gc + 1) >> 1) & 1);
 #pragma unroll
       for (int kq = 0; kq < 8; ++kq) {
         float sv[16];
@@ -871,16 +960,11 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
           const uint32_t cj = kq * 2;
           st_chunk(sm, OFF_ST + (cj >> 3) * 16384 + sw128_off(v, cj & 7), w[0], w[1], w[2], w[3]);
           st_chunk(sm, OFF_ST + ((cj + 1) >> 3) * 16384 + sw128_off(v, (cj + 1) & 7), w[4], w[5], w[6], w[7]);
-          const float* gm = s->gamma[(gc + 1) & 1];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) sv[u] *= gm[kq * 16 + u];
-          tmem_st16(taddr_q + TM_S + kq * 16, sv);
         } else if (dst) {
 #pragma unroll
           for (int u = 0; u < 16; ++u) dst[(size_t)(kq * 16 + u) * kV + v] = from_f32<ST>(sv[u]);
         }
       }
-      tmem_st_wait();
       tc_fence_before();
       fence_async_smem();
       named_bar(BAR_RG, kRG);
@@ -892,7 +976,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
     }
     if (stop) break;
   }
-  o_epilogue();
+  o_epilogue(false, gc);
   named_bar(BAR_RG, kRG);
   if (leader_warp) {
     if (lane == 0) mma_commit(&s->bar[B_DRAIN_RG]);
