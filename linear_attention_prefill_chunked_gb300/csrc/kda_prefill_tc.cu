@@ -290,7 +290,6 @@ struct Loader {  // state of thread 0 only
     tma_prefetch_3d(&p.tm_k, 64, kh, t0);
     tma_prefetch_3d(&p.tm_q, 0, kh, t0);
     tma_prefetch_3d(&p.tm_q, 64, kh, t0);
-    tma_prefetch_3d(&p.tm_g, 0, h, t0);
     tma_prefetch_3d(&p.tm_v, 0, h, t0);
     tma_prefetch_3d(&p.tm_v, 64, h, t0);
   }
@@ -482,8 +481,27 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           mma_bf16(tbase + TM_AB, a, b, idesc, st > 0 ? 1u : 0u);
         }
         mma_commit(&s->bar[B_AB_DONE]);
+        if (have_next) tma_prefetch_3d(&p.tm_g, 0, nh, nt0);  // gate of the next chunk -> L2
       }
       __syncwarp();
+      // KR = (k kap) F_s : scaled copy of this thread's CB block-0 chunks into KR
+      // (overlaps MMA-AB, which only reads CB)
+      if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const float f = c ? F1 : F0;
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = qt * 2 + jj;
+          const uint4 src = *reinterpret_cast<const uint4*>(sm + OFF_CB + sw128_off(c0 + c, j));
+          const uint32_t in[4] = {src.x, src.y, src.z, src.w};
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            w[u] = pack_bf16x2(bf_bits(in[u] & 0xFFFFu) * f, bf_bits(in[u] >> 16) * f);
+          st_chunk(sm, OFF_KR + sw128_off(c0 + c, j), w[0], w[1], w[2], w[3]);
+        }
+      }
       // ------------------------------------------------------------- A / B rows
       wait_bar(p, s, B_AB_DONE, gc & 1);
       tc_fence_after();
@@ -693,23 +711,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           st_chunk(sm, OFF_TM + sw128_off(r, j), w[0], w[1], w[2], w[3]);
         }
       }
-      // KR = (k kap) F_s : scaled copy of this thread's CB block-0 chunks into KR
-      if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const float f = c ? F1 : F0;
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = qt * 2 + jj;
-          const uint4 src = *reinterpret_cast<const uint4*>(sm + OFF_CB + sw128_off(c0 + c, j));
-          const uint32_t in[4] = {src.x, src.y, src.z, src.w};
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            w[u] = pack_bf16x2(bf_bits(in[u] & 0xFFFFu) * f, bf_bits(in[u] >> 16) * f);
-          st_chunk(sm, OFF_KR + sw128_off(c0 + c, j), w[0], w[1], w[2], w[3]);
-        }
-      }
       fence_async_smem();
       named_bar(BAR_IG, kIG);
       // ------------------------------------------------------------- U~ and W
@@ -793,11 +794,15 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   int pend_cv = 0, pend_h = 0;
   uint32_t pend_gc = 0;
 
-  auto o_epilogue = [&](bool st_in_use, uint32_t cur_gc) {
+  // Inside the loop (in_loop): MMA-3a of the pending chunk was committed by the same
+  // thread before MMA-1a of the current one, whose completion E1 already waited on, so
+  // it is complete; waiting on its barrier here could see the barrier already one phase
+  // further (MMA-3a of the current chunk) and never return.  After the loop it is waited.
+  auto o_epilogue = [&](bool in_loop, uint32_t cur_gc) {
     if (!pend) return;
     pend = false;
-    if (st_in_use) wait_bar(p, s, B_M1B, cur_gc & 1);
-    wait_bar(p, s, B_M3A, pend_gc & 1);
+    if (in_loop) wait_bar(p, s, B_M1B, cur_gc & 1);  // S^T buffer no longer read by MMA-1b
+    else wait_bar(p, s, B_M3A, pend_gc & 1);
     tc_fence_after();
 #pragma unroll
     for (int cq = 0; cq < 4; ++cq) {
@@ -900,13 +905,17 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         wait_bar(p, s, B_GAMMA0 + (gc & 1), (gc >> 1) & 1);
         const float* gm = s->gamma[gc & 1];
 #pragma unroll
-        for (int kq = 0; kq < 8; ++kq) {
-          float sv[16];
-          tmem_ld16(taddr_q + TM_S + kq * 16, sv);
+        for (int kh2 = 0; kh2 < 2; ++kh2) {
+          float sv[4][16];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(taddr_q + TM_S + (kh2 * 4 + q4) * 16, sv[q4]);
           tmem_ld_wait();
 #pragma unroll
-          for (int u = 0; u < 16; ++u) sv[u] *= gm[kq * 16 + u];
-          tmem_st16(taddr_q + TM_S + kq * 16, sv);
+          for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) sv[q4][u] *= gm[(kh2 * 4 + q4) * 16 + u];
+            tmem_st16(taddr_q + TM_S + (kh2 * 4 + q4) * 16, sv[q4]);
+          }
         }
         tmem_st_wait();
       }
