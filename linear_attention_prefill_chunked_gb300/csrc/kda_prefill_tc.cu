@@ -42,6 +42,8 @@
 // writes the final state back to the same row.
 #include <cudaTypedefs.h>
 
+#include <cstddef>
+
 #include "kda_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -102,14 +104,16 @@ struct ItemInfo {
 struct Small {
   uint64_t bar[B_COUNT];
   ItemInfo ring[kRing];
-  float beta[kC];
-  float gamma[2][kK];
+  alignas(16) float beta[kC];      // read as float4
+  alignas(16) float gamma[2][kK];  // read as float4
   uint16_t unsafe[4][8];  // [sub-chunk][16-channel group] bitmask
   uint32_t tmem_base;
   uint32_t abort;
 };
 constexpr uint32_t kSmemBytes = OFF_SMALL + sizeof(Small) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
+static_assert(offsetof(Small, beta) % 16 == 0 && offsetof(Small, gamma) % 16 == 0,
+              "vector-read arrays must be 16-byte aligned");
 
 struct TcParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_g;
@@ -332,15 +336,19 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       }
       __syncwarp();
       // ------------------------------------------------------------- prologue
-      // thread = (channel pair c0 = 2*cp, c0+1; sub-chunk qt): tokens 16*qt .. 16*qt+15
-      const int cp = t >> 2, qt = t & 3, c0 = 2 * cp;
+      // thread = (channel pair c0 = 2*cp, c0+1; sub-chunk sc).  A warp covers 64
+      // consecutive channels of one 16-token sub-chunk, so its gate, k and q reads are
+      // full rows; row writes alternate the two channels across lane groups so eight
+      // consecutive lanes always hit eight different 16-byte positions of the swizzle.
+      const int sc = warp >> 1, cp = (warp & 1) * 32 + lane, c0 = 2 * cp;
+      const int wsel = (lane >> 2) & 1;  // channel this lane writes first
       float bt = 0.f;  // beta of token t, needed only after the prologue
       if (t < kC && t < cv) bt = p.beta[(size_t)(t0 + t) * p.Hv + h];
       wait_bar(p, s, B_G_FULL, gc & 1);
       float e0[16], e1[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const int r = qt * 16 + j;
+        const int r = sc * 16 + j;
         const float2 gv = *reinterpret_cast<const float2*>(Gs + r * kK + c0);
         e0[j] = (r < cv) ? __expf(gv.x) : 1.f;  // padded rows: decay 1
         e1[j] = (r < cv) ? __expf(gv.y) : 1.f;
@@ -348,47 +356,94 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       float pm0 = 1.f, pm1 = 1.f;
 #pragma unroll
       for (int j = 0; j < 16; ++j) { pm0 *= e0[j]; pm1 *= e1[j]; }
-      float pi0[4], pi1[4];
-#pragma unroll
-      for (int q2 = 0; q2 < 4; ++q2) {
-        pi0[q2] = __shfl_sync(0xffffffffu, pm0, (lane & ~3) | q2);
-        pi1[q2] = __shfl_sync(0xffffffffu, pm1, (lane & ~3) | q2);
-      }
-      const float E0 = (qt > 0 ? pi0[0] : 1.f) * (qt > 1 ? pi0[1] : 1.f) * (qt > 2 ? pi0[2] : 1.f);
-      const float E1 = (qt > 0 ? pi1[0] : 1.f) * (qt > 1 ? pi1[1] : 1.f) * (qt > 2 ? pi1[2] : 1.f);
-      const float F0 = (qt < 1 ? pi0[1] : 1.f) * (qt < 2 ? pi0[2] : 1.f) * (qt < 3 ? pi0[3] : 1.f);
-      const float F1 = (qt < 1 ? pi1[1] : 1.f) * (qt < 2 ? pi1[2] : 1.f) * (qt < 3 ? pi1[3] : 1.f);
-#pragma unroll
-      for (int q2 = 0; q2 < 4; ++q2) {
-        const uint32_t m0 = __ballot_sync(0xffffffffu, qt == 0 && !(pi0[q2] >= kSafeMin));
-        const uint32_t m1 = __ballot_sync(0xffffffffu, qt == 0 && !(pi1[q2] >= kSafeMin));
-        uint32_t comp = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          comp |= (((m0 >> (4 * j)) & 1u) << (2 * j)) | (((m1 >> (4 * j)) & 1u) << (2 * j + 1));
-        if (lane == 0) s->unsafe[q2][warp] = (uint16_t)comp;
-      }
+      // exchange the sub-chunk products through the Tm buffer (idle until the inverse)
+      float* pis = reinterpret_cast<float*>(sm + OFF_TM);
+      *reinterpret_cast<float2*>(pis + sc * kK + c0) = make_float2(pm0, pm1);
       wait_bar(p, s, B_QK_FULL, gc & 1);
       // QG buffer and this gamma buffer are free once MMA-1b of the previous chunk ran
       if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
-      if (qt == 0) {
-        s->gamma[gc & 1][c0] = pi0[0] * pi0[1] * pi0[2] * pi0[3];
-        s->gamma[gc & 1][c0 + 1] = pi1[0] * pi1[1] * pi1[2] * pi1[3];
-      }
-      named_bar(BAR_IG, kIG);  // every thread has read g: CB blocks 1-2 may be overwritten
-      {
-        const int sc = qt;
-        float kap0[16], kap1[16];
-        {
-          float a0 = 1.f, a1 = 1.f;
+      named_bar(BAR_IG, kIG);  // products visible; every thread has read g (CB 1-2 free)
+      float pi0[4], pi1[4];
 #pragma unroll
-          for (int j = 15; j >= 0; --j) {
-            kap0[j] = a0; a0 *= e0[j];
-            kap1[j] = a1; a1 *= e1[j];
+      for (int q2 = 0; q2 < 4; ++q2) {
+        const float2 pv = *reinterpret_cast<const float2*>(pis + q2 * kK + c0);
+        pi0[q2] = pv.x;
+        pi1[q2] = pv.y;
+      }
+      const float E0 = (sc > 0 ? pi0[0] : 1.f) * (sc > 1 ? pi0[1] : 1.f) * (sc > 2 ? pi0[2] : 1.f);
+      const float E1 = (sc > 0 ? pi1[0] : 1.f) * (sc > 1 ? pi1[1] : 1.f) * (sc > 2 ? pi1[2] : 1.f);
+      const float F0 = (sc < 1 ? pi0[1] : 1.f) * (sc < 2 ? pi0[2] : 1.f) * (sc < 3 ? pi0[3] : 1.f);
+      const float F1 = (sc < 1 ? pi1[1] : 1.f) * (sc < 2 ? pi1[2] : 1.f) * (sc < 3 ? pi1[3] : 1.f);
+      if (sc == 0) {  // warps 0-1: unsafe masks and gamma for their 64 channels
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) {
+          const uint32_t m0 = __ballot_sync(0xffffffffu, !(pi0[q2] >= kSafeMin));
+          const uint32_t m1 = __ballot_sync(0xffffffffu, !(pi1[q2] >= kSafeMin));
+          if (lane < 4) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int l = 0; l < 8; ++l)
+              word |= (((m0 >> (8 * lane + l)) & 1u) << (2 * l)) |
+                      (((m1 >> (8 * lane + l)) & 1u) << (2 * l + 1));
+            s->unsafe[q2][(warp & 1) * 4 + lane] = (uint16_t)word;
           }
         }
+        *reinterpret_cast<float2*>(&s->gamma[gc & 1][c0]) =
+            make_float2(pi0[0] * pi0[1] * pi0[2] * pi0[3], pi1[0] * pi1[1] * pi1[2] * pi1[3]);
+      }
+      {
         const float ip0 = (pm0 >= kSafeMin) ? 1.f / pm0 : 0.f;  // pm = pi of this sub-chunk
         const float ip1 = (pm1 >= kSafeMin) ? 1.f / pm1 : 0.f;
+        // pass A, tokens in descending order: kap (exclusive product to the sub-chunk
+        // end) needs no array.  Writes CB block 0 (k kap), block 2 (k/rho on safe
+        // channels) and, by sub-chunk, the block-1 reference variants.
+        float ka0 = 1.f, ka1 = 1.f;
+#pragma unroll
+        for (int jh = 1; jh >= 0; --jh) {
+          float kk[2][8];
+#pragma unroll
+          for (int u = 7; u >= 0; --u) {
+            const int j = jh * 8 + u, r = sc * 16 + j;
+            const uint32_t kv = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128)) : 0u;
+            kk[0][u] = bf_bits(kv & 0xFFFFu) * ka0;
+            kk[1][u] = bf_bits(kv >> 16) * ka1;
+            ka0 *= e0[j];
+            ka1 *= e1[j];
+          }
+          const uint32_t cj = sc * 2 + jh;
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int c = c2 ^ wsel;
+            const int row = c0 + c;
+            const float ip = c ? ip1 : ip0;
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x[u] = c ? kk[1][u] : kk[0][u];
+            st_chunk(sm, OFF_CB + sw128_off(row, cj), pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                     pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+            st_chunk(sm, OFF_CB + 32768 + sw128_off(row, cj), pack_bf16x2(x[0] * ip, x[1] * ip),
+                     pack_bf16x2(x[2] * ip, x[3] * ip), pack_bf16x2(x[4] * ip, x[5] * ip),
+                     pack_bf16x2(x[6] * ip, x[7] * ip));
+            if (sc == 0) {
+              const float f1 = c ? pi1[1] : pi0[1], f12 = f1 * (c ? pi1[2] : pi0[2]);
+              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 0 + jh), pack_bf16x2(x[0] * f1, x[1] * f1),
+                       pack_bf16x2(x[2] * f1, x[3] * f1), pack_bf16x2(x[4] * f1, x[5] * f1),
+                       pack_bf16x2(x[6] * f1, x[7] * f1));
+              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 2 + jh), pack_bf16x2(x[0] * f12, x[1] * f12),
+                       pack_bf16x2(x[2] * f12, x[3] * f12), pack_bf16x2(x[4] * f12, x[5] * f12),
+                       pack_bf16x2(x[6] * f12, x[7] * f12));
+            } else if (sc == 1) {
+              const float f2 = c ? pi1[2] : pi0[2];
+              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 4 + jh), pack_bf16x2(x[0] * f2, x[1] * f2),
+                       pack_bf16x2(x[2] * f2, x[3] * f2), pack_bf16x2(x[4] * f2, x[5] * f2),
+                       pack_bf16x2(x[6] * f2, x[7] * f2));
+            } else if (sc == 3) {
+              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 6 + jh), 0u, 0u, 0u, 0u);
+            }
+          }
+        }
+        // pass B, ascending: rho (inclusive product from the sub-chunk start); q and k
+        // rows of the MMA-AB operand in place, and KG, QG.
         const float qs0 = p.scale * E0, qs1 = p.scale * E1;
         float rho0 = 1.f, rho1 = 1.f;
 #pragma unroll
@@ -397,50 +452,23 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int r = sc * 16 + jh * 8 + u;
-            const uint32_t* kp = reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128));
-            const uint32_t* qp = reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(64 + r, c0, 128));
-            kw[u] = (r < cv) ? *kp : 0u;
-            qw[u] = (r < cv) ? *qp : 0u;
+            kw[u] = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128)) : 0u;
+            qw[u] = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(64 + r, c0, 128)) : 0u;
           }
-          uint32_t o_cb0[2][4], o_dg[2][4], o_kg[2][4], o_qg[2][4], o_m1[2][4], o_m12[2][4], o_m2[2][4];
+          float kg[2][8], qg[2][8];
 #pragma unroll
-          for (int u = 0; u < 8; u += 2) {
-            float kk[2][2], dg[2][2], kg[2][2], qg[2][2], m1[2][2], m12[2][2], m2[2][2];
-#pragma unroll
-            for (int v2 = 0; v2 < 2; ++v2) {
-              const int j = jh * 8 + u + v2;
-              rho0 *= e0[j];
-              rho1 *= e1[j];
-              const float k0 = bf_bits(kw[u + v2] & 0xFFFFu), k1 = bf_bits(kw[u + v2] >> 16);
-              const float q0 = bf_bits(qw[u + v2] & 0xFFFFu), q1 = bf_bits(qw[u + v2] >> 16);
-              const float kr0 = k0 * rho0, kr1 = k1 * rho1, qr0 = q0 * rho0, qr1 = q1 * rho1;
-              kw[u + v2] = pack_bf16x2(kr0, kr1);
-              qw[u + v2] = pack_bf16x2(qr0, qr1);
-              kk[0][v2] = k0 * kap0[j];
-              kk[1][v2] = k1 * kap1[j];
-              dg[0][v2] = kk[0][v2] * ip0;
-              dg[1][v2] = kk[1][v2] * ip1;
-              kg[0][v2] = kr0 * E0;
-              kg[1][v2] = kr1 * E1;
-              qg[0][v2] = qr0 * qs0;
-              qg[1][v2] = qr1 * qs1;
-              m1[0][v2] = kk[0][v2] * pi0[1];
-              m1[1][v2] = kk[1][v2] * pi1[1];
-              m12[0][v2] = m1[0][v2] * pi0[2];
-              m12[1][v2] = m1[1][v2] * pi1[2];
-              m2[0][v2] = kk[0][v2] * pi0[2];
-              m2[1][v2] = kk[1][v2] * pi1[2];
-            }
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              o_cb0[c][u / 2] = pack_bf16x2(kk[c][0], kk[c][1]);
-              o_dg[c][u / 2] = pack_bf16x2(dg[c][0], dg[c][1]);
-              o_kg[c][u / 2] = pack_bf16x2(kg[c][0], kg[c][1]);
-              o_qg[c][u / 2] = pack_bf16x2(qg[c][0], qg[c][1]);
-              o_m1[c][u / 2] = pack_bf16x2(m1[c][0], m1[c][1]);
-              o_m12[c][u / 2] = pack_bf16x2(m12[c][0], m12[c][1]);
-              o_m2[c][u / 2] = pack_bf16x2(m2[c][0], m2[c][1]);
-            }
+          for (int u = 0; u < 8; ++u) {
+            const int j = jh * 8 + u;
+            rho0 *= e0[j];
+            rho1 *= e1[j];
+            const float kr0 = bf_bits(kw[u] & 0xFFFFu) * rho0, kr1 = bf_bits(kw[u] >> 16) * rho1;
+            const float qr0 = bf_bits(qw[u] & 0xFFFFu) * rho0, qr1 = bf_bits(qw[u] >> 16) * rho1;
+            kw[u] = pack_bf16x2(kr0, kr1);
+            qw[u] = pack_bf16x2(qr0, qr1);
+            kg[0][u] = kr0 * E0;
+            kg[1][u] = kr1 * E1;
+            qg[0][u] = qr0 * qs0;
+            qg[1][u] = qr1 * qs1;
           }
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -450,20 +478,16 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           }
           const uint32_t cj = sc * 2 + jh;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int c = c2 ^ wsel;
             const int row = c0 + c;
-            st_chunk(sm, OFF_CB + sw128_off(row, cj), o_cb0[c][0], o_cb0[c][1], o_cb0[c][2], o_cb0[c][3]);
-            st_chunk(sm, OFF_CB + 32768 + sw128_off(row, cj), o_dg[c][0], o_dg[c][1], o_dg[c][2], o_dg[c][3]);
-            st_chunk(sm, OFF_KG + sw128_off(row, cj), o_kg[c][0], o_kg[c][1], o_kg[c][2], o_kg[c][3]);
-            st_chunk(sm, OFF_QG + sw128_off(row, cj), o_qg[c][0], o_qg[c][1], o_qg[c][2], o_qg[c][3]);
-            if (sc == 0) {
-              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 0 + jh), o_m1[c][0], o_m1[c][1], o_m1[c][2], o_m1[c][3]);
-              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 2 + jh), o_m12[c][0], o_m12[c][1], o_m12[c][2], o_m12[c][3]);
-            } else if (sc == 1) {
-              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 4 + jh), o_m2[c][0], o_m2[c][1], o_m2[c][2], o_m2[c][3]);
-            } else if (sc == 3) {
-              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 6 + jh), 0u, 0u, 0u, 0u);
-            }
+            float a[8], b[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) { a[u] = c ? kg[1][u] : kg[0][u]; b[u] = c ? qg[1][u] : qg[0][u]; }
+            st_chunk(sm, OFF_KG + sw128_off(row, cj), pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                     pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+            st_chunk(sm, OFF_QG + sw128_off(row, cj), pack_bf16x2(b[0], b[1]), pack_bf16x2(b[2], b[3]),
+                     pack_bf16x2(b[4], b[5]), pack_bf16x2(b[6], b[7]));
           }
         }
       }
@@ -488,11 +512,12 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // (overlaps MMA-AB, which only reads CB)
       if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int c = c2 ^ wsel;
         const float f = c ? F1 : F0;
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
-          const int j = qt * 2 + jj;
+          const int j = sc * 2 + jj;
           const uint4 src = *reinterpret_cast<const uint4*>(sm + OFF_CB + sw128_off(c0 + c, j));
           const uint32_t in[4] = {src.x, src.y, src.z, src.w};
           uint32_t w[4];
@@ -694,19 +719,24 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         blk_store(Xs, 48, 0, acc2, -1.f, lane);
       }
       named_bar(BAR_IG, kIG);
-      // Tm = X Diag(beta) -> bf16 -> TM   (thread: row r, columns 16*qq..)
+      // Tm = X Diag(beta) -> bf16 -> TM   (thread: row r = t & 63, columns 16*qq..16*qq+15)
       {
-        const int r = t >> 2, qq = t & 3;
+        const int r = t & 63, qq = t >> 6;
 #pragma unroll
         for (int u2 = 0; u2 < 2; ++u2) {
           const int j = qq * 2 + u2;
+          const float4 xa = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8));
+          const float4 xb = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8 + 4));
+          const float4 ba = *reinterpret_cast<const float4*>(&s->beta[j * 8]);
+          const float4 bb4 = *reinterpret_cast<const float4*>(&s->beta[j * 8 + 4]);
+          const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+          const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb4.x, bb4.y, bb4.z, bb4.w};
           uint32_t w[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int i0 = j * 8 + u * 2;
-            const float v0 = (i0 <= r) ? Xs[sidx(r, i0)] * s->beta[i0] : 0.f;
-            const float v1 = (i0 + 1 <= r) ? Xs[sidx(r, i0 + 1)] * s->beta[i0 + 1] : 0.f;
-            w[u] = pack_bf16x2(v0, v1);
+            w[u] = pack_bf16x2((i0 <= r) ? xv[2 * u] * bv[2 * u] : 0.f,
+                               (i0 + 1 <= r) ? xv[2 * u + 1] * bv[2 * u + 1] : 0.f);
           }
           st_chunk(sm, OFF_TM + sw128_off(r, j), w[0], w[1], w[2], w[3]);
         }
@@ -913,7 +943,13 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
 #pragma unroll
-            for (int u = 0; u < 16; ++u) sv[q4][u] *= gm[(kh2 * 4 + q4) * 16 + u];
+            for (int u4 = 0; u4 < 4; ++u4) {
+              const float4 g4 = *reinterpret_cast<const float4*>(gm + (kh2 * 4 + q4) * 16 + u4 * 4);
+              sv[q4][u4 * 4 + 0] *= g4.x;
+              sv[q4][u4 * 4 + 1] *= g4.y;
+              sv[q4][u4 * 4 + 2] *= g4.z;
+              sv[q4][u4 * 4 + 3] *= g4.w;
+            }
             tmem_st16(taddr_q + TM_S + (kh2 * 4 + q4) * 16, sv[q4]);
           }
         }
