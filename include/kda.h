@@ -153,6 +153,38 @@ kda_status_t kda_decode(const kda_desc_t *desc, const void *q, const void *k, co
                         const int32_t *state_indices, void *o, void *workspace,
                         size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Allocation-free prefill.  The pages have no counterpart of this entry point.
+ *
+ * For callers that cannot allocate device memory when they run the prefill: code
+ * replayed inside a captured CUDA graph, plug-in hosts whose allocator belongs to
+ * someone else, or real-time paths that forbid allocation after start-up.  It
+ * takes the same arguments as kda_chunk_prefill() minus the workspace: the scratch
+ * the prefill needs (status word, work counter, sequence order) comes from a fixed
+ * array of KDA_NOALLOC_SCRATCH_BYTES bytes in the library's device memory, which
+ * every GPU that loads the library holds until the process exits.  The call never
+ * calls cudaMalloc, cudaFree or any allocating library routine.
+ *
+ *  - Limit: num_seqs <= KDA_NOALLOC_MAX_SEQS; a larger batch returns
+ *    KDA_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
+ *  - The first call on a device looks up that device's copy of the array
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array and it keeps the last call's
+ *    contents (each call clears what must start at zero).  Calls that overlap on
+ *    the GPU (different streams, no ordering between them) race on it: order them.
+ *  - Device-data errors are recorded in the shared array's status word, which this
+ *    entry point offers no way to read back; use kda_chunk_prefill() with a
+ *    workspace to diagnose inputs.
+ */
+#define KDA_NOALLOC_MAX_SEQS 16384
+#define KDA_NOALLOC_SCRATCH_BYTES (256 + 4 * KDA_NOALLOC_MAX_SEQS)
+kda_status_t kda_chunk_prefill_noalloc(const kda_desc_t *desc, const void *q, const void *k,
+                                       const void *v, const float *g, const float *beta,
+                                       const int32_t *cu_seqlens, void *state,
+                                       const int32_t *state_indices, void *final_state,
+                                       void *o, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads the device status word left in `workspace`
  * by the last prefill or decode call that used it.  Returns KDA_OK or
  * KDA_ERR_DEVICE_DATA (raw bits in *bits_out if bits_out != NULL), or

@@ -49,7 +49,8 @@ class KdaDesc(ctypes.Structure):
 
 
 EXPORTS = ("kda_chunk_prefill_workspace_size", "kda_decode_workspace_size", "kda_chunk_prefill",
-           "kda_decode", "kda_read_device_status", "kda_chunk_prefill_path", "kda_status_string")
+           "kda_decode", "kda_read_device_status", "kda_chunk_prefill_path", "kda_status_string",
+           "kda_chunk_prefill_noalloc")
 
 _lib = None
 
@@ -84,6 +85,8 @@ def load(build_if_missing: bool = True):
     lib.kda_chunk_prefill_path.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_chunk_prefill_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P]
+    lib.kda_chunk_prefill_noalloc.restype = ctypes.c_int
     _lib = lib
     return lib
 
