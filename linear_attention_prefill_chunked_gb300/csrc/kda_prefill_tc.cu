@@ -72,11 +72,11 @@ constexpr uint32_t OFF_KR = 163840;   // [128 ch][64 tokens]  KR              (K
 constexpr uint32_t OFF_ST = 180224;   // [2 K-atoms][128 v][128 B]  S^T bf16   (K-major A)
 constexpr uint32_t OFF_UT = 212992;   // [128 v][64 tokens]   U^T bf16        (K-major A)
 constexpr uint32_t OFF_SMALL = 229376;
-// CB blocks 1 and 2 are dead from MMA-AB completion to the next prologue's
-// writes; they hold, in turn: the fp32 A and B rows and X = (I + A)^-1 of the
-// inverse (AS, XS), then the TMA-staged gate g of the next chunk ([64][128] fp32).
-constexpr uint32_t OFF_AS = OFF_CB + 16384;
-constexpr uint32_t OFF_XS = OFF_CB + 32768;
+// After MMA-AB completes, the q/k buffer holds the fp32 scratch of the inverse
+// (A and B rows, then X = (I + A)^-1) until Tm is written, and CB blocks 1-2 hold
+// the TMA-staged gate g of the next chunk ([64][128] fp32) until its prologue.
+constexpr uint32_t OFF_AS = OFF_QK;
+constexpr uint32_t OFF_XS = OFF_QK + 16384;
 constexpr uint32_t OFF_G = OFF_CB + 16384;
 
 // ---- TMEM columns ------------------------------------------------------------------
@@ -237,8 +237,7 @@ __device__ __forceinline__ void blk_store(float* M, int r, int c, const float ac
 // thread 0 also schedules items and issues every TMA load, at points where the
 // group already knows the target buffer is free.
 // ======================================================================================
-struct Loader {  // state of thread 0 only
-  ItemInfo lq[kRing];
+struct Loader {  // state of thread 0 only (kept in registers: no indexed members)
   int pushed = 0;
   bool fetched_done = false;
   uint32_t n_qk = 0, n_g = 0, n_v = 0;  // chunks whose loads were issued
@@ -249,7 +248,6 @@ struct Loader {  // state of thread 0 only
     if (pushed >= kRing) wait_bar(p, s, B_ITEM_EMPTY + slot, ((pushed / kRing) - 1) & 1);
     const ItemInfo info = fetch_item(p, s);
     s->ring[slot] = info;
-    lq[slot] = info;
     mbar_arrive(&s->bar[B_ITEM_FULL + slot]);
     ++pushed;
     if (info.done) fetched_done = true;
@@ -273,15 +271,16 @@ struct Loader {  // state of thread 0 only
     tma_load_3d(sm + OFF_VB + 8192, &p.tm_v, &s->bar[B_V_FULL], 64, h, t0);
     ++n_v;
   }
-  // Chunk after (item k, local chunk lc), if already known without blocking.
-  __device__ bool next_chunk(int k, int lc, int& kh, int& h, int& t0) const {
-    const ItemInfo& cur = lq[k % kRing];
+  // Chunk after (item k, local chunk lc), if already known without blocking.  Ring
+  // slots k and k+1 cannot be refilled before this thread starts item k+2.
+  __device__ bool next_chunk(const Small* s, int k, int lc, int& kh, int& h, int& t0) const {
+    const ItemInfo& cur = s->ring[k % kRing];
     if (lc + 1 < cur.nchunks) {
       kh = cur.kh; h = cur.h; t0 = (int)(cur.bos + (int64_t)(lc + 1) * kC);
       return true;
     }
     if (pushed > k + 1) {
-      const ItemInfo& nx = lq[(k + 1) % kRing];
+      const ItemInfo& nx = s->ring[(k + 1) % kRing];
       if (!nx.done && nx.nchunks > 0) {
         kh = nx.kh; h = nx.h; t0 = (int)nx.bos;
         return true;
@@ -331,7 +330,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         if (ld.n_qk == gc) ld.load_qk(p, sm, s, kh, (int)t0);
         if (ld.n_g == gc) ld.load_g(p, sm, s, h, (int)t0);
         if (ld.n_v == gc) ld.load_v(p, sm, s, h, (int)t0);
-        have_next = ld.next_chunk(k, lc, nkh, nh, nt0);
+        have_next = ld.next_chunk(s, k, lc, nkh, nh, nt0);
         if (have_next) ld.prefetch_l2(p, nkh, nh, nt0);
       }
       __syncwarp();
@@ -411,7 +410,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             ka1 *= e1[j];
           }
           const uint32_t cj = sc * 2 + jh;
-#pragma unroll
+          // block-1 variants by sub-chunk: 0 -> k kap pi_1 (chunk jh) and k kap pi_1 pi_2
+          // (chunk 2+jh); 1 -> k kap pi_2 (chunk 4+jh); 3 -> zeros (chunk 6+jh); 2 -> none
+          const int nvar = (sc == 0) ? 2 : (sc == 2 ? 0 : 1);
+#pragma unroll 1
           for (int c2 = 0; c2 < 2; ++c2) {
             const int c = c2 ^ wsel;
             const int row = c0 + c;
@@ -424,21 +426,14 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             st_chunk(sm, OFF_CB + 32768 + sw128_off(row, cj), pack_bf16x2(x[0] * ip, x[1] * ip),
                      pack_bf16x2(x[2] * ip, x[3] * ip), pack_bf16x2(x[4] * ip, x[5] * ip),
                      pack_bf16x2(x[6] * ip, x[7] * ip));
-            if (sc == 0) {
-              const float f1 = c ? pi1[1] : pi0[1], f12 = f1 * (c ? pi1[2] : pi0[2]);
-              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 0 + jh), pack_bf16x2(x[0] * f1, x[1] * f1),
-                       pack_bf16x2(x[2] * f1, x[3] * f1), pack_bf16x2(x[4] * f1, x[5] * f1),
-                       pack_bf16x2(x[6] * f1, x[7] * f1));
-              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 2 + jh), pack_bf16x2(x[0] * f12, x[1] * f12),
-                       pack_bf16x2(x[2] * f12, x[3] * f12), pack_bf16x2(x[4] * f12, x[5] * f12),
-                       pack_bf16x2(x[6] * f12, x[7] * f12));
-            } else if (sc == 1) {
-              const float f2 = c ? pi1[2] : pi0[2];
-              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 4 + jh), pack_bf16x2(x[0] * f2, x[1] * f2),
-                       pack_bf16x2(x[2] * f2, x[3] * f2), pack_bf16x2(x[4] * f2, x[5] * f2),
-                       pack_bf16x2(x[6] * f2, x[7] * f2));
-            } else if (sc == 3) {
-              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, 6 + jh), 0u, 0u, 0u, 0u);
+            const float p1 = c ? pi1[1] : pi0[1], p2 = c ? pi1[2] : pi0[2];
+#pragma unroll 1
+            for (int e = 0; e < nvar; ++e) {
+              const float f = (sc == 0) ? (e ? p1 * p2 : p1) : (sc == 1 ? p2 : 0.f);
+              const int ch = (sc == 0) ? 2 * e + jh : (sc == 1 ? 4 + jh : 6 + jh);
+              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, ch), pack_bf16x2(x[0] * f, x[1] * f),
+                       pack_bf16x2(x[2] * f, x[3] * f), pack_bf16x2(x[4] * f, x[5] * f),
+                       pack_bf16x2(x[6] * f, x[7] * f));
             }
           }
         }
@@ -505,7 +500,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           mma_bf16(tbase + TM_AB, a, b, idesc, st > 0 ? 1u : 0u);
         }
         mma_commit(&s->bar[B_AB_DONE]);
-        if (have_next) tma_prefetch_3d(&p.tm_g, 0, nh, nt0);  // gate of the next chunk -> L2
       }
       __syncwarp();
       // KR = (k kap) F_s : scaled copy of this thread's CB block-0 chunks into KR
@@ -530,7 +524,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // ------------------------------------------------------------- A / B rows
       wait_bar(p, s, B_AB_DONE, gc & 1);
       tc_fence_after();
-      if (t == 0 && have_next && ld.n_qk == gc + 1) ld.load_qk(p, sm, s, nkh, nt0);  // QK free
+      if (t == 0 && have_next && ld.n_g == gc + 1) ld.load_g(p, sm, s, nh, nt0);  // CB 1-2 free
       __syncwarp();
       uint32_t any_unsafe = 0;
 #pragma unroll
@@ -672,53 +666,49 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // (one column per lane, two blocks per warp), then
       // X_ab = -X_aa * sum_{b<=c<a} A_ac X_cb, one block per warp per level.
       if (warp < 2) {
+        // lane = column j of diagonal block (2 blocks per warp); rows of A are read
+        // as broadcast float4 and x[rr] = -sum_{i<rr} A[rr][i] x[i] row by row.
         const int o = (warp * 2 + (lane >> 4)) * 16, j = lane & 15;
         float xv[16];
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) xv[rr] = (rr == j) ? 1.f : 0.f;
 #pragma unroll
-        for (int i = 0; i < 15; ++i)
+        for (int rr = 1; rr < 16; ++rr) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int rr = i + 1; rr < 16; ++rr) xv[rr] = fmaf(-As[sidx(o + rr, o + i)], xv[i], xv[rr]);
+          for (int i4 = 0; i4 < (rr + 3) / 4; ++i4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(As + sidx(o + rr, o + 4 * i4));
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) Xs[sidx(o + rr, o + j)] = xv[rr];
+            for (int u = 0; u < 4; ++u)
+              if (4 * i4 + u < rr) acc[u] = fmaf(av[u], xv[4 * i4 + u], acc[u]);
+          }
+          const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+          if (rr > j) xv[rr] = -sum;
+        }
+        if (lane < 32) {
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) Xs[sidx(o + rr, o + j)] = xv[rr];
+        }
       }
       named_bar(BAR_IG, kIG);
-      if (warp < 3) {  // X_{a+1,a}
-        const int a = warp;
-        float acc[2][4] = {};
-        blk_mma(acc, As, (a + 1) * 16, a * 16, Xs, a * 16, a * 16, lane);
-        blk_store(As, 0, 16 * (1 + warp), acc, 1.f, lane);  // stage P in A's upper block (0, 1+w)
-        __syncwarp();
-        float acc2[2][4] = {};
-        blk_mma(acc2, Xs, (a + 1) * 16, (a + 1) * 16, As, 0, 16 * (1 + warp), lane);
-        blk_store(Xs, (a + 1) * 16, a * 16, acc2, -1.f, lane);
+      // level d: X_{a+d,a} = -X_{a+d,a+d} P, P = sum_{a<=m<a+d} A_{a+d,m} X_{m,a} (warp a);
+      // P is staged in the unused upper block (d-1, d+a) of A.
+#pragma unroll 1
+      for (int d = 1; d <= 3; ++d) {
+        if (warp <= 3 - d) {
+          const int a = warp;
+          float acc[2][4] = {};
+#pragma unroll 1
+          for (int m = a; m < a + d; ++m) blk_mma(acc, As, (a + d) * 16, m * 16, Xs, m * 16, a * 16, lane);
+          blk_store(As, (d - 1) * 16, 16 * (d + a), acc, 1.f, lane);
+          __syncwarp();
+          float acc2[2][4] = {};
+          blk_mma(acc2, Xs, (a + d) * 16, (a + d) * 16, As, (d - 1) * 16, 16 * (d + a), lane);
+          blk_store(Xs, (a + d) * 16, a * 16, acc2, -1.f, lane);
+        }
+        named_bar(BAR_IG, kIG);
       }
-      named_bar(BAR_IG, kIG);
-      if (warp < 2) {  // X_{a+2,a}
-        const int a = warp;
-        float acc[2][4] = {};
-        blk_mma(acc, As, (a + 2) * 16, a * 16, Xs, a * 16, a * 16, lane);
-        blk_mma(acc, As, (a + 2) * 16, (a + 1) * 16, Xs, (a + 1) * 16, a * 16, lane);
-        blk_store(As, 16, 32 + 16 * warp, acc, 1.f, lane);  // stage in (1, 2+w)
-        __syncwarp();
-        float acc2[2][4] = {};
-        blk_mma(acc2, Xs, (a + 2) * 16, (a + 2) * 16, As, 16, 32 + 16 * warp, lane);
-        blk_store(Xs, (a + 2) * 16, a * 16, acc2, -1.f, lane);
-      }
-      named_bar(BAR_IG, kIG);
-      if (warp == 0) {  // X_{3,0}
-        float acc[2][4] = {};
-        blk_mma(acc, As, 48, 0, Xs, 0, 0, lane);
-        blk_mma(acc, As, 48, 16, Xs, 16, 0, lane);
-        blk_mma(acc, As, 48, 32, Xs, 32, 0, lane);
-        blk_store(As, 32, 48, acc, 1.f, lane);  // stage in (2, 3)
-        __syncwarp();
-        float acc2[2][4] = {};
-        blk_mma(acc2, Xs, 48, 48, As, 32, 48, lane);
-        blk_store(Xs, 48, 0, acc2, -1.f, lane);
-      }
-      named_bar(BAR_IG, kIG);
       // Tm = X Diag(beta) -> bf16 -> TM   (thread: row r = t & 63, columns 16*qq..16*qq+15)
       {
         const int r = t & 63, qq = t >> 6;
@@ -744,7 +734,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       fence_async_smem();
       named_bar(BAR_IG, kIG);
       // ------------------------------------------------------------- U~ and W
-      if (t == 0 && have_next && ld.n_g == gc + 1) ld.load_g(p, sm, s, nh, nt0);  // AS/XS dead
+      if (t == 0 && have_next && ld.n_qk == gc + 1) ld.load_qk(p, sm, s, nkh, nt0);  // AS/XS dead
       if (warp == 0) {
         wait_bar(p, s, B_V_FULL, gc & 1);
         if (gc > 0) wait_bar(p, s, B_E1, (gc - 1) & 1);  // U region read by the recurrence
@@ -876,31 +866,26 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       continue;
     }
     // ---- initial state: S^T row v -> ST (bf16) and TMEM S (pre-decayed by gamma of chunk 0)
-    {
-      float h0[kK];
+    wait_bar(p, s, B_GAMMA0 + (gc & 1), (gc >> 1) & 1);
+#pragma unroll 1
+    for (int kq = 0; kq < 8; ++kq) {
+      float sv[16];
 #pragma unroll
-      for (int c = 0; c < kK; ++c) h0[c] = src ? to_f32(src[(size_t)c * kV + v]) : 0.f;
-      wait_bar(p, s, B_GAMMA0 + (gc & 1), (gc >> 1) & 1);
+      for (int u = 0; u < 16; ++u) sv[u] = src ? to_f32(src[(size_t)(kq * 16 + u) * kV + v]) : 0.f;
+      uint32_t w[8];
 #pragma unroll
-      for (int kq = 0; kq < 8; ++kq) {
-        float sv[16];
+      for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(sv[2 * u], sv[2 * u + 1]);
+      const uint32_t cj = kq * 2;
+      st_chunk(sm, OFF_ST + (cj >> 3) * 16384 + sw128_off(v, cj & 7), w[0], w[1], w[2], w[3]);
+      st_chunk(sm, OFF_ST + ((cj + 1) >> 3) * 16384 + sw128_off(v, (cj + 1) & 7), w[4], w[5], w[6], w[7]);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) sv[u] = h0[kq * 16 + u];
-        uint32_t w[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(sv[2 * u], sv[2 * u + 1]);
-        const uint32_t cj = kq * 2;
-        st_chunk(sm, OFF_ST + (cj >> 3) * 16384 + sw128_off(v, cj & 7), w[0], w[1], w[2], w[3]);
-        st_chunk(sm, OFF_ST + ((cj + 1) >> 3) * 16384 + sw128_off(v, (cj + 1) & 7), w[4], w[5], w[6], w[7]);
-#pragma unroll
-        for (int u = 0; u < 16; ++u) sv[u] *= s->gamma[gc & 1][kq * 16 + u];
-        tmem_st16(taddr_q + TM_S + kq * 16, sv);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      fence_async_smem();
-      named_bar(BAR_RG, kRG);
+      for (int u = 0; u < 16; ++u) sv[u] *= s->gamma[gc & 1][kq * 16 + u];
+      tmem_st16(taddr_q + TM_S + kq * 16, sv);
     }
+    tmem_st_wait();
+    tc_fence_before();
+    fence_async_smem();
+    named_bar(BAR_RG, kRG);
 
     bool stop = false;
     for (int lc = 0; lc < info.nchunks; ++lc, ++gc) {
