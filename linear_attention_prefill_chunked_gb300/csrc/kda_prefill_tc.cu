@@ -87,7 +87,7 @@ constexpr uint32_t TM_AB = 320;  // A/B result (192), later W^T (64)
 
 constexpr int kIG = 256;  // intra-group threads (warps 0-7)
 constexpr int kRG = 128;  // recurrence-group threads (warps 8-11)
-constexpr uint32_t BAR_IG = 1, BAR_RG = 2;
+constexpr uint32_t BAR_IG = 1, BAR_RG = 2, BAR_A = 3;
 
 enum Bar {
   B_QK_FULL, B_V_FULL, B_G_FULL, B_AB_DONE, B_UW_DONE, B_GAMMA0, B_GAMMA1, B_REC_READY,
@@ -101,12 +101,21 @@ struct ItemInfo {
   int32_t done, pad;
 };
 
+// Scheduling state of the intra group's thread 0, kept in shared memory so that it
+// holds no registers across the chunk loop.
+struct LoaderState {
+  int32_t pushed, fetched_done;
+  uint32_t n_qk, n_g, n_v;                // chunks whose loads were issued
+  int32_t have_next, nkh, nh, nt0, ncv;   // the chunk after the current one, if known
+};
+
 struct Small {
   uint64_t bar[B_COUNT];
   ItemInfo ring[kRing];
   alignas(16) float beta[kC];      // read as float4
   alignas(16) float gamma[2][kK];  // read as float4
-  uint16_t unsafe[4][8];  // [sub-chunk][16-channel group] bitmask
+  uint32_t unsafe[4][2][2];  // [sub-chunk][half][parity]: bit l = channel 64*half + 2l + parity
+  LoaderState ld;
   uint32_t tmem_base;
   uint32_t abort;
 };
@@ -237,20 +246,19 @@ __device__ __forceinline__ void blk_store(float* M, int r, int c, const float ac
 // thread 0 also schedules items and issues every TMA load, at points where the
 // group already knows the target buffer is free.
 // ======================================================================================
-struct Loader {  // state of thread 0 only (kept in registers: no indexed members)
-  int pushed = 0;
-  bool fetched_done = false;
-  uint32_t n_qk = 0, n_g = 0, n_v = 0;  // chunks whose loads were issued
+struct Loader {  // used by thread 0 only
+  LoaderState* st;
 
   __device__ void push_one(const TcParams& p, Small* s) {
-    if (fetched_done) return;
+    if (st->fetched_done) return;
+    const int pushed = st->pushed;
     const int slot = pushed % kRing;
     if (pushed >= kRing) wait_bar(p, s, B_ITEM_EMPTY + slot, ((pushed / kRing) - 1) & 1);
     const ItemInfo info = fetch_item(p, s);
     s->ring[slot] = info;
     mbar_arrive(&s->bar[B_ITEM_FULL + slot]);
-    ++pushed;
-    if (info.done) fetched_done = true;
+    st->pushed = pushed + 1;
+    if (info.done) st->fetched_done = 1;
   }
   __device__ void load_qk(const TcParams& p, uint8_t* sm, Small* s, int kh, int t0) {
     mbar_expect_tx(&s->bar[B_QK_FULL], 32768);
@@ -258,31 +266,33 @@ struct Loader {  // state of thread 0 only (kept in registers: no indexed member
     tma_load_3d(sm + OFF_QK + 16384, &p.tm_k, &s->bar[B_QK_FULL], 64, kh, t0);
     tma_load_3d(sm + OFF_QK + 8192, &p.tm_q, &s->bar[B_QK_FULL], 0, kh, t0);
     tma_load_3d(sm + OFF_QK + 24576, &p.tm_q, &s->bar[B_QK_FULL], 64, kh, t0);
-    ++n_qk;
+    ++st->n_qk;
   }
   __device__ void load_g(const TcParams& p, uint8_t* sm, Small* s, int h, int t0) {
     mbar_expect_tx(&s->bar[B_G_FULL], 32768);
     tma_load_3d(sm + OFF_G, &p.tm_g, &s->bar[B_G_FULL], 0, h, t0);
-    ++n_g;
+    ++st->n_g;
   }
   __device__ void load_v(const TcParams& p, uint8_t* sm, Small* s, int h, int t0) {
     mbar_expect_tx(&s->bar[B_V_FULL], 16384);
     tma_load_3d(sm + OFF_VB + 0, &p.tm_v, &s->bar[B_V_FULL], 0, h, t0);
     tma_load_3d(sm + OFF_VB + 8192, &p.tm_v, &s->bar[B_V_FULL], 64, h, t0);
-    ++n_v;
+    ++st->n_v;
   }
   // Chunk after (item k, local chunk lc), if already known without blocking.  Ring
   // slots k and k+1 cannot be refilled before this thread starts item k+2.
-  __device__ bool next_chunk(const Small* s, int k, int lc, int& kh, int& h, int& t0) const {
+  __device__ bool next_chunk(const Small* s, int k, int lc, int& kh, int& h, int& t0, int& cv) const {
     const ItemInfo& cur = s->ring[k % kRing];
     if (lc + 1 < cur.nchunks) {
       kh = cur.kh; h = cur.h; t0 = (int)(cur.bos + (int64_t)(lc + 1) * kC);
+      cv = (int)min((int64_t)kC, cur.eos - t0);
       return true;
     }
-    if (pushed > k + 1) {
+    if (st->pushed > k + 1) {
       const ItemInfo& nx = s->ring[(k + 1) % kRing];
       if (!nx.done && nx.nchunks > 0) {
         kh = nx.kh; h = nx.h; t0 = (int)nx.bos;
+        cv = (int)min((int64_t)kC, nx.eos - nx.bos);
         return true;
       }
     }
@@ -308,12 +318,14 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
   float* As = reinterpret_cast<float*>(sm + OFF_AS);
   float* Xs = reinterpret_cast<float*>(sm + OFF_XS);
   const float* Gs = reinterpret_cast<const float*>(sm + OFF_G);
-  Loader ld;
+  Loader ld{&s->ld};
   uint32_t gc = 0;
+  float bt_next = 0.f;  // beta of the next chunk, read one chunk ahead (threads 0-63)
+  bool bt_ok = false;
 
   for (int k = 0;; ++k) {
     if (t == 0) {
-      while (ld.pushed <= k + 1 && !ld.fetched_done) ld.push_one(p, s);
+      while (ld.st->pushed <= k + 1 && !ld.st->fetched_done) ld.push_one(p, s);
     }
     __syncwarp();
     const ItemInfo info = next_item(p, s, k, t == 0, BAR_IG, kIG);
@@ -324,14 +336,11 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       if (named_bar_any(BAR_IG, kIG, aborted(s))) { stop = true; break; }
       const int64_t t0 = info.bos + (int64_t)lc * kC;
       const int cv = (int)min((int64_t)kC, info.eos - t0);
-      int nkh = 0, nh = 0, nt0 = 0;
-      bool have_next = false;
-      if (t == 0) {
-        if (ld.n_qk == gc) ld.load_qk(p, sm, s, kh, (int)t0);
-        if (ld.n_g == gc) ld.load_g(p, sm, s, h, (int)t0);
-        if (ld.n_v == gc) ld.load_v(p, sm, s, h, (int)t0);
-        have_next = ld.next_chunk(s, k, lc, nkh, nh, nt0);
-        if (have_next) ld.prefetch_l2(p, nkh, nh, nt0);
+      if (t == 0) {  // loads of this chunk not issued ahead (first chunk, or no lookahead)
+        const LoaderState* L = ld.st;
+        if (L->n_qk == gc) ld.load_qk(p, sm, s, kh, (int)t0);
+        if (L->n_g == gc) ld.load_g(p, sm, s, h, (int)t0);
+        if (L->n_v == gc) ld.load_v(p, sm, s, h, (int)t0);
       }
       __syncwarp();
       // ------------------------------------------------------------- prologue
@@ -342,7 +351,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       const int sc = warp >> 1, cp = (warp & 1) * 32 + lane, c0 = 2 * cp;
       const int wsel = (lane >> 2) & 1;  // channel this lane writes first
       float bt = 0.f;  // beta of token t, needed only after the prologue
-      if (t < kC && t < cv) bt = p.beta[(size_t)(t0 + t) * p.Hv + h];
+      if (t < kC && t < cv) bt = bt_ok ? bt_next : p.beta[(size_t)(t0 + t) * p.Hv + h];
+      bt_ok = false;
       wait_bar(p, s, B_G_FULL, gc & 1);
       float e0[16], e1[16];
 #pragma unroll
@@ -358,6 +368,14 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // exchange the sub-chunk products through the Tm buffer (idle until the inverse)
       float* pis = reinterpret_cast<float*>(sm + OFF_TM);
       *reinterpret_cast<float2*>(pis + sc * kK + c0) = make_float2(pm0, pm1);
+      {  // "unsafe" channels of this sub-chunk (product below 2^-64 or not finite)
+        const uint32_t m0 = __ballot_sync(0xffffffffu, !(pm0 >= kSafeMin));
+        const uint32_t m1 = __ballot_sync(0xffffffffu, !(pm1 >= kSafeMin));
+        if (lane == 0) {
+          s->unsafe[sc][warp & 1][0] = m0;
+          s->unsafe[sc][warp & 1][1] = m1;
+        }
+      }
       wait_bar(p, s, B_QK_FULL, gc & 1);
       // QG buffer and this gamma buffer are free once MMA-1b of the previous chunk ran
       if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
@@ -371,28 +389,12 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       }
       const float E0 = (sc > 0 ? pi0[0] : 1.f) * (sc > 1 ? pi0[1] : 1.f) * (sc > 2 ? pi0[2] : 1.f);
       const float E1 = (sc > 0 ? pi1[0] : 1.f) * (sc > 1 ? pi1[1] : 1.f) * (sc > 2 ? pi1[2] : 1.f);
-      const float F0 = (sc < 1 ? pi0[1] : 1.f) * (sc < 2 ? pi0[2] : 1.f) * (sc < 3 ? pi0[3] : 1.f);
-      const float F1 = (sc < 1 ? pi1[1] : 1.f) * (sc < 2 ? pi1[2] : 1.f) * (sc < 3 ? pi1[3] : 1.f);
-      if (sc == 0) {  // warps 0-1: unsafe masks and gamma for their 64 channels
-#pragma unroll
-        for (int q2 = 0; q2 < 4; ++q2) {
-          const uint32_t m0 = __ballot_sync(0xffffffffu, !(pi0[q2] >= kSafeMin));
-          const uint32_t m1 = __ballot_sync(0xffffffffu, !(pi1[q2] >= kSafeMin));
-          if (lane < 4) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int l = 0; l < 8; ++l)
-              word |= (((m0 >> (8 * lane + l)) & 1u) << (2 * l)) |
-                      (((m1 >> (8 * lane + l)) & 1u) << (2 * l + 1));
-            s->unsafe[q2][(warp & 1) * 4 + lane] = (uint16_t)word;
-          }
-        }
+      if (sc == 3)  // warps 6-7 (fewest block-1 variants): gamma of their 64 channels
         *reinterpret_cast<float2*>(&s->gamma[gc & 1][c0]) =
             make_float2(pi0[0] * pi0[1] * pi0[2] * pi0[3], pi1[0] * pi1[1] * pi1[2] * pi1[3]);
-      }
       {
-        const float ip0 = (pm0 >= kSafeMin) ? 1.f / pm0 : 0.f;  // pm = pi of this sub-chunk
-        const float ip1 = (pm1 >= kSafeMin) ? 1.f / pm1 : 0.f;
+        const float ip0 = (pm0 >= kSafeMin) ? __fdividef(1.f, pm0) : 0.f;  // pm = pi of this sub-chunk
+        const float ip1 = (pm1 >= kSafeMin) ? __fdividef(1.f, pm1) : 0.f;
         // pass A, tokens in descending order: kap (exclusive product to the sub-chunk
         // end) needs no array.  Writes CB block 0 (k kap), block 2 (k/rho on safe
         // channels) and, by sub-chunk, the block-1 reference variants.
@@ -493,44 +495,34 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         mbar_arrive(&s->bar[B_GAMMA0 + (gc & 1)]);
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(128, 192, 0, 1);
-#pragma unroll
+#pragma unroll 1
         for (int st = 0; st < 8; ++st) {
           const uint64_t a = sdesc_sw128(sbase + OFF_QK + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
           const uint64_t b = sdesc_sw128(sbase + OFF_CB + st * 2048, 16384, 1024);
           mma_bf16(tbase + TM_AB, a, b, idesc, st > 0 ? 1u : 0u);
         }
         mma_commit(&s->bar[B_AB_DONE]);
+        // while MMA-AB runs: the chunk after this one, and its q/k/v into L2
+        LoaderState* L = ld.st;
+        int nkh = 0, nh = 0, nt0 = 0, ncv = 0;
+        const bool hn = ld.next_chunk(s, k, lc, nkh, nh, nt0, ncv);
+        L->have_next = hn;
+        L->nkh = nkh;
+        L->nh = nh;
+        L->nt0 = nt0;
+        L->ncv = ncv;
+        if (hn) ld.prefetch_l2(p, nkh, nh, nt0);
       }
       __syncwarp();
-      // KR = (k kap) F_s : scaled copy of this thread's CB block-0 chunks into KR
-      // (overlaps MMA-AB, which only reads CB)
-      if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int c = c2 ^ wsel;
-        const float f = c ? F1 : F0;
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = sc * 2 + jj;
-          const uint4 src = *reinterpret_cast<const uint4*>(sm + OFF_CB + sw128_off(c0 + c, j));
-          const uint32_t in[4] = {src.x, src.y, src.z, src.w};
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            w[u] = pack_bf16x2(bf_bits(in[u] & 0xFFFFu) * f, bf_bits(in[u] >> 16) * f);
-          st_chunk(sm, OFF_KR + sw128_off(c0 + c, j), w[0], w[1], w[2], w[3]);
-        }
-      }
       // ------------------------------------------------------------- A / B rows
       wait_bar(p, s, B_AB_DONE, gc & 1);
       tc_fence_after();
-      if (t == 0 && have_next && ld.n_g == gc + 1) ld.load_g(p, sm, s, nh, nt0);  // CB 1-2 free
+      if (t == 0 && ld.st->have_next && ld.st->n_g == gc + 1) ld.load_g(p, sm, s, ld.st->nh, ld.st->nt0);  // CB 1-2 free
       __syncwarp();
       uint32_t any_unsafe = 0;
 #pragma unroll
       for (int q2 = 0; q2 < 4; ++q2)
-#pragma unroll
-        for (int wd = 0; wd < 8; ++wd) any_unsafe |= s->unsafe[q2][wd];
+        any_unsafe |= s->unsafe[q2][0][0] | s->unsafe[q2][0][1] | s->unsafe[q2][1][0] | s->unsafe[q2][1][1];
       {
         const int r = L & 63, a = r >> 4;
         const bool isB = L >= 64;
@@ -569,6 +561,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             for (int jc = 0; jc < 8; ++jc) {
               float4 w4;
               const int i = hx * 32 + jc * 4;
+              if ((i >> 4) > a) continue;  // blocks above the diagonal are never read
               w4.x = (i + 0 < r) ? br * x[jc * 4 + 0] : 0.f;
               w4.y = (i + 1 < r) ? br * x[jc * 4 + 1] : 0.f;
               w4.z = (i + 2 < r) ? br * x[jc * 4 + 2] : 0.f;
@@ -597,22 +590,26 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
                 make_float4(x[jc * 4], x[jc * 4 + 1], x[jc * 4 + 2], x[jc * 4 + 3]);
         }
       }
-      named_bar(BAR_IG, kIG);
-      if (any_unsafe != 0u) {
+      // TMEM lanes 0-63 (A rows) belong to warps 0, 1, 4, 5 (the "A group"), lanes
+      // 64-127 (B rows) to warps 2, 3, 6, 7; on the fast path the A group goes on to the
+      // inverse while the B group writes KR.
+      const bool agrp = quad < 2;
+      if (any_unsafe == 0u) {
+        if (agrp) named_bar(BAR_A, 128);
+      } else {
+        named_bar(BAR_IG, kIG);
         // exact pairwise terms of the diagonal sub-chunk blocks on "unsafe" channels
         if (hx == 0) {
           const int r = L & 63, a = r >> 4;
           const bool isB = L >= 64;
-          uint32_t anya = 0;
-#pragma unroll
-          for (int wd = 0; wd < 8; ++wd) anya |= s->unsafe[a][wd];
+          const uint32_t anya = s->unsafe[a][0][0] | s->unsafe[a][0][1] | s->unsafe[a][1][0] | s->unsafe[a][1][1];
           if (anya != 0u && r < cv) {
             float* row = isB ? Xs : As;
             const __nv_bfloat16* xsrc = isB ? p.q : p.k;
-            for (int wd = 0; wd < 8; ++wd) {
-              uint32_t m = s->unsafe[a][wd];
+            for (int wd = 0; wd < 4; ++wd) {
+              uint32_t m = s->unsafe[a][wd >> 1][wd & 1];
               while (m) {
-                const int c = wd * 16 + (__ffs(m) - 1);
+                const int c = 64 * (wd >> 1) + 2 * (__ffs(m) - 1) + (wd & 1);
                 m &= m - 1;
                 const float xr = __bfloat162float(xsrc[((size_t)(t0 + r) * p.Hk + kh) * kK + c]);
                 float pr = 1.f;
@@ -662,53 +659,98 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         named_bar(BAR_IG, kIG);
       }
       // ------------------------------------------------------------- inverse
-      // X = (I + A)^-1 by 16x16 blocks: diagonal blocks by forward substitution
-      // (one column per lane, two blocks per warp), then
-      // X_ab = -X_aa * sum_{b<=c<a} A_ac X_cb, one block per warp per level.
-      if (warp < 2) {
-        // lane = column j of diagonal block (2 blocks per warp); rows of A are read
-        // as broadcast float4 and x[rr] = -sum_{i<rr} A[rr][i] x[i] row by row.
-        const int o = (warp * 2 + (lane >> 4)) * 16, j = lane & 15;
-        float xv[16];
+      // X = (I + A)^-1 by the A group: 16x16 diagonal blocks by forward substitution
+      // (one column per lane, two blocks per warp), then the two 32x32 diagonal halves
+      // and the lower-left 32x32 block from the 16x16 blocks (tf32 warp MMAs).
+      if (agrp) {
+        if (warp < 2) {
+          // lane = column j of diagonal block (2 blocks per warp); rows of A are read
+          // as broadcast float4 and x[rr] = -sum_{i<rr} A[rr][i] x[i] row by row.
+          const int o = (warp * 2 + (lane >> 4)) * 16, j = lane & 15;
+          float xv[16];
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) xv[rr] = (rr == j) ? 1.f : 0.f;
+          for (int rr = 0; rr < 16; ++rr) xv[rr] = (rr == j) ? 1.f : 0.f;
 #pragma unroll
-        for (int rr = 1; rr < 16; ++rr) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int rr = 1; rr < 16; ++rr) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i4 = 0; i4 < (rr + 3) / 4; ++i4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(As + sidx(o + rr, o + 4 * i4));
-            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+            for (int i4 = 0; i4 < (rr + 3) / 4; ++i4) {
+              const float4 a4 = *reinterpret_cast<const float4*>(As + sidx(o + rr, o + 4 * i4));
+              const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (4 * i4 + u < rr) acc[u] = fmaf(av[u], xv[4 * i4 + u], acc[u]);
+              for (int u = 0; u < 4; ++u)
+                if (4 * i4 + u < rr) acc[u] = fmaf(av[u], xv[4 * i4 + u], acc[u]);
+            }
+            const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            if (rr > j) xv[rr] = -sum;
           }
-          const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-          if (rr > j) xv[rr] = -sum;
-        }
-        if (lane < 32) {
+          if (lane < 32) {
 #pragma unroll
-          for (int rr = 0; rr < 16; ++rr) Xs[sidx(o + rr, o + j)] = xv[rr];
+            for (int rr = 0; rr < 16; ++rr) Xs[sidx(o + rr, o + j)] = xv[rr];
+          }
+        }
+        named_bar(BAR_A, 128);
+        // 32x32 halves: X_{a+1,a} = -X_{a+1,a+1} (A_{a+1,a} X_aa) for a = 0, 2 (P staged
+        // in the unused upper block (a, a+1) of A) ...
+        const int aw = (warp >> 2) * 2 + (warp & 1);  // 0..3 within the A group
+        if (aw < 2) {
+          const int a = aw * 2;
+          float acc[2][4] = {};
+          blk_mma(acc, As, (a + 1) * 16, a * 16, Xs, a * 16, a * 16, lane);
+          blk_store(As, a * 16, (a + 1) * 16, acc, 1.f, lane);
+          __syncwarp();
+          float acc2[2][4] = {};
+          blk_mma(acc2, Xs, (a + 1) * 16, (a + 1) * 16, As, a * 16, (a + 1) * 16, lane);
+          blk_store(Xs, (a + 1) * 16, a * 16, acc2, -1.f, lane);
+        }
+        named_bar(BAR_A, 128);
+        // ... then the lower-left 32x32 block -X2 (A21 X1): P_kj = sum_l A_kl X_lj into the
+        // upper blocks (k-2, j+2), one 16x16 block per warp ...
+        {
+          const int kb = 2 + (aw >> 1), jb = aw & 1;
+          float acc[2][4] = {};
+#pragma unroll 1
+          for (int l = jb; l < 2; ++l) blk_mma(acc, As, kb * 16, l * 16, Xs, l * 16, jb * 16, lane);
+          blk_store(As, (kb - 2) * 16, (jb + 2) * 16, acc, 1.f, lane);
+        }
+        named_bar(BAR_A, 128);
+        // ... and X_ij = -sum_{2<=k<=i} X_ik P_kj
+        {
+          const int ib = 2 + (aw >> 1), jb = aw & 1;
+          float acc[2][4] = {};
+#pragma unroll 1
+          for (int kb = 2; kb <= ib; ++kb)
+            blk_mma(acc, Xs, ib * 16, kb * 16, As, (kb - 2) * 16, (jb + 2) * 16, lane);
+          blk_store(Xs, ib * 16, jb * 16, acc, -1.f, lane);
+        }
+      } else {
+        // KR = (k kap) F_s for sub-chunks sc-1 and sc of this thread's channel pair
+        // (F_s = product of pi after s); CB block 0 is intact until the next prologue
+        if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+          const int sk = sc - 1 + s2;
+          const float fs0 = (sk < 1 ? pi0[1] : 1.f) * (sk < 2 ? pi0[2] : 1.f) * (sk < 3 ? pi0[3] : 1.f);
+          const float fs1 = (sk < 1 ? pi1[1] : 1.f) * (sk < 2 ? pi1[2] : 1.f) * (sk < 3 ? pi1[3] : 1.f);
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int c = c2 ^ wsel;
+            const float f = c ? fs1 : fs0;
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const int j = sk * 2 + jj;
+              const uint4 src = *reinterpret_cast<const uint4*>(sm + OFF_CB + sw128_off(c0 + c, j));
+              const uint32_t in[4] = {src.x, src.y, src.z, src.w};
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                w[u] = pack_bf16x2(bf_bits(in[u] & 0xFFFFu) * f, bf_bits(in[u] >> 16) * f);
+              st_chunk(sm, OFF_KR + sw128_off(c0 + c, j), w[0], w[1], w[2], w[3]);
+            }
+          }
         }
       }
       named_bar(BAR_IG, kIG);
-      // level d: X_{a+d,a} = -X_{a+d,a+d} P, P = sum_{a<=m<a+d} A_{a+d,m} X_{m,a} (warp a);
-      // P is staged in the unused upper block (d-1, d+a) of A.
-#pragma unroll 1
-      for (int d = 1; d <= 3; ++d) {
-        if (warp <= 3 - d) {
-          const int a = warp;
-          float acc[2][4] = {};
-#pragma unroll 1
-          for (int m = a; m < a + d; ++m) blk_mma(acc, As, (a + d) * 16, m * 16, Xs, m * 16, a * 16, lane);
-          blk_store(As, (d - 1) * 16, 16 * (d + a), acc, 1.f, lane);
-          __syncwarp();
-          float acc2[2][4] = {};
-          blk_mma(acc2, Xs, (a + d) * 16, (a + d) * 16, As, (d - 1) * 16, 16 * (d + a), lane);
-          blk_store(Xs, (a + d) * 16, a * 16, acc2, -1.f, lane);
-        }
-        named_bar(BAR_IG, kIG);
-      }
       // Tm = X Diag(beta) -> bf16 -> TM   (thread: row r = t & 63, columns 16*qq..16*qq+15)
       {
         const int r = t & 63, qq = t >> 6;
@@ -733,15 +775,19 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       }
       fence_async_smem();
       named_bar(BAR_IG, kIG);
+      if (t < kC && ld.st->have_next) {
+        if (t < ld.st->ncv) bt_next = p.beta[(size_t)(ld.st->nt0 + t) * p.Hv + ld.st->nh];
+        bt_ok = true;
+      }
       // ------------------------------------------------------------- U~ and W
-      if (t == 0 && have_next && ld.n_qk == gc + 1) ld.load_qk(p, sm, s, nkh, nt0);  // AS/XS dead
+      if (t == 0 && ld.st->have_next && ld.st->n_qk == gc + 1) ld.load_qk(p, sm, s, ld.st->nkh, ld.st->nt0);  // AS/XS dead
       if (warp == 0) {
         wait_bar(p, s, B_V_FULL, gc & 1);
         if (gc > 0) wait_bar(p, s, B_E1, (gc - 1) & 1);  // U region read by the recurrence
         if (lane == 0) {
           tc_fence_after();
           const uint32_t idu = idesc_bf16(128, 64, 1, 0), idw = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
+#pragma unroll 1
           for (int st = 0; st < 4; ++st) {
             const uint64_t b = sdesc_sw128(sbase + OFF_TM + st * 32, 16, 1024);
             mma_bf16(tbase + TM_U, sdesc_sw128(sbase + OFF_VB + st * 2048, 8192, 1024), b, idu,
@@ -755,7 +801,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       }
       wait_bar(p, s, B_UW_DONE, gc & 1);
       tc_fence_after();
-      if (t == 0 && have_next && ld.n_v == gc + 1) ld.load_v(p, sm, s, nh, nt0);  // VB free
+      if (t == 0 && ld.st->have_next && ld.st->n_v == gc + 1) ld.load_v(p, sm, s, ld.st->nh, ld.st->nt0);  // VB free
       __syncwarp();
       // -W^T rows -> WB (row = channel L, tokens 32*hx ..)
       if (gc > 0) wait_bar(p, s, B_M1A, (gc - 1) & 1);
@@ -785,9 +831,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
     __syncwarp();
     wait_bar(p, s, B_DRAIN_IG, 0);
     if (lane == 0) {
-      if (ld.n_qk > 0) mbar_wait(&s->bar[B_QK_FULL], (ld.n_qk - 1) & 1);
-      if (ld.n_g > 0) mbar_wait(&s->bar[B_G_FULL], (ld.n_g - 1) & 1);
-      if (ld.n_v > 0) mbar_wait(&s->bar[B_V_FULL], (ld.n_v - 1) & 1);
+      const LoaderState* L = ld.st;
+      if (L->n_qk > 0) mbar_wait(&s->bar[B_QK_FULL], (L->n_qk - 1) & 1);
+      if (L->n_g > 0) mbar_wait(&s->bar[B_G_FULL], (L->n_g - 1) & 1);
+      if (L->n_v > 0) mbar_wait(&s->bar[B_V_FULL], (L->n_v - 1) & 1);
     }
     __syncwarp();
   }
@@ -805,10 +852,10 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   const bool leader_warp = (warp == kIG / 32);
   const uint32_t taddr_q = tbase + ((uint32_t)(quad * 32) << 16);
   const uint32_t sbase = smem_u32(sm);
-  __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + OFF_ST);  // [64][128] staging of O
   uint32_t gc = 0;
-  // The output epilogue of a chunk is deferred into the next chunk's MMA-3 window,
-  // staged row-major through the S^T buffer (free from MMA-1b until the E2 write).
+  // The output epilogue of a chunk is deferred into the next chunk's MMA-3 window.
+  // Each thread (value channel v) writes its O column straight to global memory: the
+  // 32 lanes of a warp cover 64 contiguous bytes of one output row per store.
   bool pend = false;
   int64_t pend_t0 = 0;
   int pend_cv = 0, pend_h = 0;
@@ -818,32 +865,23 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   // thread before MMA-1a of the current one, whose completion E1 already waited on, so
   // it is complete; waiting on its barrier here could see the barrier already one phase
   // further (MMA-3a of the current chunk) and never return.  After the loop it is waited.
-  auto o_epilogue = [&](bool in_loop, uint32_t cur_gc) {
+  auto o_epilogue = [&](bool in_loop) {
     if (!pend) return;
     pend = false;
-    if (in_loop) wait_bar(p, s, B_M1B, cur_gc & 1);  // S^T buffer no longer read by MMA-1b
-    else wait_bar(p, s, B_M3A, pend_gc & 1);
+    if (!in_loop) wait_bar(p, s, B_M3A, pend_gc & 1);
     tc_fence_after();
-#pragma unroll
+    __nv_bfloat16* dst = p.o + ((size_t)pend_t0 * p.Hv + pend_h) * kV + v;
+    const size_t rs = (size_t)p.Hv * kV;
+#pragma unroll 1
     for (int cq = 0; cq < 4; ++cq) {
       float ov[16];
       tmem_ld16(taddr_q + TM_O + 64 * (pend_gc & 1) + cq * 16, ov);
       tmem_ld_wait();
 #pragma unroll
-      for (int u = 0; u < 16; ++u) stage[(cq * 16 + u) * kV + v] = __float2bfloat16_rn(ov[u]);
+      for (int u = 0; u < 16; ++u)
+        if (cq * 16 + u < pend_cv) dst[(size_t)(cq * 16 + u) * rs] = __float2bfloat16_rn(ov[u]);
     }
     tc_fence_before();
-    named_bar(BAR_RG, kRG);
-    {
-      const int r = rt >> 1, hh = rt & 1;
-      if (r < pend_cv) {
-        const uint4* srow = reinterpret_cast<const uint4*>(stage + r * kV + hh * 64);
-        uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)(pend_t0 + r) * p.Hv + pend_h) * kV + hh * 64);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) dst[u] = srow[u];
-      }
-    }
-    named_bar(BAR_RG, kRG);  // staging read before S^T is rewritten
   };
 
   for (int k = 0;; ++k) {
@@ -899,13 +937,13 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         if (lane == 0) {
           tc_fence_after();
           const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
-#pragma unroll
+#pragma unroll 1
           for (int st = 0; st < 8; ++st) {
             const uint64_t a = sdesc_sw128(sbase + OFF_ST + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
             mma_bf16(tbase + TM_U, a, sdesc_sw128(sbase + OFF_WB + st * 2048, 16384, 1024), id1, 1u);
           }
           mma_commit(&s->bar[B_M1A]);
-#pragma unroll
+#pragma unroll 1
           for (int st = 0; st < 8; ++st) {
             const uint64_t a = sdesc_sw128(sbase + OFF_ST + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
             mma_bf16(tbase + TM_O + 64 * (gc & 1), a,
@@ -919,23 +957,23 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       if (lc > 0) {
         wait_bar(p, s, B_GAMMA0 + (gc & 1), (gc >> 1) & 1);
         const float* gm = s->gamma[gc & 1];
+#pragma unroll 1
+        for (int kq = 0; kq < 4; ++kq) {
+          float sv[2][16];
 #pragma unroll
-        for (int kh2 = 0; kh2 < 2; ++kh2) {
-          float sv[4][16];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(taddr_q + TM_S + (kh2 * 4 + q4) * 16, sv[q4]);
+          for (int q2 = 0; q2 < 2; ++q2) tmem_ld16(taddr_q + TM_S + (kq * 2 + q2) * 16, sv[q2]);
           tmem_ld_wait();
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q2 = 0; q2 < 2; ++q2) {
 #pragma unroll
             for (int u4 = 0; u4 < 4; ++u4) {
-              const float4 g4 = *reinterpret_cast<const float4*>(gm + (kh2 * 4 + q4) * 16 + u4 * 4);
-              sv[q4][u4 * 4 + 0] *= g4.x;
-              sv[q4][u4 * 4 + 1] *= g4.y;
-              sv[q4][u4 * 4 + 2] *= g4.z;
-              sv[q4][u4 * 4 + 3] *= g4.w;
+              const float4 g4 = *reinterpret_cast<const float4*>(gm + (kq * 2 + q2) * 16 + u4 * 4);
+              sv[q2][u4 * 4 + 0] *= g4.x;
+              sv[q2][u4 * 4 + 1] *= g4.y;
+              sv[q2][u4 * 4 + 2] *= g4.z;
+              sv[q2][u4 * 4 + 3] *= g4.w;
             }
-            tmem_st16(taddr_q + TM_S + (kh2 * 4 + q4) * 16, sv[q4]);
+            tmem_st16(taddr_q + TM_S + (kq * 2 + q2) * 16, sv[q2]);
           }
         }
         tmem_st_wait();
@@ -943,7 +981,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       // ---- E1: U^T row v -> UT (bf16)
       wait_bar(p, s, B_M1A, gc & 1);
       tc_fence_after();
-#pragma unroll
+#pragma unroll 1
       for (int cq = 0; cq < 4; ++cq) {
         float uv[16];
         tmem_ld16(taddr_q + TM_U + cq * 16, uv);
@@ -961,12 +999,12 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         mbar_arrive(&s->bar[B_E1]);
         tc_fence_after();
         const uint32_t id3 = idesc_bf16(128, 128, 0, 0), id3o = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
+#pragma unroll 1
         for (int st = 0; st < 4; ++st)
           mma_bf16(tbase + TM_S, sdesc_sw128(sbase + OFF_UT + st * 32, 16, 1024),
                    sdesc_sw128(sbase + OFF_KR + st * 32, 16, 1024), id3, 1u);
         mma_commit(&s->bar[B_M3B]);
-#pragma unroll
+#pragma unroll 1
         for (int st = 0; st < 4; ++st)
           mma_bf16(tbase + TM_O + 64 * (gc & 1), sdesc_sw128(sbase + OFF_UT + st * 32, 16, 1024),
                    sdesc_sw128(sbase + OFF_BB + st * 32, 16, 1024), id3o, 1u);
@@ -974,11 +1012,11 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       }
       __syncwarp();
       // ---- output of the previous chunk, inside this chunk's MMA-3 window
-      o_epilogue(true, gc);
+      o_epilogue(true);
       // ---- E2: S -> ST (bf16), or the final state store on the last chunk
       wait_bar(p, s, B_M3B, gc & 1);
       tc_fence_after();
-#pragma unroll
+#pragma unroll 1
       for (int kq = 0; kq < 8; ++kq) {
         float sv[16];
         tmem_ld16(taddr_q + TM_S + kq * 16, sv);
@@ -1006,7 +1044,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
     }
     if (stop) break;
   }
-  o_epilogue(false, gc);
+  o_epilogue(false);
   named_bar(BAR_RG, kRG);
   if (leader_warp) {
     if (lane == 0) mma_commit(&s->bar[B_DRAIN_RG]);
@@ -1026,6 +1064,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     for (int b = 0; b < B_COUNT; ++b) mbar_init(&s->bar[b], 1);
     for (int r = 0; r < kRing; ++r) mbar_init(&s->bar[B_ITEM_EMPTY + r], 2);
     s->abort = 0;
+    s->ld = LoaderState{};
     fence_mbar_init();
     prefetch_tensormap(&p.tm_q);
     prefetch_tensormap(&p.tm_k);
