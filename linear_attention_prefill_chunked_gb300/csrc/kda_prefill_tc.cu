@@ -165,7 +165,7 @@ __device__ __forceinline__ bool wait_bar(const TcParams& p, Small* s, int b, uin
   if (mbar_try_wait(&s->bar[b], parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait(&s->bar[b], parity)) return true;
+    if (mbar_try_wait_sleep(&s->bar[b], parity, kSleepHintNs)) return true;
     if (aborted(s)) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       fail(p, s);
@@ -307,6 +307,37 @@ struct Loader {  // used by thread 0 only
     tma_prefetch_3d(&p.tm_v, 64, h, t0);
   }
 };
+
+// Exact pairwise terms of the diagonal sub-chunk blocks on "unsafe" channels (sub-chunk
+// gate product below 2^-64), added to the raw A (As) and B (Xs) rows: thread = TMEM
+// lane L (row L & 63 of A for L < 64, of B otherwise).  Kept out of line: it never
+// runs at ordinary gates and would otherwise raise the register pressure of the
+// chunk loop.
+__device__ __noinline__ void unsafe_diag_terms(const TcParams& p, const Small* s, float* As, float* Xs,
+                                               int L, int64_t t0, int cv, int kh, int h) {
+  const int r = L & 63, a = r >> 4;
+  const bool isB = L >= 64;
+  const uint32_t anya = s->unsafe[a][0][0] | s->unsafe[a][0][1] | s->unsafe[a][1][0] | s->unsafe[a][1][1];
+  if (anya != 0u && r < cv) {
+    float* row = isB ? Xs : As;
+    const __nv_bfloat16* xsrc = isB ? p.q : p.k;
+    for (int wd = 0; wd < 4; ++wd) {
+      uint32_t m = s->unsafe[a][wd >> 1][wd & 1];
+      while (m) {
+        const int c = 64 * (wd >> 1) + 2 * (__ffs(m) - 1) + (wd & 1);
+        m &= m - 1;
+        const float xr = __bfloat162float(xsrc[((size_t)(t0 + r) * p.Hk + kh) * kK + c]);
+        float pr = 1.f;
+        for (int i = r; i >= a * 16; --i) {
+          const float ki = __bfloat162float(p.k[((size_t)(t0 + i) * p.Hk + kh) * kK + c]);
+          row[sidx(r, i)] += xr * ki * pr;
+          pr *= __expf(p.g[((size_t)(t0 + i) * p.Hv + h) * kK + c]);
+          if (pr == 0.f) break;
+        }
+      }
+    }
+  }
+}
 
 __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tbase) {
   const int t = threadIdx.x;  // 0..255
@@ -452,7 +483,9 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             kw[u] = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128)) : 0u;
             qw[u] = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(64 + r, c0, 128)) : 0u;
           }
-          float kg[2][8], qg[2][8];
+          // KG / QG of channels c0 and c0+1, packed as token pairs while they are formed
+          uint32_t kgw[2][4], qgw[2][4];
+          float pk0 = 0.f, pk1 = 0.f, pq0 = 0.f, pq1 = 0.f;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int j = jh * 8 + u;
@@ -462,10 +495,17 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             const float qr0 = bf_bits(qw[u] & 0xFFFFu) * rho0, qr1 = bf_bits(qw[u] >> 16) * rho1;
             kw[u] = pack_bf16x2(kr0, kr1);
             qw[u] = pack_bf16x2(qr0, qr1);
-            kg[0][u] = kr0 * E0;
-            kg[1][u] = kr1 * E1;
-            qg[0][u] = qr0 * qs0;
-            qg[1][u] = qr1 * qs1;
+            if (u & 1) {
+              kgw[0][u >> 1] = pack_bf16x2(pk0, kr0 * E0);
+              kgw[1][u >> 1] = pack_bf16x2(pk1, kr1 * E1);
+              qgw[0][u >> 1] = pack_bf16x2(pq0, qr0 * qs0);
+              qgw[1][u >> 1] = pack_bf16x2(pq1, qr1 * qs1);
+            } else {
+              pk0 = kr0 * E0;
+              pk1 = kr1 * E1;
+              pq0 = qr0 * qs0;
+              pq1 = qr1 * qs1;
+            }
           }
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -478,13 +518,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           for (int c2 = 0; c2 < 2; ++c2) {
             const int c = c2 ^ wsel;
             const int row = c0 + c;
-            float a[8], b[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) { a[u] = c ? kg[1][u] : kg[0][u]; b[u] = c ? qg[1][u] : qg[0][u]; }
-            st_chunk(sm, OFF_KG + sw128_off(row, cj), pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
-                     pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
-            st_chunk(sm, OFF_QG + sw128_off(row, cj), pack_bf16x2(b[0], b[1]), pack_bf16x2(b[2], b[3]),
-                     pack_bf16x2(b[4], b[5]), pack_bf16x2(b[6], b[7]));
+            st_chunk(sm, OFF_KG + sw128_off(row, cj), c ? kgw[1][0] : kgw[0][0], c ? kgw[1][1] : kgw[0][1],
+                     c ? kgw[1][2] : kgw[0][2], c ? kgw[1][3] : kgw[0][3]);
+            st_chunk(sm, OFF_QG + sw128_off(row, cj), c ? qgw[1][0] : qgw[0][0], c ? qgw[1][1] : qgw[0][1],
+                     c ? qgw[1][2] : qgw[0][2], c ? qgw[1][3] : qgw[0][3]);
           }
         }
       }
@@ -599,30 +636,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       } else {
         named_bar(BAR_IG, kIG);
         // exact pairwise terms of the diagonal sub-chunk blocks on "unsafe" channels
-        if (hx == 0) {
-          const int r = L & 63, a = r >> 4;
-          const bool isB = L >= 64;
-          const uint32_t anya = s->unsafe[a][0][0] | s->unsafe[a][0][1] | s->unsafe[a][1][0] | s->unsafe[a][1][1];
-          if (anya != 0u && r < cv) {
-            float* row = isB ? Xs : As;
-            const __nv_bfloat16* xsrc = isB ? p.q : p.k;
-            for (int wd = 0; wd < 4; ++wd) {
-              uint32_t m = s->unsafe[a][wd >> 1][wd & 1];
-              while (m) {
-                const int c = 64 * (wd >> 1) + 2 * (__ffs(m) - 1) + (wd & 1);
-                m &= m - 1;
-                const float xr = __bfloat162float(xsrc[((size_t)(t0 + r) * p.Hk + kh) * kK + c]);
-                float pr = 1.f;
-                for (int i = r; i >= a * 16; --i) {
-                  const float ki = __bfloat162float(p.k[((size_t)(t0 + i) * p.Hk + kh) * kK + c]);
-                  row[sidx(r, i)] += xr * ki * pr;
-                  pr *= __expf(p.g[((size_t)(t0 + i) * p.Hv + h) * kK + c]);
-                  if (pr == 0.f) break;
-                }
-              }
-            }
-          }
-        }
+        if (hx == 0) unsafe_diag_terms(p, s, As, Xs, L, t0, cv, kh, h);
         named_bar(BAR_IG, kIG);
         // A: mask + beta_r (in place, fp32); B: mask + scale -> bf16 -> BB
         {
@@ -664,29 +678,51 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // and the lower-left 32x32 block from the 16x16 blocks (tf32 warp MMAs).
       if (agrp) {
         if (warp < 2) {
-          // lane = column j of diagonal block (2 blocks per warp); rows of A are read
-          // as broadcast float4 and x[rr] = -sum_{i<rr} A[rr][i] x[i] row by row.
+          // lane = column j of diagonal block o (two blocks per warp).  Its 8x8 diagonal
+          // sub-blocks are inverted by forward substitution side by side (columns 0-7
+          // take rows 0-7, columns 8-15 rows 8-15; rows of A read as broadcast float4),
+          // then columns 0-7 get rows 8-15 as -X22 (A21 x), A21 the lower-left 8x8.
           const int o = (warp * 2 + (lane >> 4)) * 16, j = lane & 15;
-          float xv[16];
+          const int hb = j & 8;
+          float xv[8];
 #pragma unroll
-          for (int rr = 0; rr < 16; ++rr) xv[rr] = (rr == j) ? 1.f : 0.f;
+          for (int rr = 0; rr < 8; ++rr) xv[rr] = (hb + rr == j) ? 1.f : 0.f;
 #pragma unroll
-          for (int rr = 1; rr < 16; ++rr) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int rr = 1; rr < 8; ++rr) {
+            const float4 a0 = *reinterpret_cast<const float4*>(As + sidx(o + hb + rr, o + hb));
+            const float4 a1 = *reinterpret_cast<const float4*>(As + sidx(o + hb + rr, o + hb + 4));
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float acc[2] = {0.f, 0.f};
 #pragma unroll
-            for (int i4 = 0; i4 < (rr + 3) / 4; ++i4) {
-              const float4 a4 = *reinterpret_cast<const float4*>(As + sidx(o + rr, o + 4 * i4));
-              const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                if (4 * i4 + u < rr) acc[u] = fmaf(av[u], xv[4 * i4 + u], acc[u]);
-            }
-            const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-            if (rr > j) xv[rr] = -sum;
+            for (int i = 0; i < rr; ++i) acc[i & 1] = fmaf(av[i], xv[i], acc[i & 1]);
+            if (hb + rr > j) xv[rr] = -(acc[0] + acc[1]);
           }
-          if (lane < 32) {
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) Xs[sidx(o + rr, o + j)] = xv[rr];
+          for (int rr = 0; rr < 8; ++rr) Xs[sidx(o + hb + rr, o + j)] = xv[rr];
+          if (hb) {
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) Xs[sidx(o + rr, o + j)] = 0.f;  // upper-right 8x8
+          }
+          __syncwarp();
+          if (!hb) {
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 a0 = *reinterpret_cast<const float4*>(As + sidx(o + 8 + i, o));
+              const float4 a1 = *reinterpret_cast<const float4*>(As + sidx(o + 8 + i, o + 4));
+              y[i] = fmaf(a0.x, xv[0], fmaf(a0.y, xv[1], fmaf(a0.z, xv[2], a0.w * xv[3]))) +
+                     fmaf(a1.x, xv[4], fmaf(a1.y, xv[5], fmaf(a1.z, xv[6], a1.w * xv[7])));
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 x0 = *reinterpret_cast<const float4*>(Xs + sidx(o + 8 + i, o + 8));
+              const float4 x1 = *reinterpret_cast<const float4*>(Xs + sidx(o + 8 + i, o + 12));
+              const float xr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+              float acc[2] = {0.f, 0.f};
+#pragma unroll
+              for (int m = 0; m <= i; ++m) acc[m & 1] = fmaf(xr[m], y[m], acc[m & 1]);
+              Xs[sidx(o + 8 + i, o + j)] = -(acc[0] + acc[1]);
+            }
           }
         }
         named_bar(BAR_A, 128);
@@ -780,7 +816,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         bt_ok = true;
       }
       // ------------------------------------------------------------- U~ and W
-      if (t == 0 && ld.st->have_next && ld.st->n_qk == gc + 1) ld.load_qk(p, sm, s, ld.st->nkh, ld.st->nt0);  // AS/XS dead
       if (warp == 0) {
         wait_bar(p, s, B_V_FULL, gc & 1);
         if (gc > 0) wait_bar(p, s, B_E1, (gc - 1) & 1);  // U region read by the recurrence
@@ -796,6 +831,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
                      st > 0 ? 1u : 0u);
           }
           mma_commit(&s->bar[B_UW_DONE]);
+          // q/k of the next chunk into the buffer the inverse scratch used
+          if (ld.st->have_next && ld.st->n_qk == gc + 1) ld.load_qk(p, sm, s, ld.st->nkh, ld.st->nt0);
         }
         __syncwarp();
       }
