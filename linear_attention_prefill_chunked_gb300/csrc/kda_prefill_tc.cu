@@ -233,11 +233,11 @@ __device__ __forceinline__ void blk_store(float* M, int r, int c, const float ac
                                           int lane) {
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    M[sidx(r + g, c + 8 * nt + 2 * t)] = sgn * acc[nt][0];
-    M[sidx(r + g, c + 8 * nt + 2 * t + 1)] = sgn * acc[nt][1];
-    M[sidx(r + g + 8, c + 8 * nt + 2 * t)] = sgn * acc[nt][2];
-    M[sidx(r + g + 8, c + 8 * nt + 2 * t + 1)] = sgn * acc[nt][3];
+  for (int nt = 0; nt < 2; ++nt) {  // column pairs stay adjacent under the swizzle
+    *reinterpret_cast<float2*>(M + sidx(r + g, c + 8 * nt + 2 * t)) =
+        make_float2(sgn * acc[nt][0], sgn * acc[nt][1]);
+    *reinterpret_cast<float2*>(M + sidx(r + g + 8, c + 8 * nt + 2 * t)) =
+        make_float2(sgn * acc[nt][2], sgn * acc[nt][3]);
   }
 }
 
@@ -699,10 +699,9 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           }
 #pragma unroll
           for (int rr = 0; rr < 8; ++rr) Xs[sidx(o + hb + rr, o + j)] = xv[rr];
-          if (hb) {
-#pragma unroll
-            for (int rr = 0; rr < 8; ++rr) Xs[sidx(o + rr, o + j)] = 0.f;  // upper-right 8x8
-          }
+          // upper-right 8x8 is zero: one float4 per lane (row j/2, columns 8 + 4 (j&1) ..)
+          *reinterpret_cast<float4*>(Xs + sidx(o + (j >> 1), o + 8 + 4 * (j & 1))) =
+              make_float4(0.f, 0.f, 0.f, 0.f);
           __syncwarp();
           if (!hb) {
             float y[8];
