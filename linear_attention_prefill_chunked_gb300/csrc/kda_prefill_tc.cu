@@ -69,7 +69,7 @@ constexpr uint32_t OFF_WB = 122880;   // [128 ch][64 tokens]  -W              (M
 constexpr uint32_t OFF_QG = 139264;   // [128 ch][64 tokens]  QG              (MN-major B)
 constexpr uint32_t OFF_BB = 155648;   // [64 r][64 i]         B               (K-major B)
 constexpr uint32_t OFF_KR = 163840;   // [128 ch][64 tokens]  KR              (K-major B)
-constexpr uint32_t OFF_ST = 180224;   // [2 K-atoms][128 v][128 B]  S^T bf16   (K-major A)
+constexpr uint32_t OFF_AM = 180224;   // [k | q][128 ch][128 B]  k rho, q rho (MN-major A)
 constexpr uint32_t OFF_UT = 212992;   // [128 v][64 tokens]   U^T bf16        (K-major A)
 constexpr uint32_t OFF_SMALL = 229376;
 // After MMA-AB completes, the q/k buffer holds the fp32 scratch of the inverse
@@ -81,7 +81,8 @@ constexpr uint32_t OFF_G = OFF_CB + 16384;
 
 // ---- TMEM columns ------------------------------------------------------------------
 constexpr uint32_t TM_U = 0;     // U~ -> U (64)
-constexpr uint32_t TM_O = 64;    // O double buffer (2 x 64)
+constexpr uint32_t TM_O = 64;    // O^T (64)
+constexpr uint32_t TM_SB = 128;  // S^T as bf16 pairs: A operand of MMA-1 (64)
 constexpr uint32_t TM_S = 192;   // S^T fp32 (128)
 constexpr uint32_t TM_AB = 320;  // A/B result (192), later W^T (64)
 
@@ -483,8 +484,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             kw[u] = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128)) : 0u;
             qw[u] = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(64 + r, c0, 128)) : 0u;
           }
-          // KG / QG of channels c0 and c0+1, packed as token pairs while they are formed
-          uint32_t kgw[2][4], qgw[2][4];
+          // k rho, q rho (MN-major A operand of MMA-AB) and KG, QG of channels c0 and
+          // c0+1, packed as token pairs while they are formed
+          uint32_t kaw[2][4], qaw[2][4], kgw[2][4], qgw[2][4];
+          float pa0 = 0.f, pa1 = 0.f, pb0 = 0.f, pb1 = 0.f;
           float pk0 = 0.f, pk1 = 0.f, pq0 = 0.f, pq1 = 0.f;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -493,31 +496,35 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             rho1 *= e1[j];
             const float kr0 = bf_bits(kw[u] & 0xFFFFu) * rho0, kr1 = bf_bits(kw[u] >> 16) * rho1;
             const float qr0 = bf_bits(qw[u] & 0xFFFFu) * rho0, qr1 = bf_bits(qw[u] >> 16) * rho1;
-            kw[u] = pack_bf16x2(kr0, kr1);
-            qw[u] = pack_bf16x2(qr0, qr1);
             if (u & 1) {
+              kaw[0][u >> 1] = pack_bf16x2(pa0, kr0);
+              kaw[1][u >> 1] = pack_bf16x2(pa1, kr1);
+              qaw[0][u >> 1] = pack_bf16x2(pb0, qr0);
+              qaw[1][u >> 1] = pack_bf16x2(pb1, qr1);
               kgw[0][u >> 1] = pack_bf16x2(pk0, kr0 * E0);
               kgw[1][u >> 1] = pack_bf16x2(pk1, kr1 * E1);
               qgw[0][u >> 1] = pack_bf16x2(pq0, qr0 * qs0);
               qgw[1][u >> 1] = pack_bf16x2(pq1, qr1 * qs1);
             } else {
+              pa0 = kr0;
+              pa1 = kr1;
+              pb0 = qr0;
+              pb1 = qr1;
               pk0 = kr0 * E0;
               pk1 = kr1 * E1;
               pq0 = qr0 * qs0;
               pq1 = qr1 * qs1;
             }
           }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int r = sc * 16 + jh * 8 + u;
-            *reinterpret_cast<uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128)) = kw[u];
-            *reinterpret_cast<uint32_t*>(sm + OFF_QK + kmaj_elem(64 + r, c0, 128)) = qw[u];
-          }
           const uint32_t cj = sc * 2 + jh;
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
             const int c = c2 ^ wsel;
             const int row = c0 + c;
+            st_chunk(sm, OFF_AM + sw128_off(row, cj), c ? kaw[1][0] : kaw[0][0], c ? kaw[1][1] : kaw[0][1],
+                     c ? kaw[1][2] : kaw[0][2], c ? kaw[1][3] : kaw[0][3]);
+            st_chunk(sm, OFF_AM + 16384 + sw128_off(row, cj), c ? qaw[1][0] : qaw[0][0],
+                     c ? qaw[1][1] : qaw[0][1], c ? qaw[1][2] : qaw[0][2], c ? qaw[1][3] : qaw[0][3]);
             st_chunk(sm, OFF_KG + sw128_off(row, cj), c ? kgw[1][0] : kgw[0][0], c ? kgw[1][1] : kgw[0][1],
                      c ? kgw[1][2] : kgw[0][2], c ? kgw[1][3] : kgw[0][3]);
             st_chunk(sm, OFF_QG + sw128_off(row, cj), c ? qgw[1][0] : qgw[0][0], c ? qgw[1][1] : qgw[0][1],
@@ -531,10 +538,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       if (t == 0) {
         mbar_arrive(&s->bar[B_GAMMA0 + (gc & 1)]);
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16(128, 192, 0, 1);
+        const uint32_t idesc = idesc_bf16(128, 192, 1, 1);
 #pragma unroll 1
         for (int st = 0; st < 8; ++st) {
-          const uint64_t a = sdesc_sw128(sbase + OFF_QK + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
+          const uint64_t a = sdesc_sw128(sbase + OFF_AM + st * 2048, 16384, 1024);
           const uint64_t b = sdesc_sw128(sbase + OFF_CB + st * 2048, 16384, 1024);
           mma_bf16(tbase + TM_AB, a, b, idesc, st > 0 ? 1u : 0u);
         }
@@ -889,36 +896,6 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   const uint32_t taddr_q = tbase + ((uint32_t)(quad * 32) << 16);
   const uint32_t sbase = smem_u32(sm);
   uint32_t gc = 0;
-  // The output epilogue of a chunk is deferred into the next chunk's MMA-3 window.
-  // Each thread (value channel v) writes its O column straight to global memory: the
-  // 32 lanes of a warp cover 64 contiguous bytes of one output row per store.
-  bool pend = false;
-  int64_t pend_t0 = 0;
-  int pend_cv = 0, pend_h = 0;
-  uint32_t pend_gc = 0;
-
-  // Inside the loop (in_loop): MMA-3a of the pending chunk was committed by the same
-  // thread before MMA-1a of the current one, whose completion E1 already waited on, so
-  // it is complete; waiting on its barrier here could see the barrier already one phase
-  // further (MMA-3a of the current chunk) and never return.  After the loop it is waited.
-  auto o_epilogue = [&](bool in_loop) {
-    if (!pend) return;
-    pend = false;
-    if (!in_loop) wait_bar(p, s, B_M3A, pend_gc & 1);
-    tc_fence_after();
-    __nv_bfloat16* dst = p.o + ((size_t)pend_t0 * p.Hv + pend_h) * kV + v;
-    const size_t rs = (size_t)p.Hv * kV;
-#pragma unroll 1
-    for (int cq = 0; cq < 4; ++cq) {
-      float ov[16];
-      tmem_ld16(taddr_q + TM_O + 64 * (pend_gc & 1) + cq * 16, ov);
-      tmem_ld_wait();
-#pragma unroll
-      for (int u = 0; u < 16; ++u)
-        if (cq * 16 + u < pend_cv) dst[(size_t)(cq * 16 + u) * rs] = __float2bfloat16_rn(ov[u]);
-    }
-    tc_fence_before();
-  };
 
   for (int k = 0;; ++k) {
     const ItemInfo info = next_item(p, s, k, rt == 0, BAR_RG, kRG);
@@ -939,26 +916,24 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         for (int c = 0; c < kK; ++c) dst[(size_t)c * kV + v] = src ? src[(size_t)c * kV + v] : ST(0.f);
       continue;
     }
-    // ---- initial state: S^T row v -> ST (bf16) and TMEM S (pre-decayed by gamma of chunk 0)
+    // ---- initial state: S^T row v -> TMEM as bf16 pairs (MMA-1 operand) and as fp32
+    // pre-decayed by gamma of chunk 0
     wait_bar(p, s, B_GAMMA0 + (gc & 1), (gc >> 1) & 1);
 #pragma unroll 1
-    for (int kq = 0; kq < 8; ++kq) {
-      float sv[16];
+    for (int kq = 0; kq < 4; ++kq) {
+      float sv[32], pw[16];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) sv[u] = src ? to_f32(src[(size_t)(kq * 16 + u) * kV + v]) : 0.f;
-      uint32_t w[8];
+      for (int u = 0; u < 32; ++u) sv[u] = src ? to_f32(src[(size_t)(kq * 32 + u) * kV + v]) : 0.f;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(sv[2 * u], sv[2 * u + 1]);
-      const uint32_t cj = kq * 2;
-      st_chunk(sm, OFF_ST + (cj >> 3) * 16384 + sw128_off(v, cj & 7), w[0], w[1], w[2], w[3]);
-      st_chunk(sm, OFF_ST + ((cj + 1) >> 3) * 16384 + sw128_off(v, (cj + 1) & 7), w[4], w[5], w[6], w[7]);
+      for (int u = 0; u < 16; ++u) pw[u] = __uint_as_float(pack_bf16x2(sv[2 * u], sv[2 * u + 1]));
+      tmem_st16(taddr_q + TM_SB + kq * 16, pw);
 #pragma unroll
-      for (int u = 0; u < 16; ++u) sv[u] *= s->gamma[gc & 1][kq * 16 + u];
-      tmem_st16(taddr_q + TM_S + kq * 16, sv);
+      for (int u = 0; u < 32; ++u) sv[u] *= s->gamma[gc & 1][kq * 32 + u];
+      tmem_st16(taddr_q + TM_S + kq * 32, sv);
+      tmem_st16(taddr_q + TM_S + kq * 32 + 16, sv + 16);
     }
     tmem_st_wait();
     tc_fence_before();
-    fence_async_smem();
     named_bar(BAR_RG, kRG);
 
     bool stop = false;
@@ -974,17 +949,14 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
           tc_fence_after();
           const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
 #pragma unroll 1
-          for (int st = 0; st < 8; ++st) {
-            const uint64_t a = sdesc_sw128(sbase + OFF_ST + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
-            mma_bf16(tbase + TM_U, a, sdesc_sw128(sbase + OFF_WB + st * 2048, 16384, 1024), id1, 1u);
-          }
+          for (int st = 0; st < 8; ++st)
+            mma_bf16_ta(tbase + TM_U, tbase + TM_SB + st * 8,
+                        sdesc_sw128(sbase + OFF_WB + st * 2048, 16384, 1024), id1, 1u);
           mma_commit(&s->bar[B_M1A]);
 #pragma unroll 1
-          for (int st = 0; st < 8; ++st) {
-            const uint64_t a = sdesc_sw128(sbase + OFF_ST + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
-            mma_bf16(tbase + TM_O + 64 * (gc & 1), a,
-                     sdesc_sw128(sbase + OFF_QG + st * 2048, 16384, 1024), id1, st > 0 ? 1u : 0u);
-          }
+          for (int st = 0; st < 8; ++st)
+            mma_bf16_ta(tbase + TM_O, tbase + TM_SB + st * 8,
+                        sdesc_sw128(sbase + OFF_QG + st * 2048, 16384, 1024), id1, st > 0 ? 1u : 0u);
           mma_commit(&s->bar[B_M1B]);
         }
         __syncwarp();
@@ -1042,45 +1014,53 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         mma_commit(&s->bar[B_M3B]);
 #pragma unroll 1
         for (int st = 0; st < 4; ++st)
-          mma_bf16(tbase + TM_O + 64 * (gc & 1), sdesc_sw128(sbase + OFF_UT + st * 32, 16, 1024),
+          mma_bf16(tbase + TM_O, sdesc_sw128(sbase + OFF_UT + st * 32, 16, 1024),
                    sdesc_sw128(sbase + OFF_BB + st * 32, 16, 1024), id3o, 1u);
         mma_commit(&s->bar[B_M3A]);
       }
       __syncwarp();
-      // ---- output of the previous chunk, inside this chunk's MMA-3 window
-      o_epilogue(true);
-      // ---- E2: S -> ST (bf16), or the final state store on the last chunk
+      // ---- E2: S -> TMEM bf16 pairs for the next chunk's MMA-1, or the final state store
       wait_bar(p, s, B_M3B, gc & 1);
       tc_fence_after();
 #pragma unroll 1
-      for (int kq = 0; kq < 8; ++kq) {
-        float sv[16];
-        tmem_ld16(taddr_q + TM_S + kq * 16, sv);
+      for (int kq = 0; kq < 4; ++kq) {
+        float sv[32];
+        tmem_ld16(taddr_q + TM_S + kq * 32, sv);
+        tmem_ld16(taddr_q + TM_S + kq * 32 + 16, sv + 16);
         tmem_ld_wait();
         if (!last) {
-          uint32_t w[8];
+          float pw[16];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(sv[2 * u], sv[2 * u + 1]);
-          const uint32_t cj = kq * 2;
-          st_chunk(sm, OFF_ST + (cj >> 3) * 16384 + sw128_off(v, cj & 7), w[0], w[1], w[2], w[3]);
-          st_chunk(sm, OFF_ST + ((cj + 1) >> 3) * 16384 + sw128_off(v, (cj + 1) & 7), w[4], w[5], w[6], w[7]);
+          for (int u = 0; u < 16; ++u) pw[u] = __uint_as_float(pack_bf16x2(sv[2 * u], sv[2 * u + 1]));
+          tmem_st16(taddr_q + TM_SB + kq * 16, pw);
         } else if (dst) {
 #pragma unroll
-          for (int u = 0; u < 16; ++u) dst[(size_t)(kq * 16 + u) * kV + v] = from_f32<ST>(sv[u]);
+          for (int u = 0; u < 32; ++u) dst[(size_t)(kq * 32 + u) * kV + v] = from_f32<ST>(sv[u]);
+        }
+      }
+      tmem_st_wait();
+      // ---- output of this chunk, complete once MMA-3a ran; each thread (value channel
+      // v) writes its column straight to global memory, the 32 lanes of a warp covering
+      // 64 contiguous bytes of one output row per store
+      wait_bar(p, s, B_M3A, gc & 1);
+      tc_fence_after();
+      {
+        __nv_bfloat16* od = p.o + ((size_t)t0 * p.Hv + h) * kV + v;
+        const size_t rs = (size_t)p.Hv * kV;
+#pragma unroll 1
+        for (int cq = 0; cq < 4; ++cq) {
+          float ov[16];
+          tmem_ld16(taddr_q + TM_O + cq * 16, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            if (cq * 16 + u < cv) od[(size_t)(cq * 16 + u) * rs] = __float2bfloat16_rn(ov[u]);
         }
       }
       tc_fence_before();
-      fence_async_smem();
-      named_bar(BAR_RG, kRG);
-      pend = true;
-      pend_t0 = t0;
-      pend_cv = cv;
-      pend_h = h;
-      pend_gc = gc;
     }
     if (stop) break;
   }
-  o_epilogue(false);
   named_bar(BAR_RG, kRG);
   if (leader_warp) {
     if (lane == 0) mma_commit(&s->bar[B_DRAIN_RG]);
