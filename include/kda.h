@@ -135,6 +135,34 @@ kda_status_t kda_chunk_prefill(const kda_desc_t *desc, const void *q, const void
                                void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Chunked KDA prefill with the gate activation computed in the kernel: instead of
+ * reading the fp32 log-decay g, it reads the pre-activation a and computes, per
+ * (token t, v-head h, key channel c),
+ *
+ *   g[t,h,c] = max( -exp(A_log[h]) * softplus(a[t,h,c] + dt_bias[h,c]), lower_bound )
+ *
+ * with softplus(x) = log(1 + exp(x)).  The -exp(A_log) * softplus(a + dt_bias) form
+ * is the gate of the pages' tests (PR 30169 digest, 关键源码片段, the GDN pool test;
+ * PR 27488 digest, 关键源码片段: CuteDSLKDAKernel.extend takes A_log, dt_bias and
+ * lower_bound); here it is per key channel, as KDA's gate is.  The pages name
+ * lower_bound without a formula; it is read as a floor on g.
+ *
+ *   a            [>=T, Hv, K] qkv_dtype (16-byte aligned)
+ *   A_log        [Hv] fp32
+ *   dt_bias      [Hv, K] fp32, or NULL for zero
+ *   lower_bound  <= 0; -INFINITY for none (NaN or > 0 is KDA_ERR_INVALID_ARGUMENT)
+ *
+ * Every other argument, the workspace, the modes and the error behaviour are those
+ * of kda_chunk_prefill().  The bf16 a is half the bytes of the fp32 g it replaces.
+ */
+kda_status_t kda_chunk_prefill_act(const kda_desc_t *desc, const void *q, const void *k,
+                                   const void *v, const void *a, const float *A_log,
+                                   const float *dt_bias, float lower_bound, const float *beta,
+                                   const int32_t *cu_seqlens, void *state,
+                                   const int32_t *state_indices, void *final_state, void *o,
+                                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * One-token-per-row KDA decode, updating a state pool in place.
  *
  *   q, k   [N, Hk, K]   v [N, Hv, V]   g [>=N, Hv, K] fp32   beta [>=N, Hv] fp32

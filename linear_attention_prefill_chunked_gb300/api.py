@@ -50,7 +50,7 @@ class KdaDesc(ctypes.Structure):
 
 EXPORTS = ("kda_chunk_prefill_workspace_size", "kda_decode_workspace_size", "kda_chunk_prefill",
            "kda_decode", "kda_read_device_status", "kda_chunk_prefill_path", "kda_status_string",
-           "kda_chunk_prefill_noalloc")
+           "kda_chunk_prefill_noalloc", "kda_chunk_prefill_act")
 
 _lib = None
 
@@ -87,6 +87,9 @@ def load(build_if_missing: bool = True):
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_chunk_prefill_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P]
     lib.kda_chunk_prefill_noalloc.restype = ctypes.c_int
+    lib.kda_chunk_prefill_act.argtypes = [D, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, P, P,
+                                          ctypes.c_size_t, P]
+    lib.kda_chunk_prefill_act.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -166,10 +169,38 @@ def chunk_prefill(q, k, v, g, beta, cu_seqlens, *, state=None, state_indices=Non
     [N, Hv, K, V] tensor (or ``final_state`` if given, may be ``state``) or None
     when ``output_final_state`` is False.
     """
+    _need(g, "g", torch.float32)
+    return _prefill(q, k, v, g, None, beta, cu_seqlens, state, state_indices, final_state,
+                    output_final_state, scale, slot_stride, out, workspace, stream,
+                    cuda_core_path, chunk_prefill)
+
+
+def chunk_prefill_act(q, k, v, a, A_log, dt_bias, beta, cu_seqlens, *, lower_bound=None,
+                      state=None, state_indices=None, final_state=None, output_final_state=True,
+                      scale=None, slot_stride=0, out=None, workspace=None, stream=None,
+                      cuda_core_path=False):
+    """Chunked KDA prefill with the gate computed in the kernel (kda_chunk_prefill_act):
+    ``g = max(-exp(A_log[h]) * softplus(a + dt_bias[h]), lower_bound)``.
+
+    a [>=T, Hv, K] in the dtype of q/k/v; A_log [Hv] fp32; dt_bias [Hv, K] fp32 or None;
+    lower_bound a float <= 0 or None.  Everything else as :func:`chunk_prefill`.
+    """
+    _need(a, "a", q.dtype)
+    _need(A_log, "A_log", torch.float32)
+    if dt_bias is not None:
+        _need(dt_bias, "dt_bias", torch.float32)
+    lb = float("-inf") if lower_bound is None else float(lower_bound)
+    return _prefill(q, k, v, None, (a, A_log, dt_bias, lb), beta, cu_seqlens, state,
+                    state_indices, final_state, output_final_state, scale, slot_stride, out,
+                    workspace, stream, cuda_core_path, chunk_prefill_act)
+
+
+def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_state,
+             output_final_state, scale, slot_stride, out, workspace, stream, cuda_core_path,
+             owner):
     lib = load()
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need(t, name)
-    _need(g, "g", torch.float32)
     _need(beta, "beta", torch.float32)
     _need(cu_seqlens, "cu_seqlens", torch.int32)
     if q.dtype != k.dtype or q.dtype != v.dtype:
@@ -204,12 +235,23 @@ def chunk_prefill(q, k, v, g, beta, cu_seqlens, *, state=None, state_indices=Non
         raise KdaError(1, "kda_chunk_prefill_workspace_size")
     if workspace is None or workspace.numel() < ws_size:
         workspace = torch.empty(ws_size, dtype=torch.uint8, device=q.device)
-    rc = lib.kda_chunk_prefill(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                               _ptr(cu_seqlens), _ptr(state), _ptr(state_indices),
-                               _ptr(final_state), _ptr(out), _ptr(workspace),
-                               workspace.numel(), _stream(stream))
+    if act is None:
+        rc = lib.kda_chunk_prefill(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                   _ptr(cu_seqlens), _ptr(state), _ptr(state_indices),
+                                   _ptr(final_state), _ptr(out), _ptr(workspace),
+                                   workspace.numel(), _stream(stream))
+        name = "kda_chunk_prefill"
+    else:
+        a, A_log, dt_bias, lb = act
+        rc = lib.kda_chunk_prefill_act(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                                       _ptr(A_log), _ptr(dt_bias), lb, _ptr(beta),
+                                       _ptr(cu_seqlens), _ptr(state), _ptr(state_indices),
+                                       _ptr(final_state), _ptr(out), _ptr(workspace),
+                                       workspace.numel(), _stream(stream))
+        name = "kda_chunk_prefill_act"
     if rc != 0:
-        raise KdaError(rc, "kda_chunk_prefill")
+        raise KdaError(rc, name)
+    owner.last_workspace = workspace
     chunk_prefill.last_workspace = workspace
     return out, final_state
 

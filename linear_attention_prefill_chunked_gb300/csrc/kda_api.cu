@@ -77,16 +77,19 @@ size_t kda_decode_workspace_size(const kda_desc_t* d) {
   return kWsPayload;
 }
 
-kda_status_t kda_chunk_prefill(const kda_desc_t* d, const void* q, const void* k, const void* v,
-                               const float* g, const float* beta, const int32_t* cu_seqlens,
-                               void* state, const int32_t* state_indices, void* final_state,
-                               void* o, void* workspace, size_t workspace_bytes,
-                               cudaStream_t stream) {
+namespace {
+// Shared by kda_chunk_prefill (g given) and kda_chunk_prefill_act (g from a).
+kda_status_t prefill_common(const kda_desc_t* d, const void* q, const void* k, const void* v,
+                            const float* g, const kda::GateAct& act, const float* beta,
+                            const int32_t* cu_seqlens, void* state, const int32_t* state_indices,
+                            void* final_state, void* o, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
   if (!dims_ok(d)) return KDA_ERR_INVALID_ARGUMENT;
   if (!heads_supported(d)) return KDA_ERR_UNSUPPORTED;
   if (d->num_v_heads > 65535) return KDA_ERR_UNSUPPORTED;  // grid.y limit
   if (!cu_seqlens || !workspace || !aligned(workspace, 256)) return KDA_ERR_INVALID_ARGUMENT;
-  if (d->total_tokens > 0 && (!q || !k || !v || !g || !beta || !o))
+  const bool has_gate = act.a ? (act.A_log != nullptr) : (g != nullptr);
+  if (d->total_tokens > 0 && (!q || !k || !v || !has_gate || !beta || !o))
     return KDA_ERR_INVALID_ARGUMENT;
   const bool pool = state_indices != nullptr;
   if (pool) {
@@ -94,7 +97,7 @@ kda_status_t kda_chunk_prefill(const kda_desc_t* d, const void* q, const void* k
     if (final_state != nullptr && final_state != state) return KDA_ERR_INVALID_ARGUMENT;
   }
   {
-    const void* ptrs[] = {q, k, v, g, o, state, final_state};
+    const void* ptrs[] = {q, k, v, g, act.a, o, state, final_state};
     for (const void* p : ptrs)
       if (p && !aligned(p, 16)) return KDA_ERR_INVALID_ARGUMENT;
   }
@@ -104,7 +107,7 @@ kda_status_t kda_chunk_prefill(const kda_desc_t* d, const void* q, const void* k
   a.d = *d;
   a.scale = eff_scale(d);
   a.slot_stride = pool ? slot_pitch(d) : (int64_t)d->num_v_heads * d->head_k_dim * d->head_v_dim;
-  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu = cu_seqlens;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.act = act; a.beta = beta; a.cu = cu_seqlens;
   a.state_in = state;
   a.idx = state_indices;
   a.state_out = pool ? state : final_state;
@@ -120,6 +123,30 @@ kda_status_t kda_chunk_prefill(const kda_desc_t* d, const void* q, const void* k
   cudaError_t err = kda::prefill_tc_supported(*d) ? kda::launch_prefill_tc(a, stream)
                                                   : kda::launch_prefill_simt(a, stream);
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+}  // namespace
+
+kda_status_t kda_chunk_prefill(const kda_desc_t* d, const void* q, const void* k, const void* v,
+                               const float* g, const float* beta, const int32_t* cu_seqlens,
+                               void* state, const int32_t* state_indices, void* final_state,
+                               void* o, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+  const kda::GateAct none{nullptr, nullptr, nullptr, -INFINITY};
+  return prefill_common(d, q, k, v, g, none, beta, cu_seqlens, state, state_indices, final_state,
+                        o, workspace, workspace_bytes, stream);
+}
+
+kda_status_t kda_chunk_prefill_act(const kda_desc_t* d, const void* q, const void* k,
+                                   const void* v, const void* a, const float* A_log,
+                                   const float* dt_bias, float lower_bound, const float* beta,
+                                   const int32_t* cu_seqlens, void* state,
+                                   const int32_t* state_indices, void* final_state, void* o,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (d && d->total_tokens > 0 && (!a || !A_log)) return KDA_ERR_INVALID_ARGUMENT;
+  if (lower_bound != lower_bound || lower_bound > 0.f) return KDA_ERR_INVALID_ARGUMENT;  // NaN or > 0
+  const kda::GateAct act{a, A_log, dt_bias, lower_bound};
+  return prefill_common(d, q, k, v, nullptr, act, beta, cu_seqlens, state, state_indices,
+                        final_state, o, workspace, workspace_bytes, stream);
 }
 
 kda_status_t kda_decode(const kda_desc_t* d, const void* q, const void* k, const void* v,

@@ -55,12 +55,26 @@ __device__ __forceinline__ bool seq_bounds(const int32_t* cu, int n, int64_t T, 
 
 // Internal launchers (C++ linkage, defined in the .cu files).
 namespace kda {
+// In-kernel gate activation.  When `a` is set the log-decay is not read from g but
+// computed per (token, v-head, channel) as
+//   g = max(-exp(A_log[h]) * softplus(a + dt_bias[h][c]), lb)
+// (the gate form of the KDA / GDN tests in the sglang PR 27488 and PR 30169 digests).
+struct GateAct {
+  const void* a;         // [T, Hv, K], qkv dtype; null: g is given
+  const float* A_log;    // [Hv]
+  const float* dt_bias;  // [Hv, K] or null
+  float lb;              // lower bound of g; -inf: none
+};
+// softplus(x) = log(1 + e^x), evaluated without overflow
+__device__ __forceinline__ float softplus_f32(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
+
 struct PrefillArgs {
   kda_desc_t d;
   float scale;
   int64_t slot_stride;
   const void *q, *k, *v;
   const float *g, *beta;
+  GateAct act;               // act.a null: g is given
   const int32_t* cu;
   const void* state_in;      // pool, dense h0 or null
   const int32_t* idx;        // null in dense mode

@@ -52,7 +52,8 @@ kda_prefill_simt_kernel(const QT* __restrict__ q, const QT* __restrict__ k,
                         const float* __restrict__ beta, const int32_t* __restrict__ cu,
                         const ST* state_in, const int32_t* __restrict__ idx, ST* state_out,
                         QT* __restrict__ o, uint32_t* __restrict__ status, int Hk, int Hv,
-                        int64_t T, int64_t num_slots, int64_t slot_stride, float scale) {
+                        int64_t T, int64_t num_slots, int64_t slot_stride, float scale,
+                        GateAct act) {
   using L = SimtSmem<K, V>;
   extern __shared__ float smem[];
   float* Kb = smem + L::kb;
@@ -90,6 +91,8 @@ kda_prefill_simt_kernel(const QT* __restrict__ q, const QT* __restrict__ k,
   for (int e = tid; e < K * V; e += kSimtThreads) S[e] = src ? to_f32(src[e]) : 0.f;
 
   const int kh = h / (Hv / Hk);
+  const QT* ga = static_cast<const QT*>(act.a);
+  const float Ah = ga ? expf(act.A_log[h]) : 0.f;
   for (int64_t t0 = bos; t0 < eos; t0 += kC) {
     const int c = (int)((eos - t0) < kC ? (eos - t0) : kC);
     __syncthreads();  // previous chunk's readers of every buffer are done
@@ -100,7 +103,17 @@ kda_prefill_simt_kernel(const QT* __restrict__ q, const QT* __restrict__ k,
       const size_t qk = ((size_t)(t0 + r) * Hk + kh) * K + ch;
       Kb[r * DP + ch] = ok ? to_f32(k[qk]) : 0.f;
       Qb[r * KP + ch] = ok ? to_f32(q[qk]) : 0.f;
-      Gb[r * KP + ch] = ok ? g[((size_t)(t0 + r) * Hv + h) * K + ch] : 0.f;
+      float gv = 0.f;
+      if (ok) {
+        const size_t gi = ((size_t)(t0 + r) * Hv + h) * K + ch;
+        if (ga) {
+          const float x = to_f32(ga[gi]) + (act.dt_bias ? act.dt_bias[(size_t)h * K + ch] : 0.f);
+          gv = fmaxf(-Ah * softplus_f32(x), act.lb);
+        } else {
+          gv = g[gi];
+        }
+      }
+      Gb[r * KP + ch] = gv;
     }
     for (int e = tid; e < kC * V; e += kSimtThreads) {
       const int r = e / V, j = e % V;
@@ -208,7 +221,7 @@ cudaError_t launch_typed(const PrefillArgs& a, cudaStream_t st) {
   kern<<<grid, kSimtThreads, L::bytes, st>>>(
       (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, a.cu,
       (const ST*)a.state_in, a.idx, (ST*)a.state_out, (QT*)a.o, a.status, a.d.num_k_heads,
-      a.d.num_v_heads, a.d.total_tokens, a.d.num_slots, a.slot_stride, a.scale);
+      a.d.num_v_heads, a.d.total_tokens, a.d.num_slots, a.slot_stride, a.scale, a.act);
   return cudaGetLastError();
 }
 

@@ -129,6 +129,8 @@ struct TcParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_g;
   const __nv_bfloat16 *q, *k;
   const float *g, *beta;
+  GateAct act;        // act.a set: tm_g maps the gate input a (bf16) instead of g
+  uint32_t g_bytes;   // bytes of one staged gate tile (g: 32768, a: 16384)
   const int32_t *cu, *idx, *order;
   const void* state_in;
   void* state_out;
@@ -270,7 +272,7 @@ struct Loader {  // used by thread 0 only
     ++st->n_qk;
   }
   __device__ void load_g(const TcParams& p, uint8_t* sm, Small* s, int h, int t0) {
-    mbar_expect_tx(&s->bar[B_G_FULL], 32768);
+    mbar_expect_tx(&s->bar[B_G_FULL], p.g_bytes);
     tma_load_3d(sm + OFF_G, &p.tm_g, &s->bar[B_G_FULL], 0, h, t0);
     ++st->n_g;
   }
@@ -332,7 +334,16 @@ __device__ __noinline__ void unsafe_diag_terms(const TcParams& p, const Small* s
         for (int i = r; i >= a * 16; --i) {
           const float ki = __bfloat162float(p.k[((size_t)(t0 + i) * p.Hk + kh) * kK + c]);
           row[sidx(r, i)] += xr * ki * pr;
-          pr *= __expf(p.g[((size_t)(t0 + i) * p.Hv + h) * kK + c]);
+          const size_t gi = ((size_t)(t0 + i) * p.Hv + h) * kK + c;
+          float gv;
+          if (p.act.a) {
+            const float x = __bfloat162float(static_cast<const __nv_bfloat16*>(p.act.a)[gi]) +
+                            (p.act.dt_bias ? p.act.dt_bias[(size_t)h * kK + c] : 0.f);
+            gv = fmaxf(-__expf(p.act.A_log[h]) * softplus_f32(x), p.act.lb);
+          } else {
+            gv = p.g[gi];
+          }
+          pr *= __expf(gv);
           if (pr == 0.f) break;
         }
       }
@@ -363,6 +374,16 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
     const ItemInfo info = next_item(p, s, k, t == 0, BAR_IG, kIG);
     if (info.done) break;
     const int h = info.h, kh = info.kh;
+    // gate activation constants of this head for this thread's channel pair
+    float gA = 0.f, gdb0 = 0.f, gdb1 = 0.f;
+    if (p.act.a) {
+      const int cg = 2 * ((warp & 1) * 32 + lane);
+      gA = __expf(p.act.A_log[h]);
+      if (p.act.dt_bias) {
+        gdb0 = p.act.dt_bias[(size_t)h * kK + cg];
+        gdb1 = p.act.dt_bias[(size_t)h * kK + cg + 1];
+      }
+    }
     bool stop = false;
     for (int lc = 0; lc < info.nchunks; ++lc, ++gc) {
       if (named_bar_any(BAR_IG, kIG, aborted(s))) { stop = true; break; }
@@ -387,12 +408,26 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       bt_ok = false;
       wait_bar(p, s, B_G_FULL, gc & 1);
       float e0[16], e1[16];
+      if (!p.act.a) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int r = sc * 16 + j;
-        const float2 gv = *reinterpret_cast<const float2*>(Gs + r * kK + c0);
-        e0[j] = (r < cv) ? __expf(gv.x) : 1.f;  // padded rows: decay 1
-        e1[j] = (r < cv) ? __expf(gv.y) : 1.f;
+        for (int j = 0; j < 16; ++j) {
+          const int r = sc * 16 + j;
+          const float2 gv = *reinterpret_cast<const float2*>(Gs + r * kK + c0);
+          e0[j] = (r < cv) ? __expf(gv.x) : 1.f;  // padded rows: decay 1
+          e1[j] = (r < cv) ? __expf(gv.y) : 1.f;
+        }
+      } else {  // staged tile is a ([64][128] bf16): g = max(-A softplus(a + dt_bias), lb)
+        const uint8_t* Ga = sm + OFF_G;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = sc * 16 + j;
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(Ga + r * 256 + c0 * 2);
+          const float x0 = bf_bits(w & 0xFFFFu) + gdb0, x1 = bf_bits(w >> 16) + gdb1;
+          const float g0 = fmaxf(-gA * (fmaxf(x0, 0.f) + __logf(1.f + __expf(-fabsf(x0)))), p.act.lb);
+          const float g1 = fmaxf(-gA * (fmaxf(x1, 0.f) + __logf(1.f + __expf(-fabsf(x1)))), p.act.lb);
+          e0[j] = (r < cv) ? __expf(g0) : 1.f;
+          e1[j] = (r < cv) ? __expf(g1) : 1.f;
+        }
       }
       float pm0 = 1.f, pm1 = 1.f;
 #pragma unroll
@@ -1182,14 +1217,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, d.num_v_heads, kV, 64,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&p.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T, d.num_v_heads, kK, kK,
-                  CU_TENSOR_MAP_SWIZZLE_NONE))
+        !(a.act.a ? make_map(&p.tm_g, a.act.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, d.num_v_heads,
+                             kK, kK, CU_TENSOR_MAP_SWIZZLE_NONE)
+                  : make_map(&p.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T, d.num_v_heads, kK,
+                             kK, CU_TENSOR_MAP_SWIZZLE_NONE)))
       return cudaErrorInvalidValue;
   }
   int32_t* order = reinterpret_cast<int32_t*>(a.ws + kWsPayload);
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.k = static_cast<const __nv_bfloat16*>(a.k);
   p.g = a.g;
+  p.act = a.act;
+  p.g_bytes = a.act.a ? 16384u : 32768u;
   p.beta = a.beta;
   p.cu = a.cu;
   p.idx = a.idx;

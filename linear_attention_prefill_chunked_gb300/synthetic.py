@@ -201,3 +201,24 @@ WORKLOADS = {
     "throughput": throughput,
     "decode_batch": decode_batch,
 }
+
+
+def gate_act_inputs(T, Hv, K, *, dtype=BF16, seed=0, rows=None, A_max=16.0):
+    """Inputs of the in-kernel gate activation, drawn like the pages' gate tests
+    (sglang PR 30169 digest, 关键源码片段, the GDN pool test: A ~ U(0, 16) per head,
+    dt log-uniform in [1e-3, 1e-1] and floored at 1e-4, dt_bias the value whose
+    softplus is dt), with a key-channel axis for the KDA gate.
+
+    Returns ``(a, A_log, dt_bias)``: a [rows or T, Hv, K] ~ N(0, 1) in ``dtype``;
+    A_log [Hv] fp32; dt_bias [Hv, K] fp32.  Drawn from its own generator (seed)
+    so that the workloads of :func:`make` keep their values.
+    """
+    gen = torch.Generator().manual_seed(seed + 7919)
+    n = T if rows is None else rows
+    a = _normal((n, Hv, K), gen).to(dtype)
+    A = torch.rand(Hv, generator=gen, dtype=F32) * A_max
+    A_log = torch.log(torch.clamp(A, min=1e-6))
+    lo, hi = math.log(1e-3), math.log(1e-1)
+    dt = torch.exp(torch.rand(Hv, K, generator=gen, dtype=F32) * (hi - lo) + lo).clamp(min=1e-4)
+    dt_bias = torch.log(torch.expm1(dt))  # softplus(dt_bias) = dt
+    return a.contiguous(), A_log.contiguous(), dt_bias.contiguous()

@@ -114,3 +114,27 @@ def decode(q, k, v, g, beta, *, pool, state_indices, scale=None, num_threads: in
     cu = np.arange(n + 1, dtype=np.int32)
     return recurrence(q, k, v, g, beta, cu, scale=scale, state=pool,
                       state_indices=state_indices, num_threads=num_threads)
+
+
+def gate_activation(a, A_log, dt_bias=None, lower_bound=None):
+    """Log-decay from the gate pre-activation, in fp64:
+    ``g[t,h,c] = max(-exp(A_log[h]) * softplus(a[t,h,c] + dt_bias[h,c]), lower_bound)``.
+
+    The ``-exp(A_log) * softplus(a + dt_bias)`` form is the gate the pages' tests build
+    (sglang PR 30169 digest, 关键源码片段: the GDN pool test, one scalar per head there);
+    the KDA prefill entry takes ``A_log``, ``dt_bias`` and ``lower_bound``
+    (PR 27488 digest, 关键源码片段: ``CuteDSLKDAKernel.extend``).  Here ``a`` and
+    ``dt_bias`` carry a key-channel axis, as KDA's per-channel gate does.  The pages
+    name ``lower_bound`` without a formula; it is read as a floor on g.
+
+    softplus(x) = log(1 + e^x), evaluated as max(x, 0) + log1p(e^-|x|) so that no
+    intermediate overflows.  a [T, Hv, K]; A_log [Hv]; dt_bias [Hv, K] or None.
+    """
+    a = _f64(a)
+    A = np.exp(_f64(A_log))
+    x = a + (_f64(dt_bias)[None, :, :] if dt_bias is not None else 0.0)
+    sp = np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+    g = -A[None, :, None] * sp
+    if lower_bound is not None:
+        g = np.maximum(g, float(lower_bound))
+    return g
