@@ -61,13 +61,15 @@ def _traffic_from_profile():
     return int(kv["bytes_per_launch"])
 
 
-def algorithmic_bytes(w):
-    """Bytes the path must move once: q, k, v, g, beta in; o out; pool rows in and out."""
+def algorithmic_bytes(w, gate_act=False):
+    """Bytes the path must move once: q, k, v, g (or the gate pre-activation a with A_log and
+    dt_bias), beta in; o out; pool rows in and out."""
     T, Hk, K = w.q.shape
     Hv, V = w.v.shape[1], w.v.shape[2]
     e = w.q.element_size()
     se = w.state.element_size() if w.state is not None else 4
-    return (T * Hk * K * e * 2 + T * Hv * V * e + T * Hv * K * 4 + T * Hv * 4 + T * Hv * V * e
+    gate = (T * Hv * K * e + Hv * 4 + Hv * K * 4) if gate_act else T * Hv * K * 4
+    return (T * Hk * K * e * 2 + T * Hv * V * e + gate + T * Hv * 4 + T * Hv * V * e
             + w.N * Hv * K * V * se * 2)
 
 
@@ -205,9 +207,15 @@ def run_ours(args, dist, ws, rank, local):
                            num_slots=16, name="profile_8x1024_Hv32_K128")
     else:
         w = synthetic.throughput()
+    act = args.gate == "act"
+    if act:  # the kernel computes the gate from a bf16 pre-activation
+        a_h, A_log_h, dtb_h = synthetic.gate_act_inputs(w.T, 32, 128, seed=0)
+        w.name += "_gate_act"
     t = lambda x: x.to(dev).contiguous()
     q, k, v, g, beta, cu, idx = (t(x) for x in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens,
                                                  w.state_indices))
+    if act:
+        a_d, A_log_d, dtb_d = t(a_h), t(A_log_h), t(dtb_h)
     pool = t(w.state)
     out = torch.empty((w.T, 32, 128), dtype=torch.bfloat16, device=dev)
     desc = kda.make_desc(num_seqs=w.N, total_tokens=w.T, Hk=32, Hv=32, K=128, V=128,
@@ -217,8 +225,12 @@ def run_ours(args, dist, ws, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        kda.chunk_prefill(q, k, v, g, beta, cu, state=pool, state_indices=idx, out=out,
-                          workspace=ws_t, stream=stream)
+        if act:
+            kda.chunk_prefill_act(q, k, v, a_d, A_log_d, dtb_d, beta, cu, state=pool,
+                                  state_indices=idx, out=out, workspace=ws_t, stream=stream)
+        else:
+            kda.chunk_prefill(q, k, v, g, beta, cu, state=pool, state_indices=idx, out=out,
+                              workspace=ws_t, stream=stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -249,8 +261,8 @@ def run_ours(args, dist, ws, rank, local):
     e2e_ms, h2d, d2h = None, 0, 0
     if not args.no_e2e:
         hq, hk, hv, hg, hb, hcu, hidx = (x.contiguous().pin_memory() for x in
-                                         (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens,
-                                          w.state_indices))
+                                         (w.q, w.k, w.v, a_h if act else w.g, w.beta,
+                                          w.cu_seqlens, w.state_indices))
         h_out = torch.empty((w.T, 32, 128), dtype=torch.bfloat16).pin_memory()
         h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hg, hb, hcu, hidx))
         d2h = h_out.numel() * h_out.element_size()
@@ -258,8 +270,12 @@ def run_ours(args, dist, ws, rank, local):
         def e2e_step():
             dq, dk, dv, dg, db, dcu, didx = (x.to(dev, non_blocking=True) for x in
                                              (hq, hk, hv, hg, hb, hcu, hidx))
-            o, _ = kda.chunk_prefill(dq, dk, dv, dg, db, dcu, state=pool, state_indices=didx,
-                                     workspace=ws_t, stream=stream)
+            if act:
+                o, _ = kda.chunk_prefill_act(dq, dk, dv, dg, A_log_d, dtb_d, db, dcu, state=pool,
+                                             state_indices=didx, workspace=ws_t, stream=stream)
+            else:
+                o, _ = kda.chunk_prefill(dq, dk, dv, dg, db, dcu, state=pool, state_indices=didx,
+                                         workspace=ws_t, stream=stream)
             h_out.copy_(o, non_blocking=True)
 
         for _ in range(2):
@@ -279,7 +295,7 @@ def run_ours(args, dist, ws, rank, local):
     hbm, bf16, src = _peaks()
     ms = total_ms / args.steps
     value = ws * w.T / (ms * 1e-3)
-    nbytes = algorithmic_bytes(w)
+    nbytes = algorithmic_bytes(w, act)
     flops = algorithmic_flops(w)
     kern_ms = statistics.median(per)
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
@@ -292,7 +308,9 @@ def run_ours(args, dist, ws, rank, local):
         "config": {"workload": w.name, "tokens": w.T, "num_seqs": w.N, "Hk": 32, "Hv": 32,
                    "K": 128, "V": 128, "chunk": 64, "state_pool": "fp32, 256 slots, in place",
                    "kernel_path": "tcgen05 fused" if path == 1 else "CUDA-core fp32",
-                   "l2": "inputs larger than L2 (1.68 GB per step), no flush",
+                   "gate": ("in-kernel activation of a bf16 pre-activation" if act
+                            else "fp32 log-decay input"),
+                   "l2": f"inputs larger than L2 ({nbytes / 1e9:.2f} GB per step), no flush",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
@@ -303,12 +321,15 @@ def run_ours(args, dist, ws, rank, local):
         "e2e": {"value": (w.T / (e2e_ms * 1e-3)) if e2e_ms else None, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "note": "pinned host q/k/v/g/beta/cu_seqlens/indices copied in, o copied out each "
-                        "step; the state pool stays resident on the device"},
+                "note": f"pinned host q/k/v/{'a' if act else 'g'}/beta/cu_seqlens/indices copied in, "
+                        "o copied out each step; the state pool stays resident on the device"},
         "gpu_launches": args.steps * (2 if path == 1 else 1),
         "device_status": bits, "wall_s": wall,
     }
     if ws == 1 and not args.no_cpu_baseline:
+        if act:  # the oracle gets the gate its own activation computes from a
+            from oracle import kda_oracle
+            w.g = torch.from_numpy(kda_oracle.gate_activation(a_h, A_log_h, dtb_h)).float()
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line), flush=True)
 
@@ -321,6 +342,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gate", default="given", choices=["given", "act"],
+                    help="act: the gate computed in the kernel from a bf16 pre-activation "
+                         "(kda_chunk_prefill_act)")
     ap.add_argument("--workload", default="throughput", choices=["throughput", "profile"],
                     help="profile: 8 x 1024 tokens, Hv=32 (a smaller case for ncu captures)")
     args = ap.parse_args()

@@ -21,7 +21,7 @@
 //     block 0: k kap                  (adjacent sub-chunk pairs)
 //     block 1: k kap pi_1, k kap pi_1 pi_2, k kap pi_2, 0   (distance 2 and 3)
 //     block 2: k kap / pi_s = k / rho (diagonal sub-chunks) on channels whose
-//              sub-chunk product pi_s >= 2^-64; the remaining ("unsafe")
+//              sub-chunk product pi_s >= 2^-100; the remaining ("unsafe")
 //              channels get their diagonal terms from an exact pairwise loop.
 //   Tm = (I + A)^-1 Diag(beta): 16x16 diagonal blocks by fp32 forward
 //   substitution, off-diagonal blocks by block forward substitution with tf32
@@ -57,7 +57,10 @@ constexpr int kK = 128;
 constexpr int kV = 128;
 constexpr int kThreads = 384;
 constexpr int kRing = 4;
-constexpr float kSafeMin = 5.421010862427522e-20f;  // 2^-64
+// Sub-chunk gate products down to 2^-100 keep k rho >= |k| 2^-100 and k / rho <= 2^100
+// normal in bf16 and fp32 (8 exponent bits): the factorised diagonal blocks stay exact to
+// bf16 rounding.  Below it a channel takes the pairwise path.
+constexpr float kSafeMin = 7.888609052210118e-31f;  // 2^-100
 
 // ---- shared memory map (offsets from a 1024-aligned base) -------------------------
 constexpr uint32_t OFF_QK = 0;        // [2 K-atoms][128 rows: k 0-63 | q 64-127][128 B]
@@ -312,7 +315,7 @@ struct Loader {  // used by thread 0 only
 };
 
 // Exact pairwise terms of the diagonal sub-chunk blocks on "unsafe" channels (sub-chunk
-// gate product below 2^-64), added to the raw A (As) and B (Xs) rows: thread = TMEM
+// gate product below 2^-100), added to the raw A (As) and B (Xs) rows: thread = TMEM
 // lane L (row L & 63 of A for L < 64, of B otherwise).  Kept out of line: it never
 // runs at ordinary gates and would otherwise raise the register pressure of the
 // chunk loop.
@@ -435,7 +438,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // exchange the sub-chunk products through the Tm buffer (idle until the inverse)
       float* pis = reinterpret_cast<float*>(sm + OFF_TM);
       *reinterpret_cast<float2*>(pis + sc * kK + c0) = make_float2(pm0, pm1);
-      {  // "unsafe" channels of this sub-chunk (product below 2^-64 or not finite)
+      {  // "unsafe" channels of this sub-chunk (product below 2^-100 or not finite)
         const uint32_t m0 = __ballot_sync(0xffffffffu, !(pm0 >= kSafeMin));
         const uint32_t m1 = __ballot_sync(0xffffffffu, !(pm1 >= kSafeMin));
         if (lane == 0) {

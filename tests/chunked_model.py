@@ -16,7 +16,7 @@ Per chunk of C tokens (aligned to the sequence start, last one partial):
   off-diagonal sub-chunk blocks (row block a > column block b) factor as
       (k_r rho_r) . (k_i kap_i prod_{b<s<a} pi_s)            every factor <= 1
   diagonal blocks use (k_r rho_r) . (k_i / rho_i) on channels whose sub-chunk
-  product pi_a >= 2**-64 (so 1/rho <= 2**64), and the explicit pairwise product
+  product pi_a >= 2**-100 (so 1/rho <= 2**100), and the explicit pairwise product
   on the remaining ("unsafe") channels.
 
   Tm = (I + A)^-1 diag(beta)   (16x16 diagonal blocks by forward substitution,
@@ -25,7 +25,7 @@ Per chunk of C tokens (aligned to the sequence start, last one partial):
 """
 import numpy as np
 
-SAFE_MIN = 2.0 ** -64
+SAFE_MIN = 2.0 ** -100
 
 
 def tri_inv_unit_lower_blocked(A, bs=16):
