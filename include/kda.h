@@ -62,6 +62,12 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
 /* Descriptor flags. */
 #define KDA_FLAG_CUDA_CORE_PATH  0x1u  /* prefill: run the fp32 CUDA-core kernel even where
                                           the tensor-core kernel applies (cross-checks) */
+#define KDA_FLAG_SCALAR_GATE     0x2u  /* prefill and decode: the gate carries one value per
+                                          (token, v-head), shared by all key channels -- the
+                                          gated-delta-net (GDN) form that the pages' pool test
+                                          runs (PR 30169 digest, 关键源码片段).  g is then
+                                          [>=T, Hv] fp32 and, for kda_chunk_prefill_act, a is
+                                          [>=T, Hv] and dt_bias [Hv]. */
 
 /* Problem descriptor shared by prefill and decode. */
 typedef struct {

@@ -18,6 +18,7 @@ from . import build as _build
 
 KDA_BF16, KDA_F32 = 0, 1
 KDA_FLAG_CUDA_CORE_PATH = 0x1
+KDA_FLAG_SCALAR_GATE = 0x2
 KDA_DEVICE_BAD_SLOT, KDA_DEVICE_BAD_SEQLENS, KDA_DEVICE_PIPE_TIMEOUT = 0x1, 0x2, 0x4
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
            3: "workspace too small", 4: "CUDA error", 5: "invalid device data"}
@@ -161,8 +162,9 @@ def chunk_prefill(q, k, v, g, beta, cu_seqlens, *, state=None, state_indices=Non
                   out=None, workspace=None, stream=None, cuda_core_path=False):
     """Chunked KDA prefill.  Returns ``(o, final)``.
 
-    q, k [T, Hk, K]; v [T, Hv, V] (bf16 or fp32, same dtype); g [>=T, Hv, K] fp32;
-    beta [>=T, Hv] fp32; cu_seqlens [N+1] int32.
+    q, k [T, Hk, K]; v [T, Hv, V] (bf16 or fp32, same dtype); g [>=T, Hv, K] fp32, or
+    [>=T, Hv] for a scalar (per token and head, GDN) gate; beta [>=T, Hv] fp32;
+    cu_seqlens [N+1] int32.
     Pool mode (``state_indices`` [N] int32 given): ``state`` is the pool
     [num_slots, Hv, K, V], updated in place and returned as ``final``.
     Dense mode: ``state`` is h0 [N, Hv, K, V] or None; ``final`` is a new
@@ -183,7 +185,8 @@ def chunk_prefill_act(q, k, v, a, A_log, dt_bias, beta, cu_seqlens, *, lower_bou
     ``g = max(-exp(A_log[h]) * softplus(a + dt_bias[h]), lower_bound)``.
 
     a [>=T, Hv, K] in the dtype of q/k/v; A_log [Hv] fp32; dt_bias [Hv, K] fp32 or None;
-    lower_bound a float <= 0 or None.  Everything else as :func:`chunk_prefill`.
+    lower_bound a float <= 0 or None.  A scalar (GDN) gate: a [>=T, Hv], dt_bias [Hv].
+    Everything else as :func:`chunk_prefill`.
     """
     _need(a, "a", q.dtype)
     _need(A_log, "A_log", torch.float32)
@@ -225,9 +228,12 @@ def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_stat
             final_state = torch.empty((N, Hv, K, V), dtype=sdt, device=q.device)
     if state is not None and not pool:
         _need(state, "state")
+    gate = g if act is None else act[0]
+    scalar = gate.dim() == 2
     d = make_desc(num_seqs=N, total_tokens=T, Hk=Hk, Hv=Hv, K=K, V=V, qkv_dtype=q.dtype,
                   state_dtype=sdt, scale=scale, num_slots=num_slots, slot_stride=slot_stride,
-                  flags=KDA_FLAG_CUDA_CORE_PATH if cuda_core_path else 0)
+                  flags=(KDA_FLAG_CUDA_CORE_PATH if cuda_core_path else 0)
+                  | (KDA_FLAG_SCALAR_GATE if scalar else 0))
     if out is None:
         out = torch.empty((T, Hv, V), dtype=q.dtype, device=q.device)
     ws_size = lib.kda_chunk_prefill_workspace_size(ctypes.byref(d))
@@ -258,7 +264,9 @@ def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_stat
 
 def decode(q, k, v, g, beta, pool, state_indices=None, *, scale=None, slot_stride=0, out=None,
            workspace=None, stream=None):
-    """One-token-per-row decode, updating ``pool`` [num_slots, Hv, K, V] in place.  Returns o."""
+    """One-token-per-row decode, updating ``pool`` [num_slots, Hv, K, V] in place.  Returns o.
+
+    g [>=N, Hv, K] fp32, or [>=N, Hv] for a scalar (per row and head, GDN) gate."""
     lib = load()
     for name, t in (("q", q), ("k", k), ("v", v), ("pool", pool)):
         _need(t, name)
@@ -270,7 +278,7 @@ def decode(q, k, v, g, beta, pool, state_indices=None, *, scale=None, slot_strid
     Hv, V = v.shape[1], v.shape[2]
     d = make_desc(num_seqs=N, total_tokens=N, Hk=Hk, Hv=Hv, K=K, V=V, qkv_dtype=q.dtype,
                   state_dtype=pool.dtype, scale=scale, num_slots=pool.shape[0],
-                  slot_stride=slot_stride)
+                  slot_stride=slot_stride, flags=KDA_FLAG_SCALAR_GATE if g.dim() == 2 else 0)
     if out is None:
         out = torch.empty((N, Hv, V), dtype=q.dtype, device=q.device)
     ws_size = lib.kda_decode_workspace_size(ctypes.byref(d))

@@ -54,7 +54,7 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
                   const float* __restrict__ g, const float* __restrict__ beta,
                   ST* __restrict__ pool, const int32_t* __restrict__ idx, QT* __restrict__ o,
                   uint32_t* __restrict__ status, int Hk, int Hv, int V, int64_t num_slots,
-                  int64_t slot_stride, float scale) {
+                  int64_t slot_stride, float scale, int gk) {
   constexpr int TPR = VT / 4;               // threads per row
   constexpr int RG = kDecThreads / TPR;     // row groups
   constexpr int RPT = K / RG;               // rows per thread
@@ -81,7 +81,7 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
   const int kh = h / (Hv / Hk);
   const QT* qn = q + ((size_t)n * Hk + kh) * K;
   const QT* kn = k + ((size_t)n * Hk + kh) * K;
-  const float* gn = g + ((size_t)n * Hv + h) * K;
+  const float* gn = g + ((size_t)n * Hv + h) * gk;  // gk = K, or 1 for a scalar gate
   ST* S = pool + slot * slot_stride + (size_t)h * K * V + v0 + col;
 
   float s[RPT][4], kr[RPT], qr[RPT];
@@ -92,7 +92,7 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
 #pragma unroll
   for (int j = 0; j < RPT; ++j) {
     const int c = rg + j * RG;
-    const float e = expf(gn[c]);
+    const float e = expf(gn[gk > 1 ? c : 0]);
     kr[j] = to_f32(kn[c]);
     qr[j] = to_f32(qn[c]);
 #pragma unroll
@@ -153,12 +153,12 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
     kda_decode_kernel<QT, ST, K, 128><<<grid, kDecThreads, 0, st>>>(
         (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, (ST*)a.pool, a.idx,
         (QT*)a.o, a.status, a.d.num_k_heads, a.d.num_v_heads, V, a.d.num_slots, a.slot_stride,
-        a.scale);
+        a.scale, a.gate_k);
   else
     kda_decode_kernel<QT, ST, K, 64><<<grid, kDecThreads, 0, st>>>(
         (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, (ST*)a.pool, a.idx,
         (QT*)a.o, a.status, a.d.num_k_heads, a.d.num_v_heads, V, a.d.num_slots, a.slot_stride,
-        a.scale);
+        a.scale, a.gate_k);
   return cudaGetLastError();
 }
 

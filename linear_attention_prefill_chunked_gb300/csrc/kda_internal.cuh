@@ -75,6 +75,7 @@ struct PrefillArgs {
   const void *q, *k, *v;
   const float *g, *beta;
   GateAct act;               // act.a null: g is given
+  int gate_k;                // gate values per (token, v-head): K, or 1 (scalar gate)
   const int32_t* cu;
   const void* state_in;      // pool, dense h0 or null
   const int32_t* idx;        // null in dense mode
@@ -95,6 +96,7 @@ struct DecodeArgs {
   int64_t slot_stride;
   const void *q, *k, *v;
   const float *g, *beta;
+  int gate_k;                // K, or 1 (scalar gate)
   void* pool;
   const int32_t* idx;
   void* o;

@@ -53,7 +53,7 @@ kda_prefill_simt_kernel(const QT* __restrict__ q, const QT* __restrict__ k,
                         const ST* state_in, const int32_t* __restrict__ idx, ST* state_out,
                         QT* __restrict__ o, uint32_t* __restrict__ status, int Hk, int Hv,
                         int64_t T, int64_t num_slots, int64_t slot_stride, float scale,
-                        GateAct act) {
+                        GateAct act, int gk) {
   using L = SimtSmem<K, V>;
   extern __shared__ float smem[];
   float* Kb = smem + L::kb;
@@ -105,9 +105,10 @@ kda_prefill_simt_kernel(const QT* __restrict__ q, const QT* __restrict__ k,
       Qb[r * KP + ch] = ok ? to_f32(q[qk]) : 0.f;
       float gv = 0.f;
       if (ok) {
-        const size_t gi = ((size_t)(t0 + r) * Hv + h) * K + ch;
+        const int gc = gk > 1 ? ch : 0;  // scalar gate: one value per (token, head)
+        const size_t gi = ((size_t)(t0 + r) * Hv + h) * gk + gc;
         if (ga) {
-          const float x = to_f32(ga[gi]) + (act.dt_bias ? act.dt_bias[(size_t)h * K + ch] : 0.f);
+          const float x = to_f32(ga[gi]) + (act.dt_bias ? act.dt_bias[(size_t)h * gk + gc] : 0.f);
           gv = fmaxf(-Ah * softplus_f32(x), act.lb);
         } else {
           gv = g[gi];
@@ -221,7 +222,7 @@ cudaError_t launch_typed(const PrefillArgs& a, cudaStream_t st) {
   kern<<<grid, kSimtThreads, L::bytes, st>>>(
       (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, a.cu,
       (const ST*)a.state_in, a.idx, (ST*)a.state_out, (QT*)a.o, a.status, a.d.num_k_heads,
-      a.d.num_v_heads, a.d.total_tokens, a.d.num_slots, a.slot_stride, a.scale, a.act);
+      a.d.num_v_heads, a.d.total_tokens, a.d.num_slots, a.slot_stride, a.scale, a.act, a.gate_k);
   return cudaGetLastError();
 }
 

@@ -133,7 +133,9 @@ struct TcParams {
   const __nv_bfloat16 *q, *k;
   const float *g, *beta;
   GateAct act;        // act.a set: tm_g maps the gate input a (bf16) instead of g
-  uint32_t g_bytes;   // bytes of one staged gate tile (g: 32768, a: 16384)
+  uint32_t g_bytes;   // bytes of one staged gate tile (g: 32768, a: 16384; scalar gate: 1024)
+  int gate_k;         // 128, or 1 for a scalar gate ([T, Hv]: tiles of 64 tokens x gw heads)
+  int gw;             // scalar gate: heads per staged row (4 fp32 g or 8 bf16 a = 16 bytes)
   const int32_t *cu, *idx, *order;
   const void* state_in;
   void* state_out;
@@ -276,7 +278,10 @@ struct Loader {  // used by thread 0 only
   }
   __device__ void load_g(const TcParams& p, uint8_t* sm, Small* s, int h, int t0) {
     mbar_expect_tx(&s->bar[B_G_FULL], p.g_bytes);
-    tma_load_3d(sm + OFF_G, &p.tm_g, &s->bar[B_G_FULL], 0, h, t0);
+    if (p.gate_k == 1)  // x = first head of the 16-byte group holding h
+      tma_load_2d(sm + OFF_G, &p.tm_g, &s->bar[B_G_FULL], h & ~(p.gw - 1), t0);
+    else
+      tma_load_3d(sm + OFF_G, &p.tm_g, &s->bar[B_G_FULL], 0, h, t0);
     ++st->n_g;
   }
   __device__ void load_v(const TcParams& p, uint8_t* sm, Small* s, int h, int t0) {
@@ -337,11 +342,12 @@ __device__ __noinline__ void unsafe_diag_terms(const TcParams& p, const Small* s
         for (int i = r; i >= a * 16; --i) {
           const float ki = __bfloat162float(p.k[((size_t)(t0 + i) * p.Hk + kh) * kK + c]);
           row[sidx(r, i)] += xr * ki * pr;
-          const size_t gi = ((size_t)(t0 + i) * p.Hv + h) * kK + c;
+          const int gk = p.gate_k, gcol = gk > 1 ? c : 0;
+          const size_t gi = ((size_t)(t0 + i) * p.Hv + h) * gk + gcol;
           float gv;
           if (p.act.a) {
             const float x = __bfloat162float(static_cast<const __nv_bfloat16*>(p.act.a)[gi]) +
-                            (p.act.dt_bias ? p.act.dt_bias[(size_t)h * kK + c] : 0.f);
+                            (p.act.dt_bias ? p.act.dt_bias[(size_t)h * gk + gcol] : 0.f);
             gv = fmaxf(-__expf(p.act.A_log[h]) * softplus_f32(x), p.act.lb);
           } else {
             gv = p.g[gi];
@@ -383,8 +389,9 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       const int cg = 2 * ((warp & 1) * 32 + lane);
       gA = __expf(p.act.A_log[h]);
       if (p.act.dt_bias) {
-        gdb0 = p.act.dt_bias[(size_t)h * kK + cg];
-        gdb1 = p.act.dt_bias[(size_t)h * kK + cg + 1];
+        const int gk = p.gate_k;
+        gdb0 = p.act.dt_bias[(size_t)h * gk + (gk > 1 ? cg : 0)];
+        gdb1 = p.act.dt_bias[(size_t)h * gk + (gk > 1 ? cg + 1 : 0)];
       }
     }
     bool stop = false;
@@ -411,7 +418,21 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       bt_ok = false;
       wait_bar(p, s, B_G_FULL, gc & 1);
       float e0[16], e1[16];
-      if (!p.act.a) {
+      if (p.gate_k == 1) {  // scalar gate: staged [64 tokens][gw heads], one value per token
+        const int col = h & (p.gw - 1);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = sc * 16 + j;
+          float gv;
+          if (p.act.a) {
+            const float x = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(sm + OFF_G)[r * 8 + col]) + gdb0;
+            gv = fmaxf(-gA * (fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)))), p.act.lb);
+          } else {
+            gv = Gs[r * 4 + col];
+          }
+          e0[j] = e1[j] = (r < cv) ? __expf(gv) : 1.f;
+        }
+      } else if (!p.act.a) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int r = sc * 16 + j;
@@ -1187,6 +1208,21 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [T, Hv] gate (scalar per token and head): 2-D map, boxes of 64 tokens x (16 bytes of heads).
+bool make_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int64_t T,
+                 int H, int box_inner) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  const int64_t rows = T > 0 ? T : 1;
+  cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)H * elem};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)kC};
+  cuuint32_t es[2] = {1u, 1u};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int n = 0;
   if (!n) {
@@ -1201,8 +1237,10 @@ int sm_count() {
 }  // namespace
 
 bool prefill_tc_supported(const kda_desc_t& d) {
+  // a scalar gate is staged by 16-byte groups of heads (8 bf16 a): Hv % 8 == 0
   return d.qkv_dtype == KDA_BF16 && d.head_k_dim == kK && d.head_v_dim == kV &&
-         (d.flags & KDA_FLAG_CUDA_CORE_PATH) == 0u;
+         (d.flags & KDA_FLAG_CUDA_CORE_PATH) == 0u &&
+         ((d.flags & KDA_FLAG_SCALAR_GATE) == 0u || d.num_v_heads % 8 == 0);
 }
 
 size_t prefill_tc_workspace(const kda_desc_t& d) { return (size_t)d.num_seqs * sizeof(int32_t); }
@@ -1220,10 +1258,15 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, d.num_v_heads, kV, 64,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !(a.act.a ? make_map(&p.tm_g, a.act.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, d.num_v_heads,
-                             kK, kK, CU_TENSOR_MAP_SWIZZLE_NONE)
-                  : make_map(&p.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T, d.num_v_heads, kK,
-                             kK, CU_TENSOR_MAP_SWIZZLE_NONE)))
+        !(a.gate_k == 1
+              ? (a.act.a ? make_map_2d(&p.tm_g, a.act.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T,
+                                       d.num_v_heads, 8)
+                         : make_map_2d(&p.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T,
+                                       d.num_v_heads, 4))
+              : a.act.a ? make_map(&p.tm_g, a.act.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T,
+                                   d.num_v_heads, kK, kK, CU_TENSOR_MAP_SWIZZLE_NONE)
+                        : make_map(&p.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T,
+                                   d.num_v_heads, kK, kK, CU_TENSOR_MAP_SWIZZLE_NONE)))
       return cudaErrorInvalidValue;
   }
   int32_t* order = reinterpret_cast<int32_t*>(a.ws + kWsPayload);
@@ -1231,7 +1274,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   p.k = static_cast<const __nv_bfloat16*>(a.k);
   p.g = a.g;
   p.act = a.act;
-  p.g_bytes = a.act.a ? 16384u : 32768u;
+  p.gate_k = a.gate_k;
+  p.gw = a.act.a ? 8 : 4;
+  p.g_bytes = a.gate_k == 1 ? 1024u : (a.act.a ? 16384u : 32768u);
   p.beta = a.beta;
   p.cu = a.cu;
   p.idx = a.idx;

@@ -222,3 +222,21 @@ def gate_act_inputs(T, Hv, K, *, dtype=BF16, seed=0, rows=None, A_max=16.0):
     dt = torch.exp(torch.rand(Hv, K, generator=gen, dtype=F32) * (hi - lo) + lo).clamp(min=1e-4)
     dt_bias = torch.log(torch.expm1(dt))  # softplus(dt_bias) = dt
     return a.contiguous(), A_log.contiguous(), dt_bias.contiguous()
+
+
+def scalar_gate_inputs(T, Hv, *, dtype=BF16, seed=0, act=False, A_max=16.0):
+    """Scalar (gated-delta-net) gate inputs, one value per (token, v-head).
+
+    act=False: g [T, Hv] fp32 = -softplus(x), x ~ N(0, 1).
+    act=True: ``(a, A_log, dt_bias)`` drawn like the pages' GDN pool test (sglang PR 30169
+    digest, 关键源码片段): a [T, Hv] ~ N(0, 1) in ``dtype``, A ~ U(0, 16) -> A_log [Hv],
+    dt log-uniform in [1e-3, 1e-1] (floored at 1e-4) -> dt_bias [Hv] with softplus(dt_bias) = dt.
+    """
+    gen = torch.Generator().manual_seed(seed + 104729)
+    if not act:
+        return (-torch.nn.functional.softplus(_normal((T, Hv), gen))).contiguous()
+    a = _normal((T, Hv), gen).to(dtype)
+    A_log = torch.log(torch.clamp(torch.rand(Hv, generator=gen, dtype=F32) * A_max, min=1e-6))
+    lo, hi = math.log(1e-3), math.log(1e-1)
+    dt = torch.exp(torch.rand(Hv, generator=gen, dtype=F32) * (hi - lo) + lo).clamp(min=1e-4)
+    return a.contiguous(), A_log.contiguous(), torch.log(torch.expm1(dt)).contiguous()

@@ -75,6 +75,8 @@ def recurrence(q, k, v, g, beta, cu_seqlens, *, scale=None, state=None, state_in
     [N, Hv, K, V] (no indices) or the updated pool copy (with indices).
     """
     q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    if g.ndim == 2:  # scalar (GDN) gate [T, Hv]: the same decay on every key channel
+        g = np.ascontiguousarray(np.repeat(g[:, :, None], q.shape[2], axis=2))
     cu = np.ascontiguousarray(np.asarray(
         cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int32))
     T, Hk, K = q.shape
@@ -128,13 +130,14 @@ def gate_activation(a, A_log, dt_bias=None, lower_bound=None):
     name ``lower_bound`` without a formula; it is read as a floor on g.
 
     softplus(x) = log(1 + e^x), evaluated as max(x, 0) + log1p(e^-|x|) so that no
-    intermediate overflows.  a [T, Hv, K]; A_log [Hv]; dt_bias [Hv, K] or None.
+    intermediate overflows.  a [T, Hv, K]; A_log [Hv]; dt_bias [Hv, K] or None.  A scalar
+    (GDN) gate, as on the pages: a [T, Hv] and dt_bias [Hv], giving g [T, Hv].
     """
     a = _f64(a)
     A = np.exp(_f64(A_log))
-    x = a + (_f64(dt_bias)[None, :, :] if dt_bias is not None else 0.0)
+    x = a + (_f64(dt_bias)[None] if dt_bias is not None else 0.0)
     sp = np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
-    g = -A[None, :, None] * sp
+    g = -(A[None, :, None] if a.ndim == 3 else A[None, :]) * sp
     if lower_bound is not None:
         g = np.maximum(g, float(lower_bound))
     return g

@@ -72,7 +72,7 @@ def test_workspace_queries_and_path_selection():
     d.chunk_size = 32
     bad.append(d)
     d = _desc()
-    d.flags = 2
+    d.flags = 4                                              # no such flag
     bad.append(d)
     for b in bad:
         assert kda.prefill_workspace_size(b) == 0
@@ -83,6 +83,12 @@ def test_workspace_queries_and_path_selection():
     d.flags = 1                                              # KDA_FLAG_CUDA_CORE_PATH
     assert kda.prefill_path(d) == 0
     assert kda.prefill_path(_desc(K=64)) == 0
+    d = _desc()
+    d.flags = 2                                              # KDA_FLAG_SCALAR_GATE
+    assert kda.prefill_path(d) == (1 if d.num_v_heads % 8 == 0 else 0)
+    d = _desc(Hv=4, Hk=4)
+    d.flags = 2                                              # heads staged in groups of 8
+    assert kda.prefill_path(d) == 0
 
 
 def test_host_checked_errors_return_before_any_launch():

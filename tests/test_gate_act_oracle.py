@@ -72,3 +72,23 @@ def test_gate_feeds_the_recurrence_as_a_decay():
     v = rng.normal(size=(T, 1, V))
     _, fin = kda_oracle.recurrence(q, k, v, g, np.zeros((T, 1)), [0, T], state=S0)
     assert np.allclose(fin, S0 * 2.0 ** -T, rtol=1e-13, atol=0)
+
+
+def test_scalar_gate_is_the_channel_broadcast():
+    # a [T, Hv] gate (GDN form) must act like the same value on every key channel
+    T, Hk, Hv, K, V = 9, 1, 2, 4, 3
+    q = rng.normal(size=(T, Hk, K))
+    k = rng.normal(size=(T, Hk, K))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.normal(size=(T, Hv, V))
+    beta = rng.uniform(size=(T, Hv))
+    g2 = -rng.uniform(0.0, 2.0, size=(T, Hv))
+    g3 = np.repeat(g2[:, :, None], K, axis=2)
+    o2, s2 = kda_oracle.recurrence(q, k, v, g2, beta, [0, 4, T])
+    o3, s3 = kda_oracle.recurrence(q, k, v, g3, beta, [0, 4, T])
+    assert np.array_equal(o2, o3) and np.array_equal(s2, s3)
+    a = rng.normal(size=(T, Hv))
+    ga = kda_oracle.gate_activation(a, np.zeros(Hv), np.zeros(Hv))
+    assert ga.shape == (T, Hv)
+    assert np.allclose(ga - kda_oracle.gate_activation(-a, np.zeros(Hv), np.zeros(Hv)), -a,
+                       rtol=0, atol=1e-13)
