@@ -68,6 +68,12 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
                                           runs (PR 30169 digest, 关键源码片段).  g is then
                                           [>=T, Hv] fp32 and, for kda_chunk_prefill_act, a is
                                           [>=T, Hv] and dt_bias [Hv]. */
+#define KDA_FLAG_QK_L2NORM       0x4u  /* prefill and decode: q and k are L2-normalised per
+                                          (token, head) inside the kernel, x / max(||x||, 1e-12),
+                                          as the pages' callers do before the call (PR 27488
+                                          digest, 关键源码片段 CuteDSLKDAKernel.extend; the
+                                          tensor-core kernel re-rounds them to bf16 as the
+                                          caller's normalise-then-cast does). */
 
 /* Problem descriptor shared by prefill and decode. */
 typedef struct {

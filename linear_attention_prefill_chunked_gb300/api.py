@@ -19,6 +19,7 @@ from . import build as _build
 KDA_BF16, KDA_F32 = 0, 1
 KDA_FLAG_CUDA_CORE_PATH = 0x1
 KDA_FLAG_SCALAR_GATE = 0x2
+KDA_FLAG_QK_L2NORM = 0x4
 KDA_DEVICE_BAD_SLOT, KDA_DEVICE_BAD_SEQLENS, KDA_DEVICE_PIPE_TIMEOUT = 0x1, 0x2, 0x4
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
            3: "workspace too small", 4: "CUDA error", 5: "invalid device data"}
@@ -159,7 +160,7 @@ def read_device_status(workspace: torch.Tensor, stream=None) -> int:
 
 def chunk_prefill(q, k, v, g, beta, cu_seqlens, *, state=None, state_indices=None,
                   final_state=None, output_final_state=True, scale=None, slot_stride=0,
-                  out=None, workspace=None, stream=None, cuda_core_path=False):
+                  out=None, workspace=None, stream=None, cuda_core_path=False, qk_l2norm=False):
     """Chunked KDA prefill.  Returns ``(o, final)``.
 
     q, k [T, Hk, K]; v [T, Hv, V] (bf16 or fp32, same dtype); g [>=T, Hv, K] fp32, or
@@ -169,18 +170,19 @@ def chunk_prefill(q, k, v, g, beta, cu_seqlens, *, state=None, state_indices=Non
     [num_slots, Hv, K, V], updated in place and returned as ``final``.
     Dense mode: ``state`` is h0 [N, Hv, K, V] or None; ``final`` is a new
     [N, Hv, K, V] tensor (or ``final_state`` if given, may be ``state``) or None
-    when ``output_final_state`` is False.
+    when ``output_final_state`` is False.  ``qk_l2norm`` normalises q and k per
+    (token, head) inside the kernel (KDA_FLAG_QK_L2NORM).
     """
     _need(g, "g", torch.float32)
     return _prefill(q, k, v, g, None, beta, cu_seqlens, state, state_indices, final_state,
                     output_final_state, scale, slot_stride, out, workspace, stream,
-                    cuda_core_path, chunk_prefill)
+                    cuda_core_path, chunk_prefill, qk_l2norm)
 
 
 def chunk_prefill_act(q, k, v, a, A_log, dt_bias, beta, cu_seqlens, *, lower_bound=None,
                       state=None, state_indices=None, final_state=None, output_final_state=True,
                       scale=None, slot_stride=0, out=None, workspace=None, stream=None,
-                      cuda_core_path=False):
+                      cuda_core_path=False, qk_l2norm=False):
     """Chunked KDA prefill with the gate computed in the kernel (kda_chunk_prefill_act):
     ``g = max(-exp(A_log[h]) * softplus(a + dt_bias[h]), lower_bound)``.
 
@@ -195,12 +197,12 @@ def chunk_prefill_act(q, k, v, a, A_log, dt_bias, beta, cu_seqlens, *, lower_bou
     lb = float("-inf") if lower_bound is None else float(lower_bound)
     return _prefill(q, k, v, None, (a, A_log, dt_bias, lb), beta, cu_seqlens, state,
                     state_indices, final_state, output_final_state, scale, slot_stride, out,
-                    workspace, stream, cuda_core_path, chunk_prefill_act)
+                    workspace, stream, cuda_core_path, chunk_prefill_act, qk_l2norm)
 
 
 def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_state,
              output_final_state, scale, slot_stride, out, workspace, stream, cuda_core_path,
-             owner):
+             owner, qk_l2norm=False):
     lib = load()
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need(t, name)
@@ -233,7 +235,8 @@ def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_stat
     d = make_desc(num_seqs=N, total_tokens=T, Hk=Hk, Hv=Hv, K=K, V=V, qkv_dtype=q.dtype,
                   state_dtype=sdt, scale=scale, num_slots=num_slots, slot_stride=slot_stride,
                   flags=(KDA_FLAG_CUDA_CORE_PATH if cuda_core_path else 0)
-                  | (KDA_FLAG_SCALAR_GATE if scalar else 0))
+                  | (KDA_FLAG_SCALAR_GATE if scalar else 0)
+                  | (KDA_FLAG_QK_L2NORM if qk_l2norm else 0))
     if out is None:
         out = torch.empty((T, Hv, V), dtype=q.dtype, device=q.device)
     ws_size = lib.kda_chunk_prefill_workspace_size(ctypes.byref(d))
@@ -263,7 +266,7 @@ def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_stat
 
 
 def decode(q, k, v, g, beta, pool, state_indices=None, *, scale=None, slot_stride=0, out=None,
-           workspace=None, stream=None):
+           workspace=None, stream=None, qk_l2norm=False):
     """One-token-per-row decode, updating ``pool`` [num_slots, Hv, K, V] in place.  Returns o.
 
     g [>=N, Hv, K] fp32, or [>=N, Hv] for a scalar (per row and head, GDN) gate."""
@@ -278,7 +281,9 @@ def decode(q, k, v, g, beta, pool, state_indices=None, *, scale=None, slot_strid
     Hv, V = v.shape[1], v.shape[2]
     d = make_desc(num_seqs=N, total_tokens=N, Hk=Hk, Hv=Hv, K=K, V=V, qkv_dtype=q.dtype,
                   state_dtype=pool.dtype, scale=scale, num_slots=pool.shape[0],
-                  slot_stride=slot_stride, flags=KDA_FLAG_SCALAR_GATE if g.dim() == 2 else 0)
+                  slot_stride=slot_stride,
+                  flags=(KDA_FLAG_SCALAR_GATE if g.dim() == 2 else 0)
+                  | (KDA_FLAG_QK_L2NORM if qk_l2norm else 0))
     if out is None:
         out = torch.empty((N, Hv, V), dtype=q.dtype, device=q.device)
     ws_size = lib.kda_decode_workspace_size(ctypes.byref(d))

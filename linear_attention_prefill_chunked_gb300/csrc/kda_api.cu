@@ -14,7 +14,8 @@ bool dims_ok(const kda_desc_t* d) {
   if (d->num_k_heads <= 0 || d->num_v_heads <= 0) return false;
   if (d->num_v_heads % d->num_k_heads != 0) return false;
   if (d->chunk_size != 64) return false;
-  if ((d->flags & ~(KDA_FLAG_CUDA_CORE_PATH | KDA_FLAG_SCALAR_GATE)) != 0) return false;
+  if ((d->flags & ~(KDA_FLAG_CUDA_CORE_PATH | KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM)) != 0)
+    return false;
   if (!(d->qkv_dtype == KDA_BF16 || d->qkv_dtype == KDA_F32)) return false;
   if (!(d->state_dtype == KDA_BF16 || d->state_dtype == KDA_F32)) return false;
   if (!std::isfinite(d->scale)) return false;
@@ -109,6 +110,7 @@ kda_status_t prefill_common(const kda_desc_t* d, const void* q, const void* k, c
   a.slot_stride = pool ? slot_pitch(d) : (int64_t)d->num_v_heads * d->head_k_dim * d->head_v_dim;
   a.q = q; a.k = k; a.v = v; a.g = g; a.act = act; a.beta = beta; a.cu = cu_seqlens;
   a.gate_k = (d->flags & KDA_FLAG_SCALAR_GATE) ? 1 : d->head_k_dim;
+  a.l2norm = (d->flags & KDA_FLAG_QK_L2NORM) != 0;
   a.state_in = state;
   a.idx = state_indices;
   a.state_out = pool ? state : final_state;
@@ -175,6 +177,7 @@ kda_status_t kda_decode(const kda_desc_t* d, const void* q, const void* k, const
   a.slot_stride = slot_pitch(d);
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
   a.gate_k = (d->flags & KDA_FLAG_SCALAR_GATE) ? 1 : d->head_k_dim;
+  a.l2norm = (d->flags & KDA_FLAG_QK_L2NORM) != 0;
   a.pool = state_pool;
   a.idx = state_indices;
   a.o = o;

@@ -54,7 +54,7 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
                   const float* __restrict__ g, const float* __restrict__ beta,
                   ST* __restrict__ pool, const int32_t* __restrict__ idx, QT* __restrict__ o,
                   uint32_t* __restrict__ status, int Hk, int Hv, int V, int64_t num_slots,
-                  int64_t slot_stride, float scale, int gk) {
+                  int64_t slot_stride, float scale, int gk, bool l2norm) {
   constexpr int TPR = VT / 4;               // threads per row
   constexpr int RG = kDecThreads / TPR;     // row groups
   constexpr int RPT = K / RG;               // rows per thread
@@ -84,6 +84,31 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
   const float* gn = g + ((size_t)n * Hv + h) * gk;  // gk = K, or 1 for a scalar gate
   ST* S = pool + slot * slot_stride + (size_t)h * K * V + v0 + col;
 
+  // optional q/k normalisation: ||k||, ||q|| reduced over the row groups
+  float ik = 1.f, iq = 1.f;
+  if (l2norm) {
+    __shared__ float red_n[2][RG];
+    float sk = 0.f, sq = 0.f;
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const float kv = to_f32(kn[rg + j * RG]), qv = to_f32(qn[rg + j * RG]);
+      sk = fmaf(kv, kv, sk);
+      sq = fmaf(qv, qv, sq);
+    }
+    if (col == 0) {
+      red_n[0][rg] = sk;
+      red_n[1][rg] = sq;
+    }
+    __syncthreads();
+    float tk = 0.f, tq = 0.f;
+#pragma unroll
+    for (int r = 0; r < RG; ++r) {
+      tk += red_n[0][r];
+      tq += red_n[1][r];
+    }
+    ik = 1.f / fmaxf(sqrtf(tk), 1e-12f);
+    iq = 1.f / fmaxf(sqrtf(tq), 1e-12f);
+  }
   float s[RPT][4], kr[RPT], qr[RPT];
   // Issue every state load first (the tile is the whole cost of the kernel).
 #pragma unroll
@@ -93,8 +118,8 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
   for (int j = 0; j < RPT; ++j) {
     const int c = rg + j * RG;
     const float e = expf(gn[gk > 1 ? c : 0]);
-    kr[j] = to_f32(kn[c]);
-    qr[j] = to_f32(qn[c]);
+    kr[j] = to_f32(kn[c]) * ik;
+    qr[j] = to_f32(qn[c]) * iq;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       s[j][i] *= e;                    // decay first
@@ -153,12 +178,12 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
     kda_decode_kernel<QT, ST, K, 128><<<grid, kDecThreads, 0, st>>>(
         (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, (ST*)a.pool, a.idx,
         (QT*)a.o, a.status, a.d.num_k_heads, a.d.num_v_heads, V, a.d.num_slots, a.slot_stride,
-        a.scale, a.gate_k);
+        a.scale, a.gate_k, a.l2norm);
   else
     kda_decode_kernel<QT, ST, K, 64><<<grid, kDecThreads, 0, st>>>(
         (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, (ST*)a.pool, a.idx,
         (QT*)a.o, a.status, a.d.num_k_heads, a.d.num_v_heads, V, a.d.num_slots, a.slot_stride,
-        a.scale, a.gate_k);
+        a.scale, a.gate_k, a.l2norm);
   return cudaGetLastError();
 }
 

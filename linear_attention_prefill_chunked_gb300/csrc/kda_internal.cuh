@@ -76,6 +76,7 @@ struct PrefillArgs {
   const float *g, *beta;
   GateAct act;               // act.a null: g is given
   int gate_k;                // gate values per (token, v-head): K, or 1 (scalar gate)
+  bool l2norm;               // normalise q and k rows in the kernel
   const int32_t* cu;
   const void* state_in;      // pool, dense h0 or null
   const int32_t* idx;        // null in dense mode
@@ -97,6 +98,7 @@ struct DecodeArgs {
   const void *q, *k, *v;
   const float *g, *beta;
   int gate_k;                // K, or 1 (scalar gate)
+  bool l2norm;               // normalise q and k rows in the kernel
   void* pool;
   const int32_t* idx;
   void* o;

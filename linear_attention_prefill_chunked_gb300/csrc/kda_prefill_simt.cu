@@ -53,7 +53,7 @@ kda_prefill_simt_kernel(const QT* __restrict__ q, const QT* __restrict__ k,
                         const ST* state_in, const int32_t* __restrict__ idx, ST* state_out,
                         QT* __restrict__ o, uint32_t* __restrict__ status, int Hk, int Hv,
                         int64_t T, int64_t num_slots, int64_t slot_stride, float scale,
-                        GateAct act, int gk) {
+                        GateAct act, int gk, bool l2norm) {
   using L = SimtSmem<K, V>;
   extern __shared__ float smem[];
   float* Kb = smem + L::kb;
@@ -122,6 +122,19 @@ kda_prefill_simt_kernel(const QT* __restrict__ q, const QT* __restrict__ k,
     }
     if (tid < kC) Be[tid] = tid < c ? beta[(size_t)(t0 + tid) * Hv + h] : 0.f;
     __syncthreads();
+    if (l2norm) {  // q and k rows -> x / max(||x||, 1e-12), one warp per row
+      const int wp = tid >> 5, ln = tid & 31;
+      for (int r = wp; r < 2 * kC; r += kSimtThreads / 32) {
+        float* row = r < kC ? Kb + r * DP : Qb + (r - kC) * KP;
+        float ss = 0.f;
+        for (int ch = ln; ch < K; ch += 32) ss = fmaf(row[ch], row[ch], ss);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+        for (int ch = ln; ch < K; ch += 32) row[ch] *= inv;
+      }
+      __syncthreads();
+    }
     // ---- Gamma: inclusive cumsum per channel
     for (int ch = tid; ch < K; ch += kSimtThreads) {
       float acc = 0.f;
@@ -222,7 +235,8 @@ cudaError_t launch_typed(const PrefillArgs& a, cudaStream_t st) {
   kern<<<grid, kSimtThreads, L::bytes, st>>>(
       (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, a.cu,
       (const ST*)a.state_in, a.idx, (ST*)a.state_out, (QT*)a.o, a.status, a.d.num_k_heads,
-      a.d.num_v_heads, a.d.total_tokens, a.d.num_slots, a.slot_stride, a.scale, a.act, a.gate_k);
+      a.d.num_v_heads, a.d.total_tokens, a.d.num_slots, a.slot_stride, a.scale, a.act, a.gate_k,
+      a.l2norm);
   return cudaGetLastError();
 }
 

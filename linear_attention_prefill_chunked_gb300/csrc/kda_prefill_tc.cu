@@ -136,6 +136,7 @@ struct TcParams {
   uint32_t g_bytes;   // bytes of one staged gate tile (g: 32768, a: 16384; scalar gate: 1024)
   int gate_k;         // 128, or 1 for a scalar gate ([T, Hv]: tiles of 64 tokens x gw heads)
   int gw;             // scalar gate: heads per staged row (4 fp32 g or 8 bf16 a = 16 bytes)
+  int l2norm;         // normalise the staged q/k rows (x / max(||x||, 1e-12), back to bf16)
   const int32_t *cu, *idx, *order;
   const void* state_in;
   void* state_out;
@@ -325,7 +326,8 @@ struct Loader {  // used by thread 0 only
 // runs at ordinary gates and would otherwise raise the register pressure of the
 // chunk loop.
 __device__ __noinline__ void unsafe_diag_terms(const TcParams& p, const Small* s, float* As, float* Xs,
-                                               int L, int64_t t0, int cv, int kh, int h) {
+                                               const float* inv_nrm, int L, int64_t t0, int cv,
+                                               int kh, int h) {
   const int r = L & 63, a = r >> 4;
   const bool isB = L >= 64;
   const uint32_t anya = s->unsafe[a][0][0] | s->unsafe[a][0][1] | s->unsafe[a][1][0] | s->unsafe[a][1][1];
@@ -337,10 +339,12 @@ __device__ __noinline__ void unsafe_diag_terms(const TcParams& p, const Small* s
       while (m) {
         const int c = 64 * (wd >> 1) + 2 * (__ffs(m) - 1) + (wd & 1);
         m &= m - 1;
-        const float xr = __bfloat162float(xsrc[((size_t)(t0 + r) * p.Hk + kh) * kK + c]);
+        const float xr = __bfloat162float(xsrc[((size_t)(t0 + r) * p.Hk + kh) * kK + c]) *
+                         (p.l2norm ? inv_nrm[isB ? 64 + r : r] : 1.f);
         float pr = 1.f;
         for (int i = r; i >= a * 16; --i) {
-          const float ki = __bfloat162float(p.k[((size_t)(t0 + i) * p.Hk + kh) * kK + c]);
+          const float ki = __bfloat162float(p.k[((size_t)(t0 + i) * p.Hk + kh) * kK + c]) *
+                           (p.l2norm ? inv_nrm[i] : 1.f);
           row[sidx(r, i)] += xr * ki * pr;
           const int gk = p.gate_k, gcol = gk > 1 ? c : 0;
           const size_t gi = ((size_t)(t0 + i) * p.Hv + h) * gk + gcol;
@@ -468,6 +472,37 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         }
       }
       wait_bar(p, s, B_QK_FULL, gc & 1);
+      if (p.l2norm) {
+        // staged rows (k 0-63, q 64-127) -> x / max(||x||, 1e-12), re-rounded to bf16 as a
+        // caller's normalise-then-cast would; thread = (row, 64-channel half).  The inverse
+        // norms are kept for the pairwise path, which reads q and k from global memory.
+        const int row = t >> 1, hf = t & 1;
+        uint8_t* base = sm + OFF_QK + hf * 16384;
+        float ss = 0.f;
+#pragma unroll 2
+        for (int j = 0; j < 8; ++j) {
+          const uint4 w = *reinterpret_cast<const uint4*>(base + sw128_off(row, j));
+          const uint32_t u4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float x0 = bf_bits(u4[u] & 0xFFFFu), x1 = bf_bits(u4[u] >> 16);
+            ss = fmaf(x0, x0, fmaf(x1, x1, ss));
+          }
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        const float inv = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+#pragma unroll 2
+        for (int j = 0; j < 8; ++j) {
+          const uint4 w = *reinterpret_cast<const uint4*>(base + sw128_off(row, j));
+          const uint32_t u4[4] = {w.x, w.y, w.z, w.w};
+          uint32_t o4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            o4[u] = pack_bf16x2(bf_bits(u4[u] & 0xFFFFu) * inv, bf_bits(u4[u] >> 16) * inv);
+          st_chunk(sm, OFF_QK + hf * 16384 + sw128_off(row, j), o4[0], o4[1], o4[2], o4[3]);
+        }
+        if (hf == 0) reinterpret_cast<float*>(sm + OFF_TM + 2048)[row] = inv;
+      }
       // QG buffer and this gamma buffer are free once MMA-1b of the previous chunk ran
       if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
       named_bar(BAR_IG, kIG);  // products visible; every thread has read g (CB 1-2 free)
@@ -702,7 +737,9 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       } else {
         named_bar(BAR_IG, kIG);
         // exact pairwise terms of the diagonal sub-chunk blocks on "unsafe" channels
-        if (hx == 0) unsafe_diag_terms(p, s, As, Xs, L, t0, cv, kh, h);
+        if (hx == 0)
+          unsafe_diag_terms(p, s, As, Xs, reinterpret_cast<const float*>(sm + OFF_TM + 2048), L,
+                            t0, cv, kh, h);
         named_bar(BAR_IG, kIG);
         // A: mask + beta_r (in place, fp32); B: mask + scale -> bf16 -> BB
         {
@@ -1275,6 +1312,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   p.g = a.g;
   p.act = a.act;
   p.gate_k = a.gate_k;
+  p.l2norm = a.l2norm ? 1 : 0;
   p.gw = a.act.a ? 8 : 4;
   p.g_bytes = a.gate_k == 1 ? 1024u : (a.act.a ? 16384u : 32768u);
   p.beta = a.beta;

@@ -141,3 +141,11 @@ def gate_activation(a, A_log, dt_bias=None, lower_bound=None):
     if lower_bound is not None:
         g = np.maximum(g, float(lower_bound))
     return g
+
+
+def l2norm(x, eps=1e-12):
+    """Rows of x (last axis) divided by max(||row||_2, eps), in fp64: the q/k normalisation
+    the pages' callers apply before the prefill (sglang PR 27488 digest, 关键源码片段
+    ``CuteDSLKDAKernel.extend``), which the kernels can do in place (KDA_FLAG_QK_L2NORM)."""
+    x = _f64(x)
+    return x / np.maximum(np.linalg.norm(x, axis=-1, keepdims=True), eps)

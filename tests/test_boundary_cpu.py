@@ -72,7 +72,7 @@ def test_workspace_queries_and_path_selection():
     d.chunk_size = 32
     bad.append(d)
     d = _desc()
-    d.flags = 4                                              # no such flag
+    d.flags = 8                                              # no such flag
     bad.append(d)
     for b in bad:
         assert kda.prefill_workspace_size(b) == 0

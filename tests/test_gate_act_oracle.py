@@ -92,3 +92,14 @@ def test_scalar_gate_is_the_channel_broadcast():
     assert ga.shape == (T, Hv)
     assert np.allclose(ga - kda_oracle.gate_activation(-a, np.zeros(Hv), np.zeros(Hv)), -a,
                        rtol=0, atol=1e-13)
+
+
+def test_l2norm_rows():
+    x = rng.normal(size=(7, 3, 16)) * 5
+    x[2, 1] = 0.0
+    y = kda_oracle.l2norm(x)
+    n = np.linalg.norm(y, axis=-1)
+    assert np.allclose(np.delete(n.reshape(-1), 2 * 3 + 1), 1.0, rtol=0, atol=1e-14)
+    assert np.all(y[2, 1] == 0.0)                             # zero rows stay zero
+    assert np.allclose(kda_oracle.l2norm(3.5 * x), y, rtol=1e-14, atol=0)  # scale-free
+    assert np.all(np.sign(y) == np.sign(x))
