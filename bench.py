@@ -61,14 +61,17 @@ def _traffic_from_profile():
     return int(kv["bytes_per_launch"])
 
 
-def algorithmic_bytes(w, gate_act=False):
+def algorithmic_bytes(w, gate_act=False, scalar_gate=False):
     """Bytes the path must move once: q, k, v, g (or the gate pre-activation a with A_log and
     dt_bias), beta in; o out; pool rows in and out."""
     T, Hk, K = w.q.shape
     Hv, V = w.v.shape[1], w.v.shape[2]
     e = w.q.element_size()
     se = w.state.element_size() if w.state is not None else 4
-    gate = (T * Hv * K * e + Hv * 4 + Hv * K * 4) if gate_act else T * Hv * K * 4
+    if scalar_gate:
+        gate = T * Hv * 4
+    else:
+        gate = (T * Hv * K * e + Hv * 4 + Hv * K * 4) if gate_act else T * Hv * K * 4
     return (T * Hk * K * e * 2 + T * Hv * V * e + gate + T * Hv * 4 + T * Hv * V * e
             + w.N * Hv * K * V * se * 2)
 
@@ -208,6 +211,9 @@ def run_ours(args, dist, ws, rank, local):
     else:
         w = synthetic.throughput()
     act = args.gate == "act"
+    if args.gate == "scalar":  # one log-decay per (token, head): the GDN form
+        w.g = synthetic.scalar_gate_inputs(w.T, 32, seed=0)
+        w.name += "_scalar_gate"
     if act:  # the kernel computes the gate from a bf16 pre-activation
         a_h, A_log_h, dtb_h = synthetic.gate_act_inputs(w.T, 32, 128, seed=0)
         w.name += "_gate_act"
@@ -227,10 +233,11 @@ def run_ours(args, dist, ws, rank, local):
     def step():
         if act:
             kda.chunk_prefill_act(q, k, v, a_d, A_log_d, dtb_d, beta, cu, state=pool,
-                                  state_indices=idx, out=out, workspace=ws_t, stream=stream)
+                                  state_indices=idx, out=out, workspace=ws_t, stream=stream,
+                                  qk_l2norm=args.qk_l2norm)
         else:
             kda.chunk_prefill(q, k, v, g, beta, cu, state=pool, state_indices=idx, out=out,
-                              workspace=ws_t, stream=stream)
+                              workspace=ws_t, stream=stream, qk_l2norm=args.qk_l2norm)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -295,7 +302,7 @@ def run_ours(args, dist, ws, rank, local):
     hbm, bf16, src = _peaks()
     ms = total_ms / args.steps
     value = ws * w.T / (ms * 1e-3)
-    nbytes = algorithmic_bytes(w, act)
+    nbytes = algorithmic_bytes(w, act, args.gate == "scalar")
     flops = algorithmic_flops(w)
     kern_ms = statistics.median(per)
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
@@ -309,7 +316,9 @@ def run_ours(args, dist, ws, rank, local):
                    "K": 128, "V": 128, "chunk": 64, "state_pool": "fp32, 256 slots, in place",
                    "kernel_path": "tcgen05 fused" if path == 1 else "CUDA-core fp32",
                    "gate": ("in-kernel activation of a bf16 pre-activation" if act
-                            else "fp32 log-decay input"),
+                            else "fp32 log-decay per token and head (scalar, GDN)"
+                            if args.gate == "scalar" else "fp32 log-decay input"),
+                   "qk_l2norm": "in kernel" if args.qk_l2norm else "by the caller",
                    "l2": f"inputs larger than L2 ({nbytes / 1e9:.2f} GB per step), no flush",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -342,9 +351,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--gate", default="given", choices=["given", "act"],
+    ap.add_argument("--gate", default="given", choices=["given", "act", "scalar"],
                     help="act: the gate computed in the kernel from a bf16 pre-activation "
-                         "(kda_chunk_prefill_act)")
+                         "(kda_chunk_prefill_act); scalar: one log-decay per token and head")
+    ap.add_argument("--qk-l2norm", action="store_true",
+                    help="normalise q and k inside the kernel (KDA_FLAG_QK_L2NORM)")
     ap.add_argument("--workload", default="throughput", choices=["throughput", "profile"],
                     help="profile: 8 x 1024 tokens, Hv=32 (a smaller case for ncu captures)")
     args = ap.parse_args()
