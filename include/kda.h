@@ -194,6 +194,35 @@ kda_status_t kda_decode(const kda_desc_t *desc, const void *q, const void *k, co
                         size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Decode of speculative draft steps with a per-step state cache.  Row n of the batch is a
+ * request whose draft tokens cu_seqlens[n] .. cu_seqlens[n+1]-1 (at most max_steps of
+ * them) run one after another from pool[s_n] (s_n as in kda_decode; state_indices NULL
+ * means s_n = n).  The state after draft step j is written to
+ *
+ *     step_cache + n * cache_pitch_elems + j * (Hv*K*V)      ([Hv, K, V], state_dtype)
+ *
+ * so that a caller can keep the state of the accepted prefix.  The per-request pitch is
+ * passed explicitly: the pages fixed a cache-stride bug that inferred it from the buffer's
+ * shape, which changes when the number of drafts does (PR 37317 digest, 实现拆解 item 2).
+ * The pool row is written with the last step's state only if update_pool != 0.
+ *
+ *   desc          num_seqs = N requests, total_tokens = T draft tokens in all
+ *   q, k [T,Hk,K]; v, o [T,Hv,V]; g [T,Hv,K] (or [T,Hv] with KDA_FLAG_SCALAR_GATE);
+ *   beta [T,Hv]; cu_seqlens [N+1] int32
+ *   step_cache    NULL (no per-step states) or 16-byte aligned, with
+ *                 cache_pitch_elems >= max_steps*Hv*K*V and a multiple of 8
+ * A request longer than max_steps, or a bad cu_seqlens, sets KDA_DEVICE_BAD_SEQLENS and
+ * is skipped.  Same grid rule as kda_decode (rows on grid.x).  Errors as kda_decode.
+ */
+kda_status_t kda_decode_draft(const kda_desc_t *desc, const void *q, const void *k,
+                              const void *v, const float *g, const float *beta,
+                              const int32_t *cu_seqlens, void *state_pool,
+                              const int32_t *state_indices, void *step_cache,
+                              int64_t cache_pitch_elems, int32_t max_steps, int update_pool,
+                              void *o, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
+/*
  * Allocation-free prefill.  The pages have no counterpart of this entry point.
  *
  * For callers that cannot allocate device memory when they run the prefill: code

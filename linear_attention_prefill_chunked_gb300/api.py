@@ -52,7 +52,7 @@ class KdaDesc(ctypes.Structure):
 
 EXPORTS = ("kda_chunk_prefill_workspace_size", "kda_decode_workspace_size", "kda_chunk_prefill",
            "kda_decode", "kda_read_device_status", "kda_chunk_prefill_path", "kda_status_string",
-           "kda_chunk_prefill_noalloc", "kda_chunk_prefill_act")
+           "kda_chunk_prefill_noalloc", "kda_chunk_prefill_act", "kda_decode_draft")
 
 _lib = None
 
@@ -92,6 +92,9 @@ def load(build_if_missing: bool = True):
     lib.kda_chunk_prefill_act.argtypes = [D, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, P, P,
                                           ctypes.c_size_t, P]
     lib.kda_chunk_prefill_act.restype = ctypes.c_int
+    lib.kda_decode_draft.argtypes = [D, P, P, P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int32,
+                                     ctypes.c_int, P, P, ctypes.c_size_t, P]
+    lib.kda_decode_draft.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -297,4 +300,53 @@ def decode(q, k, v, g, beta, pool, state_indices=None, *, scale=None, slot_strid
     if rc != 0:
         raise KdaError(rc, "kda_decode")
     decode.last_workspace = workspace
+    return out
+
+
+def decode_draft(q, k, v, g, beta, cu_seqlens, pool, state_indices=None, *, cache=None,
+                 max_steps=None, update_pool=False, scale=None, slot_stride=0, out=None,
+                 workspace=None, stream=None, qk_l2norm=False):
+    """Speculative draft steps (kda_decode_draft).  Request n runs its tokens
+    cu_seqlens[n]..cu_seqlens[n+1]-1 from pool[slot n]; the state after step j goes to
+    ``cache[n].view(-1)[j*Hv*K*V:(j+1)*Hv*K*V]`` when ``cache`` is given: a tensor whose
+    first dimension is the request and whose row pitch (``cache.stride(0)`` elements) is
+    passed to the kernel as is.  The pool row gets the last state only if ``update_pool``.
+    Returns o [T, Hv, V]."""
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("pool", pool)):
+        _need(t, name)
+    _need(g, "g", torch.float32)
+    _need(beta, "beta", torch.float32)
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    if state_indices is not None:
+        _need(state_indices, "state_indices", torch.int32)
+    T, Hk, K = q.shape
+    Hv, V = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if max_steps is None:
+        max_steps = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if N > 0 else 1
+    pitch = 0
+    if cache is not None:
+        if not isinstance(cache, torch.Tensor) or not cache.is_cuda or cache.dtype != pool.dtype:
+            raise TypeError("cache must be a CUDA tensor of the pool's dtype")
+        pitch = cache.stride(0)
+    d = make_desc(num_seqs=N, total_tokens=T, Hk=Hk, Hv=Hv, K=K, V=V, qkv_dtype=q.dtype,
+                  state_dtype=pool.dtype, scale=scale, num_slots=pool.shape[0],
+                  slot_stride=slot_stride,
+                  flags=(KDA_FLAG_SCALAR_GATE if g.dim() == 2 else 0)
+                  | (KDA_FLAG_QK_L2NORM if qk_l2norm else 0))
+    if out is None:
+        out = torch.empty((T, Hv, V), dtype=q.dtype, device=q.device)
+    ws_size = lib.kda_decode_workspace_size(ctypes.byref(d))
+    if ws_size == 0:
+        raise KdaError(1, "kda_decode_workspace_size")
+    if workspace is None or workspace.numel() < ws_size:
+        workspace = torch.empty(ws_size, dtype=torch.uint8, device=q.device)
+    rc = lib.kda_decode_draft(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                              _ptr(cu_seqlens), _ptr(pool), _ptr(state_indices), _ptr(cache),
+                              pitch, int(max_steps), 1 if update_pool else 0, _ptr(out),
+                              _ptr(workspace), workspace.numel(), _stream(stream))
+    if rc != 0:
+        raise KdaError(rc, "kda_decode_draft")
+    decode_draft.last_workspace = workspace
     return out

@@ -182,6 +182,55 @@ kda_status_t kda_decode(const kda_desc_t* d, const void* q, const void* k, const
   a.idx = state_indices;
   a.o = o;
   a.status = &reinterpret_cast<kda::WsHeader*>(workspace)->status;
+  a.cu = nullptr;
+  a.cache = nullptr;
+  a.cache_pitch = 0;
+  a.max_steps = 1;
+  a.update_pool = true;
+  if (cudaMemsetAsync(workspace, 0, sizeof(kda::WsHeader), stream) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  return kda::launch_decode(a, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_decode_draft(const kda_desc_t* d, const void* q, const void* k, const void* v,
+                              const float* g, const float* beta, const int32_t* cu_seqlens,
+                              void* state_pool, const int32_t* state_indices, void* step_cache,
+                              int64_t cache_pitch_elems, int32_t max_steps, int update_pool,
+                              void* o, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+  if (!dims_ok(d)) return KDA_ERR_INVALID_ARGUMENT;
+  if (!heads_supported(d)) return KDA_ERR_UNSUPPORTED;
+  if (d->num_v_heads > 65535) return KDA_ERR_UNSUPPORTED;  // grid.y limit
+  if (!workspace || !aligned(workspace, 256) || !cu_seqlens) return KDA_ERR_INVALID_ARGUMENT;
+  if (d->total_tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARGUMENT;
+  if (d->num_seqs > 0 && !state_pool) return KDA_ERR_INVALID_ARGUMENT;
+  if (d->num_slots <= 0 || !pitch_ok(d) || max_steps < 1) return KDA_ERR_INVALID_ARGUMENT;
+  const int64_t hkv = (int64_t)d->num_v_heads * d->head_k_dim * d->head_v_dim;
+  if (step_cache && (cache_pitch_elems < (int64_t)max_steps * hkv || cache_pitch_elems % 8 != 0))
+    return KDA_ERR_INVALID_ARGUMENT;
+  {
+    const void* ptrs[] = {q, k, v, g, o, state_pool, step_cache};
+    for (const void* p : ptrs)
+      if (p && !aligned(p, 16)) return KDA_ERR_INVALID_ARGUMENT;
+  }
+  if (workspace_bytes < kda_decode_workspace_size(d)) return KDA_ERR_WORKSPACE_TOO_SMALL;
+
+  kda::DecodeArgs a;
+  a.d = *d;
+  a.scale = eff_scale(d);
+  a.slot_stride = slot_pitch(d);
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.gate_k = (d->flags & KDA_FLAG_SCALAR_GATE) ? 1 : d->head_k_dim;
+  a.l2norm = (d->flags & KDA_FLAG_QK_L2NORM) != 0;
+  a.pool = state_pool;
+  a.idx = state_indices;
+  a.o = o;
+  a.status = &reinterpret_cast<kda::WsHeader*>(workspace)->status;
+  a.cu = cu_seqlens;
+  a.cache = step_cache;
+  a.cache_pitch = cache_pitch_elems;
+  a.max_steps = max_steps;
+  a.update_pool = update_pool != 0;
   if (cudaMemsetAsync(workspace, 0, sizeof(kda::WsHeader), stream) != cudaSuccess)
     return KDA_ERR_CUDA;
   return kda::launch_decode(a, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;

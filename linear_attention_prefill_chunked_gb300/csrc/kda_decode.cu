@@ -48,13 +48,26 @@ template <> struct Vec4<__nv_bfloat16> {
   }
 };
 
+// Draft steps (speculative decoding): with `cu` set, row n is a request whose tokens
+// cu[n] .. cu[n+1]-1 run one after another from the same state; the state after step j
+// is written to cache + n * cache_pitch + j * Hv*K*V (per-request pitch passed in, not
+// inferred from a buffer shape: PR 37317 digest, 实现拆解 item 2), and the pool row is
+// written only if update_pool.  Without `cu` each row is one token and the pool is updated.
+struct DraftArgs {
+  const int32_t* cu;   // [N+1] or null
+  void* cache;         // null: no per-step states
+  int64_t cache_pitch;
+  int max_steps;
+  bool update_pool;
+};
+
 template <typename QT, typename ST, int K, int VT>
 __global__ void __launch_bounds__(kDecThreads)
 kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* __restrict__ v,
                   const float* __restrict__ g, const float* __restrict__ beta,
                   ST* __restrict__ pool, const int32_t* __restrict__ idx, QT* __restrict__ o,
                   uint32_t* __restrict__ status, int Hk, int Hv, int V, int64_t num_slots,
-                  int64_t slot_stride, float scale, int gk, bool l2norm) {
+                  int64_t slot_stride, float scale, int gk, bool l2norm, DraftArgs dr, int64_t T) {
   constexpr int TPR = VT / 4;               // threads per row
   constexpr int RG = kDecThreads / TPR;     // row groups
   constexpr int RPT = K / RG;               // rows per thread
@@ -63,6 +76,13 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
   const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * VT;
   const int tid = threadIdx.x, rg = tid / TPR, col = (tid % TPR) * 4;
 
+  int64_t bos = n, eos = n + 1;
+  if (dr.cu != nullptr) {
+    if (!seq_bounds(dr.cu, n, T, &bos, &eos) || eos - bos > dr.max_steps) {
+      if (tid == 0 && blockIdx.z == 0 && h == 0) raise_status(status, KDA_DEVICE_BAD_SEQLENS);
+      return;
+    }
+  }
   int64_t slot = n;
   if (idx != nullptr) {
     slot = resolve_slot(idx, n, num_slots);
@@ -77,95 +97,106 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
 
   __shared__ float red_w[RG][VT];
   __shared__ float red_o[RG][VT];
+  __shared__ float red_n[2][RG];
 
   const int kh = h / (Hv / Hk);
-  const QT* qn = q + ((size_t)n * Hk + kh) * K;
-  const QT* kn = k + ((size_t)n * Hk + kh) * K;
-  const float* gn = g + ((size_t)n * Hv + h) * gk;  // gk = K, or 1 for a scalar gate
   ST* S = pool + slot * slot_stride + (size_t)h * K * V + v0 + col;
-
-  // optional q/k normalisation: ||k||, ||q|| reduced over the row groups
-  float ik = 1.f, iq = 1.f;
-  if (l2norm) {
-    __shared__ float red_n[2][RG];
-    float sk = 0.f, sq = 0.f;
-#pragma unroll
-    for (int j = 0; j < RPT; ++j) {
-      const float kv = to_f32(kn[rg + j * RG]), qv = to_f32(qn[rg + j * RG]);
-      sk = fmaf(kv, kv, sk);
-      sq = fmaf(qv, qv, sq);
-    }
-    if (col == 0) {
-      red_n[0][rg] = sk;
-      red_n[1][rg] = sq;
-    }
-    __syncthreads();
-    float tk = 0.f, tq = 0.f;
-#pragma unroll
-    for (int r = 0; r < RG; ++r) {
-      tk += red_n[0][r];
-      tq += red_n[1][r];
-    }
-    ik = 1.f / fmaxf(sqrtf(tk), 1e-12f);
-    iq = 1.f / fmaxf(sqrtf(tq), 1e-12f);
-  }
-  float s[RPT][4], kr[RPT], qr[RPT];
+  float s[RPT][4];
   // Issue every state load first (the tile is the whole cost of the kernel).
 #pragma unroll
   for (int j = 0; j < RPT; ++j) Vec4<ST>::load(S + (size_t)(rg + j * RG) * V, s[j]);
-  float w[4] = {0.f, 0.f, 0.f, 0.f};
+
+  for (int64_t t = bos; t < eos; ++t) {
+    if (t > bos) __syncthreads();  // the previous step's readers of red_* are done
+    const QT* qn = q + ((size_t)t * Hk + kh) * K;
+    const QT* kn = k + ((size_t)t * Hk + kh) * K;
+    const float* gn = g + ((size_t)t * Hv + h) * gk;  // gk = K, or 1 for a scalar gate
+    // optional q/k normalisation: ||k||, ||q|| reduced over the row groups
+    float ik = 1.f, iq = 1.f;
+    if (l2norm) {
+      float sk = 0.f, sq = 0.f;
 #pragma unroll
-  for (int j = 0; j < RPT; ++j) {
-    const int c = rg + j * RG;
-    const float e = expf(gn[gk > 1 ? c : 0]);
-    kr[j] = to_f32(kn[c]) * ik;
-    qr[j] = to_f32(qn[c]) * iq;
+      for (int j = 0; j < RPT; ++j) {
+        const float kv = to_f32(kn[rg + j * RG]), qv = to_f32(qn[rg + j * RG]);
+        sk = fmaf(kv, kv, sk);
+        sq = fmaf(qv, qv, sq);
+      }
+      if (col == 0) {
+        red_n[0][rg] = sk;
+        red_n[1][rg] = sq;
+      }
+      __syncthreads();
+      float tk = 0.f, tq = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      s[j][i] *= e;                    // decay first
-      w[i] = fmaf(kr[j], s[j][i], w[i]);
+      for (int r = 0; r < RG; ++r) {
+        tk += red_n[0][r];
+        tq += red_n[1][r];
+      }
+      ik = 1.f / fmaxf(sqrtf(tk), 1e-12f);
+      iq = 1.f / fmaxf(sqrtf(tq), 1e-12f);
+    }
+    float kr[RPT], qr[RPT];
+    float w[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const int c = rg + j * RG;
+      const float e = expf(gn[gk > 1 ? c : 0]);
+      kr[j] = to_f32(kn[c]) * ik;
+      qr[j] = to_f32(qn[c]) * iq;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s[j][i] *= e;                    // decay first
+        w[i] = fmaf(kr[j], s[j][i], w[i]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) red_w[rg][col + i] = w[i];
+    __syncthreads();
+    const float b = beta[(size_t)t * Hv + h];
+    float u[4];
+    {
+      float vin[4];
+      const QT* vn = v + ((size_t)t * Hv + h) * V + v0 + col;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) vin[i] = to_f32(vn[i]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float acc = 0.f;
+#pragma unroll
+        for (int r = 0; r < RG; ++r) acc += red_w[r][col + i];
+        u[i] = b * (vin[i] - acc);
+      }
+    }
+    ST* C = dr.cache ? static_cast<ST*>(dr.cache) + n * dr.cache_pitch +
+                           (t - bos) * ((int64_t)Hv * K * V) + (size_t)h * K * V + v0 + col
+                     : nullptr;
+    float ov[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s[j][i] = fmaf(kr[j], u[i], s[j][i]);
+        ov[i] = fmaf(qr[j], s[j][i], ov[i]);
+      }
+      if (C) Vec4<ST>::store(C + (size_t)(rg + j * RG) * V, s[j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) red_o[rg][col + i] = ov[i];
+    __syncthreads();
+    if (rg == 0) {
+      QT* on = o + ((size_t)t * Hv + h) * V + v0 + col;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float acc = 0.f;
+#pragma unroll
+        for (int r = 0; r < RG; ++r) acc += red_o[r][col + i];
+        on[i] = from_f32<QT>(scale * acc);
+      }
     }
   }
+  if (dr.update_pool) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) red_w[rg][col + i] = w[i];
-  __syncthreads();
-  const float b = beta[(size_t)n * Hv + h];
-  float u[4];
-  {
-    float vin[4];
-    const QT* vn = v + ((size_t)n * Hv + h) * V + v0 + col;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) vin[i] = to_f32(vn[i]);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float acc = 0.f;
-#pragma unroll
-      for (int r = 0; r < RG; ++r) acc += red_w[r][col + i];
-      u[i] = b * (vin[i] - acc);
-    }
-  }
-  float ov[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < RPT; ++j) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      s[j][i] = fmaf(kr[j], u[i], s[j][i]);
-      ov[i] = fmaf(qr[j], s[j][i], ov[i]);
-    }
-    Vec4<ST>::store(S + (size_t)(rg + j * RG) * V, s[j]);
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) red_o[rg][col + i] = ov[i];
-  __syncthreads();
-  if (rg == 0) {
-    QT* on = o + ((size_t)n * Hv + h) * V + v0 + col;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float acc = 0.f;
-#pragma unroll
-      for (int r = 0; r < RG; ++r) acc += red_o[r][col + i];
-      on[i] = from_f32<QT>(scale * acc);
-    }
+    for (int j = 0; j < RPT; ++j) Vec4<ST>::store(S + (size_t)(rg + j * RG) * V, s[j]);
   }
 }
 
@@ -178,12 +209,14 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
     kda_decode_kernel<QT, ST, K, 128><<<grid, kDecThreads, 0, st>>>(
         (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, (ST*)a.pool, a.idx,
         (QT*)a.o, a.status, a.d.num_k_heads, a.d.num_v_heads, V, a.d.num_slots, a.slot_stride,
-        a.scale, a.gate_k, a.l2norm);
+        a.scale, a.gate_k, a.l2norm, DraftArgs{a.cu, a.cache, a.cache_pitch, a.max_steps,
+                                                 a.update_pool}, a.d.total_tokens);
   else
     kda_decode_kernel<QT, ST, K, 64><<<grid, kDecThreads, 0, st>>>(
         (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, (ST*)a.pool, a.idx,
         (QT*)a.o, a.status, a.d.num_k_heads, a.d.num_v_heads, V, a.d.num_slots, a.slot_stride,
-        a.scale, a.gate_k, a.l2norm);
+        a.scale, a.gate_k, a.l2norm, DraftArgs{a.cu, a.cache, a.cache_pitch, a.max_steps,
+                                                 a.update_pool}, a.d.total_tokens);
   return cudaGetLastError();
 }
 

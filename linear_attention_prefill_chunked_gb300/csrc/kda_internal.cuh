@@ -103,6 +103,12 @@ struct DecodeArgs {
   const int32_t* idx;
   void* o;
   uint32_t* status;
+  // draft steps (kda_decode_draft); plain decode: cu null, cache null, update_pool true
+  const int32_t* cu;
+  void* cache;
+  int64_t cache_pitch;
+  int max_steps;
+  bool update_pool;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 }  // namespace kda
