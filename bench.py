@@ -198,6 +198,57 @@ def run_reference(args, dist, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_decode(args, dist, ws, rank, local):
+    """Decode of 4096 one-token rows (64 padding rows on the sentinel) on an 8192-slot fp32
+    pool (16 GiB, resident): real rows per second, against the HBM roofline of streaming
+    each row's state tile in and out once (4,243,584 bytes per real row)."""
+    import linear_attention_prefill_chunked_gb300 as kda
+    from linear_attention_prefill_chunked_gb300 import synthetic
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kda.load()
+    w = synthetic.decode_batch(pool_device=dev)
+    t = lambda x: x.to(dev).contiguous()
+    q, k, v, g, beta, idx = (t(x) for x in (w.q, w.k, w.v, w.g, w.beta, w.state_indices))
+    pool = w.state
+    out = torch.empty_like(v)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: kda.decode(q, k, v, g, beta, pool, idx, out=out, stream=stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in ev]
+    if rank != 0:
+        return
+    real = int((w.state_indices >= 0).sum())
+    Hv, K, V = w.v.shape[1], w.q.shape[2], w.v.shape[2]
+    row_bytes = 2 * Hv * K * V * 4 + Hv * (2 * K * 2 + V * 2 + K * 4 + 4 + V * 2)
+    ms = statistics.median(per)
+    hbm, _, src = _peaks()
+    achieved = real * row_bytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "KDA decode rows/s (4096 one-token rows, Hv=32, K=V=128, fp32 pool)",
+        "value": real / (ms * 1e-3), "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "real_rows": real, "padding_rows": w.N - real,
+                   "pool": "fp32 [8192, 32, 128, 128], resident",
+                   "l2": "state tiles (16 GiB pool) larger than L2, no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None, "peak_source": src,
+                     "algorithmic_bytes_per_launch": real * row_bytes},
+        "clocks": clk.summary(), "gpu_launches": args.steps}), flush=True)
+
+
 def run_ours(args, dist, ws, rank, local):
     import linear_attention_prefill_chunked_gb300 as kda
     from linear_attention_prefill_chunked_gb300 import synthetic
@@ -356,7 +407,7 @@ def main():
                          "(kda_chunk_prefill_act); scalar: one log-decay per token and head")
     ap.add_argument("--qk-l2norm", action="store_true",
                     help="normalise q and k inside the kernel (KDA_FLAG_QK_L2NORM)")
-    ap.add_argument("--workload", default="throughput", choices=["throughput", "profile"],
+    ap.add_argument("--workload", default="throughput", choices=["throughput", "profile", "decode"],
                     help="profile: 8 x 1024 tokens, Hv=32 (a smaller case for ncu captures)")
     args = ap.parse_args()
     dist, ws, rank, local = _dist()
@@ -364,7 +415,7 @@ def main():
         if args.impl == "reference":
             run_reference(args, dist, ws, rank)
         else:
-            run_ours(args, dist, ws, rank, local)
+            (run_decode if args.workload == "decode" else run_ours)(args, dist, ws, rank, local)
     finally:
         if dist:
             dist.destroy_process_group()

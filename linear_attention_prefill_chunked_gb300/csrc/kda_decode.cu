@@ -62,7 +62,7 @@ struct DraftArgs {
 };
 
 template <typename QT, typename ST, int K, int VT>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, 2)
 kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* __restrict__ v,
                   const float* __restrict__ g, const float* __restrict__ beta,
                   ST* __restrict__ pool, const int32_t* __restrict__ idx, QT* __restrict__ o,
@@ -97,7 +97,8 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
 
   __shared__ float red_w[RG][VT];
   __shared__ float red_o[RG][VT];
-  __shared__ float red_n[2][RG];
+  __shared__ float red_n[2][kDecThreads / 32];
+  __shared__ float kq_s[3][K];  // k, q and exp(g) of the current token, shared by the block
 
   const int kh = h / (Hv / Hk);
   ST* S = pool + slot * slot_stride + (size_t)h * K * V + v0 + col;
@@ -107,46 +108,51 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
   for (int j = 0; j < RPT; ++j) Vec4<ST>::load(S + (size_t)(rg + j * RG) * V, s[j]);
 
   for (int64_t t = bos; t < eos; ++t) {
-    if (t > bos) __syncthreads();  // the previous step's readers of red_* are done
-    const QT* qn = q + ((size_t)t * Hk + kh) * K;
-    const QT* kn = k + ((size_t)t * Hk + kh) * K;
-    const float* gn = g + ((size_t)t * Hv + h) * gk;  // gk = K, or 1 for a scalar gate
-    // optional q/k normalisation: ||k||, ||q|| reduced over the row groups
+    if (t > bos) __syncthreads();  // the previous step's readers of the shared arrays are done
+    // k, q, exp(g) of token t into shared memory (registers stay with the state tile);
+    // with l2norm the two norms are reduced over the block first
+    float kv = 0.f, qv = 0.f;
+    if (tid < K) {
+      kv = to_f32(k[((size_t)t * Hk + kh) * K + tid]);
+      qv = to_f32(q[((size_t)t * Hk + kh) * K + tid]);
+      kq_s[2][tid] = expf(g[((size_t)t * Hv + h) * gk + (gk > 1 ? tid : 0)]);
+    }
     float ik = 1.f, iq = 1.f;
     if (l2norm) {
-      float sk = 0.f, sq = 0.f;
+      float sk = kv * kv, sq = qv * qv;
 #pragma unroll
-      for (int j = 0; j < RPT; ++j) {
-        const float kv = to_f32(kn[rg + j * RG]), qv = to_f32(qn[rg + j * RG]);
-        sk = fmaf(kv, kv, sk);
-        sq = fmaf(qv, qv, sq);
+      for (int o2 = 16; o2; o2 >>= 1) {
+        sk += __shfl_xor_sync(0xffffffffu, sk, o2);
+        sq += __shfl_xor_sync(0xffffffffu, sq, o2);
       }
-      if (col == 0) {
-        red_n[0][rg] = sk;
-        red_n[1][rg] = sq;
+      if ((tid & 31) == 0) {
+        red_n[0][tid >> 5] = sk;
+        red_n[1][tid >> 5] = sq;
       }
       __syncthreads();
       float tk = 0.f, tq = 0.f;
 #pragma unroll
-      for (int r = 0; r < RG; ++r) {
+      for (int r = 0; r < K / 32; ++r) {
         tk += red_n[0][r];
         tq += red_n[1][r];
       }
       ik = 1.f / fmaxf(sqrtf(tk), 1e-12f);
       iq = 1.f / fmaxf(sqrtf(tq), 1e-12f);
     }
-    float kr[RPT], qr[RPT];
+    if (tid < K) {
+      kq_s[0][tid] = kv * ik;
+      kq_s[1][tid] = qv * iq;
+    }
+    __syncthreads();
     float w[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < RPT; ++j) {
       const int c = rg + j * RG;
-      const float e = expf(gn[gk > 1 ? c : 0]);
-      kr[j] = to_f32(kn[c]) * ik;
-      qr[j] = to_f32(qn[c]) * iq;
+      const float e = kq_s[2][c], kr = kq_s[0][c];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         s[j][i] *= e;                    // decay first
-        w[i] = fmaf(kr[j], s[j][i], w[i]);
+        w[i] = fmaf(kr, s[j][i], w[i]);
       }
     }
 #pragma unroll
@@ -173,10 +179,12 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
     float ov[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < RPT; ++j) {
+      const int c = rg + j * RG;
+      const float kr = kq_s[0][c], qr = kq_s[1][c];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        s[j][i] = fmaf(kr[j], u[i], s[j][i]);
-        ov[i] = fmaf(qr[j], s[j][i], ov[i]);
+        s[j][i] = fmaf(kr, u[i], s[j][i]);
+        ov[i] = fmaf(qr, s[j][i], ov[i]);
       }
       if (C) Vec4<ST>::store(C + (size_t)(rg + j * RG) * V, s[j]);
     }
