@@ -95,7 +95,7 @@ constexpr uint32_t BAR_IG = 1, BAR_RG = 2, BAR_A = 3;
 
 enum Bar {
   B_QK_FULL, B_V_FULL, B_G_FULL, B_AB_DONE, B_UW_DONE, B_GAMMA0, B_GAMMA1, B_REC_READY,
-  B_M1A, B_M1B, B_M3A, B_M3B, B_E1, B_DRAIN_IG, B_DRAIN_RG,
+  B_M1A, B_M1B, B_M3A, B_M3B, B_E1, B_DRAIN_IG, B_DRAIN_RG, B_W_FREE,
   B_ITEM_FULL, B_ITEM_EMPTY = B_ITEM_FULL + kRing, B_COUNT = B_ITEM_EMPTY + kRing
 };
 
@@ -407,7 +407,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         const LoaderState* L = ld.st;
         if (L->n_qk == gc) ld.load_qk(p, sm, s, kh, (int)t0);
         if (L->n_g == gc) ld.load_g(p, sm, s, h, (int)t0);
-        if (L->n_v == gc) ld.load_v(p, sm, s, h, (int)t0);
       }
       __syncwarp();
       // ------------------------------------------------------------- prologue
@@ -460,8 +459,9 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       float pm0 = 1.f, pm1 = 1.f;
 #pragma unroll
       for (int j = 0; j < 16; ++j) { pm0 *= e0[j]; pm1 *= e1[j]; }
-      // exchange the sub-chunk products through the Tm buffer (idle until the inverse)
-      float* pis = reinterpret_cast<float*>(sm + OFF_TM);
+      // exchange the sub-chunk products through CB block 0 (its last readers, MMA-AB and
+      // the KR pass of the previous chunk, are done; pass A rewrites it after a barrier)
+      float* pis = reinterpret_cast<float*>(sm + OFF_CB);
       *reinterpret_cast<float2*>(pis + sc * kK + c0) = make_float2(pm0, pm1);
       {  // "unsafe" channels of this sub-chunk (product below 2^-100 or not finite)
         const uint32_t m0 = __ballot_sync(0xffffffffu, !(pm0 >= kSafeMin));
@@ -476,6 +476,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         // staged rows (k 0-63, q 64-127) -> x / max(||x||, 1e-12), re-rounded to bf16 as a
         // caller's normalise-then-cast would; thread = (row, 64-channel half).  The inverse
         // norms are kept for the pairwise path, which reads q and k from global memory.
+        if (gc > 0) wait_bar(p, s, B_UW_DONE, (gc - 1) & 1);  // Tm buffer read by MMA-U/W(c-1)
         const int row = t >> 1, hf = t & 1;
         uint8_t* base = sm + OFF_QK + hf * 16384;
         float ss = 0.f;
@@ -513,6 +514,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         pi0[q2] = pv.x;
         pi1[q2] = pv.y;
       }
+      named_bar(BAR_IG, kIG);  // every warp holds its products before pass A writes CB block 0
       const float E0 = (sc > 0 ? pi0[0] : 1.f) * (sc > 1 ? pi0[1] : 1.f) * (sc > 2 ? pi0[2] : 1.f);
       const float E1 = (sc > 0 ? pi1[0] : 1.f) * (sc > 1 ? pi1[1] : 1.f) * (sc > 2 ? pi1[2] : 1.f);
       if (sc == 3)  // warps 6-7 (fewest block-1 variants): gamma of their 64 channels
@@ -565,6 +567,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             }
           }
         }
+        // KG is read by MMA-W of the previous chunk, issued by the recurrence group
+        if (gc > 0) wait_bar(p, s, B_UW_DONE, (gc - 1) & 1);
         // pass B, ascending: rho (inclusive product from the sub-chunk start); q and k
         // rows of the MMA-AB operand in place, and KG, QG.
         const float qs0 = p.scale * E0, qs1 = p.scale * E1;
@@ -631,6 +635,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       named_bar(BAR_IG, kIG);
       if (t == 0) {
         mbar_arrive(&s->bar[B_GAMMA0 + (gc & 1)]);
+        if (gc > 0) wait_bar(p, s, B_W_FREE, (gc - 1) & 1);  // W of the last chunk read out
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(128, 192, 1, 1);
 #pragma unroll 1
@@ -656,6 +661,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       wait_bar(p, s, B_AB_DONE, gc & 1);
       tc_fence_after();
       if (t == 0 && ld.st->have_next && ld.st->n_g == gc + 1) ld.load_g(p, sm, s, ld.st->nh, ld.st->nt0);  // CB 1-2 free
+      if (t == 0 && ld.st->n_v == gc) ld.load_v(p, sm, s, h, (int)t0);  // VB free since MMA-U(c-1)
       __syncwarp();
       uint32_t any_unsafe = 0;
 #pragma unroll
@@ -917,48 +923,12 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         if (t < ld.st->ncv) bt_next = p.beta[(size_t)(ld.st->nt0 + t) * p.Hv + ld.st->nh];
         bt_ok = true;
       }
-      // ------------------------------------------------------------- U~ and W
-      if (warp == 0) {
-        wait_bar(p, s, B_V_FULL, gc & 1);
-        if (gc > 0) wait_bar(p, s, B_E1, (gc - 1) & 1);  // U region read by the recurrence
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t idu = idesc_bf16(128, 64, 1, 0), idw = idesc_bf16(128, 64, 0, 0);
-#pragma unroll 1
-          for (int st = 0; st < 4; ++st) {
-            const uint64_t b = sdesc_sw128(sbase + OFF_TM + st * 32, 16, 1024);
-            mma_bf16(tbase + TM_U, sdesc_sw128(sbase + OFF_VB + st * 2048, 8192, 1024), b, idu,
-                     st > 0 ? 1u : 0u);
-            mma_bf16(tbase + TM_AB, sdesc_sw128(sbase + OFF_KG + st * 32, 16, 1024), b, idw,
-                     st > 0 ? 1u : 0u);
-          }
-          mma_commit(&s->bar[B_UW_DONE]);
-          // q/k of the next chunk into the buffer the inverse scratch used
-          if (ld.st->have_next && ld.st->n_qk == gc + 1) ld.load_qk(p, sm, s, ld.st->nkh, ld.st->nt0);
-        }
-        __syncwarp();
+      // q/k of the next chunk into the buffer the inverse scratch used; then hand the
+      // chunk to the recurrence group (it issues MMA-U/W and reads -W out itself)
+      if (t == 0) {
+        if (ld.st->have_next && ld.st->n_qk == gc + 1) ld.load_qk(p, sm, s, ld.st->nkh, ld.st->nt0);
+        mbar_arrive(&s->bar[B_REC_READY]);
       }
-      wait_bar(p, s, B_UW_DONE, gc & 1);
-      tc_fence_after();
-      if (t == 0 && ld.st->have_next && ld.st->n_v == gc + 1) ld.load_v(p, sm, s, ld.st->nh, ld.st->nt0);  // VB free
-      __syncwarp();
-      // -W^T rows -> WB (row = channel L, tokens 32*hx ..)
-      if (gc > 0) wait_bar(p, s, B_M1A, (gc - 1) & 1);
-#pragma unroll
-      for (int cq = 0; cq < 2; ++cq) {
-        float wv[16];
-        tmem_ld16(taddr_q + TM_AB + hx * 32 + cq * 16, wv);
-        tmem_ld_wait();
-        uint32_t w[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(-wv[2 * u], -wv[2 * u + 1]);
-        st_chunk(sm, OFF_WB + sw128_off(L, hx * 4 + cq * 2), w[0], w[1], w[2], w[3]);
-        st_chunk(sm, OFF_WB + sw128_off(L, hx * 4 + cq * 2 + 1), w[4], w[5], w[6], w[7]);
-      }
-      tc_fence_before();
-      fence_async_smem();
-      named_bar(BAR_IG, kIG);
-      if (t == 0) mbar_arrive(&s->bar[B_REC_READY]);
       __syncwarp();
     }
     if (stop) break;
@@ -1038,9 +1008,51 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       const int64_t t0 = info.bos + (int64_t)lc * kC;
       const int cv = (int)min((int64_t)kC, info.eos - t0);
       const bool last = (lc + 1 == info.nchunks);
-      // ---- R1: U~ -= S W^T ; O = S QG^T   (leader warp)
+      // ---- R0 (leader warp): O = S QG^T first (frees QG and gamma for the next chunk's
+      // prologue soonest), then U~^T = V^T Tm^T and W^T = KG^T Tm^T; -W^T rows -> WB
       if (leader_warp) {
         wait_bar(p, s, B_REC_READY, gc & 1);
+        wait_bar(p, s, B_V_FULL, gc & 1);
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
+#pragma unroll 1
+          for (int st = 0; st < 8; ++st)
+            mma_bf16_ta(tbase + TM_O, tbase + TM_SB + st * 8,
+                        sdesc_sw128(sbase + OFF_QG + st * 2048, 16384, 1024), id1, st > 0 ? 1u : 0u);
+          mma_commit(&s->bar[B_M1B]);
+          const uint32_t idu = idesc_bf16(128, 64, 1, 0), idw = idesc_bf16(128, 64, 0, 0);
+#pragma unroll 1
+          for (int st = 0; st < 4; ++st) {
+            const uint64_t b = sdesc_sw128(sbase + OFF_TM + st * 32, 16, 1024);
+            mma_bf16(tbase + TM_U, sdesc_sw128(sbase + OFF_VB + st * 2048, 8192, 1024), b, idu,
+                     st > 0 ? 1u : 0u);
+            mma_bf16(tbase + TM_AB, sdesc_sw128(sbase + OFF_KG + st * 32, 16, 1024), b, idw,
+                     st > 0 ? 1u : 0u);
+          }
+          mma_commit(&s->bar[B_UW_DONE]);
+        }
+        __syncwarp();
+      }
+      wait_bar(p, s, B_UW_DONE, gc & 1);
+      tc_fence_after();
+#pragma unroll 1
+      for (int cq = 0; cq < 4; ++cq) {  // row = channel v, tokens 16 cq ..
+        float wv[16];
+        tmem_ld16(taddr_q + TM_AB + cq * 16, wv);
+        tmem_ld_wait();
+        uint32_t w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(-wv[2 * u], -wv[2 * u + 1]);
+        st_chunk(sm, OFF_WB + sw128_off(v, cq * 2), w[0], w[1], w[2], w[3]);
+        st_chunk(sm, OFF_WB + sw128_off(v, cq * 2 + 1), w[4], w[5], w[6], w[7]);
+      }
+      tc_fence_before();
+      fence_async_smem();
+      named_bar(BAR_RG, kRG);
+      if (rt == 0) mbar_arrive(&s->bar[B_W_FREE]);
+      // ---- R1: U~ -= S W^T   (leader warp)
+      if (leader_warp) {
         if (lane == 0) {
           tc_fence_after();
           const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
@@ -1049,11 +1061,6 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
             mma_bf16_ta(tbase + TM_U, tbase + TM_SB + st * 8,
                         sdesc_sw128(sbase + OFF_WB + st * 2048, 16384, 1024), id1, 1u);
           mma_commit(&s->bar[B_M1A]);
-#pragma unroll 1
-          for (int st = 0; st < 8; ++st)
-            mma_bf16_ta(tbase + TM_O, tbase + TM_SB + st * 8,
-                        sdesc_sw128(sbase + OFF_QG + st * 2048, 16384, 1024), id1, st > 0 ? 1u : 0u);
-          mma_commit(&s->bar[B_M1B]);
         }
         __syncwarp();
       }
