@@ -645,7 +645,9 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           mma_bf16(tbase + TM_AB, a, b, idesc, st > 0 ? 1u : 0u);
         }
         mma_commit(&s->bar[B_AB_DONE]);
-        // while MMA-AB runs: the chunk after this one, and its q/k/v into L2
+      } else if (t == 32) {
+        // meanwhile, on another warp: the chunk after this one, and its q/k/v into L2
+        // (read by thread 0 only after a later barrier)
         LoaderState* L = ld.st;
         int nkh = 0, nh = 0, nt0 = 0, ncv = 0;
         const bool hn = ld.next_chunk(s, k, lc, nkh, nh, nt0, ncv);
@@ -660,7 +662,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // ------------------------------------------------------------- A / B rows
       wait_bar(p, s, B_AB_DONE, gc & 1);
       tc_fence_after();
-      if (t == 0 && ld.st->have_next && ld.st->n_g == gc + 1) ld.load_g(p, sm, s, ld.st->nh, ld.st->nt0);  // CB 1-2 free
       if (t == 0 && ld.st->n_v == gc) ld.load_v(p, sm, s, h, (int)t0);  // VB free since MMA-U(c-1)
       __syncwarp();
       uint32_t any_unsafe = 0;
@@ -834,6 +835,9 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           }
         }
         named_bar(BAR_A, 128);
+        // gate of the next chunk into CB 1-2 (free since MMA-AB; the lookahead written by
+        // thread 32 before AB_DONE is ordered by the barriers since)
+        if (t == 0 && ld.st->have_next && ld.st->n_g == gc + 1) ld.load_g(p, sm, s, ld.st->nh, ld.st->nt0);
         // 32x32 halves: X_{a+1,a} = -X_{a+1,a+1} (A_{a+1,a} X_aa) for a = 0, 2 (P staged
         // in the unused upper block (a, a+1) of A) ...
         const int aw = (warp >> 2) * 2 + (warp & 1);  // 0..3 within the A group
