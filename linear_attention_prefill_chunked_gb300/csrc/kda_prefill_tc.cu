@@ -548,22 +548,29 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             const int c = c2 ^ wsel;
             const int row = c0 + c;
             const float ip = c ? ip1 : ip0;
-            float x[8];
+            // k kap of this channel's 8 tokens as bf16 pairs.  The block-1 variants scale the
+            // pairs with one packed bf16 product each; block 2 (the diagonal sub-chunk
+            // blocks, where a second rounding shows in the output) rounds its fp32 product once.
+            uint32_t x2[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) x[u] = c ? kk[1][u] : kk[0][u];
-            st_chunk(sm, OFF_CB + sw128_off(row, cj), pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
-                     pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
-            st_chunk(sm, OFF_CB + 32768 + sw128_off(row, cj), pack_bf16x2(x[0] * ip, x[1] * ip),
-                     pack_bf16x2(x[2] * ip, x[3] * ip), pack_bf16x2(x[4] * ip, x[5] * ip),
-                     pack_bf16x2(x[6] * ip, x[7] * ip));
+            for (int u = 0; u < 4; ++u)
+              x2[u] = c ? pack_bf16x2(kk[1][2 * u], kk[1][2 * u + 1]) : pack_bf16x2(kk[0][2 * u], kk[0][2 * u + 1]);
+            st_chunk(sm, OFF_CB + sw128_off(row, cj), x2[0], x2[1], x2[2], x2[3]);
+            {
+              float x[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) x[u] = (c ? kk[1][u] : kk[0][u]) * ip;
+              st_chunk(sm, OFF_CB + 32768 + sw128_off(row, cj), pack_bf16x2(x[0], x[1]),
+                       pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+            }
             const float p1 = c ? pi1[1] : pi0[1], p2 = c ? pi1[2] : pi0[2];
 #pragma unroll 1
             for (int e = 0; e < nvar; ++e) {
               const float f = (sc == 0) ? (e ? p1 * p2 : p1) : (sc == 1 ? p2 : 0.f);
               const int ch = (sc == 0) ? 2 * e + jh : (sc == 1 ? 4 + jh : 6 + jh);
-              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, ch), pack_bf16x2(x[0] * f, x[1] * f),
-                       pack_bf16x2(x[2] * f, x[3] * f), pack_bf16x2(x[4] * f, x[5] * f),
-                       pack_bf16x2(x[6] * f, x[7] * f));
+              const uint32_t ff = pack_bf16x2(f, f);
+              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, ch), bmul2(x2[0], ff), bmul2(x2[1], ff),
+                       bmul2(x2[2], ff), bmul2(x2[3], ff));
             }
           }
         }
@@ -584,9 +591,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           }
           // k rho, q rho (MN-major A operand of MMA-AB) and KG, QG of channels c0 and
           // c0+1, packed as token pairs while they are formed
-          uint32_t kaw[2][4], qaw[2][4], kgw[2][4], qgw[2][4];
+          uint32_t kaw[2][4], qaw[2][4];
           float pa0 = 0.f, pa1 = 0.f, pb0 = 0.f, pb1 = 0.f;
-          float pk0 = 0.f, pk1 = 0.f, pq0 = 0.f, pq1 = 0.f;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int j = jh * 8 + u;
@@ -599,19 +605,11 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
               kaw[1][u >> 1] = pack_bf16x2(pa1, kr1);
               qaw[0][u >> 1] = pack_bf16x2(pb0, qr0);
               qaw[1][u >> 1] = pack_bf16x2(pb1, qr1);
-              kgw[0][u >> 1] = pack_bf16x2(pk0, kr0 * E0);
-              kgw[1][u >> 1] = pack_bf16x2(pk1, kr1 * E1);
-              qgw[0][u >> 1] = pack_bf16x2(pq0, qr0 * qs0);
-              qgw[1][u >> 1] = pack_bf16x2(pq1, qr1 * qs1);
             } else {
               pa0 = kr0;
               pa1 = kr1;
               pb0 = qr0;
               pb1 = qr1;
-              pk0 = kr0 * E0;
-              pk1 = kr1 * E1;
-              pq0 = qr0 * qs0;
-              pq1 = qr1 * qs1;
             }
           }
           const uint32_t cj = sc * 2 + jh;
@@ -623,10 +621,15 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
                      c ? kaw[1][2] : kaw[0][2], c ? kaw[1][3] : kaw[0][3]);
             st_chunk(sm, OFF_AM + 16384 + sw128_off(row, cj), c ? qaw[1][0] : qaw[0][0],
                      c ? qaw[1][1] : qaw[0][1], c ? qaw[1][2] : qaw[0][2], c ? qaw[1][3] : qaw[0][3]);
-            st_chunk(sm, OFF_KG + sw128_off(row, cj), c ? kgw[1][0] : kgw[0][0], c ? kgw[1][1] : kgw[0][1],
-                     c ? kgw[1][2] : kgw[0][2], c ? kgw[1][3] : kgw[0][3]);
-            st_chunk(sm, OFF_QG + sw128_off(row, cj), c ? qgw[1][0] : qgw[0][0], c ? qgw[1][1] : qgw[0][1],
-                     c ? qgw[1][2] : qgw[0][2], c ? qgw[1][3] : qgw[0][3]);
+            // KG = (k rho) E and QG = (q rho) scale E as packed products of the pairs above
+            const uint32_t eg = c ? pack_bf16x2(E1, E1) : pack_bf16x2(E0, E0);
+            st_chunk(sm, OFF_KG + sw128_off(row, cj), bmul2(c ? kaw[1][0] : kaw[0][0], eg),
+                     bmul2(c ? kaw[1][1] : kaw[0][1], eg), bmul2(c ? kaw[1][2] : kaw[0][2], eg),
+                     bmul2(c ? kaw[1][3] : kaw[0][3], eg));
+            const uint32_t eq = c ? pack_bf16x2(qs1, qs1) : pack_bf16x2(qs0, qs0);
+            st_chunk(sm, OFF_QG + sw128_off(row, cj), bmul2(c ? qaw[1][0] : qaw[0][0], eq),
+                     bmul2(c ? qaw[1][1] : qaw[0][1], eq), bmul2(c ? qaw[1][2] : qaw[0][2], eq),
+                     bmul2(c ? qaw[1][3] : qaw[0][3], eq));
           }
         }
       }

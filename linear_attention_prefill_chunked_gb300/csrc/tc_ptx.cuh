@@ -232,6 +232,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Lane-wise bf16 product of two bf16 pairs, rounded to nearest even.
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a stack of
 // 128-byte-swizzled atoms (8 rows x 128 B, atoms 1024 B apart).
 __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk) {
