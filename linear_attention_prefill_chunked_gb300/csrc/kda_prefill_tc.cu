@@ -107,10 +107,13 @@ struct ItemInfo {
 
 // Scheduling state of the intra group's thread 0, kept in shared memory so that it
 // holds no registers across the chunk loop.
+struct NextChunk {  // the chunk after chunk gc of this CTA, if known when gc's MMA-AB ran
+  int32_t have, kh, h, t0, cv;
+};
 struct LoaderState {
   int32_t pushed, fetched_done;
-  uint32_t n_qk, n_g, n_v;                // chunks whose loads were issued
-  int32_t have_next, nkh, nh, nt0, ncv;   // the chunk after the current one, if known
+  uint32_t n_qk, n_g, n_v;  // chunks whose loads were issued (q/k and v by either group)
+  NextChunk nx[2];          // by chunk parity
 };
 
 struct Small {
@@ -252,10 +255,13 @@ __device__ __forceinline__ void blk_store(float* M, int r, int c, const float ac
 
 // ======================================================================================
 // Intra group (warps 0-7, 256 threads): S-independent work of each chunk.  Its
-// thread 0 also schedules items and issues every TMA load, at points where the
-// group already knows the target buffer is free.
+// thread 0 also schedules items.  A TMA issue blocks its thread for hundreds of
+// cycles, so each load is issued by a thread with slack at a point where that thread
+// already knows the target buffer is free: the gate by warp 4 while warps 0-1 invert
+// the diagonal blocks, q/k and v of a chunk found by the lookahead by the recurrence
+// group's leader, the rest (a chunk not known one chunk ahead) by thread 0.
 // ======================================================================================
-struct Loader {  // used by thread 0 only
+struct Loader {  // item scheduling by intra thread 0; loads by the threads named at each call
   LoaderState* st;
 
   __device__ void push_one(const TcParams& p, Small* s) {
@@ -275,7 +281,7 @@ struct Loader {  // used by thread 0 only
     tma_load_3d(sm + OFF_QK + 16384, &p.tm_k, &s->bar[B_QK_FULL], 64, kh, t0);
     tma_load_3d(sm + OFF_QK + 8192, &p.tm_q, &s->bar[B_QK_FULL], 0, kh, t0);
     tma_load_3d(sm + OFF_QK + 24576, &p.tm_q, &s->bar[B_QK_FULL], 64, kh, t0);
-    ++st->n_qk;
+    atomicAdd(&st->n_qk, 1u);
   }
   __device__ void load_g(const TcParams& p, uint8_t* sm, Small* s, int h, int t0) {
     mbar_expect_tx(&s->bar[B_G_FULL], p.g_bytes);
@@ -289,7 +295,7 @@ struct Loader {  // used by thread 0 only
     mbar_expect_tx(&s->bar[B_V_FULL], 16384);
     tma_load_3d(sm + OFF_VB + 0, &p.tm_v, &s->bar[B_V_FULL], 0, h, t0);
     tma_load_3d(sm + OFF_VB + 8192, &p.tm_v, &s->bar[B_V_FULL], 64, h, t0);
-    ++st->n_v;
+    atomicAdd(&st->n_v, 1u);
   }
   // Chunk after (item k, local chunk lc), if already known without blocking.  Ring
   // slots k and k+1 cannot be refilled before this thread starts item k+2.
@@ -403,10 +409,12 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       if (named_bar_any(BAR_IG, kIG, aborted(s))) { stop = true; break; }
       const int64_t t0 = info.bos + (int64_t)lc * kC;
       const int cv = (int)min((int64_t)kC, info.eos - t0);
-      if (t == 0) {  // loads of this chunk not issued ahead (first chunk, or no lookahead)
-        const LoaderState* L = ld.st;
-        if (L->n_qk == gc) ld.load_qk(p, sm, s, kh, (int)t0);
-        if (L->n_g == gc) ld.load_g(p, sm, s, h, (int)t0);
+      // q/k and v of this chunk were issued by the recurrence group iff the previous
+      // chunk's lookahead found it; otherwise thread 0 issues them here and after MMA-AB
+      const bool ahead = gc > 0 && ld.st->nx[(gc - 1) & 1].have;
+      if (t == 0) {
+        if (!ahead) ld.load_qk(p, sm, s, kh, (int)t0);
+        if (ld.st->n_g == gc) ld.load_g(p, sm, s, h, (int)t0);
       }
       __syncwarp();
       // ------------------------------------------------------------- prologue
@@ -650,22 +658,18 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         mma_commit(&s->bar[B_AB_DONE]);
       } else if (t == 32) {
         // meanwhile, on another warp: the chunk after this one, and its q/k/v into L2
-        // (read by thread 0 only after a later barrier)
-        LoaderState* L = ld.st;
-        int nkh = 0, nh = 0, nt0 = 0, ncv = 0;
-        const bool hn = ld.next_chunk(s, k, lc, nkh, nh, nt0, ncv);
-        L->have_next = hn;
-        L->nkh = nkh;
-        L->nh = nh;
-        L->nt0 = nt0;
-        L->ncv = ncv;
-        if (hn) ld.prefetch_l2(p, nkh, nh, nt0);
+        // (read by the A group after a later barrier, by the recurrence group after
+        // REC_READY of this chunk and before its W_FREE)
+        NextChunk nx{};
+        nx.have = ld.next_chunk(s, k, lc, nx.kh, nx.h, nx.t0, nx.cv);
+        ld.st->nx[gc & 1] = nx;
+        if (nx.have) ld.prefetch_l2(p, nx.kh, nx.h, nx.t0);
       }
       __syncwarp();
       // ------------------------------------------------------------- A / B rows
       wait_bar(p, s, B_AB_DONE, gc & 1);
       tc_fence_after();
-      if (t == 0 && ld.st->n_v == gc) ld.load_v(p, sm, s, h, (int)t0);  // VB free since MMA-U(c-1)
+      if (t == 0 && !ahead) ld.load_v(p, sm, s, h, (int)t0);  // VB free since MMA-U(c-1)
       __syncwarp();
       uint32_t any_unsafe = 0;
 #pragma unroll
@@ -790,6 +794,12 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // (one column per lane, two blocks per warp), then the two 32x32 diagonal halves
       // and the lower-left 32x32 block from the 16x16 blocks (tf32 warp MMAs).
       if (agrp) {
+        // gate of the next chunk into CB 1-2 (free since MMA-AB) by warp 4, idle during the
+        // diagonal blocks; the lookahead of thread 32 is ordered by the A-group barrier
+        if (t == 128) {
+          const NextChunk& nx = ld.st->nx[gc & 1];
+          if (nx.have && ld.st->n_g == gc + 1) ld.load_g(p, sm, s, nx.h, nx.t0);
+        }
         if (warp < 2) {
           // lane = column j of diagonal block o (two blocks per warp).  Its 8x8 diagonal
           // sub-blocks are inverted by forward substitution side by side (columns 0-7
@@ -838,9 +848,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           }
         }
         named_bar(BAR_A, 128);
-        // gate of the next chunk into CB 1-2 (free since MMA-AB; the lookahead written by
-        // thread 32 before AB_DONE is ordered by the barriers since)
-        if (t == 0 && ld.st->have_next && ld.st->n_g == gc + 1) ld.load_g(p, sm, s, ld.st->nh, ld.st->nt0);
         // 32x32 halves: X_{a+1,a} = -X_{a+1,a+1} (A_{a+1,a} X_aa) for a = 0, 2 (P staged
         // in the unused upper block (a, a+1) of A) ...
         const int aw = (warp >> 2) * 2 + (warp & 1);  // 0..3 within the A group
@@ -926,33 +933,24 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       }
       fence_async_smem();
       named_bar(BAR_IG, kIG);
-      if (t < kC && ld.st->have_next) {
-        if (t < ld.st->ncv) bt_next = p.beta[(size_t)(ld.st->nt0 + t) * p.Hv + ld.st->nh];
+      if (t < kC && ld.st->nx[gc & 1].have) {
+        const NextChunk& nx = ld.st->nx[gc & 1];
+        if (t < nx.cv) bt_next = p.beta[(size_t)(nx.t0 + t) * p.Hv + nx.h];
         bt_ok = true;
       }
-      // q/k of the next chunk into the buffer the inverse scratch used; then hand the
-      // chunk to the recurrence group (it issues MMA-U/W and reads -W out itself)
-      if (t == 0) {
-        if (ld.st->have_next && ld.st->n_qk == gc + 1) ld.load_qk(p, sm, s, ld.st->nkh, ld.st->nt0);
-        mbar_arrive(&s->bar[B_REC_READY]);
-      }
+      // hand the chunk to the recurrence group: it issues MMA-U/W, reads -W out itself
+      // and loads q/k of the next chunk into the buffer the inverse scratch used
+      if (t == 0) mbar_arrive(&s->bar[B_REC_READY]);
       __syncwarp();
     }
     if (stop) break;
   }
-  // drain: this group's MMAs and the loads it issued, before the CTA releases TMEM
+  // drain: this group's MMAs, before the CTA releases TMEM (loads drain at the end)
   named_bar(BAR_IG, kIG);
   if (warp == 0) {
     if (lane == 0) mma_commit(&s->bar[B_DRAIN_IG]);
     __syncwarp();
     wait_bar(p, s, B_DRAIN_IG, 0);
-    if (lane == 0) {
-      const LoaderState* L = ld.st;
-      if (L->n_qk > 0) mbar_wait(&s->bar[B_QK_FULL], (L->n_qk - 1) & 1);
-      if (L->n_g > 0) mbar_wait(&s->bar[B_G_FULL], (L->n_g - 1) & 1);
-      if (L->n_v > 0) mbar_wait(&s->bar[B_V_FULL], (L->n_v - 1) & 1);
-    }
-    __syncwarp();
   }
 }
 
@@ -968,6 +966,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   const bool leader_warp = (warp == kIG / 32);
   const uint32_t taddr_q = tbase + ((uint32_t)(quad * 32) << 16);
   const uint32_t sbase = smem_u32(sm);
+  Loader ld{&s->ld};
   uint32_t gc = 0;
 
   for (int k = 0;; ++k) {
@@ -1019,6 +1018,12 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       // prologue soonest), then U~^T = V^T Tm^T and W^T = KG^T Tm^T; -W^T rows -> WB
       if (leader_warp) {
         wait_bar(p, s, B_REC_READY, gc & 1);
+        // q/k of the next chunk, if the lookahead found it (QK buffer free since Tm)
+        if (lane == 0) {
+          const NextChunk& nx = s->ld.nx[gc & 1];
+          if (nx.have) ld.load_qk(p, sm, s, nx.kh, nx.t0);
+        }
+        __syncwarp();
         wait_bar(p, s, B_V_FULL, gc & 1);
         if (lane == 0) {
           tc_fence_after();
@@ -1053,6 +1058,10 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(-wv[2 * u], -wv[2 * u + 1]);
         st_chunk(sm, OFF_WB + sw128_off(v, cq * 2), w[0], w[1], w[2], w[3]);
         st_chunk(sm, OFF_WB + sw128_off(v, cq * 2 + 1), w[4], w[5], w[6], w[7]);
+      }
+      if (rt == 0) {  // v of the next chunk (VB free since MMA-U); read before W_FREE
+        const NextChunk& nx = s->ld.nx[gc & 1];
+        if (nx.have) ld.load_v(p, sm, s, nx.h, nx.t0);
       }
       tc_fence_before();
       fence_async_smem();
@@ -1207,6 +1216,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) {  // loads still in flight (issued ahead of a chunk never run)
+    const LoaderState* L = &s->ld;
+    if (L->n_qk > 0) mbar_wait(&s->bar[B_QK_FULL], (L->n_qk - 1) & 1);
+    if (L->n_g > 0) mbar_wait(&s->bar[B_G_FULL], (L->n_g - 1) & 1);
+    if (L->n_v > 0) mbar_wait(&s->bar[B_V_FULL], (L->n_v - 1) & 1);
+  }
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
