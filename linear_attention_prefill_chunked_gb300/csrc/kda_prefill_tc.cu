@@ -75,11 +75,13 @@ constexpr uint32_t OFF_KR = 163840;   // [128 ch][64 tokens]  KR              (K
 constexpr uint32_t OFF_AM = 180224;   // [k | q][128 ch][128 B]  k rho, q rho (MN-major A)
 constexpr uint32_t OFF_UT = 212992;   // [128 v][64 tokens]   U^T bf16        (K-major A)
 constexpr uint32_t OFF_SMALL = 229376;
-// After MMA-AB completes, the q/k buffer holds the fp32 scratch of the inverse
-// (A and B rows, then X = (I + A)^-1) until Tm is written, and CB blocks 1-2 hold
-// the TMA-staged gate g of the next chunk ([64][128] fp32) until its prologue.
-constexpr uint32_t OFF_AS = OFF_QK;
-constexpr uint32_t OFF_XS = OFF_QK + 16384;
+// After MMA-AB completes, the AM buffer holds the fp32 scratch of the inverse (A and B
+// rows, then X = (I + A)^-1) until Tm is written, the q/k buffer q and k of the next
+// chunk, and CB blocks 1-2 the TMA-staged gate of the next chunk, turned into e = exp(g)
+// ([64][128] fp32) in place when it is given as fp32 g.  Otherwise the prologue writes
+// e into the AM buffer.
+constexpr uint32_t OFF_AS = OFF_AM;
+constexpr uint32_t OFF_XS = OFF_AM + 16384;
 constexpr uint32_t OFF_G = OFF_CB + 16384;
 
 // ---- TMEM columns ------------------------------------------------------------------
@@ -91,7 +93,7 @@ constexpr uint32_t TM_AB = 320;  // A/B result (192), later W^T (64)
 
 constexpr int kIG = 256;  // intra-group threads (warps 0-7)
 constexpr int kRG = 128;  // recurrence-group threads (warps 8-11)
-constexpr uint32_t BAR_IG = 1, BAR_RG = 2, BAR_A = 3;
+constexpr uint32_t BAR_IG = 1, BAR_RG = 2, BAR_A = 3, BAR_B = 4;
 
 enum Bar {
   B_QK_FULL, B_V_FULL, B_G_FULL, B_AB_DONE, B_UW_DONE, B_GAMMA0, B_GAMMA1, B_REC_READY,
@@ -105,8 +107,8 @@ struct ItemInfo {
   int32_t done, pad;
 };
 
-// Scheduling state of the intra group's thread 0, kept in shared memory so that it
-// holds no registers across the chunk loop.
+// Scheduling and load state of the threads that claim items and issue loads, kept in
+// shared memory so that it holds no registers across the chunk loop.
 struct NextChunk {  // the chunk after chunk gc of this CTA, if known when gc's MMA-AB ran
   int32_t have, kh, h, t0, cv;
 };
@@ -121,7 +123,8 @@ struct Small {
   ItemInfo ring[kRing];
   alignas(16) float beta[kC];      // read as float4
   alignas(16) float gamma[2][kK];  // read as float4
-  uint32_t unsafe[4][2][2];  // [sub-chunk][half][parity]: bit l = channel 64*half + 2l + parity
+  // [chunk parity][sub-chunk][half][parity]: bit l = channel 64*half + 2l + parity
+  uint32_t unsafe[2][4][2][2];
   LoaderState ld;
   uint32_t tmem_base;
   uint32_t abort;
@@ -255,13 +258,14 @@ __device__ __forceinline__ void blk_store(float* M, int r, int c, const float ac
 
 // ======================================================================================
 // Intra group (warps 0-7, 256 threads): S-independent work of each chunk.  Its
-// thread 0 also schedules items.  A TMA issue blocks its thread for hundreds of
-// cycles, so each load is issued by a thread with slack at a point where that thread
-// already knows the target buffer is free: the gate by warp 4 while warps 0-1 invert
-// the diagonal blocks, q/k and v of a chunk found by the lookahead by the recurrence
-// group's leader, the rest (a chunk not known one chunk ahead) by thread 0.
+// thread 0 claims the first item (the recurrence group each later one).  A TMA issue
+// blocks its thread for hundreds of cycles, so each load is issued by a thread with
+// slack at a point where that thread already knows the target buffer is free: for a
+// chunk found by the lookahead, q/k by warp 4 while MMA-AB of the chunk before runs,
+// the gate by warp 4 while warps 0-1 invert its diagonal blocks, v by the recurrence
+// group's leader; for a chunk not known one chunk ahead, by thread 0.
 // ======================================================================================
-struct Loader {  // item scheduling by intra thread 0; loads by the threads named at each call
+struct Loader {  // item claims and loads, by the threads named at each call
   LoaderState* st;
 
   __device__ void push_one(const TcParams& p, Small* s) {
@@ -289,7 +293,7 @@ struct Loader {  // item scheduling by intra thread 0; loads by the threads name
       tma_load_2d(sm + OFF_G, &p.tm_g, &s->bar[B_G_FULL], h & ~(p.gw - 1), t0);
     else
       tma_load_3d(sm + OFF_G, &p.tm_g, &s->bar[B_G_FULL], 0, h, t0);
-    ++st->n_g;
+    atomicAdd(&st->n_g, 1u);
   }
   __device__ void load_v(const TcParams& p, uint8_t* sm, Small* s, int h, int t0) {
     mbar_expect_tx(&s->bar[B_V_FULL], 16384);
@@ -297,16 +301,17 @@ struct Loader {  // item scheduling by intra thread 0; loads by the threads name
     tma_load_3d(sm + OFF_VB + 8192, &p.tm_v, &s->bar[B_V_FULL], 64, h, t0);
     atomicAdd(&st->n_v, 1u);
   }
-  // Chunk after (item k, local chunk lc), if already known without blocking.  Ring
-  // slots k and k+1 cannot be refilled before this thread starts item k+2.
-  __device__ bool next_chunk(const Small* s, int k, int lc, int& kh, int& h, int& t0, int& cv) const {
+  // Chunk after (item k, local chunk lc), if already known without blocking: item k+1
+  // counts once its ring entry is complete (its ITEM_FULL phase, which also orders the
+  // entry's contents).  Ring slots k and k+1 cannot be refilled during item k.
+  __device__ bool next_chunk(Small* s, int k, int lc, int& kh, int& h, int& t0, int& cv) const {
     const ItemInfo& cur = s->ring[k % kRing];
     if (lc + 1 < cur.nchunks) {
       kh = cur.kh; h = cur.h; t0 = (int)(cur.bos + (int64_t)(lc + 1) * kC);
       cv = (int)min((int64_t)kC, cur.eos - t0);
       return true;
     }
-    if (st->pushed > k + 1) {
+    if (mbar_try_wait(&s->bar[B_ITEM_FULL + (k + 1) % kRing], ((k + 1) / kRing) & 1)) {
       const ItemInfo& nx = s->ring[(k + 1) % kRing];
       if (!nx.done && nx.nchunks > 0) {
         kh = nx.kh; h = nx.h; t0 = (int)nx.bos;
@@ -316,11 +321,8 @@ struct Loader {  // item scheduling by intra thread 0; loads by the threads name
     }
     return false;
   }
-  __device__ void prefetch_l2(const TcParams& p, int kh, int h, int t0) {
-    tma_prefetch_3d(&p.tm_k, 0, kh, t0);
-    tma_prefetch_3d(&p.tm_k, 64, kh, t0);
-    tma_prefetch_3d(&p.tm_q, 0, kh, t0);
-    tma_prefetch_3d(&p.tm_q, 64, kh, t0);
+  __device__ void prefetch_l2(const TcParams& p, int h, int t0) {  // gate and v
+    if (p.gate_k > 1) tma_prefetch_3d(&p.tm_g, 0, h, t0);
     tma_prefetch_3d(&p.tm_v, 0, h, t0);
     tma_prefetch_3d(&p.tm_v, 64, h, t0);
   }
@@ -331,17 +333,17 @@ struct Loader {  // item scheduling by intra thread 0; loads by the threads name
 // lane L (row L & 63 of A for L < 64, of B otherwise).  Kept out of line: it never
 // runs at ordinary gates and would otherwise raise the register pressure of the
 // chunk loop.
-__device__ __noinline__ void unsafe_diag_terms(const TcParams& p, const Small* s, float* As, float* Xs,
-                                               const float* inv_nrm, int L, int64_t t0, int cv,
-                                               int kh, int h) {
+__device__ __noinline__ void unsafe_diag_terms(const TcParams& p, const uint32_t (*uns)[2][2], float* As,
+                                               float* Xs, const float* inv_nrm, int L, int64_t t0,
+                                               int cv, int kh, int h) {
   const int r = L & 63, a = r >> 4;
   const bool isB = L >= 64;
-  const uint32_t anya = s->unsafe[a][0][0] | s->unsafe[a][0][1] | s->unsafe[a][1][0] | s->unsafe[a][1][1];
+  const uint32_t anya = uns[a][0][0] | uns[a][0][1] | uns[a][1][0] | uns[a][1][1];
   if (anya != 0u && r < cv) {
     float* row = isB ? Xs : As;
     const __nv_bfloat16* xsrc = isB ? p.q : p.k;
     for (int wd = 0; wd < 4; ++wd) {
-      uint32_t m = s->unsafe[a][wd >> 1][wd & 1];
+      uint32_t m = uns[a][wd >> 1][wd & 1];
       while (m) {
         const int c = 64 * (wd >> 1) + 2 * (__ffs(m) - 1) + (wd & 1);
         m &= m - 1;
@@ -370,6 +372,78 @@ __device__ __noinline__ void unsafe_diag_terms(const TcParams& p, const Small* s
   }
 }
 
+// exp(x) as one ex2 on the multi-function unit, results below 2^-126 flushed to zero:
+// an e that low puts its channel's sub-chunk product below 2^-100, so the channel takes
+// the pairwise path, and products formed from it differ from exact by under 2^-126.
+__device__ __forceinline__ float exp_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));  // log2(e)
+  return y;
+}
+
+// e = exp(g) of one chunk as fp32 [64 tokens][128 channels] at offset eoff (rows >= cv:
+// 1; in place over a staged fp32 g, each element read and written by the same thread),
+// the sub-chunk products pi into CB block 0 ([4][128] fp32) and the masks of "unsafe"
+// channels (pi below 2^-100, or not finite) into `uns`, from the staged gate of head h
+// (col: its column in a staged scalar-gate group).  Run by nw warps (4 or 8; wg = index
+// among them): warp wg covers channels 64 (wg & 1) .. 64 (wg & 1) + 63 of sub-chunks
+// wg / 2 + i nw / 2, so its reads and writes are full rows.
+__device__ __forceinline__ void gate_exp(uint8_t* sm, uint32_t eoff, uint32_t (*uns)[2][2], GateAct act,
+                                         int gate_k, int col, int h, int cv, int wg, int nw, int lane) {
+  const int half = wg & 1, c0 = 2 * (half * 32 + lane);
+  float* Es = reinterpret_cast<float*>(sm + eoff);
+  float* pis = reinterpret_cast<float*>(sm + OFF_CB);
+  const float* Gs = reinterpret_cast<const float*>(sm + OFF_G);
+  const bool has_act = act.a != nullptr;
+  // gate activation constants of head h for this lane's channel pair
+  float gA = 0.f, gdb0 = 0.f, gdb1 = 0.f;
+  if (has_act) {
+    gA = __expf(act.A_log[h]);
+    if (act.dt_bias) {
+      gdb0 = act.dt_bias[(size_t)h * gate_k + (gate_k > 1 ? c0 : 0)];
+      gdb1 = act.dt_bias[(size_t)h * gate_k + (gate_k > 1 ? c0 + 1 : 0)];
+    }
+  }
+  for (int sc = wg >> 1; sc < 4; sc += nw >> 1) {
+    float pm0 = 1.f, pm1 = 1.f;
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+      const int r = sc * 16 + j;
+      float g0, g1;
+      if (gate_k == 1) {  // scalar gate: staged [64 tokens][gw heads], one value per token
+        if (has_act) {
+          const float x = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(sm + OFF_G)[r * 8 + col]) + gdb0;
+          g0 = fmaxf(-gA * (fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)))), act.lb);
+        } else {
+          g0 = Gs[r * 4 + col];
+        }
+        g1 = g0;
+      } else if (!has_act) {
+        const float2 gv = *reinterpret_cast<const float2*>(Gs + r * kK + c0);
+        g0 = gv.x;
+        g1 = gv.y;
+      } else {  // staged tile is a ([64][128] bf16): g = max(-A softplus(a + dt_bias), lb)
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(sm + OFF_G + r * 256 + c0 * 2);
+        const float x0 = bf_bits(w & 0xFFFFu) + gdb0, x1 = bf_bits(w >> 16) + gdb1;
+        g0 = fmaxf(-gA * (fmaxf(x0, 0.f) + __logf(1.f + __expf(-fabsf(x0)))), act.lb);
+        g1 = fmaxf(-gA * (fmaxf(x1, 0.f) + __logf(1.f + __expf(-fabsf(x1)))), act.lb);
+      }
+      const float e0 = (r < cv) ? exp_ftz(g0) : 1.f;  // padded rows: decay 1
+      const float e1 = (r < cv) ? exp_ftz(g1) : 1.f;
+      *reinterpret_cast<float2*>(Es + r * kK + c0) = make_float2(e0, e1);
+      pm0 *= e0;
+      pm1 *= e1;
+    }
+    *reinterpret_cast<float2*>(pis + sc * kK + c0) = make_float2(pm0, pm1);
+    const uint32_t m0 = __ballot_sync(0xffffffffu, !(pm0 >= kSafeMin));
+    const uint32_t m1 = __ballot_sync(0xffffffffu, !(pm1 >= kSafeMin));
+    if (lane == 0) {
+      uns[sc][half][0] = m0;
+      uns[sc][half][1] = m1;
+    }
+  }
+}
+
 __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tbase) {
   const int t = threadIdx.x;  // 0..255
   const int warp = t >> 5, lane = t & 31;
@@ -379,39 +453,30 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
   const uint32_t sbase = smem_u32(sm);
   float* As = reinterpret_cast<float*>(sm + OFF_AS);
   float* Xs = reinterpret_cast<float*>(sm + OFF_XS);
-  const float* Gs = reinterpret_cast<const float*>(sm + OFF_G);
   Loader ld{&s->ld};
   uint32_t gc = 0;
   float bt_next = 0.f;  // beta of the next chunk, read one chunk ahead (threads 0-63)
   bool bt_ok = false;
 
+  // item 0; each later item is claimed by the recurrence group near the end of the one
+  // before it
+  if (t == 0) ld.push_one(p, s);
+  __syncwarp();
   for (int k = 0;; ++k) {
-    if (t == 0) {
-      while (ld.st->pushed <= k + 1 && !ld.st->fetched_done) ld.push_one(p, s);
-    }
-    __syncwarp();
     const ItemInfo info = next_item(p, s, k, t == 0, BAR_IG, kIG);
     if (info.done) break;
     const int h = info.h, kh = info.kh;
-    // gate activation constants of this head for this thread's channel pair
-    float gA = 0.f, gdb0 = 0.f, gdb1 = 0.f;
-    if (p.act.a) {
-      const int cg = 2 * ((warp & 1) * 32 + lane);
-      gA = __expf(p.act.A_log[h]);
-      if (p.act.dt_bias) {
-        const int gk = p.gate_k;
-        gdb0 = p.act.dt_bias[(size_t)h * gk + (gk > 1 ? cg : 0)];
-        gdb1 = p.act.dt_bias[(size_t)h * gk + (gk > 1 ? cg + 1 : 0)];
-      }
-    }
     bool stop = false;
     for (int lc = 0; lc < info.nchunks; ++lc, ++gc) {
       if (named_bar_any(BAR_IG, kIG, aborted(s))) { stop = true; break; }
       const int64_t t0 = info.bos + (int64_t)lc * kC;
       const int cv = (int)min((int64_t)kC, info.eos - t0);
-      // q/k and v of this chunk were issued by the recurrence group iff the previous
-      // chunk's lookahead found it; otherwise thread 0 issues them here and after MMA-AB
+      // q/k, v and the gate of this chunk were issued during the previous chunk iff its
+      // lookahead found this one; a given fp32 gate was turned into e in place by the B
+      // group during the previous chunk of the same item.  Otherwise thread 0 issues the
+      // loads here (v after MMA-AB) and the group computes e into the AM buffer here.
       const bool ahead = gc > 0 && ld.st->nx[(gc - 1) & 1].have;
+      const bool e_ahead = lc > 0 && p.gate_k > 1 && !p.act.a;
       if (t == 0) {
         if (!ahead) ld.load_qk(p, sm, s, kh, (int)t0);
         if (ld.st->n_g == gc) ld.load_g(p, sm, s, h, (int)t0);
@@ -427,57 +492,9 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       float bt = 0.f;  // beta of token t, needed only after the prologue
       if (t < kC && t < cv) bt = bt_ok ? bt_next : p.beta[(size_t)(t0 + t) * p.Hv + h];
       bt_ok = false;
-      wait_bar(p, s, B_G_FULL, gc & 1);
-      float e0[16], e1[16];
-      if (p.gate_k == 1) {  // scalar gate: staged [64 tokens][gw heads], one value per token
-        const int col = h & (p.gw - 1);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = sc * 16 + j;
-          float gv;
-          if (p.act.a) {
-            const float x = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(sm + OFF_G)[r * 8 + col]) + gdb0;
-            gv = fmaxf(-gA * (fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)))), p.act.lb);
-          } else {
-            gv = Gs[r * 4 + col];
-          }
-          e0[j] = e1[j] = (r < cv) ? __expf(gv) : 1.f;
-        }
-      } else if (!p.act.a) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = sc * 16 + j;
-          const float2 gv = *reinterpret_cast<const float2*>(Gs + r * kK + c0);
-          e0[j] = (r < cv) ? __expf(gv.x) : 1.f;  // padded rows: decay 1
-          e1[j] = (r < cv) ? __expf(gv.y) : 1.f;
-        }
-      } else {  // staged tile is a ([64][128] bf16): g = max(-A softplus(a + dt_bias), lb)
-        const uint8_t* Ga = sm + OFF_G;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = sc * 16 + j;
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(Ga + r * 256 + c0 * 2);
-          const float x0 = bf_bits(w & 0xFFFFu) + gdb0, x1 = bf_bits(w >> 16) + gdb1;
-          const float g0 = fmaxf(-gA * (fmaxf(x0, 0.f) + __logf(1.f + __expf(-fabsf(x0)))), p.act.lb);
-          const float g1 = fmaxf(-gA * (fmaxf(x1, 0.f) + __logf(1.f + __expf(-fabsf(x1)))), p.act.lb);
-          e0[j] = (r < cv) ? __expf(g0) : 1.f;
-          e1[j] = (r < cv) ? __expf(g1) : 1.f;
-        }
-      }
-      float pm0 = 1.f, pm1 = 1.f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) { pm0 *= e0[j]; pm1 *= e1[j]; }
-      // exchange the sub-chunk products through CB block 0 (its last readers, MMA-AB and
-      // the KR pass of the previous chunk, are done; pass A rewrites it after a barrier)
-      float* pis = reinterpret_cast<float*>(sm + OFF_CB);
-      *reinterpret_cast<float2*>(pis + sc * kK + c0) = make_float2(pm0, pm1);
-      {  // "unsafe" channels of this sub-chunk (product below 2^-100 or not finite)
-        const uint32_t m0 = __ballot_sync(0xffffffffu, !(pm0 >= kSafeMin));
-        const uint32_t m1 = __ballot_sync(0xffffffffu, !(pm1 >= kSafeMin));
-        if (lane == 0) {
-          s->unsafe[sc][warp & 1][0] = m0;
-          s->unsafe[sc][warp & 1][1] = m1;
-        }
+      if (!e_ahead) {
+        wait_bar(p, s, B_G_FULL, gc & 1);
+        gate_exp(sm, OFF_AM, s->unsafe[gc & 1], p.act, p.gate_k, h & (p.gw - 1), h, cv, warp, 8, lane);
       }
       wait_bar(p, s, B_QK_FULL, gc & 1);
       if (p.l2norm) {
@@ -514,7 +531,18 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       }
       // QG buffer and this gamma buffer are free once MMA-1b of the previous chunk ran
       if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
-      named_bar(BAR_IG, kIG);  // products visible; every thread has read g (CB 1-2 free)
+      named_bar(BAR_IG, kIG);  // e and the products visible
+      float e0[16], e1[16];
+      {
+        const float* Es = reinterpret_cast<const float*>(sm + (e_ahead ? OFF_G : OFF_AM));
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 ev = *reinterpret_cast<const float2*>(Es + (sc * 16 + j) * kK + c0);
+          e0[j] = ev.x;
+          e1[j] = ev.y;
+        }
+      }
+      const float* pis = reinterpret_cast<const float*>(sm + OFF_CB);
       float pi0[4], pi1[4];
 #pragma unroll
       for (int q2 = 0; q2 < 4; ++q2) {
@@ -522,7 +550,11 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         pi0[q2] = pv.x;
         pi1[q2] = pv.y;
       }
-      named_bar(BAR_IG, kIG);  // every warp holds its products before pass A writes CB block 0
+      // pi of this thread's own sub-chunk
+      const float pm0 = sc == 0 ? pi0[0] : sc == 1 ? pi0[1] : sc == 2 ? pi0[2] : pi0[3];
+      const float pm1 = sc == 0 ? pi1[0] : sc == 1 ? pi1[1] : sc == 2 ? pi1[2] : pi1[3];
+      // every warp holds e and the products before pass A/B overwrite CB and AM
+      named_bar(BAR_IG, kIG);
       const float E0 = (sc > 0 ? pi0[0] : 1.f) * (sc > 1 ? pi0[1] : 1.f) * (sc > 2 ? pi0[2] : 1.f);
       const float E1 = (sc > 0 ? pi1[0] : 1.f) * (sc > 1 ? pi1[1] : 1.f) * (sc > 2 ? pi1[2] : 1.f);
       if (sc == 3)  // warps 6-7 (fewest block-1 variants): gamma of their 64 channels
@@ -656,25 +688,57 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           mma_bf16(tbase + TM_AB, a, b, idesc, st > 0 ? 1u : 0u);
         }
         mma_commit(&s->bar[B_AB_DONE]);
-      } else if (t == 32) {
-        // meanwhile, on another warp: the chunk after this one, and its q/k/v into L2
-        // (read by the A group after a later barrier, by the recurrence group after
-        // REC_READY of this chunk and before its W_FREE)
+      } else if (t == 128) {
+        // meanwhile, on warp 4: the chunk after this one (read by the A group after a
+        // later barrier, by the whole group after the one before Tm, by the recurrence
+        // group after REC_READY and before W_FREE); its q/k, and its gate and v into L2
         NextChunk nx{};
         nx.have = ld.next_chunk(s, k, lc, nx.kh, nx.h, nx.t0, nx.cv);
         ld.st->nx[gc & 1] = nx;
-        if (nx.have) ld.prefetch_l2(p, nx.kh, nx.h, nx.t0);
+        if (nx.have) {
+          ld.load_qk(p, sm, s, nx.kh, nx.t0);  // q/k buffer free since pass B
+          ld.prefetch_l2(p, nx.h, nx.t0);
+        }
       }
       __syncwarp();
+      if (quad >= 2) {
+        // KR = (k kap) F_s for sub-chunks sc-1 and sc of this thread's channel pair
+        // (F_s = product of pi after s), by the B group while the tensor core runs MMA-AB
+        if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+          const int sk = sc - 1 + s2;
+          const float fs0 = (sk < 1 ? pi0[1] : 1.f) * (sk < 2 ? pi0[2] : 1.f) * (sk < 3 ? pi0[3] : 1.f);
+          const float fs1 = (sk < 1 ? pi1[1] : 1.f) * (sk < 2 ? pi1[2] : 1.f) * (sk < 3 ? pi1[3] : 1.f);
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int c = c2 ^ wsel;
+            const float f = c ? fs1 : fs0;
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const int j = sk * 2 + jj;
+              const uint4 src = *reinterpret_cast<const uint4*>(sm + OFF_CB + sw128_off(c0 + c, j));
+              const uint32_t in[4] = {src.x, src.y, src.z, src.w};
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                w[u] = pack_bf16x2(bf_bits(in[u] & 0xFFFFu) * f, bf_bits(in[u] >> 16) * f);
+              st_chunk(sm, OFF_KR + sw128_off(c0 + c, j), w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
       // ------------------------------------------------------------- A / B rows
       wait_bar(p, s, B_AB_DONE, gc & 1);
       tc_fence_after();
       if (t == 0 && !ahead) ld.load_v(p, sm, s, h, (int)t0);  // VB free since MMA-U(c-1)
+
       __syncwarp();
       uint32_t any_unsafe = 0;
 #pragma unroll
       for (int q2 = 0; q2 < 4; ++q2)
-        any_unsafe |= s->unsafe[q2][0][0] | s->unsafe[q2][0][1] | s->unsafe[q2][1][0] | s->unsafe[q2][1][1];
+        any_unsafe |= s->unsafe[gc & 1][q2][0][0] | s->unsafe[gc & 1][q2][0][1] | s->unsafe[gc & 1][q2][1][0] |
+                      s->unsafe[gc & 1][q2][1][1];
       {
         const int r = L & 63, a = r >> 4;
         const bool isB = L >= 64;
@@ -752,8 +816,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         named_bar(BAR_IG, kIG);
         // exact pairwise terms of the diagonal sub-chunk blocks on "unsafe" channels
         if (hx == 0)
-          unsafe_diag_terms(p, s, As, Xs, reinterpret_cast<const float*>(sm + OFF_TM + 2048), L,
-                            t0, cv, kh, h);
+          unsafe_diag_terms(p, s->unsafe[gc & 1], As, Xs, reinterpret_cast<const float*>(sm + OFF_TM + 2048),
+                            L, t0, cv, kh, h);
         named_bar(BAR_IG, kIG);
         // A: mask + beta_r (in place, fp32); B: mask + scale -> bf16 -> BB
         {
@@ -795,10 +859,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // and the lower-left 32x32 block from the 16x16 blocks (tf32 warp MMAs).
       if (agrp) {
         // gate of the next chunk into CB 1-2 (free since MMA-AB) by warp 4, idle during the
-        // diagonal blocks; the lookahead of thread 32 is ordered by the A-group barrier
-        if (t == 128) {
+        // diagonal blocks
+        if (t == 128 && ld.st->nx[gc & 1].have) {
           const NextChunk& nx = ld.st->nx[gc & 1];
-          if (nx.have && ld.st->n_g == gc + 1) ld.load_g(p, sm, s, nx.h, nx.t0);
+          ld.load_g(p, sm, s, nx.h, nx.t0);
         }
         if (warp < 2) {
           // lane = column j of diagonal block o (two blocks per warp).  Its 8x8 diagonal
@@ -882,30 +946,15 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           blk_store(Xs, ib * 16, jb * 16, acc, -1.f, lane);
         }
       } else {
-        // KR = (k kap) F_s for sub-chunks sc-1 and sc of this thread's channel pair
-        // (F_s = product of pi after s); CB block 0 is intact until the next prologue
-        if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
-#pragma unroll
-        for (int s2 = 0; s2 < 2; ++s2) {
-          const int sk = sc - 1 + s2;
-          const float fs0 = (sk < 1 ? pi0[1] : 1.f) * (sk < 2 ? pi0[2] : 1.f) * (sk < 3 ? pi0[3] : 1.f);
-          const float fs1 = (sk < 1 ? pi1[1] : 1.f) * (sk < 2 ? pi1[2] : 1.f) * (sk < 3 ? pi1[3] : 1.f);
-#pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            const int c = c2 ^ wsel;
-            const float f = c ? fs1 : fs0;
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-              const int j = sk * 2 + jj;
-              const uint4 src = *reinterpret_cast<const uint4*>(sm + OFF_CB + sw128_off(c0 + c, j));
-              const uint32_t in[4] = {src.x, src.y, src.z, src.w};
-              uint32_t w[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                w[u] = pack_bf16x2(bf_bits(in[u] & 0xFFFFu) * f, bf_bits(in[u] >> 16) * f);
-              st_chunk(sm, OFF_KR + sw128_off(c0 + c, j), w[0], w[1], w[2], w[3]);
-            }
-          }
+        // while the A group inverts: e, products and masks of the next chunk of this item
+        // (whose gate warp 4 loads: the lookahead within an item always succeeds).  CB
+        // block 0 is free once every B-group thread is past KR (the barrier).
+        named_bar(BAR_B, 128);
+        if (lc + 1 < info.nchunks && p.gate_k > 1 && !p.act.a) {
+          const int ncv = (int)min((int64_t)kC, info.eos - (t0 + kC));
+          wait_bar(p, s, B_G_FULL, (gc + 1) & 1);
+          gate_exp(sm, OFF_G, s->unsafe[(gc + 1) & 1], p.act, p.gate_k, 0, h, ncv, (warp >> 2) * 2 + (warp & 1),
+                   4, lane);
         }
       }
       named_bar(BAR_IG, kIG);
@@ -984,6 +1033,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       if (p.state_out) dst = static_cast<ST*>(p.state_out) + ((size_t)info.n * p.Hv) * kK * kV + hoff;
     }
     if (info.nchunks == 0) {  // empty sequence: the final state is the initial one
+      if (rt == 32) ld.push_one(p, s);  // claim of the next item (see the chunk loop)
       if (dst && dst != src)
         for (int c = 0; c < kK; ++c) dst[(size_t)c * kV + v] = src ? src[(size_t)c * kV + v] : ST(0.f);
       continue;
@@ -1014,16 +1064,14 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       const int64_t t0 = info.bos + (int64_t)lc * kC;
       const int cv = (int)min((int64_t)kC, info.eos - t0);
       const bool last = (lc + 1 == info.nchunks);
+      // claim the next item late, about two chunks before this one ends, so that a CTA
+      // takes new work only when it is about to run out (dynamic longest-first
+      // scheduling); the claim's global round trips overlap this group's slack
+      if (rt == 32 && lc == (info.nchunks > 3 ? info.nchunks - 3 : 0)) ld.push_one(p, s);
       // ---- R0 (leader warp): O = S QG^T first (frees QG and gamma for the next chunk's
       // prologue soonest), then U~^T = V^T Tm^T and W^T = KG^T Tm^T; -W^T rows -> WB
       if (leader_warp) {
         wait_bar(p, s, B_REC_READY, gc & 1);
-        // q/k of the next chunk, if the lookahead found it (QK buffer free since Tm)
-        if (lane == 0) {
-          const NextChunk& nx = s->ld.nx[gc & 1];
-          if (nx.have) ld.load_qk(p, sm, s, nx.kh, nx.t0);
-        }
-        __syncwarp();
         wait_bar(p, s, B_V_FULL, gc & 1);
         if (lane == 0) {
           tc_fence_after();
