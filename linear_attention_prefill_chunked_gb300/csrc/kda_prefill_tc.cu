@@ -1239,8 +1239,10 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
 template <typename ST>
 __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, formed as an offset into the shared array (not through an
+  // integer round trip) so that the compiler keeps every derived pointer in the shared
+  // window and emits shared loads and stores rather than generic ones
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Small* s = reinterpret_cast<Small*>(sm + OFF_SMALL);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
