@@ -78,8 +78,8 @@ constexpr uint32_t OFF_SMALL = 229376;
 // After MMA-AB completes, the AM buffer holds the fp32 scratch of the inverse (A and B
 // rows, then X = (I + A)^-1) until Tm is written, the q/k buffer q and k of the next
 // chunk, and CB blocks 1-2 the TMA-staged gate of the next chunk, turned into e = exp(g)
-// ([64][128] fp32) in place when it is given as fp32 g.  Otherwise the prologue writes
-// e into the AM buffer.
+// ([64][128] fp32) in place when it is given as fp32 g (otherwise each prologue thread
+// forms its e in registers).
 constexpr uint32_t OFF_AS = OFF_AM;
 constexpr uint32_t OFF_XS = OFF_AM + 16384;
 constexpr uint32_t OFF_G = OFF_CB + 16384;
@@ -381,56 +381,28 @@ __device__ __forceinline__ float exp_ftz(float x) {
   return y;
 }
 
-// e = exp(g) of one chunk as fp32 [64 tokens][128 channels] at offset eoff (rows >= cv:
-// 1; in place over a staged fp32 g, each element read and written by the same thread),
-// the sub-chunk products pi into CB block 0 ([4][128] fp32) and the masks of "unsafe"
-// channels (pi below 2^-100, or not finite) into `uns`, from the staged gate of head h
-// (col: its column in a staged scalar-gate group).  Run by nw warps (4 or 8; wg = index
+// e = exp(g) of one chunk in place over its staged fp32 gate g ([64 tokens][128
+// channels]; each element read and written by the same thread; rows >= cv: 1), the
+// sub-chunk products pi into CB block 0 ([4][128] fp32) and the masks of "unsafe"
+// channels (pi below 2^-100, or not finite) into `uns`.  Run by nw warps (wg = index
 // among them): warp wg covers channels 64 (wg & 1) .. 64 (wg & 1) + 63 of sub-chunks
-// wg / 2 + i nw / 2, so its reads and writes are full rows.
-__device__ __forceinline__ void gate_exp(uint8_t* sm, uint32_t eoff, uint32_t (*uns)[2][2], GateAct act,
-                                         int gate_k, int col, int h, int cv, int wg, int nw, int lane) {
+// wg / 2 + i nw / 2, so its reads and writes are full rows.  The products are taken
+// token by token in order, as the prologue forms them.
+__device__ __forceinline__ void gate_exp_inplace(uint8_t* sm, uint32_t (*uns)[2][2], int cv, int wg, int nw,
+                                                 int lane) {
   const int half = wg & 1, c0 = 2 * (half * 32 + lane);
-  float* Es = reinterpret_cast<float*>(sm + eoff);
+  float* Es = reinterpret_cast<float*>(sm + OFF_G);
   float* pis = reinterpret_cast<float*>(sm + OFF_CB);
-  const float* Gs = reinterpret_cast<const float*>(sm + OFF_G);
-  const bool has_act = act.a != nullptr;
-  // gate activation constants of head h for this lane's channel pair
-  float gA = 0.f, gdb0 = 0.f, gdb1 = 0.f;
-  if (has_act) {
-    gA = __expf(act.A_log[h]);
-    if (act.dt_bias) {
-      gdb0 = act.dt_bias[(size_t)h * gate_k + (gate_k > 1 ? c0 : 0)];
-      gdb1 = act.dt_bias[(size_t)h * gate_k + (gate_k > 1 ? c0 + 1 : 0)];
-    }
-  }
   for (int sc = wg >> 1; sc < 4; sc += nw >> 1) {
     float pm0 = 1.f, pm1 = 1.f;
 #pragma unroll 4
     for (int j = 0; j < 16; ++j) {
       const int r = sc * 16 + j;
-      float g0, g1;
-      if (gate_k == 1) {  // scalar gate: staged [64 tokens][gw heads], one value per token
-        if (has_act) {
-          const float x = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(sm + OFF_G)[r * 8 + col]) + gdb0;
-          g0 = fmaxf(-gA * (fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)))), act.lb);
-        } else {
-          g0 = Gs[r * 4 + col];
-        }
-        g1 = g0;
-      } else if (!has_act) {
-        const float2 gv = *reinterpret_cast<const float2*>(Gs + r * kK + c0);
-        g0 = gv.x;
-        g1 = gv.y;
-      } else {  // staged tile is a ([64][128] bf16): g = max(-A softplus(a + dt_bias), lb)
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(sm + OFF_G + r * 256 + c0 * 2);
-        const float x0 = bf_bits(w & 0xFFFFu) + gdb0, x1 = bf_bits(w >> 16) + gdb1;
-        g0 = fmaxf(-gA * (fmaxf(x0, 0.f) + __logf(1.f + __expf(-fabsf(x0)))), act.lb);
-        g1 = fmaxf(-gA * (fmaxf(x1, 0.f) + __logf(1.f + __expf(-fabsf(x1)))), act.lb);
-      }
-      const float e0 = (r < cv) ? exp_ftz(g0) : 1.f;  // padded rows: decay 1
-      const float e1 = (r < cv) ? exp_ftz(g1) : 1.f;
-      *reinterpret_cast<float2*>(Es + r * kK + c0) = make_float2(e0, e1);
+      float2* ep = reinterpret_cast<float2*>(Es + r * kK + c0);
+      const float2 gv = *ep;
+      const float e0 = (r < cv) ? exp_ftz(gv.x) : 1.f;  // padded rows: decay 1
+      const float e1 = (r < cv) ? exp_ftz(gv.y) : 1.f;
+      *ep = make_float2(e0, e1);
       pm0 *= e0;
       pm1 *= e1;
     }
@@ -474,7 +446,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // q/k, v and the gate of this chunk were issued during the previous chunk iff its
       // lookahead found this one; a given fp32 gate was turned into e in place by the B
       // group during the previous chunk of the same item.  Otherwise thread 0 issues the
-      // loads here (v after MMA-AB) and the group computes e into the AM buffer here.
+      // loads here (v after MMA-AB) and each thread computes its e here.
       const bool ahead = gc > 0 && ld.st->nx[(gc - 1) & 1].have;
       const bool e_ahead = lc > 0 && p.gate_k > 1 && !p.act.a;
       if (t == 0) {
@@ -492,9 +464,66 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       float bt = 0.f;  // beta of token t, needed only after the prologue
       if (t < kC && t < cv) bt = bt_ok ? bt_next : p.beta[(size_t)(t0 + t) * p.Hv + h];
       bt_ok = false;
-      if (!e_ahead) {
+      float e0[16], e1[16];
+      if (!e_ahead) {  // e of this chunk from the staged gate, into registers
         wait_bar(p, s, B_G_FULL, gc & 1);
-        gate_exp(sm, OFF_AM, s->unsafe[gc & 1], p.act, p.gate_k, h & (p.gw - 1), h, cv, warp, 8, lane);
+        const float* Gs = reinterpret_cast<const float*>(sm + OFF_G);
+        float gA = 0.f, gdb0 = 0.f, gdb1 = 0.f;  // activation constants of head h, channels c0, c0+1
+        if (p.act.a) {
+          gA = __expf(p.act.A_log[h]);
+          if (p.act.dt_bias) {
+            const int gk = p.gate_k;
+            gdb0 = p.act.dt_bias[(size_t)h * gk + (gk > 1 ? c0 : 0)];
+            gdb1 = p.act.dt_bias[(size_t)h * gk + (gk > 1 ? c0 + 1 : 0)];
+          }
+        }
+        const int col = h & (p.gw - 1);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = sc * 16 + j;
+          float g0, g1;
+          if (p.gate_k == 1) {  // scalar gate: staged [64 tokens][gw heads], one value per token
+            if (p.act.a) {
+              const float x = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(sm + OFF_G)[r * 8 + col]) + gdb0;
+              g0 = fmaxf(-gA * (fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)))), p.act.lb);
+            } else {
+              g0 = Gs[r * 4 + col];
+            }
+            g1 = g0;
+          } else if (!p.act.a) {
+            const float2 gv = *reinterpret_cast<const float2*>(Gs + r * kK + c0);
+            g0 = gv.x;
+            g1 = gv.y;
+          } else {  // staged tile is a ([64][128] bf16): g = max(-A softplus(a + dt_bias), lb)
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(sm + OFF_G + r * 256 + c0 * 2);
+            const float x0 = bf_bits(w & 0xFFFFu) + gdb0, x1 = bf_bits(w >> 16) + gdb1;
+            g0 = fmaxf(-gA * (fmaxf(x0, 0.f) + __logf(1.f + __expf(-fabsf(x0)))), p.act.lb);
+            g1 = fmaxf(-gA * (fmaxf(x1, 0.f) + __logf(1.f + __expf(-fabsf(x1)))), p.act.lb);
+          }
+          e0[j] = (r < cv) ? exp_ftz(g0) : 1.f;  // padded rows: decay 1
+          e1[j] = (r < cv) ? exp_ftz(g1) : 1.f;
+        }
+        float pm0 = 1.f, pm1 = 1.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          pm0 *= e0[j];
+          pm1 *= e1[j];
+        }
+        *reinterpret_cast<float2*>(reinterpret_cast<float*>(sm + OFF_CB) + sc * kK + c0) = make_float2(pm0, pm1);
+        const uint32_t m0 = __ballot_sync(0xffffffffu, !(pm0 >= kSafeMin));
+        const uint32_t m1 = __ballot_sync(0xffffffffu, !(pm1 >= kSafeMin));
+        if (lane == 0) {
+          s->unsafe[gc & 1][sc][warp & 1][0] = m0;
+          s->unsafe[gc & 1][sc][warp & 1][1] = m1;
+        }
+      } else {  // turned into e in place by the B group during the previous chunk
+        const float* Es = reinterpret_cast<const float*>(sm + OFF_G);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 ev = *reinterpret_cast<const float2*>(Es + (sc * 16 + j) * kK + c0);
+          e0[j] = ev.x;
+          e1[j] = ev.y;
+        }
       }
       wait_bar(p, s, B_QK_FULL, gc & 1);
       if (p.l2norm) {
@@ -531,17 +560,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       }
       // QG buffer and this gamma buffer are free once MMA-1b of the previous chunk ran
       if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
-      named_bar(BAR_IG, kIG);  // e and the products visible
-      float e0[16], e1[16];
-      {
-        const float* Es = reinterpret_cast<const float*>(sm + (e_ahead ? OFF_G : OFF_AM));
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float2 ev = *reinterpret_cast<const float2*>(Es + (sc * 16 + j) * kK + c0);
-          e0[j] = ev.x;
-          e1[j] = ev.y;
-        }
-      }
+      named_bar(BAR_IG, kIG);  // the products visible
       const float* pis = reinterpret_cast<const float*>(sm + OFF_CB);
       float pi0[4], pi1[4];
 #pragma unroll
@@ -953,42 +972,17 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         if (lc + 1 < info.nchunks && p.gate_k > 1 && !p.act.a) {
           const int ncv = (int)min((int64_t)kC, info.eos - (t0 + kC));
           wait_bar(p, s, B_G_FULL, (gc + 1) & 1);
-          gate_exp(sm, OFF_G, s->unsafe[(gc + 1) & 1], p.act, p.gate_k, 0, h, ncv, (warp >> 2) * 2 + (warp & 1),
-                   4, lane);
+          gate_exp_inplace(sm, s->unsafe[(gc + 1) & 1], ncv, (warp >> 2) * 2 + (warp & 1), 4, lane);
         }
       }
-      named_bar(BAR_IG, kIG);
-      // Tm = X Diag(beta) -> bf16 -> TM   (thread: row r = t & 63, columns 16*qq..16*qq+15)
-      {
-        const int r = t & 63, qq = t >> 6;
-#pragma unroll
-        for (int u2 = 0; u2 < 2; ++u2) {
-          const int j = qq * 2 + u2;
-          const float4 xa = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8));
-          const float4 xb = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8 + 4));
-          const float4 ba = *reinterpret_cast<const float4*>(&s->beta[j * 8]);
-          const float4 bb4 = *reinterpret_cast<const float4*>(&s->beta[j * 8 + 4]);
-          const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-          const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb4.x, bb4.y, bb4.z, bb4.w};
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i0 = j * 8 + u * 2;
-            w[u] = pack_bf16x2((i0 <= r) ? xv[2 * u] * bv[2 * u] : 0.f,
-                               (i0 + 1 <= r) ? xv[2 * u + 1] * bv[2 * u + 1] : 0.f);
-          }
-          st_chunk(sm, OFF_TM + sw128_off(r, j), w[0], w[1], w[2], w[3]);
-        }
-      }
-      fence_async_smem();
       named_bar(BAR_IG, kIG);
       if (t < kC && ld.st->nx[gc & 1].have) {
         const NextChunk& nx = ld.st->nx[gc & 1];
         if (t < nx.cv) bt_next = p.beta[(size_t)(nx.t0 + t) * p.Hv + nx.h];
         bt_ok = true;
       }
-      // hand the chunk to the recurrence group: it issues MMA-U/W, reads -W out itself
-      // and loads q/k of the next chunk into the buffer the inverse scratch used
+      // hand the chunk to the recurrence group: it forms Tm from X, issues MMA-U/W and
+      // reads -W out itself
       if (t == 0) mbar_arrive(&s->bar[B_REC_READY]);
       __syncwarp();
     }
@@ -1068,11 +1062,11 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       // takes new work only when it is about to run out (dynamic longest-first
       // scheduling); the claim's global round trips overlap this group's slack
       if (rt == 32 && lc == (info.nchunks > 3 ? info.nchunks - 3 : 0)) ld.push_one(p, s);
-      // ---- R0 (leader warp): O = S QG^T first (frees QG and gamma for the next chunk's
-      // prologue soonest), then U~^T = V^T Tm^T and W^T = KG^T Tm^T; -W^T rows -> WB
+      // ---- R0: O = S QG^T first (leader; frees QG and gamma for the next chunk's prologue
+      // soonest), Tm = X Diag(beta) -> bf16 (all), then U~^T = V^T Tm^T and
+      // W^T = KG^T Tm^T (leader); -W^T rows -> WB
+      wait_bar(p, s, B_REC_READY, gc & 1);
       if (leader_warp) {
-        wait_bar(p, s, B_REC_READY, gc & 1);
-        wait_bar(p, s, B_V_FULL, gc & 1);
         if (lane == 0) {
           tc_fence_after();
           const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
@@ -1081,6 +1075,38 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
             mma_bf16_ta(tbase + TM_O, tbase + TM_SB + st * 8,
                         sdesc_sw128(sbase + OFF_QG + st * 2048, 16384, 1024), id1, st > 0 ? 1u : 0u);
           mma_commit(&s->bar[B_M1B]);
+        }
+        __syncwarp();
+      }
+      {  // Tm (thread: row r = rt & 63, columns 32 (rt >> 6) .. +31), zero above the diagonal;
+         // X (AM buffer) and beta stay until the intra group's next pass B, after UW_DONE
+        const float* Xs = reinterpret_cast<const float*>(sm + OFF_XS);
+        const int r = rt & 63, qh = rt >> 6;
+#pragma unroll 1
+        for (int u2 = 0; u2 < 4; ++u2) {
+          const int j = qh * 4 + u2;
+          const float4 xa = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8));
+          const float4 xb = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8 + 4));
+          const float4 ba = *reinterpret_cast<const float4*>(&s->beta[j * 8]);
+          const float4 bb4 = *reinterpret_cast<const float4*>(&s->beta[j * 8 + 4]);
+          const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+          const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb4.x, bb4.y, bb4.z, bb4.w};
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i0 = j * 8 + u * 2;
+            w[u] = pack_bf16x2((i0 <= r) ? xv[2 * u] * bv[2 * u] : 0.f,
+                               (i0 + 1 <= r) ? xv[2 * u + 1] * bv[2 * u + 1] : 0.f);
+          }
+          st_chunk(sm, OFF_TM + sw128_off(r, j), w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_async_smem();
+      named_bar(BAR_RG, kRG);
+      if (leader_warp) {
+        wait_bar(p, s, B_V_FULL, gc & 1);
+        if (lane == 0) {
+          tc_fence_after();
           const uint32_t idu = idesc_bf16(128, 64, 1, 0), idw = idesc_bf16(128, 64, 0, 0);
 #pragma unroll 1
           for (int st = 0; st < 4; ++st) {
