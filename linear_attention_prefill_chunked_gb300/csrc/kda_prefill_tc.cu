@@ -16,13 +16,13 @@
 //
 //   A[r,i] = beta_r sum_c k_r k_i prod_{j=i+1..r} e_j    (i < r)
 //   B[r,i] = scale  sum_c q_r k_i prod_{j=i+1..r} e_j    (i <= r)
-//   computed by ONE MMA  [k rho; q rho] (128 x 128) x CB^T (128 x 192) where
+//   computed by ONE MMA  [k rho; q rho] (128 x 128) x CB^T (128 x 176) where
 //   CB holds the column tokens pre-scaled for each sub-chunk reference:
 //     block 0: k kap                  (adjacent sub-chunk pairs)
-//     block 1: k kap pi_1, k kap pi_1 pi_2, k kap pi_2, 0   (distance 2 and 3)
-//     block 2: k kap / pi_s = k / rho (diagonal sub-chunks) on channels whose
+//     block 1: k kap / pi_s = k / rho (diagonal sub-chunks) on channels whose
 //              sub-chunk product pi_s >= 2^-100; the remaining ("unsafe")
 //              channels get their diagonal terms from an exact pairwise loop.
+//     block 2: k kap pi_1, k kap pi_1 pi_2, k kap pi_2   (distance 2 and 3)
 //   Tm = (I + A)^-1 Diag(beta): 16x16 diagonal blocks by fp32 forward
 //   substitution, off-diagonal blocks by block forward substitution with tf32
 //   warp MMAs (tiny, latency-bound 16x16 products)
@@ -33,10 +33,10 @@
 //     S^T = S^T Diag(gamma) + U^T KR   (KR = k kap F, gamma = prod e)
 //
 // CTA = 12 warps, one CTA per SM, persistent over (sequence, head) items sorted
-// longest first and fetched from a global counter:
-//   warps 0-7   intra group (S-independent work of chunk c+1); its thread 0 also
-//               fetches items and issues the TMA loads of q, k, v and g
-//   warps 8-11  recurrence group (state update and output of chunk c)
+// longest first and claimed from a global counter near the end of the item before:
+//   warps 0-7   intra group (S-independent work of chunk c+1; the B-group warps
+//               2, 3, 6, 7 also turn the gate of chunk c+2 into e)
+//   warps 8-11  recurrence group (Tm, state update and output of chunk c)
 // Pool I/O (sglang PR 30169 digest, 实现拆解 items 1-3) is fused: the
 // recurrence group reads h0 from pool[state_indices[n]] (-1 -> last slot) and
 // writes the final state back to the same row.
@@ -576,15 +576,17 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       named_bar(BAR_IG, kIG);
       const float E0 = (sc > 0 ? pi0[0] : 1.f) * (sc > 1 ? pi0[1] : 1.f) * (sc > 2 ? pi0[2] : 1.f);
       const float E1 = (sc > 0 ? pi1[0] : 1.f) * (sc > 1 ? pi1[1] : 1.f) * (sc > 2 ? pi1[2] : 1.f);
-      if (sc == 3)  // warps 6-7 (fewest block-1 variants): gamma of their 64 channels
+      if (sc == 3)  // warps 6-7 (no block-2 references): gamma of their 64 channels
         *reinterpret_cast<float2*>(&s->gamma[gc & 1][c0]) =
             make_float2(pi0[0] * pi0[1] * pi0[2] * pi0[3], pi1[0] * pi1[1] * pi1[2] * pi1[3]);
       {
         const float ip0 = (pm0 >= kSafeMin) ? __fdividef(1.f, pm0) : 0.f;  // pm = pi of this sub-chunk
         const float ip1 = (pm1 >= kSafeMin) ? __fdividef(1.f, pm1) : 0.f;
         // pass A, tokens in descending order: kap (exclusive product to the sub-chunk
-        // end) needs no array.  Writes CB block 0 (k kap), block 2 (k/rho on safe
-        // channels) and, by sub-chunk, the block-1 reference variants.
+        // end) needs no array.  Writes CB block 0 (k kap), block 1 (k/rho on safe channels:
+        // the diagonal sub-chunk blocks) and, by sub-chunk, the block-2 references of the
+        // blocks two and three sub-chunks below the diagonal: sub-chunk 0 -> k kap pi_1
+        // (chunk jh) and k kap pi_1 pi_2 (chunk 2+jh), sub-chunk 1 -> k kap pi_2 (chunk 4+jh).
         float ka0 = 1.f, ka1 = 1.f;
 #pragma unroll
         for (int jh = 1; jh >= 0; --jh) {
@@ -599,37 +601,37 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             ka1 *= e1[j];
           }
           const uint32_t cj = sc * 2 + jh;
-          // block-1 variants by sub-chunk: 0 -> k kap pi_1 (chunk jh) and k kap pi_1 pi_2
-          // (chunk 2+jh); 1 -> k kap pi_2 (chunk 4+jh); 3 -> zeros (chunk 6+jh); 2 -> none
-          const int nvar = (sc == 0) ? 2 : (sc == 2 ? 0 : 1);
-#pragma unroll 1
+          // both channels' 8 tokens as bf16 pairs: k kap, and k kap / pi rounded once from
+          // fp32 (a second rounding on the diagonal blocks shows in the output); the
+          // references scale the k kap pairs with one packed bf16 product each
+          uint32_t xa[2][4], xd[2][4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            xa[0][u] = pack_bf16x2(kk[0][2 * u], kk[0][2 * u + 1]);
+            xa[1][u] = pack_bf16x2(kk[1][2 * u], kk[1][2 * u + 1]);
+            xd[0][u] = pack_bf16x2(kk[0][2 * u] * ip0, kk[0][2 * u + 1] * ip0);
+            xd[1][u] = pack_bf16x2(kk[1][2 * u] * ip1, kk[1][2 * u + 1] * ip1);
+          }
+#pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
             const int c = c2 ^ wsel;
             const int row = c0 + c;
-            const float ip = c ? ip1 : ip0;
-            // k kap of this channel's 8 tokens as bf16 pairs.  The block-1 variants scale the
-            // pairs with one packed bf16 product each; block 2 (the diagonal sub-chunk
-            // blocks, where a second rounding shows in the output) rounds its fp32 product once.
-            uint32_t x2[4];
+            uint32_t w[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              x2[u] = c ? pack_bf16x2(kk[1][2 * u], kk[1][2 * u + 1]) : pack_bf16x2(kk[0][2 * u], kk[0][2 * u + 1]);
-            st_chunk(sm, OFF_CB + sw128_off(row, cj), x2[0], x2[1], x2[2], x2[3]);
-            {
-              float x[8];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) x[u] = (c ? kk[1][u] : kk[0][u]) * ip;
-              st_chunk(sm, OFF_CB + 32768 + sw128_off(row, cj), pack_bf16x2(x[0], x[1]),
-                       pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
-            }
-            const float p1 = c ? pi1[1] : pi0[1], p2 = c ? pi1[2] : pi0[2];
-#pragma unroll 1
-            for (int e = 0; e < nvar; ++e) {
-              const float f = (sc == 0) ? (e ? p1 * p2 : p1) : (sc == 1 ? p2 : 0.f);
-              const int ch = (sc == 0) ? 2 * e + jh : (sc == 1 ? 4 + jh : 6 + jh);
-              const uint32_t ff = pack_bf16x2(f, f);
-              st_chunk(sm, OFF_CB + 16384 + sw128_off(row, ch), bmul2(x2[0], ff), bmul2(x2[1], ff),
-                       bmul2(x2[2], ff), bmul2(x2[3], ff));
+            for (int u = 0; u < 4; ++u) w[u] = c ? xa[1][u] : xa[0][u];
+            st_chunk(sm, OFF_CB + sw128_off(row, cj), w[0], w[1], w[2], w[3]);
+            st_chunk(sm, OFF_CB + 16384 + sw128_off(row, cj), c ? xd[1][0] : xd[0][0], c ? xd[1][1] : xd[0][1],
+                     c ? xd[1][2] : xd[0][2], c ? xd[1][3] : xd[0][3]);
+            if (sc < 2) {
+              const float p1 = c ? pi1[1] : pi0[1], p2 = c ? pi1[2] : pi0[2];
+              const uint32_t ff = (sc == 0) ? pack_bf16x2(p1, p1) : pack_bf16x2(p2, p2);
+              st_chunk(sm, OFF_CB + 32768 + sw128_off(row, (sc == 0 ? 0 : 4) + jh), bmul2(w[0], ff),
+                       bmul2(w[1], ff), bmul2(w[2], ff), bmul2(w[3], ff));
+              if (sc == 0) {
+                const uint32_t f2 = pack_bf16x2(p1 * p2, p1 * p2);
+                st_chunk(sm, OFF_CB + 32768 + sw128_off(row, 2 + jh), bmul2(w[0], f2), bmul2(w[1], f2),
+                         bmul2(w[2], f2), bmul2(w[3], f2));
+              }
             }
           }
         }
@@ -699,7 +701,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         mbar_arrive(&s->bar[B_GAMMA0 + (gc & 1)]);
         if (gc > 0) wait_bar(p, s, B_W_FREE, (gc - 1) & 1);  // W of the last chunk read out
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16(128, 192, 1, 1);
+        const uint32_t idesc = idesc_bf16(128, 176, 1, 1);  // the last 16 CB columns are unused
 #pragma unroll 1
         for (int st = 0; st < 8; ++st) {
           const uint64_t a = sdesc_sw128(sbase + OFF_AM + st * 2048, 16384, 1024);
@@ -767,10 +769,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         for (int bb = 0; bb < 2; ++bb) {
           const int b = hx * 2 + bb;
           auto colof = [](int aa, int b_) -> int {
-            if (b_ == aa) return 128 + 16 * aa;
+            if (b_ == aa) return 64 + 16 * aa;
             if (b_ == aa - 1) return 16 * b_;
-            if (b_ == aa - 2) return aa == 2 ? 64 : 96;
-            if (b_ == aa - 3) return 80;
+            if (b_ == aa - 2) return aa == 2 ? 128 : 160;
+            if (b_ == aa - 3) return 144;
             return -1;
           };
           const int cc0 = (b <= a0) ? colof(a0, b) : -1;
