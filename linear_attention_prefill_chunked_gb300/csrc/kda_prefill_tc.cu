@@ -261,9 +261,9 @@ __device__ __forceinline__ void blk_store(float* M, int r, int c, const float ac
 // thread 0 claims the first item (the recurrence group each later one).  A TMA issue
 // blocks its thread for hundreds of cycles, so each load is issued by a thread with
 // slack at a point where that thread already knows the target buffer is free: for a
-// chunk found by the lookahead, q/k by warp 4 while MMA-AB of the chunk before runs,
-// the gate by warp 4 while warps 0-1 invert its diagonal blocks, v by the recurrence
-// group's leader; for a chunk not known one chunk ahead, by thread 0.
+// chunk found by the lookahead, q/k by warp 4 while MMA-AB of the chunk before runs and
+// the gate by warp 4 while warps 0-1 invert its diagonal blocks; for a chunk not known
+// one chunk ahead, by thread 0; v of every chunk by warp 5 during its own MMA-AB.
 // ======================================================================================
 struct Loader {  // item claims and loads, by the threads named at each call
   LoaderState* st;
@@ -321,10 +321,8 @@ struct Loader {  // item claims and loads, by the threads named at each call
     }
     return false;
   }
-  __device__ void prefetch_l2(const TcParams& p, int h, int t0) {  // gate and v
+  __device__ void prefetch_l2(const TcParams& p, int h, int t0) {  // the gate
     if (p.gate_k > 1) tma_prefetch_3d(&p.tm_g, 0, h, t0);
-    tma_prefetch_3d(&p.tm_v, 0, h, t0);
-    tma_prefetch_3d(&p.tm_v, 64, h, t0);
   }
 };
 
@@ -443,10 +441,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       if (named_bar_any(BAR_IG, kIG, aborted(s))) { stop = true; break; }
       const int64_t t0 = info.bos + (int64_t)lc * kC;
       const int cv = (int)min((int64_t)kC, info.eos - t0);
-      // q/k, v and the gate of this chunk were issued during the previous chunk iff its
+      // q/k and the gate of this chunk were issued during the previous chunk iff its
       // lookahead found this one; a given fp32 gate was turned into e in place by the B
       // group during the previous chunk of the same item.  Otherwise thread 0 issues the
-      // loads here (v after MMA-AB) and each thread computes its e here.
+      // loads here and each thread computes its e here.  (v: during MMA-AB, always.)
       const bool ahead = gc > 0 && ld.st->nx[(gc - 1) & 1].have;
       const bool e_ahead = lc > 0 && p.gate_k > 1 && !p.act.a;
       if (t == 0) {
@@ -712,7 +710,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       } else if (t == 128) {
         // meanwhile, on warp 4: the chunk after this one (read by the A group after a
         // later barrier, by the whole group after the one before Tm, by the recurrence
-        // group after REC_READY and before W_FREE); its q/k, and its gate and v into L2
+        // group after REC_READY); its q/k, and its gate into L2
         NextChunk nx{};
         nx.have = ld.next_chunk(s, k, lc, nx.kh, nx.h, nx.t0, nx.cv);
         ld.st->nx[gc & 1] = nx;
@@ -720,6 +718,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           ld.load_qk(p, sm, s, nx.kh, nx.t0);  // q/k buffer free since pass B
           ld.prefetch_l2(p, nx.h, nx.t0);
         }
+      } else if (t == 160) {
+        // and on warp 5: v of this chunk, for MMA-U of the recurrence group (the v buffer
+        // is free since MMA-U of the previous chunk, which pass B waited for)
+        ld.load_v(p, sm, s, h, (int)t0);
       }
       __syncwarp();
       if (quad >= 2) {
@@ -752,7 +754,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // ------------------------------------------------------------- A / B rows
       wait_bar(p, s, B_AB_DONE, gc & 1);
       tc_fence_after();
-      if (t == 0 && !ahead) ld.load_v(p, sm, s, h, (int)t0);  // VB free since MMA-U(c-1)
 
       __syncwarp();
       uint32_t any_unsafe = 0;
@@ -1134,10 +1135,6 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(-wv[2 * u], -wv[2 * u + 1]);
         st_chunk(sm, OFF_WB + sw128_off(v, cq * 2), w[0], w[1], w[2], w[3]);
         st_chunk(sm, OFF_WB + sw128_off(v, cq * 2 + 1), w[4], w[5], w[6], w[7]);
-      }
-      if (rt == 0) {  // v of the next chunk (VB free since MMA-U); read before W_FREE
-        const NextChunk& nx = s->ld.nx[gc & 1];
-        if (nx.have) ld.load_v(p, sm, s, nx.h, nx.t0);
       }
       tc_fence_before();
       fence_async_smem();
