@@ -979,13 +979,36 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         }
       }
       named_bar(BAR_IG, kIG);
+      // Tm = X Diag(beta) -> bf16 -> TM   (thread: row r = t & 63, columns 16*qq..16*qq+15)
+      {
+        const int r = t & 63, qq = t >> 6;
+#pragma unroll
+        for (int u2 = 0; u2 < 2; ++u2) {
+          const int j = qq * 2 + u2;
+          const float4 xa = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8));
+          const float4 xb = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8 + 4));
+          const float4 ba = *reinterpret_cast<const float4*>(&s->beta[j * 8]);
+          const float4 bb4 = *reinterpret_cast<const float4*>(&s->beta[j * 8 + 4]);
+          const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+          const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb4.x, bb4.y, bb4.z, bb4.w};
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i0 = j * 8 + u * 2;
+            w[u] = pack_bf16x2((i0 <= r) ? xv[2 * u] * bv[2 * u] : 0.f,
+                               (i0 + 1 <= r) ? xv[2 * u + 1] * bv[2 * u + 1] : 0.f);
+          }
+          st_chunk(sm, OFF_TM + sw128_off(r, j), w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_async_smem();
+      named_bar(BAR_IG, kIG);
       if (t < kC && ld.st->nx[gc & 1].have) {
         const NextChunk& nx = ld.st->nx[gc & 1];
         if (t < nx.cv) bt_next = p.beta[(size_t)(nx.t0 + t) * p.Hv + nx.h];
         bt_ok = true;
       }
-      // hand the chunk to the recurrence group: it forms Tm from X, issues MMA-U/W and
-      // reads -W out itself
+      // hand the chunk to the recurrence group: it issues MMA-U/W and reads -W out itself
       if (t == 0) mbar_arrive(&s->bar[B_REC_READY]);
       __syncwarp();
     }
@@ -1065,11 +1088,11 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       // takes new work only when it is about to run out (dynamic longest-first
       // scheduling); the claim's global round trips overlap this group's slack
       if (rt == 32 && lc == (info.nchunks > 3 ? info.nchunks - 3 : 0)) ld.push_one(p, s);
-      // ---- R0: O = S QG^T first (leader; frees QG and gamma for the next chunk's prologue
-      // soonest), Tm = X Diag(beta) -> bf16 (all), then U~^T = V^T Tm^T and
-      // W^T = KG^T Tm^T (leader); -W^T rows -> WB
-      wait_bar(p, s, B_REC_READY, gc & 1);
+      // ---- R0 (leader warp): O = S QG^T first (frees QG and gamma for the next chunk's
+      // prologue soonest), then U~^T = V^T Tm^T and W^T = KG^T Tm^T; -W^T rows -> WB
       if (leader_warp) {
+        wait_bar(p, s, B_REC_READY, gc & 1);
+        wait_bar(p, s, B_V_FULL, gc & 1);
         if (lane == 0) {
           tc_fence_after();
           const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
@@ -1078,38 +1101,6 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
             mma_bf16_ta(tbase + TM_O, tbase + TM_SB + st * 8,
                         sdesc_sw128(sbase + OFF_QG + st * 2048, 16384, 1024), id1, st > 0 ? 1u : 0u);
           mma_commit(&s->bar[B_M1B]);
-        }
-        __syncwarp();
-      }
-      {  // Tm (thread: row r = rt & 63, columns 32 (rt >> 6) .. +31), zero above the diagonal;
-         // X (AM buffer) and beta stay until the intra group's next pass B, after UW_DONE
-        const float* Xs = reinterpret_cast<const float*>(sm + OFF_XS);
-        const int r = rt & 63, qh = rt >> 6;
-#pragma unroll 1
-        for (int u2 = 0; u2 < 4; ++u2) {
-          const int j = qh * 4 + u2;
-          const float4 xa = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8));
-          const float4 xb = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8 + 4));
-          const float4 ba = *reinterpret_cast<const float4*>(&s->beta[j * 8]);
-          const float4 bb4 = *reinterpret_cast<const float4*>(&s->beta[j * 8 + 4]);
-          const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-          const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb4.x, bb4.y, bb4.z, bb4.w};
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i0 = j * 8 + u * 2;
-            w[u] = pack_bf16x2((i0 <= r) ? xv[2 * u] * bv[2 * u] : 0.f,
-                               (i0 + 1 <= r) ? xv[2 * u + 1] * bv[2 * u + 1] : 0.f);
-          }
-          st_chunk(sm, OFF_TM + sw128_off(r, j), w[0], w[1], w[2], w[3]);
-        }
-      }
-      fence_async_smem();
-      named_bar(BAR_RG, kRG);
-      if (leader_warp) {
-        wait_bar(p, s, B_V_FULL, gc & 1);
-        if (lane == 0) {
-          tc_fence_after();
           const uint32_t idu = idesc_bf16(128, 64, 1, 0), idw = idesc_bf16(128, 64, 0, 0);
 #pragma unroll 1
           for (int st = 0; st < 4; ++st) {
