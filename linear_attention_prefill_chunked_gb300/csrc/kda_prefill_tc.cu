@@ -77,9 +77,9 @@ constexpr uint32_t OFF_UT = 212992;   // [128 v][64 tokens]   U^T bf16        (K
 constexpr uint32_t OFF_SMALL = 229376;
 // After MMA-AB completes, the AM buffer holds the fp32 scratch of the inverse (A and B
 // rows, then X = (I + A)^-1) until Tm is written, the q/k buffer q and k of the next
-// chunk, and CB blocks 1-2 the TMA-staged gate of the next chunk, turned into e = exp(g)
-// ([64][128] fp32) in place when it is given as fp32 g (otherwise each prologue thread
-// forms its e in registers).
+// chunk, and CB blocks 1-2 the TMA-staged gate of the next chunk, which the B group turns
+// into e = exp(g) ([64][128] fp32) in the same buffer when that chunk is in the same item
+// (otherwise each prologue thread forms its e in registers).
 constexpr uint32_t OFF_AS = OFF_AM;
 constexpr uint32_t OFF_XS = OFF_AM + 16384;
 constexpr uint32_t OFF_G = OFF_CB + 16384;
@@ -414,6 +414,74 @@ __device__ __forceinline__ void gate_exp_inplace(uint8_t* sm, uint32_t (*uns)[2]
   }
 }
 
+// The same for a staged activated gate (a, bf16 [64][128]) or a staged scalar gate
+// ([64 tokens][gw heads], col = this head's column), by the four B-group warps (wg 0-3,
+// sub-chunks wg / 2 and wg / 2 + 2).  The fp32 e rows overwrite the staged input (e row r
+// covers a rows 2r and 2r+1; the scalar tile lies under the first two), so every thread
+// reads all of its inputs before the group's barrier and writes only after it.
+__device__ __forceinline__ void gate_act_exp_b(const TcParams& p, uint8_t* sm, uint32_t (*uns)[2][2], int h,
+                                               int cv, int wg, int lane) {
+  const int half = wg & 1, c0 = 2 * (half * 32 + lane), sc0 = wg >> 1;
+  const int gk = p.gate_k, col = h & (p.gw - 1);
+  float* Es = reinterpret_cast<float*>(sm + OFF_G);
+  float* pis = reinterpret_cast<float*>(sm + OFF_CB);
+  uint32_t raw[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int r = (sc0 + 2 * (i >> 4)) * 16 + (i & 15);
+    if (gk == 1)
+      raw[i] = p.act.a ? (uint32_t)reinterpret_cast<const uint16_t*>(sm + OFF_G)[r * 8 + col]
+                       : reinterpret_cast<const uint32_t*>(sm + OFF_G)[r * 4 + col];
+    else
+      raw[i] = *reinterpret_cast<const uint32_t*>(sm + OFF_G + r * 256 + c0 * 2);
+  }
+  float gA = 0.f, gdb0 = 0.f, gdb1 = 0.f;  // activation constants of head h, channels c0, c0+1
+  if (p.act.a) {
+    gA = __expf(p.act.A_log[h]);
+    if (p.act.dt_bias) {
+      gdb0 = p.act.dt_bias[(size_t)h * gk + (gk > 1 ? c0 : 0)];
+      gdb1 = p.act.dt_bias[(size_t)h * gk + (gk > 1 ? c0 + 1 : 0)];
+    }
+  }
+  named_bar(BAR_B, 128);
+#pragma unroll
+  for (int i2 = 0; i2 < 2; ++i2) {
+    const int sc = sc0 + 2 * i2;
+    float pm0 = 1.f, pm1 = 1.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int r = sc * 16 + j;
+      const uint32_t w = raw[i2 * 16 + j];
+      float g0, g1;
+      if (gk == 1) {
+        if (p.act.a) {
+          const float x = bf_bits(w) + gdb0;
+          g0 = fmaxf(-gA * (fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)))), p.act.lb);
+        } else {
+          g0 = __uint_as_float(w);
+        }
+        g1 = g0;
+      } else {
+        const float x0 = bf_bits(w & 0xFFFFu) + gdb0, x1 = bf_bits(w >> 16) + gdb1;
+        g0 = fmaxf(-gA * (fmaxf(x0, 0.f) + __logf(1.f + __expf(-fabsf(x0)))), p.act.lb);
+        g1 = fmaxf(-gA * (fmaxf(x1, 0.f) + __logf(1.f + __expf(-fabsf(x1)))), p.act.lb);
+      }
+      const float e0 = (r < cv) ? exp_ftz(g0) : 1.f;  // padded rows: decay 1
+      const float e1 = (r < cv) ? exp_ftz(g1) : 1.f;
+      *reinterpret_cast<float2*>(Es + r * kK + c0) = make_float2(e0, e1);
+      pm0 *= e0;
+      pm1 *= e1;
+    }
+    *reinterpret_cast<float2*>(pis + sc * kK + c0) = make_float2(pm0, pm1);
+    const uint32_t m0 = __ballot_sync(0xffffffffu, !(pm0 >= kSafeMin));
+    const uint32_t m1 = __ballot_sync(0xffffffffu, !(pm1 >= kSafeMin));
+    if (lane == 0) {
+      uns[sc][half][0] = m0;
+      uns[sc][half][1] = m1;
+    }
+  }
+}
+
 __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tbase) {
   const int t = threadIdx.x;  // 0..255
   const int warp = t >> 5, lane = t & 31;
@@ -442,11 +510,11 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       const int64_t t0 = info.bos + (int64_t)lc * kC;
       const int cv = (int)min((int64_t)kC, info.eos - t0);
       // q/k and the gate of this chunk were issued during the previous chunk iff its
-      // lookahead found this one; a given fp32 gate was turned into e in place by the B
-      // group during the previous chunk of the same item.  Otherwise thread 0 issues the
-      // loads here and each thread computes its e here.  (v: during MMA-AB, always.)
+      // lookahead found this one; its gate was turned into e (fp32, in the staging buffer)
+      // by the B group during the previous chunk of the same item.  Otherwise thread 0
+      // issues the loads here and each thread computes its e here.  (v: during MMA-AB.)
       const bool ahead = gc > 0 && ld.st->nx[(gc - 1) & 1].have;
-      const bool e_ahead = lc > 0 && p.gate_k > 1 && !p.act.a;
+      const bool e_ahead = lc > 0;
       if (t == 0) {
         if (!ahead) ld.load_qk(p, sm, s, kh, (int)t0);
         if (ld.st->n_g == gc) ld.load_g(p, sm, s, h, (int)t0);
@@ -972,10 +1040,14 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         // (whose gate warp 4 loads: the lookahead within an item always succeeds).  CB
         // block 0 is free once every B-group thread is past KR (the barrier).
         named_bar(BAR_B, 128);
-        if (lc + 1 < info.nchunks && p.gate_k > 1 && !p.act.a) {
+        if (lc + 1 < info.nchunks) {
           const int ncv = (int)min((int64_t)kC, info.eos - (t0 + kC));
+          const int wgb = (warp >> 2) * 2 + (warp & 1);
           wait_bar(p, s, B_G_FULL, (gc + 1) & 1);
-          gate_exp_inplace(sm, s->unsafe[(gc + 1) & 1], ncv, (warp >> 2) * 2 + (warp & 1), 4, lane);
+          if (p.gate_k > 1 && !p.act.a)
+            gate_exp_inplace(sm, s->unsafe[(gc + 1) & 1], ncv, wgb, 4, lane);
+          else
+            gate_act_exp_b(p, sm, s->unsafe[(gc + 1) & 1], h, ncv, wgb, lane);
         }
       }
       named_bar(BAR_IG, kIG);

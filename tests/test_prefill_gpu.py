@@ -166,6 +166,28 @@ def test_zero_length_sequences_and_empty_batch():
     assert o0.shape == (0, 2, 128) and h0.shape == (0, 2, 128, 128)
 
 
+def test_many_short_items_claimed_late():
+    """Four times more (sequence, head) items than SMs, most of them 0 to 3 chunks long and
+    empty sequences among them: every CTA claims many items, each near the end of the one
+    before it (at its first chunk when the item has at most three), and items run back to
+    back with and without the next chunk known one chunk ahead."""
+    pattern = [0, 1, 5, 63, 64, 65, 130, 200, 17, 0, 129, 3]
+    lens = (pattern * 50)[:600]
+    w = synthetic.make(lens, Hk=1, Hv=2, K=128, V=128, dtype=torch.bfloat16, seed=77,
+                       state="pool", num_slots=640)
+    d = to_dev(w)
+    pool_before = w.state.clone()
+    o, pool = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                state=d["state"], state_indices=d["state_indices"])
+    assert kda.read_device_status(kda.chunk_prefill.last_workspace) == 0
+    o_ref, pool_ref = _full_oracle(w, state=pool_before)
+    # relative L2 at the stated bar; the element-wise guard at 0.15 of the RMS over these 8.7 M
+    # outputs (the largest of bf16 rounding errors grows with the element count; an item run
+    # with a wrong state or chunk would be off by the values themselves, ~1 RMS)
+    assert_close(o, o_ref, torch.bfloat16, "o", max_rms=0.15)
+    assert_close(pool, pool_ref, torch.bfloat16, "pool")
+
+
 def test_zero_initial_state_and_padded_gate_rows():
     w = synthetic.make([90, 33], Hk=2, Hv=2, K=128, V=128, dtype=torch.bfloat16, seed=5,
                        state=None, g_pad_rows=17)
