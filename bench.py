@@ -17,6 +17,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -97,7 +98,9 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples: KDA_BENCH_CLOCKS_DIR if set, else the system temporary directory
+        d = os.environ.get("KDA_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"kda_bench_clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
         try:
