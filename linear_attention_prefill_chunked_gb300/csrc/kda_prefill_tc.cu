@@ -89,7 +89,7 @@ constexpr uint32_t TM_U = 0;     // U~ -> U (64)
 constexpr uint32_t TM_O = 64;    // O^T (64)
 constexpr uint32_t TM_SB = 128;  // S^T as bf16 pairs: A operand of MMA-1 (64)
 constexpr uint32_t TM_S = 192;   // S^T fp32 (128)
-constexpr uint32_t TM_AB = 320;  // A/B result (192), later W^T (64)
+constexpr uint32_t TM_AB = 320;  // A/B result (176 of 192), later W^T (64)
 
 constexpr int kIG = 256;  // intra-group threads (warps 0-7)
 constexpr int kRG = 128;  // recurrence-group threads (warps 8-11)
@@ -114,7 +114,7 @@ struct NextChunk {  // the chunk after chunk gc of this CTA, if known when gc's 
 };
 struct LoaderState {
   int32_t pushed, fetched_done;
-  uint32_t n_qk, n_g, n_v;  // chunks whose loads were issued (q/k and v by either group)
+  uint32_t n_qk, n_g, n_v;  // chunks whose loads were issued (by whichever thread issued them)
   NextChunk nx[2];          // by chunk parity
 };
 
