@@ -154,6 +154,23 @@ def _dist():
     return None, 1, 0, local
 
 
+def max_over_ranks(dist, x):
+    """Largest of the ranks' x (x itself without a process group).  Every rank must call it.
+    NCCL reduces a tensor on the rank's GPU, gloo one in host memory."""
+    if not dist:
+        return x
+    dev = (torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl"
+           else torch.device("cpu"))
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(ws, units_per_rank, ms):
+    """Whole-job throughput: the units all ws replicas processed over the slowest one's time."""
+    return ws * units_per_rank / (ms * 1e-3)
+
+
 def cpu_baseline(w, num_threads=0, heads=SAMPLE_HEADS):
     """Time the fp64 oracle on a bounded sample: all sequences, v-heads 0..heads-1."""
     from oracle import kda_oracle
@@ -188,12 +205,13 @@ def run_reference(args, dist, ws, rank):
             times.append(cb)
     val = statistics.median(t["value"] for t in times)
     ms = w.T / val * 1e3
-    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": 1,
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": w.name, "tokens": w.T, "num_seqs": w.N, "Hk": 32, "Hv": 32,
-                       "K": 128, "V": 128, "parallelism": "host threads over (sequence, head)"},
+                       "K": 128, "V": 128,
+                       "parallelism": "host threads over (sequence, head); rank 0 only"},
             "cpu_baseline": {k: times[-1][k] for k in ("kind", "cores", "sample")} | {"value": val,
                                                                                       "unit": "tokens/s"},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -230,17 +248,17 @@ def run_decode(args, dist, ws, rank, local):
             ev[i][1].record(stream)
         torch.cuda.synchronize()
     per = [a.elapsed_time(b) for a, b in ev]
+    ms = max_over_ranks(dist, statistics.median(per))
     if rank != 0:
         return
     real = int((w.state_indices >= 0).sum())
     Hv, K, V = w.v.shape[1], w.q.shape[2], w.v.shape[2]
     row_bytes = 2 * Hv * K * V * 4 + Hv * (2 * K * 2 + V * 2 + K * 4 + 4 + V * 2)
-    ms = statistics.median(per)
     hbm, _, src = _peaks()
     achieved = real * row_bytes / (ms * 1e-3) / 1e9
     print(json.dumps({
         "metric": "KDA decode rows/s (4096 one-token rows, Hv=32, K=V=128, fp32 pool)",
-        "value": real / (ms * 1e-3), "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+        "value": job_rate(ws, real, ms), "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "real_rows": real, "padding_rows": w.N - real,
@@ -310,11 +328,8 @@ def run_ours(args, dist, ws, rank, local):
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     per = [a.elapsed_time(b) for a, b in ev]  # ms, one launch sequence each
-    total_ms = sum(per)
+    total_ms = max_over_ranks(dist, sum(per))
     if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
         dist.barrier()
     bits = kda.read_device_status(ws_t)
 
@@ -349,13 +364,13 @@ def run_ours(args, dist, ws, rank, local):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / e2e_steps)
 
     if rank != 0:
         return
     hbm, bf16, src = _peaks()
     ms = total_ms / args.steps
-    value = ws * w.T / (ms * 1e-3)
+    value = job_rate(ws, w.T, ms)
     nbytes = algorithmic_bytes(w, act, args.gate == "scalar")
     flops = algorithmic_flops(w)
     kern_ms = statistics.median(per)
@@ -381,7 +396,7 @@ def run_ours(args, dist, ws, rank, local):
                      "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
                      "roofline_time_ms": t_roof * 1e3, "frac_of_roofline_time": t_roof * 1e3 / kern_ms},
         "clocks": clk.summary(),
-        "e2e": {"value": (w.T / (e2e_ms * 1e-3)) if e2e_ms else None, "unit": "tokens/s",
+        "e2e": {"value": job_rate(ws, w.T, e2e_ms) if e2e_ms else None, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "note": f"pinned host q/k/v/{'a' if act else 'g'}/beta/cu_seqlens/indices copied in, "
