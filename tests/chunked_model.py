@@ -142,3 +142,43 @@ def chunked_forward(q, k, v, g, beta, cu, S0, scale, C=64, s=16):
                 S = Qc["gamma"][:, None] * S + Qc["KR"].T @ U
             fin[n, h] = S
     return o, fin
+
+
+def split_state_passing(q, k, v, g, beta, cu, S0, scale, split_chunks, C=64, s=16):
+    """The same prefill with every sequence longer than split_chunks chunks cut at that
+    chunk boundary into two segments that need not run one after the other.
+
+    The update is affine in the state, S_t = M_t S_p + S_t^loc with M_t the product of the
+    per-token maps (I - beta k k^T) Diag(e^g) since the cut, so the second segment runs twice
+    from the cut on, independently of the first: once from a zero state with the real values
+    (o^loc, S^loc), once from the identity with zero values (its outputs are
+    y_t = scale M_t^T q_t, its final state M_end).  The combine, once the first segment has
+    produced S_p, is two products:  o_t = o_t^loc + y_t^T S_p  and  S_end = M_end S_p + S^loc.
+    """
+    T, Hk, K = q.shape
+    Hv, V = v.shape[1:]
+    N = len(cu) - 1
+    o = np.zeros((T, Hv, V))
+    fin = np.zeros((N, Hv, K, V))
+    for n in range(N):
+        a, b = int(cu[n]), int(cu[n + 1])
+        cut = a + split_chunks * C
+        if cut >= b:  # too short to split
+            on, fn = chunked_forward(q[a:b], k[a:b], v[a:b], g[a:b], beta[a:b], [0, b - a],
+                                     S0[n:n + 1], scale, C, s)
+            o[a:b], fin[n] = on, fn[0]
+            continue
+        seg1 = lambda x: x[a:cut]
+        seg2 = lambda x: x[cut:b]
+        o1, Sp = chunked_forward(seg1(q), seg1(k), seg1(v), seg1(g), seg1(beta), [0, cut - a],
+                                 S0[n:n + 1], scale, C, s)
+        o2l, S2l = chunked_forward(seg2(q), seg2(k), seg2(v), seg2(g), seg2(beta), [0, b - cut],
+                                   np.zeros((1, Hv, K, V)), scale, C, s)
+        eye = np.broadcast_to(np.eye(K), (1, Hv, K, K)).copy()
+        y, Mend = chunked_forward(seg2(q), seg2(k), np.zeros((b - cut, Hv, K)), seg2(g),
+                                  seg2(beta), [0, b - cut], eye, scale, C, s)
+        o[a:cut] = o1
+        for h in range(Hv):
+            o[cut:b, h] = o2l[:, h] + y[:, h] @ Sp[0, h]
+            fin[n, h] = Mend[0, h] @ Sp[0, h] + S2l[0, h]
+    return o, fin

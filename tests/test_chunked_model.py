@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 from oracle import kda_oracle
-from tests.chunked_model import chunked_forward, tri_inv_unit_lower_blocked
+from tests.chunked_model import chunked_forward, split_state_passing, tri_inv_unit_lower_blocked
 
 
 def _inputs(rng, lens, Hk, Hv, K, V, gate_scale=None):
@@ -51,3 +51,21 @@ def test_chunked_model_equals_token_recurrence(lens, gate_scale):
     np.testing.assert_allclose(o, o_ref, rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(f, f_ref, rtol=1e-10, atol=1e-12)
     assert np.all(np.isfinite(o))
+
+
+@pytest.mark.parametrize("split_chunks,gate_scale", [(1, None), (2, None), (1, np.log(1000.0))])
+def test_split_state_passing_equals_token_recurrence(split_chunks, gate_scale):
+    """A long sequence cut in two segments that run independently (the second one twice: from
+    zero with the values, from the identity without them) and combined by two products gives
+    the recurrence's outputs and final state: the algebra a split of the longest chains across
+    CTAs would use."""
+    rng = np.random.default_rng(7 + split_chunks)
+    lens = [200, 40, 129]
+    Hk, Hv, K, V = 1, 2, 16, 8
+    q, k, v, g, b, cu = _inputs(rng, lens, Hk, Hv, K, V, gate_scale)
+    S0 = rng.standard_normal((len(lens), Hv, K, V)) * 0.1
+    scale = K ** -0.5
+    o_ref, f_ref = kda_oracle.recurrence(q, k, v, g, b, cu, scale=scale, state=S0)
+    o, f = split_state_passing(q, k, v, g, b, cu, S0, scale, split_chunks)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(f, f_ref, rtol=1e-10, atol=1e-12)
