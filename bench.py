@@ -41,12 +41,12 @@ def _peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def _traffic_from_profile():
-    """DRAM bytes per launch from the committed ncu summary, or None if the kernel
+def _traffic_from_profile(summary="kda_prefill_tc_traffic.txt", source="kda_prefill_tc.cu"):
+    """DRAM bytes per launch from a committed ncu summary, or None if the kernel
     source changed since those counters were taken."""
     import hashlib
-    p = os.path.join(ROOT, "profiles", "kda_prefill_tc_traffic.txt")
-    src = os.path.join(ROOT, "linear_attention_prefill_chunked_gb300", "csrc", "kda_prefill_tc.cu")
+    p = os.path.join(ROOT, "profiles", summary)
+    src = os.path.join(ROOT, "linear_attention_prefill_chunked_gb300", "csrc", source)
     if not (os.path.exists(p) and os.path.exists(src)):
         return None
     kv = {}
@@ -229,7 +229,10 @@ def run_decode(args, dist, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     kda.load()
-    w = synthetic.decode_batch(pool_device=dev)
+    if args.workload == "decode_small":  # 512 rows on a 2 GiB pool: small enough for an ncu capture
+        w = synthetic.decode_batch(num_rows=512, num_pad=8, num_slots=1024, pool_device=dev)
+    else:
+        w = synthetic.decode_batch(pool_device=dev)
     t = lambda x: x.to(dev).contiguous()
     q, k, v, g, beta, idx = (t(x) for x in (w.q, w.k, w.v, w.g, w.beta, w.state_indices))
     pool = w.state
@@ -257,15 +260,18 @@ def run_decode(args, dist, ws, rank, local):
     hbm, _, src = _peaks()
     achieved = real * row_bytes / (ms * 1e-3) / 1e9
     print(json.dumps({
-        "metric": "KDA decode rows/s (4096 one-token rows, Hv=32, K=V=128, fp32 pool)",
+        "metric": f"KDA decode rows/s ({w.N} one-token rows, Hv=32, K=V=128, fp32 pool)",
         "value": job_rate(ws, real, ms), "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "real_rows": real, "padding_rows": w.N - real,
-                   "pool": "fp32 [8192, 32, 128, 128], resident",
-                   "l2": "state tiles (16 GiB pool) larger than L2, no flush"},
+                   "pool": f"fp32 [{pool.shape[0]}, 32, 128, 128], resident",
+                   "l2": f"state tiles ({pool.numel() * 4 / 2**30:.0f} GiB pool) larger than L2, no flush"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None, "peak_source": src,
+                     "frac": achieved / hbm,
+                     "traffic": (_traffic_from_profile("kda_decode_traffic.txt", "kda_decode.cu")
+                                 if args.workload == "decode" else None),
+                     "peak_source": src,
                      "algorithmic_bytes_per_launch": real * row_bytes},
         "clocks": clk.summary(), "gpu_launches": args.steps}), flush=True)
 
@@ -425,15 +431,17 @@ def main():
                          "(kda_chunk_prefill_act); scalar: one log-decay per token and head")
     ap.add_argument("--qk-l2norm", action="store_true",
                     help="normalise q and k inside the kernel (KDA_FLAG_QK_L2NORM)")
-    ap.add_argument("--workload", default="throughput", choices=["throughput", "profile", "decode"],
-                    help="profile: 8 x 1024 tokens, Hv=32 (a smaller case for ncu captures)")
+    ap.add_argument("--workload", default="throughput",
+                    choices=["throughput", "profile", "decode", "decode_small"],
+                    help="profile: 8 x 1024 tokens, Hv=32; decode_small: 512 decode rows on a "
+                         "2 GiB pool (smaller cases for ncu captures)")
     args = ap.parse_args()
     dist, ws, rank, local = _dist()
     try:
         if args.impl == "reference":
             run_reference(args, dist, ws, rank)
         else:
-            (run_decode if args.workload == "decode" else run_ours)(args, dist, ws, rank, local)
+            (run_decode if args.workload.startswith("decode") else run_ours)(args, dist, ws, rank, local)
     finally:
         if dist:
             dist.destroy_process_group()
