@@ -127,6 +127,91 @@ def _need(t, name, dtype=None, cuda=True):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _shape(t, name, dims, min_rows=None):
+    """t has len(dims) dimensions matching dims (None matches any size); with min_rows its
+    first dimension is at least that.  The C ABI takes plain pointers, so this is where a
+    tensor too small for the descriptor is caught, before any launch."""
+    if t.dim() != len(dims) or any(d is not None and t.shape[i] != d for i, d in enumerate(dims)):
+        want = "[" + ", ".join("*" if d is None else str(d) for d in dims) + "]"
+        raise ValueError(f"{name} must have shape {want}, got {list(t.shape)}")
+    if min_rows is not None and t.shape[0] < min_rows:
+        raise ValueError(f"{name} needs at least {min_rows} rows, got {t.shape[0]}")
+
+
+def _gate_shape(gate, name, T, Hv, K):
+    """[>=T, Hv, K] per key channel, or [>=T, Hv] for a scalar gate."""
+    if gate.dim() == 2:
+        _shape(gate, name, (None, Hv), min_rows=T)
+    else:
+        _shape(gate, name, (None, Hv, K), min_rows=T)
+
+
+def _pool_shape(pool, name, Hv, K, V, slot_stride):
+    if slot_stride == 0:
+        _shape(pool, name, (None, Hv, K, V))
+    elif pool.dim() < 1 or pool.numel() < (pool.shape[0] - 1) * slot_stride + Hv * K * V:
+        raise ValueError(f"{name} is too small for {pool.shape[0]} slots of pitch {slot_stride}")
+
+
+def check_prefill_shapes(q, k, v, gate, beta, cu_seqlens, *, state=None, state_indices=None,
+                         final_state=None, out=None, A_log=None, dt_bias=None, slot_stride=0):
+    """Shape checks of a prefill call (host only; see :func:`chunk_prefill`)."""
+    _shape(q, "q", (None, None, None))
+    T, Hk, K = q.shape
+    _shape(k, "k", (T, Hk, K))
+    _shape(v, "v", (T, None, None))
+    Hv, V = v.shape[1], v.shape[2]
+    if Hk == 0 or Hv % Hk != 0:
+        raise ValueError(f"the v-head count {Hv} must be a multiple of the k-head count {Hk}")
+    _gate_shape(gate, "g" if A_log is None else "a", T, Hv, K)
+    _shape(beta, "beta", (None, Hv), min_rows=T)
+    _shape(cu_seqlens, "cu_seqlens", (None,), min_rows=1)
+    N = cu_seqlens.shape[0] - 1
+    if A_log is not None:
+        _shape(A_log, "A_log", (Hv,))
+        if dt_bias is not None:
+            _shape(dt_bias, "dt_bias", (Hv,) if gate.dim() == 2 else (Hv, K))
+    if state_indices is not None:
+        _shape(state_indices, "state_indices", (N,))
+        if state is not None:
+            _pool_shape(state, "state", Hv, K, V, slot_stride)
+    else:
+        if state is not None:
+            _shape(state, "state", (N, Hv, K, V))
+        if final_state is not None:
+            _shape(final_state, "final_state", (N, Hv, K, V))
+    if out is not None:
+        _shape(out, "out", (T, Hv, V))
+        if out.dtype != q.dtype:
+            raise TypeError(f"out must be {q.dtype}, got {out.dtype}")
+
+
+def check_decode_shapes(q, k, v, g, beta, pool, *, state_indices=None, out=None, slot_stride=0,
+                        cu_seqlens=None):
+    """Shape checks of a decode call (one row per token, or draft steps per request when
+    ``cu_seqlens`` is given; host only)."""
+    _shape(q, "q", (None, None, None))
+    T, Hk, K = q.shape
+    _shape(k, "k", (T, Hk, K))
+    _shape(v, "v", (T, None, None))
+    Hv, V = v.shape[1], v.shape[2]
+    if Hk == 0 or Hv % Hk != 0:
+        raise ValueError(f"the v-head count {Hv} must be a multiple of the k-head count {Hk}")
+    _gate_shape(g, "g", T, Hv, K)
+    _shape(beta, "beta", (None, Hv), min_rows=T)
+    _pool_shape(pool, "pool", Hv, K, V, slot_stride)
+    N = T
+    if cu_seqlens is not None:
+        _shape(cu_seqlens, "cu_seqlens", (None,), min_rows=1)
+        N = cu_seqlens.shape[0] - 1
+    if state_indices is not None:
+        _shape(state_indices, "state_indices", (N,))
+    if out is not None:
+        _shape(out, "out", (T, Hv, V))
+        if out.dtype != q.dtype:
+            raise TypeError(f"out must be {q.dtype}, got {out.dtype}")
+
+
 def make_desc(*, num_seqs, total_tokens, Hk, Hv, K, V, qkv_dtype, state_dtype=torch.float32,
               scale=None, num_slots=0, slot_stride=0, flags=0) -> KdaDesc:
     d = KdaDesc()
@@ -213,6 +298,13 @@ def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_stat
     _need(cu_seqlens, "cu_seqlens", torch.int32)
     if q.dtype != k.dtype or q.dtype != v.dtype:
         raise TypeError("q, k and v must share one dtype")
+    for name, t in (("state", state), ("final_state", final_state), ("out", out)):
+        if t is not None:
+            _need(t, name)
+    check_prefill_shapes(q, k, v, g if act is None else act[0], beta, cu_seqlens, state=state,
+                         state_indices=state_indices, final_state=final_state, out=out,
+                         A_log=None if act is None else act[1],
+                         dt_bias=None if act is None else act[2], slot_stride=slot_stride)
     T, Hk, K = q.shape
     Hv, V = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
@@ -280,6 +372,10 @@ def decode(q, k, v, g, beta, pool, state_indices=None, *, scale=None, slot_strid
     _need(beta, "beta", torch.float32)
     if state_indices is not None:
         _need(state_indices, "state_indices", torch.int32)
+    if out is not None:
+        _need(out, "out")
+    check_decode_shapes(q, k, v, g, beta, pool, state_indices=state_indices, out=out,
+                        slot_stride=slot_stride)
     N, Hk, K = q.shape
     Hv, V = v.shape[1], v.shape[2]
     d = make_desc(num_seqs=N, total_tokens=N, Hk=Hk, Hv=Hv, K=K, V=V, qkv_dtype=q.dtype,
@@ -320,6 +416,10 @@ def decode_draft(q, k, v, g, beta, cu_seqlens, pool, state_indices=None, *, cach
     _need(cu_seqlens, "cu_seqlens", torch.int32)
     if state_indices is not None:
         _need(state_indices, "state_indices", torch.int32)
+    if out is not None:
+        _need(out, "out")
+    check_decode_shapes(q, k, v, g, beta, pool, state_indices=state_indices, out=out,
+                        slot_stride=slot_stride, cu_seqlens=cu_seqlens)
     T, Hk, K = q.shape
     Hv, V = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
@@ -330,6 +430,12 @@ def decode_draft(q, k, v, g, beta, cu_seqlens, pool, state_indices=None, *, cach
         if not isinstance(cache, torch.Tensor) or not cache.is_cuda or cache.dtype != pool.dtype:
             raise TypeError("cache must be a CUDA tensor of the pool's dtype")
         pitch = cache.stride(0)
+        step = Hv * K * V
+        avail = cache.untyped_storage().nbytes() // cache.element_size() - cache.storage_offset()
+        if cache.dim() < 1 or cache.shape[0] < N or pitch < max_steps * step or \
+                (N > 0 and (N - 1) * pitch + max_steps * step > avail):
+            raise ValueError(f"cache must hold {N} requests of {max_steps} states "
+                             f"({step} elements each) at its row pitch {pitch}")
     d = make_desc(num_seqs=N, total_tokens=T, Hk=Hk, Hv=Hv, K=K, V=V, qkv_dtype=q.dtype,
                   state_dtype=pool.dtype, scale=scale, num_slots=pool.shape[0],
                   slot_stride=slot_stride,
