@@ -19,7 +19,11 @@
  * General rules for every entry point
  * -----------------------------------
  *  - All tensor pointers are DEVICE pointers, owned by the caller; tensors are
- *    packed, contiguous and row-major with the shapes given below.
+ *    packed, contiguous and row-major with the shapes given below.  The library
+ *    sees no sizes: every buffer must hold at least the shape stated for it
+ *    (the Python binding checks shapes before calling).
+ *  - q, k, v, g (or a), o and the state buffers must be 16-byte aligned (they
+ *    are moved by TMA); an unaligned one is KDA_ERR_INVALID_ARGUMENT.
  *  - Calls are asynchronous on `stream`.  They never allocate device memory and
  *    never synchronise the host (the pages measured both as the dominant host
  *    cost: a ~200 MB re-allocation per call and a device->host `.item()` in the
