@@ -286,6 +286,11 @@ def run_ours(args, dist, ws, rank, local):
     if args.workload == "profile":
         w = synthetic.make([1024] * 8, Hk=32, Hv=32, K=128, V=128, seed=5, state="pool",
                            num_slots=16, name="profile_8x1024_Hv32_K128")
+    elif args.workload == "many_short":  # 8192 prompts of 1..8 tokens: the work-list order step
+        gen = torch.Generator().manual_seed(8192)
+        lens = torch.randint(1, 9, (8192,), generator=gen).tolist()
+        w = synthetic.make(lens, Hk=32, Hv=32, K=128, V=128, gen=gen, state="pool",
+                           num_slots=8193, name="many_short_8192seq_Hv32_K128")
     else:
         w = synthetic.throughput()
     act = args.gate == "act"
@@ -432,9 +437,10 @@ def main():
     ap.add_argument("--qk-l2norm", action="store_true",
                     help="normalise q and k inside the kernel (KDA_FLAG_QK_L2NORM)")
     ap.add_argument("--workload", default="throughput",
-                    choices=["throughput", "profile", "decode", "decode_small"],
+                    choices=["throughput", "profile", "many_short", "decode", "decode_small"],
                     help="profile: 8 x 1024 tokens, Hv=32; decode_small: 512 decode rows on a "
-                         "2 GiB pool (smaller cases for ncu captures)")
+                         "2 GiB pool (smaller cases for ncu captures); many_short: 8192 "
+                         "sequences of 1 to 8 tokens")
     args = ap.parse_args()
     dist, ws, rank, local = _dist()
     try:

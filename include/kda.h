@@ -229,9 +229,9 @@ kda_status_t kda_decode_draft(const kda_desc_t *desc, const void *q, const void 
 /*
  * Allocation-free prefill.  The pages have no counterpart of this entry point.
  *
- * For callers that cannot allocate device memory when they run the prefill: code
- * replayed inside a captured CUDA graph, plug-in hosts whose allocator belongs to
- * someone else, or real-time paths that forbid allocation after start-up.  It
+ * For callers that cannot allocate device memory when they run the prefill:
+ * plug-in hosts whose device allocator belongs to someone else, and real-time paths
+ * that forbid allocation after start-up.  It
  * takes the same arguments as kda_chunk_prefill() minus the workspace: the scratch
  * the prefill needs (status word, work counter, sequence order) comes from a fixed
  * array of KDA_NOALLOC_SCRATCH_BYTES bytes in the library's device memory, which

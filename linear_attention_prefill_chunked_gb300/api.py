@@ -180,6 +180,10 @@ def check_prefill_shapes(q, k, v, gate, beta, cu_seqlens, *, state=None, state_i
             _shape(state, "state", (N, Hv, K, V))
         if final_state is not None:
             _shape(final_state, "final_state", (N, Hv, K, V))
+        # the kernels write the final state in the element type of the initial one: a
+        # final_state of another dtype would be written past its end (or only half filled)
+        if state is not None and final_state is not None and state.dtype != final_state.dtype:
+            raise TypeError(f"final_state must be {state.dtype} like state, got {final_state.dtype}")
     if out is not None:
         _shape(out, "out", (T, Hv, V))
         if out.dtype != q.dtype:

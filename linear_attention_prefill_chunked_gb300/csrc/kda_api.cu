@@ -119,6 +119,9 @@ kda_status_t prefill_common(const kda_desc_t* d, const void* q, const void* k, c
   a.ws_bytes = workspace_bytes;
   a.status = &reinterpret_cast<kda::WsHeader*>(workspace)->status;
 
+  // An error left by earlier, unrelated work is cleared here, so that the launch checks
+  // below report failures of this call's own launches only.
+  (void)cudaGetLastError();
   // The header (status word, scheduler counter) starts every call at zero.
   if (cudaMemsetAsync(workspace, 0, sizeof(kda::WsHeader), stream) != cudaSuccess)
     return KDA_ERR_CUDA;
@@ -187,6 +190,7 @@ kda_status_t kda_decode(const kda_desc_t* d, const void* q, const void* k, const
   a.cache_pitch = 0;
   a.max_steps = 1;
   a.update_pool = true;
+  (void)cudaGetLastError();  // report this call's own launch errors only
   if (cudaMemsetAsync(workspace, 0, sizeof(kda::WsHeader), stream) != cudaSuccess)
     return KDA_ERR_CUDA;
   return kda::launch_decode(a, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
@@ -231,6 +235,7 @@ kda_status_t kda_decode_draft(const kda_desc_t* d, const void* q, const void* k,
   a.cache_pitch = cache_pitch_elems;
   a.max_steps = max_steps;
   a.update_pool = update_pool != 0;
+  (void)cudaGetLastError();  // report this call's own launch errors only
   if (cudaMemsetAsync(workspace, 0, sizeof(kda::WsHeader), stream) != cudaSuccess)
     return KDA_ERR_CUDA;
   return kda::launch_decode(a, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;

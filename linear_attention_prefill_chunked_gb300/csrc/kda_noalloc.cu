@@ -2,8 +2,8 @@
 // that cannot allocate device memory.
 //
 // Some callers cannot call cudaMalloc at the point where they run the prefill:
-// code replayed inside a captured CUDA graph, plug-in hosts whose allocator is
-// owned by someone else, or real-time paths that forbid allocation after start-up.
+// plug-in hosts whose device allocator is owned by someone else, and real-time
+// paths that forbid allocation after start-up.
 // This entry point gives them the prefill with its scratch (the device status
 // word, the work counter and the longest-first sequence order) taken from a
 // fixed array that lives in the library's own device memory instead of a

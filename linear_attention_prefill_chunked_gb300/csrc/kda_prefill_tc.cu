@@ -1363,25 +1363,52 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
-// Sequences ordered longest first (ties by index) so the longest (sequence, head)
-// chains start first on the persistent grid.
-__global__ void kda_order_kernel(const int32_t* __restrict__ cu, int N, int64_t T,
-                                 int32_t* __restrict__ order) {
-  for (int n = threadIdx.x; n < N; n += blockDim.x) {
-    const int64_t a = cu[n], b = cu[n + 1];
-    const int64_t ln = (a >= 0 && b >= a && b <= T) ? b - a : 0;
-    int rank = 0;
-    for (int m = 0; m < N; ++m) {
-      const int64_t am = cu[m], bm = cu[m + 1];
-      const int64_t lm = (am >= 0 && bm >= am && bm <= T) ? bm - am : 0;
-      rank += (lm > ln) || (lm == ln && m < n);
-    }
-    order[rank] = n;
-  }
+// Sequences ordered by chunk count, most chunks first, so that the longest (sequence,
+// head) chains start first on the persistent grid.  One block of kOrderKeys threads runs a
+// counting sort: a histogram of the keys, an exclusive scan over the keys in descending
+// order, then a scatter.  O(N) work over the block's threads for any N.  Chunk counts of
+// kOrderKeys - 1 or more share the top key; ties land in any order, which only decides
+// which CTA claims an item first -- every item computes the same result on any CTA.
+constexpr int kOrderKeys = 1024;
+__device__ __forceinline__ int order_key(const int32_t* cu, int n, int64_t T) {
+  const int64_t a = cu[n], b = cu[n + 1];
+  const int64_t len = (a >= 0 && b >= a && b <= T) ? b - a : 0;  // bad bounds: checked later
+  return (int)min((len + kC - 1) / kC, (int64_t)(kOrderKeys - 1));
 }
-__global__ void kda_identity_order_kernel(int N, int32_t* __restrict__ order) {
-  for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += gridDim.x * blockDim.x)
-    order[n] = n;
+__global__ void __launch_bounds__(kOrderKeys) kda_order_kernel(const int32_t* __restrict__ cu, int N,
+                                                               int64_t T, int32_t* __restrict__ order) {
+  __shared__ int cnt[kOrderKeys];
+  __shared__ int wsum[kOrderKeys / 32];
+  const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
+  cnt[t] = 0;
+  __syncthreads();
+  for (int n = t; n < N; n += kOrderKeys) atomicAdd(&cnt[order_key(cu, n, T)], 1);
+  __syncthreads();
+  // thread t holds key kOrderKeys-1-t: an exclusive scan over threads counts the
+  // sequences with a larger key, i.e. the first position of key kb in the order
+  const int kb = kOrderKeys - 1 - t;
+  const int c = cnt[kb];
+  int x = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[wp] = x;
+  __syncthreads();
+  if (wp == 0) {
+    int w = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    wsum[lane] = w;
+  }
+  __syncthreads();
+  cnt[kb] = x - c + (wp > 0 ? wsum[wp - 1] : 0);
+  __syncthreads();
+  for (int n = t; n < N; n += kOrderKeys) order[atomicAdd(&cnt[order_key(cu, n, T)], 1)] = n;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
@@ -1500,10 +1527,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   p.slot_stride = a.slot_stride;
   p.scale = a.scale;
 
-  if (d.num_seqs <= 8192)
-    kda_order_kernel<<<1, 1024, 0, st>>>(a.cu, d.num_seqs, T, order);
-  else
-    kda_identity_order_kernel<<<64, 256, 0, st>>>(d.num_seqs, order);
+  kda_order_kernel<<<1, kOrderKeys, 0, st>>>(a.cu, d.num_seqs, T, order);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int grid = std::min(sm_count(), std::max(1, p.num_items));

@@ -88,3 +88,14 @@ def test_decode_shape_checks():
     api.check_decode_shapes(*dict(ok, pool=torch.zeros(SLOTS, pitch)).values(), slot_stride=pitch)
     with pytest.raises(ValueError):
         api.check_decode_shapes(*dict(ok, pool=torch.zeros(SLOTS, 64)).values(), slot_stride=pitch)
+
+
+def test_dense_final_state_dtype_must_match_state():
+    """Dense mode writes the final state in the initial state's element type, so a mismatched
+    final_state would be overrun (fp32 state, bf16 final) or half filled (the reverse)."""
+    for sdt, fdt in ((torch.float32, BF), (BF, torch.float32)):
+        with pytest.raises(TypeError):
+            _check_prefill(state_indices=None, state=torch.zeros(N, HV, K, V, dtype=sdt),
+                           final_state=torch.zeros(N, HV, K, V, dtype=fdt))
+    _check_prefill(state_indices=None, state=torch.zeros(N, HV, K, V, dtype=BF),
+                   final_state=torch.zeros(N, HV, K, V, dtype=BF))

@@ -4,14 +4,13 @@ Tolerances (relative L2 over the tensor): 1e-2 with bf16 inputs, 1e-4 with fp32
 inputs; every output finite; pool mode bit-identical to dense gather/scatter
 (sglang PR 30169 digest, 关键源码片段 test_gdn_chunk_cutedsl_pool_mode_matches_dense).
 """
-import numpy as np
 import pytest
 import torch
 
 import linear_attention_prefill_chunked_gb300 as kda
 from linear_attention_prefill_chunked_gb300 import synthetic
 from oracle import kda_oracle
-from tests._util import assert_close, oracle_sampled, to_dev
+from tests._util import assert_close, assert_items_close, assert_rows_close, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -60,41 +59,39 @@ def test_pool_mode_matches_dense_bitwise_and_oracle(state_dtype):
     assert int(slots[-1]) == pool.shape[0] - 1
 
 
-def test_large_decay_finite_and_close():
-    w = synthetic.large_decay()
+def _full_size_case(w):
+    """One prefill of a full-size workload in pool mode, compared in full with one
+    whole-workload oracle call: every (sequence, v-head) item of o and every written pool
+    row, each on its own; pool rows no sequence names stay bit-identical."""
     d = to_dev(w)
     pool_before = w.state.clone()
     o, _ = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
                              state=d["state"], state_indices=d["state_indices"])
-    torch.cuda.synchronize()
+    assert kda.read_device_status(kda.chunk_prefill.last_workspace) == 0
     assert torch.isfinite(o).all()
     assert torch.isfinite(d["state"]).all()
-    pairs = [(0, 0), (3, 7), (5, 19), (7, 31), (2, int(torch.argmax(w.g.mean((0, 2)))))]
-    ref = oracle_sampled(w, pairs, state_before=pool_before)
-    cu = w.cu_seqlens.tolist()
-    slots = w.state_indices.tolist()
-    for (n, h), (o_ref, s_ref) in ref.items():
-        assert_close(o[cu[n]:cu[n + 1], h], o_ref, torch.bfloat16, f"o seq {n} head {h}")
-        assert_close(d["state"][slots[n], h], s_ref, torch.bfloat16, f"state seq {n} head {h}")
+    o_ref, pool_ref = _full_oracle(w, state=pool_before)
+    e_o = assert_items_close(o, o_ref, w.cu_seqlens.tolist(), torch.bfloat16, "o")
+    slots = torch.where(w.state_indices >= 0, w.state_indices,
+                        torch.full_like(w.state_indices, w.state.shape[0] - 1)).long()
+    e_s = assert_rows_close(d["state"][slots.cuda()], pool_ref[slots.numpy()], torch.bfloat16,
+                            "written pool rows")
+    untouched = torch.ones(w.state.shape[0], dtype=torch.bool)
+    untouched[slots] = False
+    assert torch.equal(d["state"][untouched.cuda()].cpu(), pool_before[untouched])
+    return e_o, e_s
 
 
-def test_throughput_workload_sampled():
-    w = synthetic.throughput()
-    d = to_dev(w)
-    pool_before = w.state.clone()
-    o, _ = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
-                             state=d["state"], state_indices=d["state_indices"])
-    torch.cuda.synchronize()
-    assert torch.isfinite(o).all()
-    lens = w.lens
-    longest = int(np.argmax(lens))
-    pairs = [(longest, 0), (longest, 31), (int(np.argmin(lens)), 5), (3, 17), (9, 8)]
-    ref = oracle_sampled(w, pairs, state_before=pool_before)
-    cu = w.cu_seqlens.tolist()
-    slots = w.state_indices.tolist()
-    for (n, h), (o_ref, s_ref) in ref.items():
-        assert_close(o[cu[n]:cu[n + 1], h], o_ref, torch.bfloat16, f"o seq {n} head {h}")
-        assert_close(d["state"][slots[n], h], s_ref, torch.bfloat16, f"state seq {n} head {h}")
+def test_large_decay_full():
+    """Config 3: 8 x 4096 tokens, Hv = 32, per-chunk log-decay sums near -6e4 (the gate
+    magnitude at which the pages' fp32 exponent overflowed: PR 27488 digest, 功能与动机)."""
+    _full_size_case(synthetic.large_decay())
+
+
+def test_throughput_workload_full():
+    """Config 4, the benchmark's workload (32768 tokens in 16 sequences, Hv = 32), in the
+    launch configuration the benchmark times."""
+    _full_size_case(synthetic.throughput())
 
 
 @pytest.mark.parametrize("K,V,dtype", [(64, 128, torch.float32), (128, 64, torch.bfloat16),
@@ -186,6 +183,28 @@ def test_many_short_items_claimed_late():
     # with a wrong state or chunk would be off by the values themselves, ~1 RMS)
     assert_close(o, o_ref, torch.bfloat16, "o", max_rms=0.15)
     assert_close(pool, pool_ref, torch.bfloat16, "pool")
+
+
+def test_sixteen_thousand_sequences_longest_first():
+    """16384 sequences, most of 0 to 5 tokens with longer ones spread among them: the
+    longest-first order of the work list is built on the device (a counting sort over chunk
+    counts, no host sync) for a batch of this size too, and every item is claimed and run
+    once.  Every (sequence, head) item and every written pool row against the oracle."""
+    gen = torch.Generator().manual_seed(123)
+    lens = torch.randint(0, 6, (16384,), generator=gen)
+    longer = torch.randperm(16384, generator=gen)[:40]
+    lens[longer] = torch.randint(60, 400, (40,), generator=gen)
+    w = synthetic.make(lens.tolist(), Hk=1, Hv=2, K=128, V=128, dtype=torch.bfloat16, seed=124,
+                       state="pool", num_slots=16385, state_dtype=torch.bfloat16)
+    d = to_dev(w)
+    pool_before = w.state.clone()
+    o, pool = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                state=d["state"], state_indices=d["state_indices"])
+    assert kda.read_device_status(kda.chunk_prefill.last_workspace) == 0
+    o_ref, pool_ref = _full_oracle(w, state=pool_before)
+    assert_items_close(o, o_ref, w.cu_seqlens.tolist(), torch.bfloat16, "o", max_rms=0.15)
+    slots = w.state_indices.long()
+    assert_rows_close(pool[slots.cuda()], pool_ref[slots.numpy()], torch.bfloat16, "pool rows")
 
 
 def test_zero_initial_state_and_padded_gate_rows():
