@@ -193,6 +193,140 @@ def cpu_baseline(w, num_threads=0, heads=SAMPLE_HEADS):
                        f"to full-width tokens")}
 
 
+def per_core_rate(w, tokens=4096):
+    """The oracle on one core: one (sequence, v-head) pair of ``tokens`` tokens (the first
+    tokens of the longest sequence, head 0), in tokens per second per core."""
+    from oracle import kda_oracle
+    n = max(range(w.N), key=lambda i: w.lens[i])
+    a = int(w.cu_seqlens[n])
+    L = min(tokens, w.lens[n])
+    sl = slice(a, a + L)
+    t0 = time.perf_counter()
+    kda_oracle.recurrence(w.q[sl, :1], w.k[sl, :1], w.v[sl, :1], w.g[sl, :1], w.beta[sl, :1],
+                          [0, L], scale=w.scale, num_threads=1)
+    dt = time.perf_counter() - t0
+    return {"value": L / dt, "unit": "tokens/s per core (one v-head)",
+            "sample": f"one (sequence, v-head) pair of {L} tokens on 1 thread, {dt:.3f} s"}
+
+
+def config_parity(dev):
+    """Each workload configuration once more on the GPU from fresh inputs, against the oracle
+    (wall time and host threads of the oracle, relative L2 of o and of the final states over
+    the whole tensor).  The decode configuration runs 512 of its rows on a 1024-slot pool;
+    the test suite compares all 4032 of them."""
+    import numpy as np
+
+    import linear_attention_prefill_chunked_gb300 as kda
+    from linear_attention_prefill_chunked_gb300 import synthetic
+    from oracle import kda_oracle
+
+    def rel(x, ref):
+        x = x.detach().cpu().double().numpy() if hasattr(x, "detach") else np.asarray(x)
+        return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300))
+
+    t = lambda x: None if x is None else x.to(dev).contiguous()
+    out = {}
+    cases = [("tiny_varlen", synthetic.tiny_varlen(), False),
+             ("pool_varlen_fp32_pool", synthetic.pool_varlen(), True),
+             ("pool_varlen_bf16_pool", synthetic.pool_varlen(state_dtype=torch.bfloat16), True),
+             ("large_decay", synthetic.large_decay(), True),
+             ("throughput", synthetic.throughput(), True)]
+    for name, w, pool_mode in cases:
+        st = t(w.state)
+        o, fin = kda.chunk_prefill(t(w.q), t(w.k), t(w.v), t(w.g), t(w.beta), t(w.cu_seqlens),
+                                   state=st, state_indices=t(w.state_indices) if pool_mode else None)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        o_ref, s_ref = kda_oracle.recurrence(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens,
+                                             scale=w.scale, state=w.state,
+                                             state_indices=w.state_indices if pool_mode else None)
+        dt = time.perf_counter() - t0
+        if pool_mode:  # the written rows
+            sl = torch.where(w.state_indices >= 0, w.state_indices,
+                             torch.full_like(w.state_indices, w.state.shape[0] - 1)).long()
+            e_s = rel(st[sl.to(dev)], s_ref[sl.numpy()])
+        else:
+            e_s = rel(fin, s_ref)
+        out[name] = {"rel_l2_o": rel(o, o_ref), "rel_l2_state": e_s,
+                     "finite": bool(torch.isfinite(o).all()), "oracle_s": round(dt, 3),
+                     "oracle_threads": os.cpu_count()}
+    w = synthetic.decode_batch(num_rows=512, num_pad=8, num_slots=1024, pool_device=dev)
+    real = np.flatnonzero(w.state_indices.numpy() >= 0)
+    slots = w.state_indices[real].long()
+    before = w.state[slots.to(dev)].cpu()
+    o = kda.decode(t(w.q), t(w.k), t(w.v), t(w.g), t(w.beta), w.state, t(w.state_indices))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    o_ref, s_ref = kda_oracle.recurrence(w.q[real], w.k[real], w.v[real], w.g[real], w.beta[real],
+                                         np.arange(real.size + 1), scale=w.scale, state=before)
+    dt = time.perf_counter() - t0
+    out["decode_512_rows"] = {"rel_l2_o": rel(o[torch.from_numpy(real).to(dev)], o_ref),
+                              "rel_l2_state": rel(w.state[slots.to(dev)], s_ref),
+                              "finite": bool(torch.isfinite(o).all()), "oracle_s": round(dt, 3),
+                              "oracle_threads": os.cpu_count()}
+    return out
+
+
+def e2e_pipelined(w, dev, stream, pool, ws_t, act, act_dev, steps):
+    """End to end through the public API (chunk_prefill / chunk_prefill_act) from pinned host
+    memory: every step copies its inputs host -> device and reads its output o back.  Steps
+    run as a pipeline over two device input sets: the copy-in of step i+1 (on one copy stream)
+    and the read-back of step i-1 (on another) overlap the prefill of step i, each stream
+    waiting on events only.  Returns (ms per step, host->device and device->host bytes per
+    step); the time runs from the first copy-in to the end of the last read-back."""
+    import linear_attention_prefill_chunked_gb300 as kda
+    host = [x.contiguous().pin_memory() for x in
+            (w.q, w.k, w.v, act_dev[0] if act else w.g, w.beta, w.cu_seqlens, w.state_indices)]
+    h_out = [torch.empty((w.T, 32, 128), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    sets = [[torch.empty_like(x, device=dev) for x in host] for _ in range(2)]
+    outs = [torch.empty((w.T, 32, 128), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    h2d = sum(x.numel() * x.element_size() for x in host)
+    d2h = h_out[0].numel() * h_out[0].element_size()
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=False)
+
+    def run(n):
+        e_in, e_done, e_out = [None] * n, [None] * n, [None] * n
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(e_done[i - 2])   # set b no longer read by step i-2
+                for d, h in zip(sets[b], host):
+                    d.copy_(h, non_blocking=True)
+                e_in[i] = ev()
+                e_in[i].record(s_in)
+            stream.wait_event(e_in[i])
+            if i >= 2:
+                stream.wait_event(e_out[i - 2])      # out b read back
+            dq, dk, dv, dg, db, dcu, didx = sets[b]
+            if act:
+                kda.chunk_prefill_act(dq, dk, dv, dg, act_dev[1], act_dev[2], db, dcu, state=pool,
+                                      state_indices=didx, out=outs[b], workspace=ws_t,
+                                      stream=stream)
+            else:
+                kda.chunk_prefill(dq, dk, dv, dg, db, dcu, state=pool, state_indices=didx,
+                                  out=outs[b], workspace=ws_t, stream=stream)
+            e_done[i] = ev()
+            e_done[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(e_done[i])
+                h_out[b].copy_(outs[b], non_blocking=True)
+                e_out[i] = ev()
+                e_out[i].record(s_out)
+        return e_out[n - 1]
+
+    run(2)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    last = run(steps)
+    s_in.wait_event(last)
+    e1.record(s_in)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
 def run_reference(args, dist, ws, rank):
     from linear_attention_prefill_chunked_gb300 import synthetic
     if rank != 0:
@@ -325,12 +459,21 @@ def run_ours(args, dist, ws, rank, local):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     with ClockSampler(local) as clk:
+        # untimed calls for about a second with the clock sampler running, so that its record
+        # covers the GPU under sustained load right up to (and through) the timed steps
+        soak = 0
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < args.clock_soak_s:
+            for _ in range(10):
+                step()
+            soak += 10
+            torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
         t0 = time.perf_counter()
         for i in range(args.steps):
             ev[i][0].record(stream)
@@ -344,47 +487,20 @@ def run_ours(args, dist, ws, rank, local):
         dist.barrier()
     bits = kda.read_device_status(ws_t)
 
-    # End to end through the public API from pinned host buffers (copies inside).
     e2e_ms, h2d, d2h = None, 0, 0
     if not args.no_e2e:
-        hq, hk, hv, hg, hb, hcu, hidx = (x.contiguous().pin_memory() for x in
-                                         (w.q, w.k, w.v, a_h if act else w.g, w.beta,
-                                          w.cu_seqlens, w.state_indices))
-        h_out = torch.empty((w.T, 32, 128), dtype=torch.bfloat16).pin_memory()
-        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hg, hb, hcu, hidx))
-        d2h = h_out.numel() * h_out.element_size()
-
-        def e2e_step():
-            dq, dk, dv, dg, db, dcu, didx = (x.to(dev, non_blocking=True) for x in
-                                             (hq, hk, hv, hg, hb, hcu, hidx))
-            if act:
-                o, _ = kda.chunk_prefill_act(dq, dk, dv, dg, A_log_d, dtb_d, db, dcu, state=pool,
-                                             state_indices=didx, workspace=ws_t, stream=stream)
-            else:
-                o, _ = kda.chunk_prefill(dq, dk, dv, dg, db, dcu, state=pool, state_indices=didx,
-                                         workspace=ws_t, stream=stream)
-            h_out.copy_(o, non_blocking=True)
-
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        e2e_steps = max(2, min(args.steps, 5))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / e2e_steps)
+        e2e_ms, h2d, d2h = e2e_pipelined(w, dev, stream, pool, ws_t, act,
+                                         (a_h, A_log_d, dtb_d) if act else None, args.e2e_steps)
+        e2e_ms = max_over_ranks(dist, e2e_ms)
 
     if rank != 0:
         return
     hbm, bf16, src = _peaks()
-    ms = total_ms / args.steps
+    ms = total_ms / args.steps  # mean over the timed steps, used for value and roofline alike
     value = job_rate(ws, w.T, ms)
     nbytes = algorithmic_bytes(w, act, args.gate == "scalar")
     flops = algorithmic_flops(w)
-    kern_ms = statistics.median(per)
+    kern_ms = ms
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
     t_roof = max(nbytes / (hbm * 1e9), flops / (bf16 * 1e12))
     traffic = _traffic_from_profile() if path == 1 else None
@@ -406,12 +522,15 @@ def run_ours(args, dist, ws, rank, local):
                      "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else src,
                      "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
                      "roofline_time_ms": t_roof * 1e3, "frac_of_roofline_time": t_roof * 1e3 / kern_ms},
-        "clocks": clk.summary(),
+        "clocks": clk.summary() | {"window": f"{soak} untimed calls over ~{args.clock_soak_s:g} s of "
+                                             f"sustained load, then the {args.steps} timed steps"},
         "e2e": {"value": job_rate(ws, w.T, e2e_ms) if e2e_ms else None, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "note": f"pinned host q/k/v/{'a' if act else 'g'}/beta/cu_seqlens/indices copied in, "
-                        "o copied out each step; the state pool stays resident on the device"},
+                "note": f"each step copies its pinned host q/k/v/{'a' if act else 'g'}/beta/cu_seqlens/"
+                        "indices in and reads o back; steps are pipelined over two device input "
+                        "sets (copies of step i+1 and the read-back of step i-1 overlap the "
+                        "prefill of step i); the state pool stays resident on the device"},
         "gpu_launches": args.steps * (2 if path == 1 else 1),
         "device_status": bits, "wall_s": wall,
     }
@@ -420,6 +539,10 @@ def run_ours(args, dist, ws, rank, local):
             from oracle import kda_oracle
             w.g = torch.from_numpy(kda_oracle.gate_activation(a_h, A_log_h, dtb_h)).float()
         line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"]["per_core"] = per_core_rate(w)
+        if not args.no_parity and args.workload == "throughput" and args.gate == "given" \
+                and not args.qk_l2norm:
+            line["parity"] = config_parity(dev)
     print(json.dumps(line), flush=True)
 
 
@@ -431,6 +554,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--no-parity", action="store_true",
+                    help="skip the per-configuration oracle comparison of the default run")
+    ap.add_argument("--clock-soak-s", type=float, default=1.0,
+                    help="seconds of untimed calls, clock sampler running, before the timed steps")
     ap.add_argument("--gate", default="given", choices=["given", "act", "scalar"],
                     help="act: the gate computed in the kernel from a bf16 pre-activation "
                          "(kda_chunk_prefill_act); scalar: one log-decay per token and head")

@@ -101,11 +101,23 @@ typedef struct {
     uint32_t flags;            /* KDA_FLAG_* bits; every other bit must be 0           */
 } kda_desc_t;
 
-/* Bytes of workspace kda_chunk_prefill() needs for this descriptor (0 on an
+/* Bytes of workspace kda_chunk_prefill() wants for this descriptor (0 on an
  * invalid descriptor).  The workspace is caller-owned device memory, aligned to
  * 256 bytes, reusable across calls on the same stream; its contents need no
- * initialisation. */
+ * initialisation.  It holds the device status word, the work list and, for the
+ * tensor-core path, room to cut up to 4 of the longest sequences in two (the
+ * final states of the parts and up to 8192 rows of tail outputs, [rows][Hv][K]
+ * bf16): a sequence much longer than the batch's share per SM would keep its
+ * SMs busy long after the others, so its tail runs in parallel with its head
+ * and is completed by an exact affine combine (the state after the cut is
+ * M S_p + S_loc; outputs gain S_p^T y).  With Hv = 32 that is up to ~88 MB. */
 size_t kda_chunk_prefill_workspace_size(const kda_desc_t *desc);
+
+/* The least workspace kda_chunk_prefill() accepts (status word and work list):
+ * with less than kda_chunk_prefill_workspace_size() bytes no sequence is cut,
+ * which gives the same results up to rounding, more slowly when one sequence
+ * dominates the batch. */
+size_t kda_chunk_prefill_min_workspace_size(const kda_desc_t *desc);
 
 /* Bytes of workspace kda_decode() needs (status word only). */
 size_t kda_decode_workspace_size(const kda_desc_t *desc);
@@ -136,13 +148,16 @@ size_t kda_decode_workspace_size(const kda_desc_t *desc);
  *                dense mode: [N, Hv, K, V] state_dtype, or NULL to skip; may
  *                equal `state` (in-place update).
  *   o            [T, Hv, V] qkv_dtype, fully overwritten for every valid token.
- *   workspace    kda_chunk_prefill_workspace_size(desc) bytes, 256-byte aligned.
+ *   workspace    kda_chunk_prefill_workspace_size(desc) bytes (at least
+ *                kda_chunk_prefill_min_workspace_size(desc)), 256-byte aligned.
  *
  * State layout: S[k][v] row-major per (slot or sequence, v-head).
  * Pool mode and dense mode run the same kernels and the same arithmetic; only
  * the addresses differ, so o and the written state rows are bit-identical
  * between the two modes (PR 30169 digest, 实现拆解 item 4).
- * Run to run, results are bit-identical (no atomics in any reduction).
+ * Run to run, results are bit-identical (no atomics in any reduction), for the
+ * same inputs and workspace size; which sequences are cut depends only on the
+ * sequence lengths, Hv, the GPU's SM count and the workspace size.
  */
 kda_status_t kda_chunk_prefill(const kda_desc_t *desc, const void *q, const void *k,
                                const void *v, const float *g, const float *beta,
@@ -236,7 +251,9 @@ kda_status_t kda_decode_draft(const kda_desc_t *desc, const void *q, const void 
  * the prefill needs (status word, work counter, sequence order) comes from a fixed
  * array of KDA_NOALLOC_SCRATCH_BYTES bytes in the library's device memory, which
  * every GPU that loads the library holds until the process exits.  The call never
- * calls cudaMalloc, cudaFree or any allocating library routine.
+ * calls cudaMalloc, cudaFree or any allocating library routine.  The array has no
+ * room to cut long sequences, so every sequence runs whole (the results of
+ * kda_chunk_prefill() with kda_chunk_prefill_min_workspace_size() bytes).
  *
  *  - Limit: num_seqs <= KDA_NOALLOC_MAX_SEQS; a larger batch returns
  *    KDA_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.

@@ -50,7 +50,8 @@ class KdaDesc(ctypes.Structure):
     ]
 
 
-EXPORTS = ("kda_chunk_prefill_workspace_size", "kda_decode_workspace_size", "kda_chunk_prefill",
+EXPORTS = ("kda_chunk_prefill_workspace_size", "kda_chunk_prefill_min_workspace_size",
+           "kda_decode_workspace_size", "kda_chunk_prefill",
            "kda_decode", "kda_read_device_status", "kda_chunk_prefill_path", "kda_status_string",
            "kda_chunk_prefill_noalloc", "kda_chunk_prefill_act", "kda_decode_draft")
 
@@ -75,6 +76,8 @@ def load(build_if_missing: bool = True):
     D = ctypes.POINTER(KdaDesc)
     lib.kda_chunk_prefill_workspace_size.argtypes = [D]
     lib.kda_chunk_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.kda_chunk_prefill_min_workspace_size.argtypes = [D]
+    lib.kda_chunk_prefill_min_workspace_size.restype = ctypes.c_size_t
     lib.kda_decode_workspace_size.argtypes = [D]
     lib.kda_decode_workspace_size.restype = ctypes.c_size_t
     lib.kda_chunk_prefill.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
@@ -236,6 +239,12 @@ def prefill_workspace_size(desc: KdaDesc) -> int:
     return int(load().kda_chunk_prefill_workspace_size(ctypes.byref(desc)))
 
 
+def prefill_min_workspace_size(desc: KdaDesc) -> int:
+    """Least workspace the prefill accepts: no sequence is cut in two with less than
+    :func:`prefill_workspace_size`."""
+    return int(load().kda_chunk_prefill_min_workspace_size(ctypes.byref(desc)))
+
+
 def prefill_path(desc: KdaDesc) -> int:
     """1 = fused tensor-core path, 0 = CUDA-core path, -1 = invalid descriptor."""
     return int(load().kda_chunk_prefill_path(ctypes.byref(desc)))
@@ -341,7 +350,8 @@ def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_stat
     ws_size = lib.kda_chunk_prefill_workspace_size(ctypes.byref(d))
     if ws_size == 0:
         raise KdaError(1, "kda_chunk_prefill_workspace_size")
-    if workspace is None or workspace.numel() < ws_size:
+    if workspace is None or workspace.numel() < lib.kda_chunk_prefill_min_workspace_size(
+            ctypes.byref(d)):
         workspace = torch.empty(ws_size, dtype=torch.uint8, device=q.device)
     if act is None:
         rc = lib.kda_chunk_prefill(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),

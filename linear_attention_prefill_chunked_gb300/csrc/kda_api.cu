@@ -73,6 +73,12 @@ size_t kda_chunk_prefill_workspace_size(const kda_desc_t* d) {
   return kWsPayload + round_up(extra, 256);
 }
 
+size_t kda_chunk_prefill_min_workspace_size(const kda_desc_t* d) {
+  if (!dims_ok(d) || !heads_supported(d)) return 0;
+  size_t extra = kda::prefill_tc_supported(*d) ? kda::prefill_tc_min_workspace(*d) : 0;
+  return kWsPayload + round_up(extra, 256);
+}
+
 size_t kda_decode_workspace_size(const kda_desc_t* d) {
   if (!dims_ok(d) || !heads_supported(d)) return 0;
   return kWsPayload;
@@ -102,7 +108,7 @@ kda_status_t prefill_common(const kda_desc_t* d, const void* q, const void* k, c
     for (const void* p : ptrs)
       if (p && !aligned(p, 16)) return KDA_ERR_INVALID_ARGUMENT;
   }
-  if (workspace_bytes < kda_chunk_prefill_workspace_size(d)) return KDA_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < kda_chunk_prefill_min_workspace_size(d)) return KDA_ERR_WORKSPACE_TOO_SMALL;
 
   kda::PrefillArgs a;
   a.d = *d;

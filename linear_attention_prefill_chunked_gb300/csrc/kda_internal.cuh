@@ -14,7 +14,9 @@ namespace kda {
 struct WsHeader {
   uint32_t status;        // KDA_DEVICE_* bits
   uint32_t next_item;     // dynamic work counter of the persistent prefill
-  uint32_t reserved[62];
+  uint32_t num_entries;   // work-list entries written by the planning kernel
+  uint32_t num_splits;    // sequences the planning kernel cut in two
+  uint32_t reserved[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 constexpr size_t kWsPayload = 256;
@@ -88,7 +90,8 @@ struct PrefillArgs {
 };
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st);
-size_t prefill_tc_workspace(const kda_desc_t& d);
+size_t prefill_tc_workspace(const kda_desc_t& d);      // beyond the header, with splitting
+size_t prefill_tc_min_workspace(const kda_desc_t& d);  // beyond the header, no splitting
 bool prefill_tc_supported(const kda_desc_t& d);
 
 struct DecodeArgs {

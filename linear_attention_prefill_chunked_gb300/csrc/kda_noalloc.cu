@@ -47,7 +47,7 @@ extern "C" kda_status_t kda_chunk_prefill_noalloc(const kda_desc_t* desc, const 
                                                   void* state, const int32_t* state_indices,
                                                   void* final_state, void* o,
                                                   cudaStream_t stream) {
-  const size_t need = kda_chunk_prefill_workspace_size(desc);
+  const size_t need = kda_chunk_prefill_min_workspace_size(desc);
   if (need == 0) return KDA_ERR_INVALID_ARGUMENT;
   if (need > (size_t)KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;

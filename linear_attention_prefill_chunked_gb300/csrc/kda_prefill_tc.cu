@@ -101,10 +101,25 @@ enum Bar {
   B_ITEM_FULL, B_ITEM_EMPTY = B_ITEM_FULL + kRing, B_COUNT = B_ITEM_EMPTY + kRing
 };
 
+// Kinds of work-list entries.  A long sequence may be cut in two at a chunk boundary
+// (see kda_plan_kernel): its head runs as usual but leaves its final state S_p in the
+// split scratch; its tail runs twice from the cut, once from a zero state (outputs o_loc,
+// final state S_loc) and once with the values set to zero from the identity matrix
+// (outputs y_t = scale M_t^T q_t into the split scratch, final state M, the product of the
+// tail's transition matrices).  The state is affine in its start value, so the combine
+// kernel completes the tail as o_t = o_loc_t + S_p^T y_t and S_end = M S_p + S_loc.
+enum ItemKind : int32_t { KIND_WHOLE = 0, KIND_HEAD = 1, KIND_TAIL = 2, KIND_TAIL_ID = 3 };
+
+struct SplitInfo {  // one cut sequence
+  int32_t n, cut;     // sequence, chunks in its head
+  int32_t ytok0;      // first row of its tail in the y scratch
+  int32_t ntok;       // tokens in its tail
+};
+
 struct ItemInfo {
   int32_t n, h, kh, nchunks;
   int64_t bos, eos, slot;  // slot: pool row, or -1 in dense mode
-  int32_t done, pad;
+  int32_t done, kind, split, ybase;  // ybase: y-scratch row of token bos (KIND_TAIL_ID)
 };
 
 // Scheduling and load state of the threads that claim items and issue loads, kept in
@@ -128,6 +143,7 @@ struct Small {
   LoaderState ld;
   uint32_t tmem_base;
   uint32_t abort;
+  uint32_t num_items;  // work-list entries x Hv
 };
 constexpr uint32_t kSmemBytes = OFF_SMALL + sizeof(Small) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
@@ -143,13 +159,18 @@ struct TcParams {
   int gate_k;         // 128, or 1 for a scalar gate ([T, Hv]: tiles of 64 tokens x gw heads)
   int gw;             // scalar gate: heads per staged row (4 fp32 g or 8 bf16 a = 16 bytes)
   int l2norm;         // normalise the staged q/k rows (x / max(||x||, 1e-12), back to bf16)
-  const int32_t *cu, *idx, *order;
+  const int32_t *cu, *idx;
+  const uint32_t* work;      // work list: sequence | kind << 28, longest first
+  const SplitInfo* splits;   // cut sequences
+  const WsHeader* hdr;       // entries and cuts of the work list
+  float *sp, *sl, *mm;       // split scratch: [cuts][Hv][K][V] fp32 each
+  __nv_bfloat16* y;          // split scratch: [tail tokens][Hv][K]
   const void* state_in;
   void* state_out;
   __nv_bfloat16* o;
   uint32_t* status;
   uint32_t* next_item;
-  int32_t N, Hk, Hv, num_items;
+  int32_t N, Hk, Hv;
   int64_t T, num_slots, slot_stride;
   float scale;
 };
@@ -189,13 +210,14 @@ __device__ __forceinline__ bool wait_bar(const TcParams& p, Small* s, int b, uin
   }
 }
 
-// Fetches the next valid (sequence, head) item from the global counter.
+// Fetches the next valid item (work-list entry, head) from the global counter.
 __device__ ItemInfo fetch_item(const TcParams& p, Small* s) {
   ItemInfo info{};
   for (;;) {
-    const uint32_t it = aborted(s) ? (uint32_t)p.num_items : atomicAdd(p.next_item, 1u);
-    if (it >= (uint32_t)p.num_items) { info.done = 1; return info; }
-    const int n = p.order[it / p.Hv], h = it % p.Hv;
+    const uint32_t it = aborted(s) ? s->num_items : atomicAdd(p.next_item, 1u);
+    if (it >= s->num_items) { info.done = 1; return info; }
+    const uint32_t code = p.work[it / p.Hv];
+    const int n = (int)(code & 0x0FFFFFFFu), kind = (int)(code >> 28), h = it % p.Hv;
     int64_t bos, eos;
     if (!seq_bounds(p.cu, n, p.T, &bos, &eos)) { raise_status(p.status, KDA_DEVICE_BAD_SEQLENS); continue; }
     int64_t sl = -1;
@@ -203,9 +225,26 @@ __device__ ItemInfo fetch_item(const TcParams& p, Small* s) {
       sl = resolve_slot(p.idx, n, p.num_slots);
       if (sl < 0) { raise_status(p.status, KDA_DEVICE_BAD_SLOT); continue; }
     }
+    info.split = -1;
+    info.ybase = 0;
+    if (kind != KIND_WHOLE) {
+      const int ns = (int)p.hdr->num_splits;
+      for (int i = 0; i < ns; ++i)
+        if (p.splits[i].n == n) info.split = i;
+      if (info.split < 0) continue;  // not reachable: every cut entry has its record
+      const SplitInfo sp = p.splits[info.split];
+      const int64_t cut = bos + (int64_t)sp.cut * kC;
+      if (kind == KIND_HEAD) {
+        eos = cut;
+      } else {
+        bos = cut;
+        info.ybase = sp.ytok0;
+      }
+    }
     info.n = n; info.h = h; info.kh = h / (p.Hv / p.Hk);
     info.bos = bos; info.eos = eos; info.slot = sl;
     info.nchunks = (int)((eos - bos + kC - 1) / kC);
+    info.kind = kind;
     info.done = 0;
     return info;
   }
@@ -788,8 +827,14 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         }
       } else if (t == 160) {
         // and on warp 5: v of this chunk, for MMA-U of the recurrence group (the v buffer
-        // is free since MMA-U of the previous chunk, which pass B waited for)
-        ld.load_v(p, sm, s, h, (int)t0);
+        // is free since MMA-U of the previous chunk, which pass B waited for); the identity
+        // pass of a cut tail has zero values and no MMA-U, so its phase completes bare
+        if (info.kind == KIND_TAIL_ID) {
+          mbar_arrive(&s->bar[B_V_FULL]);
+          atomicAdd(&ld.st->n_v, 1u);
+        } else {
+          ld.load_v(p, sm, s, h, (int)t0);
+        }
       }
       __syncwarp();
       if (quad >= 2) {
@@ -1116,13 +1161,22 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
     const int h = info.h;
     const ST* src = nullptr;
     ST* dst = nullptr;
+    float* dst32 = nullptr;  // final state of a cut sequence's part, into the split scratch
+    const bool ident = info.kind == KIND_TAIL_ID;  // starts from I, zero values, o -> y
     const size_t hoff = (size_t)h * kK * kV;
-    if (info.slot >= 0) {
-      src = static_cast<const ST*>(p.state_in) + info.slot * p.slot_stride + hoff;
-      dst = static_cast<ST*>(p.state_out) + info.slot * p.slot_stride + hoff;
-    } else {
-      if (p.state_in) src = static_cast<const ST*>(p.state_in) + ((size_t)info.n * p.Hv) * kK * kV + hoff;
-      if (p.state_out) dst = static_cast<ST*>(p.state_out) + ((size_t)info.n * p.Hv) * kK * kV + hoff;
+    if (info.kind == KIND_WHOLE || info.kind == KIND_HEAD) {
+      if (info.slot >= 0) {
+        src = static_cast<const ST*>(p.state_in) + info.slot * p.slot_stride + hoff;
+        dst = static_cast<ST*>(p.state_out) + info.slot * p.slot_stride + hoff;
+      } else {
+        if (p.state_in) src = static_cast<const ST*>(p.state_in) + ((size_t)info.n * p.Hv) * kK * kV + hoff;
+        if (p.state_out) dst = static_cast<ST*>(p.state_out) + ((size_t)info.n * p.Hv) * kK * kV + hoff;
+      }
+    }
+    if (info.kind != KIND_WHOLE) {
+      const size_t so = ((size_t)info.split * p.Hv) * kK * kV + hoff;
+      dst32 = (info.kind == KIND_HEAD ? p.sp : info.kind == KIND_TAIL ? p.sl : p.mm) + so;
+      dst = nullptr;
     }
     if (info.nchunks == 0) {  // empty sequence: the final state is the initial one
       if (rt == 32) ld.push_one(p, s);  // claim of the next item (see the chunk loop)
@@ -1137,7 +1191,8 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
     for (int kq = 0; kq < 4; ++kq) {
       float sv[32], pw[16];
 #pragma unroll
-      for (int u = 0; u < 32; ++u) sv[u] = src ? to_f32(src[(size_t)(kq * 32 + u) * kV + v]) : 0.f;
+      for (int u = 0; u < 32; ++u)
+        sv[u] = src ? to_f32(src[(size_t)(kq * 32 + u) * kV + v]) : (ident && kq * 32 + u == v ? 1.f : 0.f);
 #pragma unroll
       for (int u = 0; u < 16; ++u) pw[u] = __uint_as_float(pack_bf16x2(sv[2 * u], sv[2 * u + 1]));
       tmem_st16(taddr_q + TM_SB + kq * 16, pw);
@@ -1177,8 +1232,9 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
 #pragma unroll 1
           for (int st = 0; st < 4; ++st) {
             const uint64_t b = sdesc_sw128(sbase + OFF_TM + st * 32, 16, 1024);
-            mma_bf16(tbase + TM_U, sdesc_sw128(sbase + OFF_VB + st * 2048, 8192, 1024), b, idu,
-                     st > 0 ? 1u : 0u);
+            if (!ident)
+              mma_bf16(tbase + TM_U, sdesc_sw128(sbase + OFF_VB + st * 2048, 8192, 1024), b, idu,
+                       st > 0 ? 1u : 0u);
             mma_bf16(tbase + TM_AB, sdesc_sw128(sbase + OFF_KG + st * 32, 16, 1024), b, idw,
                      st > 0 ? 1u : 0u);
           }
@@ -1209,9 +1265,10 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
           tc_fence_after();
           const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
 #pragma unroll 1
-          for (int st = 0; st < 8; ++st)
+          for (int st = 0; st < 8; ++st)  // onto U~ (the identity pass: U~ = 0, no MMA-U)
             mma_bf16_ta(tbase + TM_U, tbase + TM_SB + st * 8,
-                        sdesc_sw128(sbase + OFF_WB + st * 2048, 16384, 1024), id1, 1u);
+                        sdesc_sw128(sbase + OFF_WB + st * 2048, 16384, 1024), id1,
+                        (ident && st == 0) ? 0u : 1u);
           mma_commit(&s->bar[B_M1A]);
         }
         __syncwarp();
@@ -1288,6 +1345,9 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
 #pragma unroll
           for (int u = 0; u < 16; ++u) pw[u] = __uint_as_float(pack_bf16x2(sv[2 * u], sv[2 * u + 1]));
           tmem_st16(taddr_q + TM_SB + kq * 16, pw);
+        } else if (dst32) {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) dst32[(size_t)(kq * 32 + u) * kV + v] = sv[u];
         } else if (dst) {
 #pragma unroll
           for (int u = 0; u < 32; ++u) dst[(size_t)(kq * 32 + u) * kV + v] = from_f32<ST>(sv[u]);
@@ -1300,7 +1360,9 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       wait_bar(p, s, B_M3A, gc & 1);
       tc_fence_after();
       {
-        __nv_bfloat16* od = p.o + ((size_t)t0 * p.Hv + h) * kV + v;
+        // the identity pass writes y (K = V wide rows) into the split scratch instead of o
+        __nv_bfloat16* od = ident ? p.y + ((size_t)(t0 - info.bos + info.ybase) * p.Hv + h) * kV + v
+                                  : p.o + ((size_t)t0 * p.Hv + h) * kV + v;
         const size_t rs = (size_t)p.Hv * kV;
 #pragma unroll 1
         for (int cq = 0; cq < 4; ++cq) {
@@ -1337,6 +1399,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     for (int b = 0; b < B_COUNT; ++b) mbar_init(&s->bar[b], 1);
     for (int r = 0; r < kRing; ++r) mbar_init(&s->bar[B_ITEM_EMPTY + r], 2);
     s->abort = 0;
+    s->num_items = p.hdr->num_entries * (uint32_t)p.Hv;
     s->ld = LoaderState{};
     fence_mbar_init();
     prefetch_tensormap(&p.tm_q);
@@ -1363,29 +1426,41 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
-// Sequences ordered by chunk count, most chunks first, so that the longest (sequence,
-// head) chains start first on the persistent grid.  One block of kOrderKeys threads runs a
-// counting sort: a histogram of the keys, an exclusive scan over the keys in descending
-// order, then a scatter.  O(N) work over the block's threads for any N.  Chunk counts of
-// kOrderKeys - 1 or more share the top key; ties land in any order, which only decides
-// which CTA claims an item first -- every item computes the same result on any CTA.
+// ---- planning: the work list, longest first, with the longest sequences cut in two --------
+// One block of kOrderKeys threads, before the prefill kernel on the same stream (no host
+// sync).  Entries are ordered by chunk count, most chunks first, so that the longest
+// (entry, head) chains start first on the persistent grid; a counting sort over the chunk
+// counts (a histogram, an exclusive scan over the keys in descending order, a scatter), O(N)
+// for any N.  Counts of kOrderKeys - 1 or more share the top key; ties land in any order,
+// which only decides which CTA claims an item first -- every item computes the same result
+// on any CTA.
+//
+// Cuts.  The grid runs about L = Hv * (all chunks) / grid chunks per CTA; a sequence longer
+// than 1.05 L (and of at least kCutMinChunks chunks) would hold its CTAs well past the others,
+// so up to `max_cuts` of the longest such sequences are cut after a = max(ceil(c / 2), ceil(L))
+// of their c chunks.  Each cut adds the tail's identity pass (the tail's chunks once more) and
+// shortens the longest chain from c to a; the combine kernel finishes the tail.  A cut needs
+// room for its tail's y rows (ytok_max rows in all).  The cuts depend only on the sequence
+// lengths, Hv, the grid and the workspace size, so pool and dense calls cut alike.
 constexpr int kOrderKeys = 1024;
-__device__ __forceinline__ int order_key(const int32_t* cu, int n, int64_t T) {
+constexpr int kMaxCuts = 4;
+constexpr int kCutMinChunks = 8;
+constexpr uint32_t kCodeN = 0x0FFFFFFFu;
+
+__device__ __forceinline__ int64_t seq_len_checked(const int32_t* cu, int n, int64_t T) {
   const int64_t a = cu[n], b = cu[n + 1];
-  const int64_t len = (a >= 0 && b >= a && b <= T) ? b - a : 0;  // bad bounds: checked later
-  return (int)min((len + kC - 1) / kC, (int64_t)(kOrderKeys - 1));
+  return (a >= 0 && b >= a && b <= T) ? b - a : 0;  // bad bounds: reported by the prefill
 }
-__global__ void __launch_bounds__(kOrderKeys) kda_order_kernel(const int32_t* __restrict__ cu, int N,
-                                                               int64_t T, int32_t* __restrict__ order) {
-  __shared__ int cnt[kOrderKeys];
-  __shared__ int wsum[kOrderKeys / 32];
+__device__ __forceinline__ int64_t chunks_of(const int32_t* cu, int n, int64_t T) {
+  return (seq_len_checked(cu, n, T) + kC - 1) / kC;
+}
+__device__ __forceinline__ int order_key(int64_t chunks) {
+  return (int)min(chunks, (int64_t)(kOrderKeys - 1));
+}
+// Exclusive scan over the keys in descending order: cnt[k] becomes the first position of
+// key k in the list.  Thread t holds key kOrderKeys-1-t.
+__device__ void scan_keys_desc(int* cnt, int* wsum) {
   const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
-  cnt[t] = 0;
-  __syncthreads();
-  for (int n = t; n < N; n += kOrderKeys) atomicAdd(&cnt[order_key(cu, n, T)], 1);
-  __syncthreads();
-  // thread t holds key kOrderKeys-1-t: an exclusive scan over threads counts the
-  // sequences with a larger key, i.e. the first position of key kb in the order
   const int kb = kOrderKeys - 1 - t;
   const int c = cnt[kb];
   int x = c;
@@ -1408,7 +1483,243 @@ __global__ void __launch_bounds__(kOrderKeys) kda_order_kernel(const int32_t* __
   __syncthreads();
   cnt[kb] = x - c + (wp > 0 ? wsum[wp - 1] : 0);
   __syncthreads();
-  for (int n = t; n < N; n += kOrderKeys) order[atomicAdd(&cnt[order_key(cu, n, T)], 1)] = n;
+}
+
+__global__ void __launch_bounds__(kOrderKeys) kda_plan_kernel(const int32_t* __restrict__ cu, int N,
+                                                              int64_t T, int Hv, int grid, int max_cuts,
+                                                              int ytok_max, uint32_t* __restrict__ work,
+                                                              SplitInfo* __restrict__ splits,
+                                                              WsHeader* __restrict__ hdr) {
+  __shared__ int cnt[kOrderKeys];
+  __shared__ int wsum[kOrderKeys / 32];
+  __shared__ unsigned long long total;
+  __shared__ int cut_n[kMaxCuts], cut_a[kMaxCuts], ncut;
+  const int t = threadIdx.x;
+  cnt[t] = 0;
+  if (t == 0) total = 0ull;
+  __syncthreads();
+  unsigned long long mine = 0;
+  for (int n = t; n < N; n += kOrderKeys) {
+    const int64_t c = chunks_of(cu, n, T);
+    mine += (unsigned long long)c;
+    atomicAdd(&cnt[order_key(c)], 1);
+  }
+  atomicAdd(&total, mine);
+  __syncthreads();
+  scan_keys_desc(cnt, wsum);
+  for (int n = t; n < N; n += kOrderKeys) work[atomicAdd(&cnt[order_key(chunks_of(cu, n, T))], 1)] = (uint32_t)n;
+  __syncthreads();
+  if (t == 0) {  // the cuts, longest sequence first
+    int nc = 0, ytok = 0;
+    const double L = (double)Hv * (double)total / (double)grid;
+    for (int i = 0; i < N && nc < max_cuts; ++i) {
+      const int n = (int)work[i];
+      const int64_t c = chunks_of(cu, n, T);
+      if (c < kCutMinChunks) break;
+      if ((double)c <= 1.05 * L) {
+        if (order_key(c) < kOrderKeys - 1) break;  // sorted exactly below the top key
+        continue;
+      }
+      const int64_t a = max((c + 1) / 2, (int64_t)ceil(L));
+      if (a >= c) continue;
+      const int64_t tail = seq_len_checked(cu, n, T) - a * kC;
+      if ((int64_t)ytok + tail > (int64_t)ytok_max) continue;
+      splits[nc] = SplitInfo{n, (int32_t)a, ytok, (int32_t)tail};
+      cut_n[nc] = n;
+      cut_a[nc] = (int)a;
+      ytok += (int)tail;
+      ++nc;
+    }
+    ncut = nc;
+    hdr->num_splits = (uint32_t)nc;
+    hdr->num_entries = (uint32_t)(N + 2 * nc);
+  }
+  __syncthreads();
+  if (ncut == 0) return;  // the sequence order stands
+  // the list again with the cut sequences' three entries (head; tail; tail identity pass)
+  cnt[t] = 0;
+  __syncthreads();
+  const int nc = ncut;
+  auto cut_of = [&](int n) -> int {
+    for (int i = 0; i < nc; ++i)
+      if (cut_n[i] == n) return i;
+    return -1;
+  };
+  for (int n = t; n < N; n += kOrderKeys) {
+    const int64_t c = chunks_of(cu, n, T);
+    const int i = cut_of(n);
+    if (i < 0) {
+      atomicAdd(&cnt[order_key(c)], 1);
+    } else {
+      atomicAdd(&cnt[order_key(cut_a[i])], 1);
+      atomicAdd(&cnt[order_key(c - cut_a[i])], 2);
+    }
+  }
+  __syncthreads();
+  scan_keys_desc(cnt, wsum);
+  for (int n = t; n < N; n += kOrderKeys) {
+    const int64_t c = chunks_of(cu, n, T);
+    const int i = cut_of(n);
+    if (i < 0) {
+      work[atomicAdd(&cnt[order_key(c)], 1)] = (uint32_t)n;
+    } else {
+      work[atomicAdd(&cnt[order_key(cut_a[i])], 1)] = (uint32_t)n | ((uint32_t)KIND_HEAD << 28);
+      const int k = order_key(c - cut_a[i]);
+      const int pos = atomicAdd(&cnt[k], 2);
+      work[pos] = (uint32_t)n | ((uint32_t)KIND_TAIL << 28);
+      work[pos + 1] = (uint32_t)n | ((uint32_t)KIND_TAIL_ID << 28);
+    }
+  }
+}
+
+// ---- combine: completes the tails of the cut sequences --------------------------------------
+// For cut s and v-head h, with S_p the head's final state, M and S_loc the final states of the
+// tail's identity and zero-start passes, and y the identity pass's outputs:
+//   o_t += S_p^T y_t          for every tail token t (bf16 warp MMAs, fp32 sums, o re-rounded)
+//   S_end = M S_p + S_loc     into the pool row or the dense final state (fp32 FMAs)
+// Units: (cut, head, group of kCombTok tail tokens) for o and (cut, head) for the state, over
+// a grid that leaves at once when the planning kernel made no cut.
+constexpr int kCombThreads = 256;
+constexpr int kCombTok = 256;
+constexpr int kCombPitch = 136;  // bf16 row pitch of the staged tiles (conflict-free fragments)
+constexpr uint32_t kCombSmem = (128 + 64) * kCombPitch * 2;
+
+struct CombineParams {
+  const WsHeader* hdr;
+  const SplitInfo* splits;
+  const float *sp, *sl, *mm;
+  const __nv_bfloat16* y;
+  __nv_bfloat16* o;
+  const int32_t *cu, *idx;
+  void* state_out;
+  int32_t Hv;
+  int64_t num_slots, slot_stride;
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9},"
+      " {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <typename ST>
+__global__ void __launch_bounds__(kCombThreads) kda_combine_kernel(const __grid_constant__ CombineParams p) {
+  const int ns = (int)p.hdr->num_splits;
+  if (ns == 0) return;
+  extern __shared__ __align__(16) uint8_t csm[];
+  __nv_bfloat16* spT = reinterpret_cast<__nv_bfloat16*>(csm);           // [v][k], S_p^T
+  __nv_bfloat16* yt = spT + 128 * kCombPitch;                            // [64 tokens][k]
+  float* fs = reinterpret_cast<float*>(csm);                             // state units
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Hv = p.Hv;
+  int total = 0;
+  for (int i = 0; i < ns; ++i) total += ((p.splits[i].ntok + kCombTok - 1) / kCombTok + 1) * Hv;
+  for (int u = blockIdx.x; u < total; u += gridDim.x) {
+    int si = 0, r = u;
+    for (; si < ns; ++si) {
+      const int per = ((p.splits[si].ntok + kCombTok - 1) / kCombTok + 1) * Hv;
+      if (r < per) break;
+      r -= per;
+    }
+    const SplitInfo sp = p.splits[si];
+    const int ngrp = (sp.ntok + kCombTok - 1) / kCombTok;
+    const size_t so = ((size_t)si * Hv) * 16384;
+    __syncthreads();  // the smem of the previous unit is no longer read
+    if (r < ngrp * Hv) {
+      // ---- o of tail tokens [g * kCombTok, ...) of head h
+      const int h = r % Hv, g = r / Hv;
+      const float* S = p.sp + so + (size_t)h * 16384;  // [k][v]
+      for (int e = tid; e < 16384; e += kCombThreads) {
+        const int k = e >> 7, v = e & 127;
+        spT[v * kCombPitch + k] = __float2bfloat16_rn(S[e]);
+      }
+      const int64_t tail0 = (int64_t)p.cu[sp.n] + (int64_t)sp.cut * kC;  // first tail token
+      const int t_end = min(sp.ntok, (g + 1) * kCombTok);
+      for (int tb = g * kCombTok; tb < t_end; tb += 64) {
+        const int nt = min(64, t_end - tb);
+        __syncthreads();
+        for (int e = tid; e < 64 * 16; e += kCombThreads) {  // 16-byte pieces of y rows
+          const int row = e >> 4, c8 = (e & 15) * 8;
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (row < nt)
+            w = *reinterpret_cast<const uint4*>(p.y + ((size_t)(sp.ytok0 + tb + row) * Hv + h) * 128 + c8);
+          *reinterpret_cast<uint4*>(yt + row * kCombPitch + c8) = w;
+        }
+        __syncthreads();
+        const int r0 = (warp & 3) * 16, n0 = (warp >> 2) * 64;
+        const int gq = lane >> 2, tq = lane & 3;
+        float acc[8][4] = {};
+#pragma unroll
+        for (int kb = 0; kb < 128; kb += 16) {
+          uint32_t a[4];
+          a[0] = *reinterpret_cast<const uint32_t*>(yt + (r0 + gq) * kCombPitch + kb + 2 * tq);
+          a[1] = *reinterpret_cast<const uint32_t*>(yt + (r0 + gq + 8) * kCombPitch + kb + 2 * tq);
+          a[2] = *reinterpret_cast<const uint32_t*>(yt + (r0 + gq) * kCombPitch + kb + 2 * tq + 8);
+          a[3] = *reinterpret_cast<const uint32_t*>(yt + (r0 + gq + 8) * kCombPitch + kb + 2 * tq + 8);
+#pragma unroll
+          for (int nt8 = 0; nt8 < 8; ++nt8) {
+            const __nv_bfloat16* bp = spT + (n0 + nt8 * 8 + gq) * kCombPitch + kb + 2 * tq;
+            mma_bf16_16816(acc[nt8], a, *reinterpret_cast<const uint32_t*>(bp),
+                           *reinterpret_cast<const uint32_t*>(bp + 8));
+          }
+        }
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int row = r0 + gq + hr * 8;
+          if (row < nt) {
+            __nv_bfloat16* orow = p.o + ((size_t)(tail0 + tb + row) * Hv + h) * 128;
+#pragma unroll
+            for (int nt8 = 0; nt8 < 8; ++nt8) {
+              const int col = n0 + nt8 * 8 + 2 * tq;
+              __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(orow + col);
+              const float2 cur = __bfloat1622float2(*op);
+              *op = __floats2bfloat162_rn(cur.x + acc[nt8][hr * 2], cur.y + acc[nt8][hr * 2 + 1]);
+            }
+          }
+        }
+      }
+    } else {
+      // ---- final state of head h: S_end = M S_p + S_loc
+      const int h = r - ngrp * Hv;
+      ST* dst = nullptr;
+      if (p.state_out) {
+        if (p.idx) {
+          const int64_t sl = resolve_slot(p.idx, sp.n, p.num_slots);
+          if (sl >= 0) dst = static_cast<ST*>(p.state_out) + sl * p.slot_stride + (size_t)h * 16384;
+        } else {
+          dst = static_cast<ST*>(p.state_out) + ((size_t)sp.n * Hv + h) * 16384;
+        }
+      }
+      if (!dst) continue;
+      const float* M = p.mm + so + (size_t)h * 16384;
+      const float* S = p.sp + so + (size_t)h * 16384;
+      const float* SL = p.sl + so + (size_t)h * 16384;
+      const int v = tid & 127, k0 = (tid >> 7) * 64;
+      float acc[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = SL[(size_t)(k0 + i) * 128 + v];
+      float* Ms = fs;              // [128 k][32 j]
+      float* Ss = fs + 128 * 32;   // [32 j][128 v]
+      for (int j0 = 0; j0 < 128; j0 += 32) {
+        __syncthreads();
+        for (int e = tid; e < 128 * 32; e += kCombThreads) {
+          Ms[e] = M[(size_t)(e >> 5) * 128 + j0 + (e & 31)];
+          Ss[e] = S[(size_t)(j0 + (e >> 7)) * 128 + (e & 127)];
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int j = 0; j < 32; ++j) {
+          const float sv = Ss[j * 128 + v];
+#pragma unroll
+          for (int i = 0; i < 64; ++i) acc[i] = fmaf(Ms[(k0 + i) * 32 + j], sv, acc[i]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 64; ++i) dst[(size_t)(k0 + i) * 128 + v] = from_f32<ST>(acc[i]);
+    }
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
@@ -1474,7 +1785,43 @@ bool prefill_tc_supported(const kda_desc_t& d) {
          ((d.flags & KDA_FLAG_SCALAR_GATE) == 0u || d.num_v_heads % 8 == 0);
 }
 
-size_t prefill_tc_workspace(const kda_desc_t& d) { return (size_t)d.num_seqs * sizeof(int32_t); }
+namespace {
+// Workspace after the 256-byte header: the work list (one 32-bit entry per sequence plus two
+// per cut), then, when cuts are allowed, the cut records, the head / tail / identity-pass
+// final states (fp32 [cuts][Hv][K][V] each) and the y rows of the tails ([rows][Hv][K] bf16).
+struct WsLayout {
+  size_t work, splits, sp, sl, mm, y, end;
+};
+WsLayout ws_layout(const kda_desc_t& d, int cuts, int64_t ytok) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  WsLayout L;
+  size_t off = kWsPayload;
+  L.work = off;
+  off += up(sizeof(uint32_t) * ((size_t)d.num_seqs + 2 * (size_t)cuts));
+  L.splits = off;
+  off += up(sizeof(SplitInfo) * (size_t)cuts);
+  const size_t st = (size_t)cuts * d.num_v_heads * kK * kV * sizeof(float);
+  L.sp = off;
+  off += st;
+  L.sl = off;
+  off += st;
+  L.mm = off;
+  off += st;
+  L.y = off;
+  off += up((size_t)ytok * d.num_v_heads * kK * sizeof(__nv_bfloat16));
+  L.end = off;
+  return L;
+}
+// Cut capacity of a workspace of the full size: up to kMaxCuts sequences, tails of up to
+// 8192 tokens in all.
+int full_cuts(const kda_desc_t& d) { return (int)std::min<int64_t>(d.num_seqs, kMaxCuts); }
+int64_t full_ytok(const kda_desc_t& d) { return std::min<int64_t>(d.total_tokens, 8192); }
+}  // namespace
+
+size_t prefill_tc_workspace(const kda_desc_t& d) {
+  return ws_layout(d, full_cuts(d), full_ytok(d)).end - kWsPayload;
+}
+size_t prefill_tc_min_workspace(const kda_desc_t& d) { return ws_layout(d, 0, 0).end - kWsPayload; }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   const kda_desc_t& d = a.d;
@@ -1500,7 +1847,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
                                    d.num_v_heads, kK, kK, CU_TENSOR_MAP_SWIZZLE_NONE)))
       return cudaErrorInvalidValue;
   }
-  int32_t* order = reinterpret_cast<int32_t*>(a.ws + kWsPayload);
+  // cuts only with a workspace of the full size (a smaller one, down to the minimum, runs
+  // every sequence whole)
+  const WsLayout full = ws_layout(d, full_cuts(d), full_ytok(d));
+  const bool can_cut = a.ws_bytes >= full.end && d.num_seqs < (int)kCodeN;
+  const WsLayout L = can_cut ? full : ws_layout(d, 0, 0);
+  p.work = reinterpret_cast<const uint32_t*>(a.ws + L.work);
+  p.splits = reinterpret_cast<const SplitInfo*>(a.ws + L.splits);
+  p.hdr = reinterpret_cast<const WsHeader*>(a.ws);
+  p.sp = reinterpret_cast<float*>(a.ws + L.sp);
+  p.sl = reinterpret_cast<float*>(a.ws + L.sl);
+  p.mm = reinterpret_cast<float*>(a.ws + L.mm);
+  p.y = reinterpret_cast<__nv_bfloat16*>(a.ws + L.y);
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.k = static_cast<const __nv_bfloat16*>(a.k);
   p.g = a.g;
@@ -1512,7 +1870,6 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   p.beta = a.beta;
   p.cu = a.cu;
   p.idx = a.idx;
-  p.order = order;
   p.state_in = a.state_in;
   p.state_out = a.state_out;
   p.o = static_cast<__nv_bfloat16*>(a.o);
@@ -1521,26 +1878,58 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   p.N = d.num_seqs;
   p.Hk = d.num_k_heads;
   p.Hv = d.num_v_heads;
-  p.num_items = d.num_seqs * d.num_v_heads;
   p.T = T;
   p.num_slots = d.num_slots;
   p.slot_stride = a.slot_stride;
   p.scale = a.scale;
 
-  kda_order_kernel<<<1, kOrderKeys, 0, st>>>(a.cu, d.num_seqs, T, order);
+  const int max_cuts = can_cut ? full_cuts(d) : 0;
+  const int64_t max_items = ((int64_t)d.num_seqs + 2 * max_cuts) * d.num_v_heads;
+  const int grid = (int)std::min<int64_t>(sm_count(), std::max<int64_t>(1, max_items));
+  kda_plan_kernel<<<1, kOrderKeys, 0, st>>>(a.cu, d.num_seqs, T, d.num_v_heads, grid, max_cuts,
+                                            can_cut ? (int)full_ytok(d) : 0,
+                                            reinterpret_cast<uint32_t*>(a.ws + L.work),
+                                            reinterpret_cast<SplitInfo*>(a.ws + L.splits),
+                                            reinterpret_cast<WsHeader*>(a.ws));
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const int grid = std::min(sm_count(), std::max(1, p.num_items));
+  CombineParams cp;
+  cp.hdr = p.hdr;
+  cp.splits = p.splits;
+  cp.sp = p.sp;
+  cp.sl = p.sl;
+  cp.mm = p.mm;
+  cp.y = p.y;
+  cp.o = p.o;
+  cp.cu = p.cu;
+  cp.idx = p.idx;
+  cp.state_out = p.state_out;
+  cp.Hv = d.num_v_heads;
+  cp.num_slots = d.num_slots;
+  cp.slot_stride = a.slot_stride;
+  const int cgrid = 2 * sm_count();
   if (d.state_dtype == KDA_BF16) {
     auto kern = kda_prefill_tc_kernel<__nv_bfloat16>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (err != cudaSuccess) return err;
     kern<<<grid, kThreads, kSmemBytes, st>>>(p);
+    if (max_cuts > 0) {
+      auto comb = kda_combine_kernel<__nv_bfloat16>;
+      err = cudaFuncSetAttribute(comb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCombSmem);
+      if (err != cudaSuccess) return err;
+      comb<<<cgrid, kCombThreads, kCombSmem, st>>>(cp);
+    }
   } else {
     auto kern = kda_prefill_tc_kernel<float>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (err != cudaSuccess) return err;
     kern<<<grid, kThreads, kSmemBytes, st>>>(p);
+    if (max_cuts > 0) {
+      auto comb = kda_combine_kernel<float>;
+      err = cudaFuncSetAttribute(comb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCombSmem);
+      if (err != cudaSuccess) return err;
+      comb<<<cgrid, kCombThreads, kCombSmem, st>>>(cp);
+    }
   }
   return cudaGetLastError();
 }
