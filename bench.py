@@ -531,7 +531,9 @@ def run_ours(args, dist, ws, rank, local):
                         "indices in and reads o back; steps are pipelined over two device input "
                         "sets (copies of step i+1 and the read-back of step i-1 overlap the "
                         "prefill of step i); the state pool stays resident on the device"},
-        "gpu_launches": args.steps * (2 if path == 1 else 1),
+        # tensor-core path: planning + prefill + combine (the combine returns at once when
+        # nothing was cut); CUDA-core path: the prefill
+        "gpu_launches": args.steps * (3 if path == 1 else 1),
         "device_status": bits, "wall_s": wall,
     }
     if ws == 1 and not args.no_cpu_baseline:

@@ -79,6 +79,16 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
                                           tensor-core kernel re-rounds them to bf16 as the
                                           caller's normalise-then-cast does). */
 
+#define KDA_FLAG_STATE_VK        0x8u  /* prefill and decode: every state buffer (pool, dense
+                                          initial / final states, draft-step cache) holds each
+                                          head's state transposed, [V][K] (row v is the state's
+                                          column v), the [num_slots, Hv, head_v_dim, head_k_dim]
+                                          pool of the pages' GDN test (PR 30169 digest, 关键源码
+                                          片段).  Default: [K][V].  The prefill runs the same
+                                          arithmetic either way (results bit-identical to the
+                                          default layout's, transposed); the decode reduces over
+                                          the key channels in another order. */
+
 /* Problem descriptor shared by prefill and decode. */
 typedef struct {
     int32_t num_seqs;          /* N (prefill: packed sequences; decode: rows)          */
@@ -274,6 +284,19 @@ kda_status_t kda_chunk_prefill_noalloc(const kda_desc_t *desc, const void *q, co
                                        const int32_t *cu_seqlens, void *state,
                                        const int32_t *state_indices, void *final_state,
                                        void *o, cudaStream_t stream);
+
+/*
+ * Bound of the internal pipeline waits of the tensor-core prefill, for launches made
+ * after the call (process-wide; 0 restores the default of 2 seconds; more than 2 s is
+ * KDA_ERR_INVALID_ARGUMENT).  The pages have no counterpart: it is the watchdog of this
+ * library's own kernels.  Every wait between the kernel's producer and consumer warps
+ * gives up after this long; the kernel then sets KDA_DEVICE_PIPE_TIMEOUT, stops taking
+ * work, lets the loads and matrix operations it issued finish (those last waits keep the
+ * full 2 s bound) and returns -- it never traps.  Outputs of such a call are unspecified;
+ * the next call starts clean.  A bound far below a chunk's latency (a microsecond or
+ * less) makes the waits give up on purpose, which is how the failure path is tested.
+ */
+kda_status_t kda_set_pipeline_wait_limit(uint64_t nanoseconds);
 
 /* Synchronises `stream`, then reads the device status word left in `workspace`
  * by the last prefill or decode call that used it.  Returns KDA_OK or

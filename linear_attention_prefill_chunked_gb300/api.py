@@ -20,6 +20,7 @@ KDA_BF16, KDA_F32 = 0, 1
 KDA_FLAG_CUDA_CORE_PATH = 0x1
 KDA_FLAG_SCALAR_GATE = 0x2
 KDA_FLAG_QK_L2NORM = 0x4
+KDA_FLAG_STATE_VK = 0x8
 KDA_DEVICE_BAD_SLOT, KDA_DEVICE_BAD_SEQLENS, KDA_DEVICE_PIPE_TIMEOUT = 0x1, 0x2, 0x4
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
            3: "workspace too small", 4: "CUDA error", 5: "invalid device data"}
@@ -53,7 +54,8 @@ class KdaDesc(ctypes.Structure):
 EXPORTS = ("kda_chunk_prefill_workspace_size", "kda_chunk_prefill_min_workspace_size",
            "kda_decode_workspace_size", "kda_chunk_prefill",
            "kda_decode", "kda_read_device_status", "kda_chunk_prefill_path", "kda_status_string",
-           "kda_chunk_prefill_noalloc", "kda_chunk_prefill_act", "kda_decode_draft")
+           "kda_chunk_prefill_noalloc", "kda_chunk_prefill_act", "kda_decode_draft",
+           "kda_set_pipeline_wait_limit")
 
 _lib = None
 
@@ -98,6 +100,8 @@ def load(build_if_missing: bool = True):
     lib.kda_decode_draft.argtypes = [D, P, P, P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int32,
                                      ctypes.c_int, P, P, ctypes.c_size_t, P]
     lib.kda_decode_draft.restype = ctypes.c_int
+    lib.kda_set_pipeline_wait_limit.argtypes = [ctypes.c_uint64]
+    lib.kda_set_pipeline_wait_limit.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -156,14 +160,23 @@ def _pool_shape(pool, name, Hv, K, V, slot_stride):
         raise ValueError(f"{name} is too small for {pool.shape[0]} slots of pitch {slot_stride}")
 
 
+def _state_dims(K, V, state_layout):
+    """Trailing dims of one head's state: (K, V), or (V, K) for the transposed layout."""
+    if state_layout not in ("kv", "vk"):
+        raise ValueError(f"state_layout must be 'kv' or 'vk', got {state_layout!r}")
+    return (K, V) if state_layout == "kv" else (V, K)
+
+
 def check_prefill_shapes(q, k, v, gate, beta, cu_seqlens, *, state=None, state_indices=None,
-                         final_state=None, out=None, A_log=None, dt_bias=None, slot_stride=0):
+                         final_state=None, out=None, A_log=None, dt_bias=None, slot_stride=0,
+                         state_layout="kv"):
     """Shape checks of a prefill call (host only; see :func:`chunk_prefill`)."""
     _shape(q, "q", (None, None, None))
     T, Hk, K = q.shape
     _shape(k, "k", (T, Hk, K))
     _shape(v, "v", (T, None, None))
     Hv, V = v.shape[1], v.shape[2]
+    SA, SB = _state_dims(K, V, state_layout)
     if Hk == 0 or Hv % Hk != 0:
         raise ValueError(f"the v-head count {Hv} must be a multiple of the k-head count {Hk}")
     _gate_shape(gate, "g" if A_log is None else "a", T, Hv, K)
@@ -177,12 +190,12 @@ def check_prefill_shapes(q, k, v, gate, beta, cu_seqlens, *, state=None, state_i
     if state_indices is not None:
         _shape(state_indices, "state_indices", (N,))
         if state is not None:
-            _pool_shape(state, "state", Hv, K, V, slot_stride)
+            _pool_shape(state, "state", Hv, SA, SB, slot_stride)
     else:
         if state is not None:
-            _shape(state, "state", (N, Hv, K, V))
+            _shape(state, "state", (N, Hv, SA, SB))
         if final_state is not None:
-            _shape(final_state, "final_state", (N, Hv, K, V))
+            _shape(final_state, "final_state", (N, Hv, SA, SB))
         # the kernels write the final state in the element type of the initial one: a
         # final_state of another dtype would be written past its end (or only half filled)
         if state is not None and final_state is not None and state.dtype != final_state.dtype:
@@ -194,7 +207,7 @@ def check_prefill_shapes(q, k, v, gate, beta, cu_seqlens, *, state=None, state_i
 
 
 def check_decode_shapes(q, k, v, g, beta, pool, *, state_indices=None, out=None, slot_stride=0,
-                        cu_seqlens=None):
+                        cu_seqlens=None, state_layout="kv"):
     """Shape checks of a decode call (one row per token, or draft steps per request when
     ``cu_seqlens`` is given; host only)."""
     _shape(q, "q", (None, None, None))
@@ -206,7 +219,7 @@ def check_decode_shapes(q, k, v, g, beta, pool, *, state_indices=None, out=None,
         raise ValueError(f"the v-head count {Hv} must be a multiple of the k-head count {Hk}")
     _gate_shape(g, "g", T, Hv, K)
     _shape(beta, "beta", (None, Hv), min_rows=T)
-    _pool_shape(pool, "pool", Hv, K, V, slot_stride)
+    _pool_shape(pool, "pool", Hv, *_state_dims(K, V, state_layout), slot_stride)
     N = T
     if cu_seqlens is not None:
         _shape(cu_seqlens, "cu_seqlens", (None,), min_rows=1)
@@ -250,6 +263,14 @@ def prefill_path(desc: KdaDesc) -> int:
     return int(load().kda_chunk_prefill_path(ctypes.byref(desc)))
 
 
+def set_pipeline_wait_limit(nanoseconds: int = 0) -> None:
+    """Bound of the tensor-core prefill's internal waits for later launches (0: the default
+    2 s).  A timeout sets KDA_DEVICE_PIPE_TIMEOUT in the device status; the call returns."""
+    rc = load().kda_set_pipeline_wait_limit(int(nanoseconds))
+    if rc != 0:
+        raise KdaError(rc, "kda_set_pipeline_wait_limit")
+
+
 def read_device_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronise the stream and return the device status bits of the last call."""
     bits = ctypes.c_uint32(0)
@@ -261,7 +282,8 @@ def read_device_status(workspace: torch.Tensor, stream=None) -> int:
 
 def chunk_prefill(q, k, v, g, beta, cu_seqlens, *, state=None, state_indices=None,
                   final_state=None, output_final_state=True, scale=None, slot_stride=0,
-                  out=None, workspace=None, stream=None, cuda_core_path=False, qk_l2norm=False):
+                  out=None, workspace=None, stream=None, cuda_core_path=False, qk_l2norm=False,
+                  state_layout="kv"):
     """Chunked KDA prefill.  Returns ``(o, final)``.
 
     q, k [T, Hk, K]; v [T, Hv, V] (bf16 or fp32, same dtype); g [>=T, Hv, K] fp32, or
@@ -272,18 +294,19 @@ def chunk_prefill(q, k, v, g, beta, cu_seqlens, *, state=None, state_indices=Non
     Dense mode: ``state`` is h0 [N, Hv, K, V] or None; ``final`` is a new
     [N, Hv, K, V] tensor (or ``final_state`` if given, may be ``state``) or None
     when ``output_final_state`` is False.  ``qk_l2norm`` normalises q and k per
-    (token, head) inside the kernel (KDA_FLAG_QK_L2NORM).
+    (token, head) inside the kernel (KDA_FLAG_QK_L2NORM).  ``state_layout="vk"`` stores every
+    head's state transposed, [V, K] (the pages' pool layout; KDA_FLAG_STATE_VK).
     """
     _need(g, "g", torch.float32)
     return _prefill(q, k, v, g, None, beta, cu_seqlens, state, state_indices, final_state,
                     output_final_state, scale, slot_stride, out, workspace, stream,
-                    cuda_core_path, chunk_prefill, qk_l2norm)
+                    cuda_core_path, chunk_prefill, qk_l2norm, state_layout)
 
 
 def chunk_prefill_act(q, k, v, a, A_log, dt_bias, beta, cu_seqlens, *, lower_bound=None,
                       state=None, state_indices=None, final_state=None, output_final_state=True,
                       scale=None, slot_stride=0, out=None, workspace=None, stream=None,
-                      cuda_core_path=False, qk_l2norm=False):
+                      cuda_core_path=False, qk_l2norm=False, state_layout="kv"):
     """Chunked KDA prefill with the gate computed in the kernel (kda_chunk_prefill_act):
     ``g = max(-exp(A_log[h]) * softplus(a + dt_bias[h]), lower_bound)``.
 
@@ -298,12 +321,12 @@ def chunk_prefill_act(q, k, v, a, A_log, dt_bias, beta, cu_seqlens, *, lower_bou
     lb = float("-inf") if lower_bound is None else float(lower_bound)
     return _prefill(q, k, v, None, (a, A_log, dt_bias, lb), beta, cu_seqlens, state,
                     state_indices, final_state, output_final_state, scale, slot_stride, out,
-                    workspace, stream, cuda_core_path, chunk_prefill_act, qk_l2norm)
+                    workspace, stream, cuda_core_path, chunk_prefill_act, qk_l2norm, state_layout)
 
 
 def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_state,
              output_final_state, scale, slot_stride, out, workspace, stream, cuda_core_path,
-             owner, qk_l2norm=False):
+             owner, qk_l2norm=False, state_layout="kv"):
     lib = load()
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need(t, name)
@@ -317,7 +340,8 @@ def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_stat
     check_prefill_shapes(q, k, v, g if act is None else act[0], beta, cu_seqlens, state=state,
                          state_indices=state_indices, final_state=final_state, out=out,
                          A_log=None if act is None else act[1],
-                         dt_bias=None if act is None else act[2], slot_stride=slot_stride)
+                         dt_bias=None if act is None else act[2], slot_stride=slot_stride,
+                         state_layout=state_layout)
     T, Hk, K = q.shape
     Hv, V = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
@@ -335,7 +359,8 @@ def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_stat
         if state is not None:
             _need(state, "state")
         if final_state is None and output_final_state:
-            final_state = torch.empty((N, Hv, K, V), dtype=sdt, device=q.device)
+            final_state = torch.empty((N, Hv, *_state_dims(K, V, state_layout)), dtype=sdt,
+                                      device=q.device)
     if state is not None and not pool:
         _need(state, "state")
     gate = g if act is None else act[0]
@@ -344,7 +369,8 @@ def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_stat
                   state_dtype=sdt, scale=scale, num_slots=num_slots, slot_stride=slot_stride,
                   flags=(KDA_FLAG_CUDA_CORE_PATH if cuda_core_path else 0)
                   | (KDA_FLAG_SCALAR_GATE if scalar else 0)
-                  | (KDA_FLAG_QK_L2NORM if qk_l2norm else 0))
+                  | (KDA_FLAG_QK_L2NORM if qk_l2norm else 0)
+                  | (KDA_FLAG_STATE_VK if state_layout == "vk" else 0))
     if out is None:
         out = torch.empty((T, Hv, V), dtype=q.dtype, device=q.device)
     ws_size = lib.kda_chunk_prefill_workspace_size(ctypes.byref(d))
@@ -375,8 +401,9 @@ def _prefill(q, k, v, g, act, beta, cu_seqlens, state, state_indices, final_stat
 
 
 def decode(q, k, v, g, beta, pool, state_indices=None, *, scale=None, slot_stride=0, out=None,
-           workspace=None, stream=None, qk_l2norm=False):
-    """One-token-per-row decode, updating ``pool`` [num_slots, Hv, K, V] in place.  Returns o.
+           workspace=None, stream=None, qk_l2norm=False, state_layout="kv"):
+    """One-token-per-row decode, updating ``pool`` [num_slots, Hv, K, V] (or [.., V, K] with
+    ``state_layout="vk"``) in place.  Returns o.
 
     g [>=N, Hv, K] fp32, or [>=N, Hv] for a scalar (per row and head, GDN) gate."""
     lib = load()
@@ -389,14 +416,15 @@ def decode(q, k, v, g, beta, pool, state_indices=None, *, scale=None, slot_strid
     if out is not None:
         _need(out, "out")
     check_decode_shapes(q, k, v, g, beta, pool, state_indices=state_indices, out=out,
-                        slot_stride=slot_stride)
+                        slot_stride=slot_stride, state_layout=state_layout)
     N, Hk, K = q.shape
     Hv, V = v.shape[1], v.shape[2]
     d = make_desc(num_seqs=N, total_tokens=N, Hk=Hk, Hv=Hv, K=K, V=V, qkv_dtype=q.dtype,
                   state_dtype=pool.dtype, scale=scale, num_slots=pool.shape[0],
                   slot_stride=slot_stride,
                   flags=(KDA_FLAG_SCALAR_GATE if g.dim() == 2 else 0)
-                  | (KDA_FLAG_QK_L2NORM if qk_l2norm else 0))
+                  | (KDA_FLAG_QK_L2NORM if qk_l2norm else 0)
+                  | (KDA_FLAG_STATE_VK if state_layout == "vk" else 0))
     if out is None:
         out = torch.empty((N, Hv, V), dtype=q.dtype, device=q.device)
     ws_size = lib.kda_decode_workspace_size(ctypes.byref(d))
@@ -415,7 +443,7 @@ def decode(q, k, v, g, beta, pool, state_indices=None, *, scale=None, slot_strid
 
 def decode_draft(q, k, v, g, beta, cu_seqlens, pool, state_indices=None, *, cache=None,
                  max_steps=None, update_pool=False, scale=None, slot_stride=0, out=None,
-                 workspace=None, stream=None, qk_l2norm=False):
+                 workspace=None, stream=None, qk_l2norm=False, state_layout="kv"):
     """Speculative draft steps (kda_decode_draft).  Request n runs its tokens
     cu_seqlens[n]..cu_seqlens[n+1]-1 from pool[slot n]; the state after step j goes to
     ``cache[n].view(-1)[j*Hv*K*V:(j+1)*Hv*K*V]`` when ``cache`` is given: a tensor whose
@@ -433,7 +461,7 @@ def decode_draft(q, k, v, g, beta, cu_seqlens, pool, state_indices=None, *, cach
     if out is not None:
         _need(out, "out")
     check_decode_shapes(q, k, v, g, beta, pool, state_indices=state_indices, out=out,
-                        slot_stride=slot_stride, cu_seqlens=cu_seqlens)
+                        slot_stride=slot_stride, cu_seqlens=cu_seqlens, state_layout=state_layout)
     T, Hk, K = q.shape
     Hv, V = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
@@ -454,7 +482,8 @@ def decode_draft(q, k, v, g, beta, cu_seqlens, pool, state_indices=None, *, cach
                   state_dtype=pool.dtype, scale=scale, num_slots=pool.shape[0],
                   slot_stride=slot_stride,
                   flags=(KDA_FLAG_SCALAR_GATE if g.dim() == 2 else 0)
-                  | (KDA_FLAG_QK_L2NORM if qk_l2norm else 0))
+                  | (KDA_FLAG_QK_L2NORM if qk_l2norm else 0)
+                  | (KDA_FLAG_STATE_VK if state_layout == "vk" else 0))
     if out is None:
         out = torch.empty((T, Hv, V), dtype=q.dtype, device=q.device)
     ws_size = lib.kda_decode_workspace_size(ctypes.byref(d))

@@ -1,8 +1,17 @@
 // kda_api.cu -- the extern "C" boundary: argument validation, workspace sizing,
 // dispatch to the tensor-core or CUDA-core prefill, decode, status readback.
+#include <atomic>
 #include <cmath>
 
 #include "kda_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace kda {
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{tc::kWaitLimitNs};
+}  // namespace
+uint64_t pipeline_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+}  // namespace kda
 
 namespace {
 
@@ -14,7 +23,8 @@ bool dims_ok(const kda_desc_t* d) {
   if (d->num_k_heads <= 0 || d->num_v_heads <= 0) return false;
   if (d->num_v_heads % d->num_k_heads != 0) return false;
   if (d->chunk_size != 64) return false;
-  if ((d->flags & ~(KDA_FLAG_CUDA_CORE_PATH | KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM)) != 0)
+  if ((d->flags & ~(KDA_FLAG_CUDA_CORE_PATH | KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM |
+                    KDA_FLAG_STATE_VK)) != 0)
     return false;
   if (!(d->qkv_dtype == KDA_BF16 || d->qkv_dtype == KDA_F32)) return false;
   if (!(d->state_dtype == KDA_BF16 || d->state_dtype == KDA_F32)) return false;
@@ -117,6 +127,7 @@ kda_status_t prefill_common(const kda_desc_t* d, const void* q, const void* k, c
   a.q = q; a.k = k; a.v = v; a.g = g; a.act = act; a.beta = beta; a.cu = cu_seqlens;
   a.gate_k = (d->flags & KDA_FLAG_SCALAR_GATE) ? 1 : d->head_k_dim;
   a.l2norm = (d->flags & KDA_FLAG_QK_L2NORM) != 0;
+  a.state_vk = (d->flags & KDA_FLAG_STATE_VK) != 0;
   a.state_in = state;
   a.idx = state_indices;
   a.state_out = pool ? state : final_state;
@@ -187,6 +198,7 @@ kda_status_t kda_decode(const kda_desc_t* d, const void* q, const void* k, const
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
   a.gate_k = (d->flags & KDA_FLAG_SCALAR_GATE) ? 1 : d->head_k_dim;
   a.l2norm = (d->flags & KDA_FLAG_QK_L2NORM) != 0;
+  a.state_vk = (d->flags & KDA_FLAG_STATE_VK) != 0;
   a.pool = state_pool;
   a.idx = state_indices;
   a.o = o;
@@ -232,6 +244,7 @@ kda_status_t kda_decode_draft(const kda_desc_t* d, const void* q, const void* k,
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
   a.gate_k = (d->flags & KDA_FLAG_SCALAR_GATE) ? 1 : d->head_k_dim;
   a.l2norm = (d->flags & KDA_FLAG_QK_L2NORM) != 0;
+  a.state_vk = (d->flags & KDA_FLAG_STATE_VK) != 0;
   a.pool = state_pool;
   a.idx = state_indices;
   a.o = o;
@@ -245,6 +258,13 @@ kda_status_t kda_decode_draft(const kda_desc_t* d, const void* q, const void* k,
   if (cudaMemsetAsync(workspace, 0, sizeof(kda::WsHeader), stream) != cudaSuccess)
     return KDA_ERR_CUDA;
   return kda::launch_decode(a, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_set_pipeline_wait_limit(uint64_t nanoseconds) {
+  if (nanoseconds > kda::tc::kWaitLimitNs) return KDA_ERR_INVALID_ARGUMENT;
+  kda::g_wait_limit_ns.store(nanoseconds == 0 ? kda::tc::kWaitLimitNs : nanoseconds,
+                             std::memory_order_relaxed);
+  return KDA_OK;
 }
 
 kda_status_t kda_read_device_status(const void* workspace, uint32_t* bits_out,

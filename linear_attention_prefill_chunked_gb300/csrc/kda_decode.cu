@@ -208,11 +208,150 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
   }
 }
 
+// The same step on states stored transposed (KDA_FLAG_STATE_VK: row v of a head's state
+// holds S[:, v], K contiguous values -- the layout of the pages' GDN pool test).  A CTA holds
+// VT state rows (value channels v0 ..) with all K key channels: TPR = K/4 threads cover one
+// row with 16-byte accesses, so both reductions over the key channels (S^T k, S^T q) are
+// shuffles within the row's threads, and u needs no exchange at all.
+template <typename QT, typename ST, int K, int VT>
+__global__ void __launch_bounds__(kDecThreads, 2)
+kda_decode_vk_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* __restrict__ v,
+                     const float* __restrict__ g, const float* __restrict__ beta,
+                     ST* __restrict__ pool, const int32_t* __restrict__ idx, QT* __restrict__ o,
+                     uint32_t* __restrict__ status, int Hk, int Hv, int V, int64_t num_slots,
+                     int64_t slot_stride, float scale, int gk, bool l2norm, DraftArgs dr, int64_t T) {
+  constexpr int TPR = K / 4;                // threads per row (16 or 32: within one warp)
+  constexpr int RG = kDecThreads / TPR;     // row groups
+  constexpr int RPT = VT / RG;              // rows per thread
+  static_assert(VT % RG == 0, "VT must split over the row groups");
+
+  const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * VT;
+  const int tid = threadIdx.x, rg = tid / TPR, col = (tid % TPR) * 4;
+
+  int64_t bos = n, eos = n + 1;
+  if (dr.cu != nullptr) {
+    if (!seq_bounds(dr.cu, n, T, &bos, &eos) || eos - bos > dr.max_steps) {
+      if (tid == 0 && blockIdx.z == 0 && h == 0) raise_status(status, KDA_DEVICE_BAD_SEQLENS);
+      return;
+    }
+  }
+  int64_t slot = n;
+  if (idx != nullptr) {
+    slot = resolve_slot(idx, n, num_slots);
+    if (slot < 0) {
+      if (tid == 0 && blockIdx.z == 0) raise_status(status, KDA_DEVICE_BAD_SLOT);
+      return;
+    }
+  } else if (slot >= num_slots) {
+    if (tid == 0 && blockIdx.z == 0) raise_status(status, KDA_DEVICE_BAD_SLOT);
+    return;
+  }
+
+  __shared__ float red_n[2][kDecThreads / 32];
+  __shared__ float kq_s[3][K];
+
+  const int kh = h / (Hv / Hk);
+  ST* S = pool + slot * slot_stride + (size_t)h * K * V + (size_t)v0 * K + col;
+  float s[RPT][4];
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) Vec4<ST>::load(S + (size_t)(rg + j * RG) * K, s[j]);
+
+  for (int64_t t = bos; t < eos; ++t) {
+    if (t > bos) __syncthreads();
+    float kv = 0.f, qv = 0.f;
+    if (tid < K) {
+      kv = to_f32(k[((size_t)t * Hk + kh) * K + tid]);
+      qv = to_f32(q[((size_t)t * Hk + kh) * K + tid]);
+      kq_s[2][tid] = expf(g[((size_t)t * Hv + h) * gk + (gk > 1 ? tid : 0)]);
+    }
+    float ik = 1.f, iq = 1.f;
+    if (l2norm) {
+      float sk = kv * kv, sq = qv * qv;
+#pragma unroll
+      for (int o2 = 16; o2; o2 >>= 1) {
+        sk += __shfl_xor_sync(0xffffffffu, sk, o2);
+        sq += __shfl_xor_sync(0xffffffffu, sq, o2);
+      }
+      if ((tid & 31) == 0) {
+        red_n[0][tid >> 5] = sk;
+        red_n[1][tid >> 5] = sq;
+      }
+      __syncthreads();
+      float tk = 0.f, tq = 0.f;
+#pragma unroll
+      for (int r = 0; r < K / 32; ++r) {
+        tk += red_n[0][r];
+        tq += red_n[1][r];
+      }
+      ik = 1.f / fmaxf(sqrtf(tk), 1e-12f);
+      iq = 1.f / fmaxf(sqrtf(tq), 1e-12f);
+    }
+    if (tid < K) {
+      kq_s[0][tid] = kv * ik;
+      kq_s[1][tid] = qv * iq;
+    }
+    __syncthreads();
+    float kr[4], qr[4], er[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      kr[i] = kq_s[0][col + i];
+      qr[i] = kq_s[1][col + i];
+      er[i] = kq_s[2][col + i];
+    }
+    const float b = beta[(size_t)t * Hv + h];
+    const QT* vn = v + ((size_t)t * Hv + h) * V + v0;
+    ST* C = dr.cache ? static_cast<ST*>(dr.cache) + n * dr.cache_pitch +
+                           (t - bos) * ((int64_t)Hv * K * V) + (size_t)h * K * V + (size_t)v0 * K + col
+                     : nullptr;
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const int row = rg + j * RG;
+      float w = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s[j][i] *= er[i];  // decay first
+        w = fmaf(kr[i], s[j][i], w);
+      }
+#pragma unroll
+      for (int o2 = TPR / 2; o2; o2 >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o2);
+      const float u = b * (to_f32(vn[row]) - w);
+      float ov = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s[j][i] = fmaf(kr[i], u, s[j][i]);
+        ov = fmaf(qr[i], s[j][i], ov);
+      }
+#pragma unroll
+      for (int o2 = TPR / 2; o2; o2 >>= 1) ov += __shfl_xor_sync(0xffffffffu, ov, o2);
+      if (col == 0) o[((size_t)t * Hv + h) * V + v0 + row] = from_f32<QT>(scale * ov);
+      if (C) Vec4<ST>::store(C + (size_t)row * K, s[j]);
+    }
+  }
+  if (dr.update_pool) {
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) Vec4<ST>::store(S + (size_t)(rg + j * RG) * K, s[j]);
+  }
+}
+
 template <typename QT, typename ST, int K>
 cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
   const int V = a.d.head_v_dim;
   const int VT = V >= 128 ? 128 : 64;
   dim3 grid((unsigned)a.d.num_seqs, (unsigned)a.d.num_v_heads, (unsigned)(V / VT));
+  const DraftArgs dr{a.cu, a.cache, a.cache_pitch, a.max_steps, a.update_pool};
+  if (a.state_vk) {
+    if (VT == 128)
+      kda_decode_vk_kernel<QT, ST, K, 128><<<grid, kDecThreads, 0, st>>>(
+          (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, (ST*)a.pool, a.idx,
+          (QT*)a.o, a.status, a.d.num_k_heads, a.d.num_v_heads, V, a.d.num_slots, a.slot_stride,
+          a.scale, a.gate_k, a.l2norm, dr, a.d.total_tokens);
+    else
+      kda_decode_vk_kernel<QT, ST, K, 64><<<grid, kDecThreads, 0, st>>>(
+          (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, (ST*)a.pool, a.idx,
+          (QT*)a.o, a.status, a.d.num_k_heads, a.d.num_v_heads, V, a.d.num_slots, a.slot_stride,
+          a.scale, a.gate_k, a.l2norm, dr, a.d.total_tokens);
+    return cudaGetLastError();
+  }
   if (VT == 128)
     kda_decode_kernel<QT, ST, K, 128><<<grid, kDecThreads, 0, st>>>(
         (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, (ST*)a.pool, a.idx,

@@ -79,6 +79,7 @@ struct PrefillArgs {
   GateAct act;               // act.a null: g is given
   int gate_k;                // gate values per (token, v-head): K, or 1 (scalar gate)
   bool l2norm;               // normalise q and k rows in the kernel
+  bool state_vk;             // states stored [V][K] per head (KDA_FLAG_STATE_VK)
   const int32_t* cu;
   const void* state_in;      // pool, dense h0 or null
   const int32_t* idx;        // null in dense mode
@@ -88,6 +89,9 @@ struct PrefillArgs {
   uint8_t* ws;               // workspace base
   size_t ws_bytes;
 };
+// Bound of the tensor-core prefill's pipeline waits for launches from now on
+// (kda_set_pipeline_wait_limit; 2 s by default).
+uint64_t pipeline_wait_limit_ns();
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t st);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st);
 size_t prefill_tc_workspace(const kda_desc_t& d);      // beyond the header, with splitting
@@ -102,6 +106,7 @@ struct DecodeArgs {
   const float *g, *beta;
   int gate_k;                // K, or 1 (scalar gate)
   bool l2norm;               // normalise q and k rows in the kernel
+  bool state_vk;             // states stored [V][K] per head (KDA_FLAG_STATE_VK)
   void* pool;
   const int32_t* idx;
   void* o;

@@ -53,7 +53,7 @@ kda_prefill_simt_kernel(const QT* __restrict__ q, const QT* __restrict__ k,
                         const ST* state_in, const int32_t* __restrict__ idx, ST* state_out,
                         QT* __restrict__ o, uint32_t* __restrict__ status, int Hk, int Hv,
                         int64_t T, int64_t num_slots, int64_t slot_stride, float scale,
-                        GateAct act, int gk, bool l2norm) {
+                        GateAct act, int gk, bool l2norm, bool state_vk) {
   using L = SimtSmem<K, V>;
   extern __shared__ float smem[];
   float* Kb = smem + L::kb;
@@ -88,7 +88,9 @@ kda_prefill_simt_kernel(const QT* __restrict__ q, const QT* __restrict__ k,
     if (state_in) src = state_in + ((size_t)n * Hv + h) * K * V;
     if (state_out) dst = state_out + ((size_t)n * Hv + h) * K * V;
   }
-  for (int e = tid; e < K * V; e += kSimtThreads) S[e] = src ? to_f32(src[e]) : 0.f;
+  // S is [K][V] in shared memory; a transposed state buffer ([V][K]) is read across
+  for (int e = tid; e < K * V; e += kSimtThreads)
+    S[e] = src ? to_f32(src[state_vk ? (e % V) * K + e / V : e]) : 0.f;
 
   const int kh = h / (Hv / Hk);
   const QT* ga = static_cast<const QT*>(act.a);
@@ -221,7 +223,8 @@ kda_prefill_simt_kernel(const QT* __restrict__ q, const QT* __restrict__ k,
   }
   __syncthreads();
   if (dst)
-    for (int e = tid; e < K * V; e += kSimtThreads) dst[e] = from_f32<ST>(S[e]);
+    for (int e = tid; e < K * V; e += kSimtThreads)
+      dst[state_vk ? (e % V) * K + e / V : e] = from_f32<ST>(S[e]);
 }
 
 template <typename QT, typename ST, int K, int V>
@@ -236,7 +239,7 @@ cudaError_t launch_typed(const PrefillArgs& a, cudaStream_t st) {
       (const QT*)a.q, (const QT*)a.k, (const QT*)a.v, a.g, a.beta, a.cu,
       (const ST*)a.state_in, a.idx, (ST*)a.state_out, (QT*)a.o, a.status, a.d.num_k_heads,
       a.d.num_v_heads, a.d.total_tokens, a.d.num_slots, a.slot_stride, a.scale, a.act, a.gate_k,
-      a.l2norm);
+      a.l2norm, a.state_vk);
   return cudaGetLastError();
 }
 

@@ -159,6 +159,7 @@ struct TcParams {
   int gate_k;         // 128, or 1 for a scalar gate ([T, Hv]: tiles of 64 tokens x gw heads)
   int gw;             // scalar gate: heads per staged row (4 fp32 g or 8 bf16 a = 16 bytes)
   int l2norm;         // normalise the staged q/k rows (x / max(||x||, 1e-12), back to bf16)
+  int state_vk;       // state buffers hold each head's state as [V][K] (KDA_FLAG_STATE_VK)
   const int32_t *cu, *idx;
   const uint32_t* work;      // work list: sequence | kind << 28, longest first
   const SplitInfo* splits;   // cut sequences
@@ -170,6 +171,7 @@ struct TcParams {
   __nv_bfloat16* o;
   uint32_t* status;
   uint32_t* next_item;
+  uint64_t wait_limit_ns;    // bound of the pipeline waits (kWaitLimitNs unless set shorter)
   int32_t N, Hk, Hv;
   int64_t T, num_slots, slot_stride;
   float scale;
@@ -194,16 +196,24 @@ __device__ __forceinline__ void fail(const TcParams& p, Small* s) {
 __device__ __forceinline__ bool aborted(Small* s) {
   return *reinterpret_cast<volatile uint32_t*>(&s->abort) != 0u;
 }
-// Bounded wait.  A timeout marks the CTA aborted and every later wait fails at
-// once; callers never branch on the result inside a chunk (control flow stays
-// uniform so every named barrier is reached), they leave at chunk boundaries.
+// Bounded wait of the pipeline, given up after p.wait_limit_ns.  A timeout marks the CTA
+// aborted and every later wait fails at once; callers never branch on the result inside a
+// chunk (control flow stays uniform so every named barrier is reached), they leave at chunk
+// boundaries, no load is issued once the CTA is aborted, and the drains before the CTA
+// exits keep the full limit (mbar_wait), so that no MMA or TMA is in flight when it frees
+// its tensor memory.
+// A bound shorter than the suspend hint polls with test_wait (try_wait may itself suspend
+// the thread until the phase completes, which would let a short bound never run out).
 __device__ __forceinline__ bool wait_bar(const TcParams& p, Small* s, int b, uint32_t parity) {
-  if (mbar_try_wait(&s->bar[b], parity)) return true;
+  const bool poll = p.wait_limit_ns < kSleepHintNs;
+  if (poll ? mbar_test_wait(&s->bar[b], parity) : mbar_try_wait(&s->bar[b], parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait_sleep(&s->bar[b], parity, kSleepHintNs)) return true;
+    if (poll ? mbar_test_wait(&s->bar[b], parity)
+             : mbar_try_wait_sleep(&s->bar[b], parity, kSleepHintNs))
+      return true;
     if (aborted(s)) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > p.wait_limit_ns) {
       fail(p, s);
       return false;
     }
@@ -318,7 +328,11 @@ struct Loader {  // item claims and loads, by the threads named at each call
     st->pushed = pushed + 1;
     if (info.done) st->fetched_done = 1;
   }
+  // Each load is issued only while the CTA is not aborted: the issuing thread has then
+  // seen the buffer's previous phase complete (its own wait succeeded), so no two loads
+  // of one buffer are ever in flight.
   __device__ void load_qk(const TcParams& p, uint8_t* sm, Small* s, int kh, int t0) {
+    if (aborted(s)) return;
     mbar_expect_tx(&s->bar[B_QK_FULL], 32768);
     tma_load_3d(sm + OFF_QK + 0, &p.tm_k, &s->bar[B_QK_FULL], 0, kh, t0);
     tma_load_3d(sm + OFF_QK + 16384, &p.tm_k, &s->bar[B_QK_FULL], 64, kh, t0);
@@ -327,6 +341,7 @@ struct Loader {  // item claims and loads, by the threads named at each call
     atomicAdd(&st->n_qk, 1u);
   }
   __device__ void load_g(const TcParams& p, uint8_t* sm, Small* s, int h, int t0) {
+    if (aborted(s)) return;
     mbar_expect_tx(&s->bar[B_G_FULL], p.g_bytes);
     if (p.gate_k == 1)  // x = first head of the 16-byte group holding h
       tma_load_2d(sm + OFF_G, &p.tm_g, &s->bar[B_G_FULL], h & ~(p.gw - 1), t0);
@@ -335,6 +350,7 @@ struct Loader {  // item claims and loads, by the threads named at each call
     atomicAdd(&st->n_g, 1u);
   }
   __device__ void load_v(const TcParams& p, uint8_t* sm, Small* s, int h, int t0) {
+    if (aborted(s)) return;
     mbar_expect_tx(&s->bar[B_V_FULL], 16384);
     tma_load_3d(sm + OFF_VB + 0, &p.tm_v, &s->bar[B_V_FULL], 0, h, t0);
     tma_load_3d(sm + OFF_VB + 8192, &p.tm_v, &s->bar[B_V_FULL], 64, h, t0);
@@ -830,8 +846,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         // is free since MMA-U of the previous chunk, which pass B waited for); the identity
         // pass of a cut tail has zero values and no MMA-U, so its phase completes bare
         if (info.kind == KIND_TAIL_ID) {
-          mbar_arrive(&s->bar[B_V_FULL]);
-          atomicAdd(&ld.st->n_v, 1u);
+          if (!aborted(s)) {
+            mbar_arrive(&s->bar[B_V_FULL]);
+            atomicAdd(&ld.st->n_v, 1u);
+          }
         } else {
           ld.load_v(p, sm, s, h, (int)t0);
         }
@@ -1136,8 +1154,42 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
   if (warp == 0) {
     if (lane == 0) mma_commit(&s->bar[B_DRAIN_IG]);
     __syncwarp();
-    wait_bar(p, s, B_DRAIN_IG, 0);
+    mbar_wait(&s->bar[B_DRAIN_IG], 0);  // the full limit, aborted or not
   }
+}
+
+// 32 consecutive key channels of row v of a transposed ([V][K]) state, as fp32, with
+// 16-byte loads and stores (each thread owns its row).
+__device__ __forceinline__ void row32_load(const float* p, float* r) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 x = reinterpret_cast<const float4*>(p)[i];
+    r[4 * i] = x.x; r[4 * i + 1] = x.y; r[4 * i + 2] = x.z; r[4 * i + 3] = x.w;
+  }
+}
+__device__ __forceinline__ void row32_load(const __nv_bfloat16* p, float* r) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 x = reinterpret_cast<const uint4*>(p)[i];
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      r[8 * i + 2 * j] = bf_bits(w[j] & 0xFFFFu);
+      r[8 * i + 2 * j + 1] = bf_bits(w[j] >> 16);
+    }
+  }
+}
+__device__ __forceinline__ void row32_store(float* p, const float* r) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    reinterpret_cast<float4*>(p)[i] = make_float4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+}
+__device__ __forceinline__ void row32_store(__nv_bfloat16* p, const float* r) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    reinterpret_cast<uint4*>(p)[i] =
+        make_uint4(pack_bf16x2(r[8 * i], r[8 * i + 1]), pack_bf16x2(r[8 * i + 2], r[8 * i + 3]),
+                   pack_bf16x2(r[8 * i + 4], r[8 * i + 5]), pack_bf16x2(r[8 * i + 6], r[8 * i + 7]));
 }
 
 // ======================================================================================
@@ -1190,9 +1242,13 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
 #pragma unroll 1
     for (int kq = 0; kq < 4; ++kq) {
       float sv[32], pw[16];
+      if (src && p.state_vk) {
+        row32_load(src + (size_t)v * kK + kq * 32, sv);  // row v: S[k][v] for 32 k
+      } else {
 #pragma unroll
-      for (int u = 0; u < 32; ++u)
-        sv[u] = src ? to_f32(src[(size_t)(kq * 32 + u) * kV + v]) : (ident && kq * 32 + u == v ? 1.f : 0.f);
+        for (int u = 0; u < 32; ++u)
+          sv[u] = src ? to_f32(src[(size_t)(kq * 32 + u) * kV + v]) : (ident && kq * 32 + u == v ? 1.f : 0.f);
+      }
 #pragma unroll
       for (int u = 0; u < 16; ++u) pw[u] = __uint_as_float(pack_bf16x2(sv[2 * u], sv[2 * u + 1]));
       tmem_st16(taddr_q + TM_SB + kq * 16, pw);
@@ -1349,8 +1405,12 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
 #pragma unroll
           for (int u = 0; u < 32; ++u) dst32[(size_t)(kq * 32 + u) * kV + v] = sv[u];
         } else if (dst) {
+          if (p.state_vk) {
+            row32_store(dst + (size_t)v * kK + kq * 32, sv);
+          } else {
 #pragma unroll
-          for (int u = 0; u < 32; ++u) dst[(size_t)(kq * 32 + u) * kV + v] = from_f32<ST>(sv[u]);
+            for (int u = 0; u < 32; ++u) dst[(size_t)(kq * 32 + u) * kV + v] = from_f32<ST>(sv[u]);
+          }
         }
       }
       tmem_st_wait();
@@ -1382,7 +1442,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   if (leader_warp) {
     if (lane == 0) mma_commit(&s->bar[B_DRAIN_RG]);
     __syncwarp();
-    wait_bar(p, s, B_DRAIN_RG, 0);
+    mbar_wait(&s->bar[B_DRAIN_RG], 0);  // the full limit, aborted or not
   }
 }
 
@@ -1395,11 +1455,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Small* s = reinterpret_cast<Small*>(sm + OFF_SMALL);
   const int warp = threadIdx.x >> 5;
+  // the combine kernel after this one may be scheduled as SMs free up (it waits for this
+  // grid before reading anything)
+  grid_dep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int b = 0; b < B_COUNT; ++b) mbar_init(&s->bar[b], 1);
     for (int r = 0; r < kRing; ++r) mbar_init(&s->bar[B_ITEM_EMPTY + r], 2);
     s->abort = 0;
-    s->num_items = p.hdr->num_entries * (uint32_t)p.Hv;
     s->ld = LoaderState{};
     fence_mbar_init();
     prefetch_tensormap(&p.tm_q);
@@ -1408,6 +1470,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     prefetch_tensormap(&p.tm_g);
   }
   if (warp == 0) tmem_alloc(&s->tmem_base, 512);
+  // everything above overlaps the planning kernel; the work list is read only after it
+  grid_dep_wait();
+  if (threadIdx.x == 0) s->num_items = p.hdr->num_entries * (uint32_t)p.Hv;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1485,6 +1550,8 @@ __device__ void scan_keys_desc(int* cnt, int* wsum) {
   __syncthreads();
 }
 
+constexpr int kPlanCache = 4096;  // sequences whose lengths and order the block keeps on chip
+
 __global__ void __launch_bounds__(kOrderKeys) kda_plan_kernel(const int32_t* __restrict__ cu, int N,
                                                               int64_t T, int Hv, int grid, int max_cuts,
                                                               int ytok_max, uint32_t* __restrict__ work,
@@ -1492,29 +1559,40 @@ __global__ void __launch_bounds__(kOrderKeys) kda_plan_kernel(const int32_t* __r
                                                               WsHeader* __restrict__ hdr) {
   __shared__ int cnt[kOrderKeys];
   __shared__ int wsum[kOrderKeys / 32];
+  grid_dep_launch_dependents();  // the prefill kernel may start its prologue meanwhile
+  __shared__ int len_s[kPlanCache];       // lengths of the first kPlanCache sequences
+  __shared__ uint32_t order_s[kPlanCache];  // the first kPlanCache entries of the order
   __shared__ unsigned long long total;
   __shared__ int cut_n[kMaxCuts], cut_a[kMaxCuts], ncut;
   const int t = threadIdx.x;
+  // lengths from cu_seqlens once; later reads come from shared memory
+  auto len_of = [&](int n) -> int64_t { return n < kPlanCache ? (int64_t)len_s[n] : seq_len_checked(cu, n, T); };
+  auto chunks = [&](int n) -> int64_t { return (len_of(n) + kC - 1) / kC; };
   cnt[t] = 0;
   if (t == 0) total = 0ull;
+  for (int n = t; n < N && n < kPlanCache; n += kOrderKeys) len_s[n] = (int)seq_len_checked(cu, n, T);
   __syncthreads();
   unsigned long long mine = 0;
   for (int n = t; n < N; n += kOrderKeys) {
-    const int64_t c = chunks_of(cu, n, T);
+    const int64_t c = chunks(n);
     mine += (unsigned long long)c;
     atomicAdd(&cnt[order_key(c)], 1);
   }
   atomicAdd(&total, mine);
   __syncthreads();
   scan_keys_desc(cnt, wsum);
-  for (int n = t; n < N; n += kOrderKeys) work[atomicAdd(&cnt[order_key(chunks_of(cu, n, T))], 1)] = (uint32_t)n;
+  for (int n = t; n < N; n += kOrderKeys) {
+    const int pos = atomicAdd(&cnt[order_key(chunks(n))], 1);
+    work[pos] = (uint32_t)n;
+    if (pos < kPlanCache) order_s[pos] = (uint32_t)n;
+  }
   __syncthreads();
   if (t == 0) {  // the cuts, longest sequence first
     int nc = 0, ytok = 0;
     const double L = (double)Hv * (double)total / (double)grid;
     for (int i = 0; i < N && nc < max_cuts; ++i) {
-      const int n = (int)work[i];
-      const int64_t c = chunks_of(cu, n, T);
+      const int n = (int)(i < kPlanCache ? order_s[i] : work[i]);
+      const int64_t c = chunks(n);
       if (c < kCutMinChunks) break;
       if ((double)c <= 1.05 * L) {
         if (order_key(c) < kOrderKeys - 1) break;  // sorted exactly below the top key
@@ -1522,7 +1600,7 @@ __global__ void __launch_bounds__(kOrderKeys) kda_plan_kernel(const int32_t* __r
       }
       const int64_t a = max((c + 1) / 2, (int64_t)ceil(L));
       if (a >= c) continue;
-      const int64_t tail = seq_len_checked(cu, n, T) - a * kC;
+      const int64_t tail = len_of(n) - a * kC;
       if ((int64_t)ytok + tail > (int64_t)ytok_max) continue;
       splits[nc] = SplitInfo{n, (int32_t)a, ytok, (int32_t)tail};
       cut_n[nc] = n;
@@ -1546,7 +1624,7 @@ __global__ void __launch_bounds__(kOrderKeys) kda_plan_kernel(const int32_t* __r
     return -1;
   };
   for (int n = t; n < N; n += kOrderKeys) {
-    const int64_t c = chunks_of(cu, n, T);
+    const int64_t c = chunks(n);
     const int i = cut_of(n);
     if (i < 0) {
       atomicAdd(&cnt[order_key(c)], 1);
@@ -1558,7 +1636,7 @@ __global__ void __launch_bounds__(kOrderKeys) kda_plan_kernel(const int32_t* __r
   __syncthreads();
   scan_keys_desc(cnt, wsum);
   for (int n = t; n < N; n += kOrderKeys) {
-    const int64_t c = chunks_of(cu, n, T);
+    const int64_t c = chunks(n);
     const int i = cut_of(n);
     if (i < 0) {
       work[atomicAdd(&cnt[order_key(c)], 1)] = (uint32_t)n;
@@ -1577,12 +1655,15 @@ __global__ void __launch_bounds__(kOrderKeys) kda_plan_kernel(const int32_t* __r
 // tail's identity and zero-start passes, and y the identity pass's outputs:
 //   o_t += S_p^T y_t          for every tail token t (bf16 warp MMAs, fp32 sums, o re-rounded)
 //   S_end = M S_p + S_loc     into the pool row or the dense final state (fp32 FMAs)
-// Units: (cut, head, group of kCombTok tail tokens) for o and (cut, head) for the state, over
-// a grid that leaves at once when the planning kernel made no cut.
+// Units: (cut, head, group of kCombTok tail tokens) for o and (cut, head, 16 state rows) for
+// the state, over a grid that leaves at once when the planning kernel made no cut.  Global
+// accesses are 16-byte and coalesced; o is read, corrected and written a row piece at a time.
 constexpr int kCombThreads = 256;
 constexpr int kCombTok = 256;
-constexpr int kCombPitch = 136;  // bf16 row pitch of the staged tiles (conflict-free fragments)
-constexpr uint32_t kCombSmem = (128 + 64) * kCombPitch * 2;
+constexpr int kCombPitch = 136;  // bf16 row pitch of the staged S_p and y tiles
+constexpr int kCombAccPitch = 132;  // fp32 row pitch of the staged correction
+constexpr uint32_t kCombSmem = (128 + 64) * kCombPitch * 2 + 64 * kCombAccPitch * 4;
+static_assert((16 + 128) * 128 * 4 <= kCombSmem, "state units stage M rows and S_p");
 
 struct CombineParams {
   const WsHeader* hdr;
@@ -1592,7 +1673,7 @@ struct CombineParams {
   __nv_bfloat16* o;
   const int32_t *cu, *idx;
   void* state_out;
-  int32_t Hv;
+  int32_t Hv, state_vk;
   int64_t num_slots, slot_stride;
 };
 
@@ -1603,51 +1684,93 @@ __device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// Four 8x8 bf16 matrices, transposed on the way: lanes 8m..8m+7 give the row addresses of
+// matrix m; each lane receives the (2 tq, 2 tq + 1) x g elements of each matrix.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t r[4], const void* addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(addr)));
+}
+
+__device__ __forceinline__ int comb_o_units(const SplitInfo& sp, int Hv) {
+  return (sp.ntok + kCombTok - 1) / kCombTok * Hv;
+}
 
 template <typename ST>
 __global__ void __launch_bounds__(kCombThreads) kda_combine_kernel(const __grid_constant__ CombineParams p) {
+  grid_dep_wait();  // the prefill grid has finished and its writes are visible
   const int ns = (int)p.hdr->num_splits;
   if (ns == 0) return;
   extern __shared__ __align__(16) uint8_t csm[];
-  __nv_bfloat16* spT = reinterpret_cast<__nv_bfloat16*>(csm);           // [v][k], S_p^T
-  __nv_bfloat16* yt = spT + 128 * kCombPitch;                            // [64 tokens][k]
-  float* fs = reinterpret_cast<float*>(csm);                             // state units
+  __nv_bfloat16* spk = reinterpret_cast<__nv_bfloat16*>(csm);            // S_p [k][v] bf16
+  __nv_bfloat16* yt = spk + 128 * kCombPitch;                            // y [64 tokens][k]
+  float* acc_s = reinterpret_cast<float*>(yt + 64 * kCombPitch);         // [64 tokens][v]
+  float* ms = reinterpret_cast<float*>(csm);                             // state units: M rows
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hv = p.Hv;
   int total = 0;
-  for (int i = 0; i < ns; ++i) total += ((p.splits[i].ntok + kCombTok - 1) / kCombTok + 1) * Hv;
+  for (int i = 0; i < ns; ++i) total += comb_o_units(p.splits[i], Hv) + 8 * Hv;
   for (int u = blockIdx.x; u < total; u += gridDim.x) {
     int si = 0, r = u;
     for (; si < ns; ++si) {
-      const int per = ((p.splits[si].ntok + kCombTok - 1) / kCombTok + 1) * Hv;
+      const int per = comb_o_units(p.splits[si], Hv) + 8 * Hv;
       if (r < per) break;
       r -= per;
     }
     const SplitInfo sp = p.splits[si];
-    const int ngrp = (sp.ntok + kCombTok - 1) / kCombTok;
+    const int no = comb_o_units(sp, Hv);
     const size_t so = ((size_t)si * Hv) * 16384;
-    __syncthreads();  // the smem of the previous unit is no longer read
-    if (r < ngrp * Hv) {
-      // ---- o of tail tokens [g * kCombTok, ...) of head h
+    __syncthreads();  // the previous unit's shared memory is no longer read
+    if (r < no) {
+      // ---- o of tail tokens [g * kCombTok, ...) of head h; the y rows and o pieces of a
+      // 64-token tile are loaded into registers one tile ahead of the MMAs that use them
       const int h = r % Hv, g = r / Hv;
-      const float* S = p.sp + so + (size_t)h * 16384;  // [k][v]
-      for (int e = tid; e < 16384; e += kCombThreads) {
-        const int k = e >> 7, v = e & 127;
-        spT[v * kCombPitch + k] = __float2bfloat16_rn(S[e]);
-      }
+      const float4* S4 = reinterpret_cast<const float4*>(p.sp + so + (size_t)h * 16384);
+      float4 sreg[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sreg[i] = S4[tid + i * kCombThreads];  // all in flight
       const int64_t tail0 = (int64_t)p.cu[sp.n] + (int64_t)sp.cut * kC;  // first tail token
-      const int t_end = min(sp.ntok, (g + 1) * kCombTok);
-      for (int tb = g * kCombTok; tb < t_end; tb += 64) {
+      const int t_beg = g * kCombTok, t_end = min(sp.ntok, (g + 1) * kCombTok);
+      auto load_y = [&](int tb, uint4 (&yr)[4]) {
         const int nt = min(64, t_end - tb);
-        __syncthreads();
-        for (int e = tid; e < 64 * 16; e += kCombThreads) {  // 16-byte pieces of y rows
-          const int row = e >> 4, c8 = (e & 15) * 8;
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (row < nt)
-            w = *reinterpret_cast<const uint4*>(p.y + ((size_t)(sp.ytok0 + tb + row) * Hv + h) * 128 + c8);
-          *reinterpret_cast<uint4*>(yt + row * kCombPitch + c8) = w;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int e = tid + i * kCombThreads, row = e >> 4, c8 = (e & 15) * 8;
+          yr[i] = row < nt ? *reinterpret_cast<const uint4*>(
+                                 p.y + ((size_t)(sp.ytok0 + tb + row) * Hv + h) * 128 + c8)
+                           : make_uint4(0u, 0u, 0u, 0u);
         }
+      };
+      uint4 yr[4];
+      load_y(t_beg, yr);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {  // S_p [k][v] as bf16
+        const int e = tid + i * kCombThreads, k = e >> 5, v4 = (e & 31) * 4;
+        uint2 w;
+        w.x = pack_bf16x2(sreg[i].x, sreg[i].y);
+        w.y = pack_bf16x2(sreg[i].z, sreg[i].w);
+        *reinterpret_cast<uint2*>(spk + k * kCombPitch + v4) = w;
+      }
+      for (int tb = t_beg; tb < t_end; tb += 64) {
+        const int nt = min(64, t_end - tb);
+        __syncthreads();  // acc_s / yt of the previous tile consumed
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int e = tid + i * kCombThreads, row = e >> 4, c8 = (e & 15) * 8;
+          *reinterpret_cast<uint4*>(yt + row * kCombPitch + c8) = yr[i];
+        }
+        // this tile's o pieces and the next tile's y rows, in flight during the MMAs
+        uint4 orr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int e = tid + i * kCombThreads, row = e >> 4, c8 = (e & 15) * 8;
+          orr[i] = row < nt ? *reinterpret_cast<const uint4*>(
+                                  p.o + ((size_t)(tail0 + tb + row) * Hv + h) * 128 + c8)
+                            : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (tb + 64 < t_end) load_y(tb + 64, yr);
         __syncthreads();
+        // warp: tokens r0..r0+15, values n0..n0+63
         const int r0 = (warp & 3) * 16, n0 = (warp >> 2) * 64;
         const int gq = lane >> 2, tq = lane & 3;
         float acc[8][4] = {};
@@ -1659,30 +1782,44 @@ __global__ void __launch_bounds__(kCombThreads) kda_combine_kernel(const __grid_
           a[2] = *reinterpret_cast<const uint32_t*>(yt + (r0 + gq) * kCombPitch + kb + 2 * tq + 8);
           a[3] = *reinterpret_cast<const uint32_t*>(yt + (r0 + gq + 8) * kCombPitch + kb + 2 * tq + 8);
 #pragma unroll
-          for (int nt8 = 0; nt8 < 8; ++nt8) {
-            const __nv_bfloat16* bp = spT + (n0 + nt8 * 8 + gq) * kCombPitch + kb + 2 * tq;
-            mma_bf16_16816(acc[nt8], a, *reinterpret_cast<const uint32_t*>(bp),
-                           *reinterpret_cast<const uint32_t*>(bp + 8));
+          for (int np = 0; np < 4; ++np) {  // two 8-wide value tiles per ldmatrix
+            uint32_t b[4];
+            const int mrow = kb + (lane & 15);
+            const int mcol = n0 + np * 16 + (lane >> 4) * 8;
+            ldsm_x4_trans(b, spk + mrow * kCombPitch + mcol);
+            mma_bf16_16816(acc[np * 2], a, b[0], b[1]);
+            mma_bf16_16816(acc[np * 2 + 1], a, b[2], b[3]);
           }
         }
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int row = r0 + gq + hr * 8;
-          if (row < nt) {
-            __nv_bfloat16* orow = p.o + ((size_t)(tail0 + tb + row) * Hv + h) * 128;
+        for (int nt8 = 0; nt8 < 8; ++nt8) {
+          const int col = n0 + nt8 * 8 + 2 * tq;
+          *reinterpret_cast<float2*>(acc_s + (r0 + gq) * kCombAccPitch + col) =
+              make_float2(acc[nt8][0], acc[nt8][1]);
+          *reinterpret_cast<float2*>(acc_s + (r0 + gq + 8) * kCombAccPitch + col) =
+              make_float2(acc[nt8][2], acc[nt8][3]);
+        }
+        __syncthreads();
 #pragma unroll
-            for (int nt8 = 0; nt8 < 8; ++nt8) {
-              const int col = n0 + nt8 * 8 + 2 * tq;
-              __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(orow + col);
-              const float2 cur = __bfloat1622float2(*op);
-              *op = __floats2bfloat162_rn(cur.x + acc[nt8][hr * 2], cur.y + acc[nt8][hr * 2 + 1]);
-            }
+        for (int i = 0; i < 4; ++i) {  // o rows, 16 bytes at a time
+          const int e = tid + i * kCombThreads, row = e >> 4, c8 = (e & 15) * 8;
+          if (row < nt) {
+            const float* cs = acc_s + row * kCombAccPitch + c8;
+            const uint32_t in[4] = {orr[i].x, orr[i].y, orr[i].z, orr[i].w};
+            uint32_t outw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              outw[j] = pack_bf16x2(__uint_as_float(in[j] << 16) + cs[2 * j],
+                                    __uint_as_float(in[j] & 0xFFFF0000u) + cs[2 * j + 1]);
+            *reinterpret_cast<uint4*>(p.o + ((size_t)(tail0 + tb + row) * Hv + h) * 128 + c8) =
+                make_uint4(outw[0], outw[1], outw[2], outw[3]);
           }
         }
       }
     } else {
-      // ---- final state of head h: S_end = M S_p + S_loc
-      const int h = r - ngrp * Hv;
+      // ---- rows 16 rb .. 16 rb + 15 of head h's final state: S_end = M S_p + S_loc, with
+      // S_p and the 16 rows of M staged in shared memory (every load in flight at once)
+      const int rr = r - no, h = rr >> 3, rb = rr & 7;
       ST* dst = nullptr;
       if (p.state_out) {
         if (p.idx) {
@@ -1693,31 +1830,32 @@ __global__ void __launch_bounds__(kCombThreads) kda_combine_kernel(const __grid_
         }
       }
       if (!dst) continue;
-      const float* M = p.mm + so + (size_t)h * 16384;
-      const float* S = p.sp + so + (size_t)h * 16384;
+      const float4* M4 = reinterpret_cast<const float4*>(p.mm + so + (size_t)h * 16384 + rb * 16 * 128);
+      const float4* S4 = reinterpret_cast<const float4*>(p.sp + so + (size_t)h * 16384);
       const float* SL = p.sl + so + (size_t)h * 16384;
-      const int v = tid & 127, k0 = (tid >> 7) * 64;
-      float acc[64];
+      float* ss = ms + 16 * 128;  // S_p [j][v]
+      const int v = tid & 127, k0 = (tid >> 7) * 8;  // rows 16 rb + k0 .. + 7
+      float acc[8];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = SL[(size_t)(k0 + i) * 128 + v];
-      float* Ms = fs;              // [128 k][32 j]
-      float* Ss = fs + 128 * 32;   // [32 j][128 v]
-      for (int j0 = 0; j0 < 128; j0 += 32) {
-        __syncthreads();
-        for (int e = tid; e < 128 * 32; e += kCombThreads) {
-          Ms[e] = M[(size_t)(e >> 5) * 128 + j0 + (e & 31)];
-          Ss[e] = S[(size_t)(j0 + (e >> 7)) * 128 + (e & 127)];
-        }
-        __syncthreads();
+      for (int i = 0; i < 8; ++i) acc[i] = SL[(size_t)(rb * 16 + k0 + i) * 128 + v];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) reinterpret_cast<float4*>(ms)[tid + i * kCombThreads] = M4[tid + i * kCombThreads];
 #pragma unroll 4
-        for (int j = 0; j < 32; ++j) {
-          const float sv = Ss[j * 128 + v];
+      for (int i = 0; i < 16; ++i) reinterpret_cast<float4*>(ss)[tid + i * kCombThreads] = S4[tid + i * kCombThreads];
+      __syncthreads();
+#pragma unroll 8
+      for (int j = 0; j < 128; ++j) {
+        const float sv = ss[j * 128 + v];
 #pragma unroll
-          for (int i = 0; i < 64; ++i) acc[i] = fmaf(Ms[(k0 + i) * 32 + j], sv, acc[i]);
-        }
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(ms[(k0 + i) * 128 + j], sv, acc[i]);
       }
+      if (p.state_vk) {  // row v, key channels 16 rb + k0 .. + 7: two 16-byte pieces (fp32)
 #pragma unroll
-      for (int i = 0; i < 64; ++i) dst[(size_t)(k0 + i) * 128 + v] = from_f32<ST>(acc[i]);
+        for (int i = 0; i < 8; ++i) dst[(size_t)v * 128 + rb * 16 + k0 + i] = from_f32<ST>(acc[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[(size_t)(rb * 16 + k0 + i) * 128 + v] = from_f32<ST>(acc[i]);
+      }
     }
   }
 }
@@ -1763,6 +1901,34 @@ bool make_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int e
   return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The prefill kernel, and the combine kernel when cuts are possible, each launched with
+// programmatic stream serialisation: a kernel may be scheduled while the one before it on
+// the stream still runs, and waits for it in grid_dep_wait before reading its results.
+template <typename KP, typename KC>
+cudaError_t launch_pair(KP kern, KC comb, const TcParams& p, const CombineParams& cp, int grid,
+                        int cgrid, bool with_combine, cudaStream_t st) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (err != cudaSuccess) return err;
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  err = cudaLaunchKernelEx(&cfg, kern, p);
+  if (err != cudaSuccess || !with_combine) return err;
+  err = cudaFuncSetAttribute(comb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCombSmem);
+  if (err != cudaSuccess) return err;
+  cfg.gridDim = dim3((unsigned)cgrid);
+  cfg.blockDim = dim3(kCombThreads);
+  cfg.dynamicSmemBytes = kCombSmem;
+  return cudaLaunchKernelEx(&cfg, comb, cp);
 }
 
 int sm_count() {
@@ -1865,6 +2031,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   p.act = a.act;
   p.gate_k = a.gate_k;
   p.l2norm = a.l2norm ? 1 : 0;
+  p.state_vk = a.state_vk ? 1 : 0;
   p.gw = a.act.a ? 8 : 4;
   p.g_bytes = a.gate_k == 1 ? 1024u : (a.act.a ? 16384u : 32768u);
   p.beta = a.beta;
@@ -1882,6 +2049,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   p.num_slots = d.num_slots;
   p.slot_stride = a.slot_stride;
   p.scale = a.scale;
+  p.wait_limit_ns = pipeline_wait_limit_ns();
 
   const int max_cuts = can_cut ? full_cuts(d) : 0;
   const int64_t max_items = ((int64_t)d.num_seqs + 2 * max_cuts) * d.num_v_heads;
@@ -1905,33 +2073,15 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   cp.idx = p.idx;
   cp.state_out = p.state_out;
   cp.Hv = d.num_v_heads;
+  cp.state_vk = a.state_vk ? 1 : 0;
   cp.num_slots = d.num_slots;
   cp.slot_stride = a.slot_stride;
   const int cgrid = 2 * sm_count();
-  if (d.state_dtype == KDA_BF16) {
-    auto kern = kda_prefill_tc_kernel<__nv_bfloat16>;
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (err != cudaSuccess) return err;
-    kern<<<grid, kThreads, kSmemBytes, st>>>(p);
-    if (max_cuts > 0) {
-      auto comb = kda_combine_kernel<__nv_bfloat16>;
-      err = cudaFuncSetAttribute(comb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCombSmem);
-      if (err != cudaSuccess) return err;
-      comb<<<cgrid, kCombThreads, kCombSmem, st>>>(cp);
-    }
-  } else {
-    auto kern = kda_prefill_tc_kernel<float>;
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (err != cudaSuccess) return err;
-    kern<<<grid, kThreads, kSmemBytes, st>>>(p);
-    if (max_cuts > 0) {
-      auto comb = kda_combine_kernel<float>;
-      err = cudaFuncSetAttribute(comb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCombSmem);
-      if (err != cudaSuccess) return err;
-      comb<<<cgrid, kCombThreads, kCombSmem, st>>>(cp);
-    }
-  }
-  return cudaGetLastError();
+  return d.state_dtype == KDA_BF16
+             ? launch_pair(kda_prefill_tc_kernel<__nv_bfloat16>, kda_combine_kernel<__nv_bfloat16>, p, cp,
+                           grid, cgrid, max_cuts > 0, st)
+             : launch_pair(kda_prefill_tc_kernel<float>, kda_combine_kernel<float>, p, cp, grid, cgrid,
+                           max_cuts > 0, st);
 }
 
 }  // namespace kda

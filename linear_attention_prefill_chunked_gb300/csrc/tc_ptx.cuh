@@ -41,6 +41,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of the phase with the given parity (try_wait may suspend the thread
+// for a while before it returns false; test_wait never does).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // As mbar_try_wait, but the thread may be suspended (up to about hint_ns) until the
 // phase completes, instead of returning at once: a waiting warp then takes no issue
 // slots from the warps doing work.
@@ -95,6 +107,17 @@ __device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t nthreads, bo
       : "memory");
   return r != 0;
 }
+
+// ---- programmatic dependent launch ------------------------------------------------
+// The next kernel on the stream (launched with programmatic stream serialisation) may be
+// scheduled from now on; it still waits for this grid in grid_dep_wait before reading
+// what this grid writes.
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grids this one depends on have completed and their memory writes are
+// visible (returns at once when the kernel was launched without the dependency).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---- TMEM allocation (whole warp) -----------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

@@ -72,7 +72,7 @@ def test_workspace_queries_and_path_selection():
     d.chunk_size = 32
     bad.append(d)
     d = _desc()
-    d.flags = 8                                              # no such flag
+    d.flags = 16                                             # no such flag
     bad.append(d)
     for b in bad:
         assert kda.prefill_workspace_size(b) == 0
@@ -83,6 +83,11 @@ def test_workspace_queries_and_path_selection():
     d.flags = 1                                              # KDA_FLAG_CUDA_CORE_PATH
     assert kda.prefill_path(d) == 0
     assert kda.prefill_path(_desc(K=64)) == 0
+    d = _desc()
+    d.flags = 8                                              # KDA_FLAG_STATE_VK: same path
+    assert kda.prefill_path(d) == 1
+    # the least workspace (no long sequence cut) is below the full size
+    assert 256 <= kda.prefill_min_workspace_size(_desc()) < kda.prefill_workspace_size(_desc())
     d = _desc()
     d.flags = 2                                              # KDA_FLAG_SCALAR_GATE
     assert kda.prefill_path(d) == (1 if d.num_v_heads % 8 == 0 else 0)
@@ -120,3 +125,13 @@ def test_host_checked_errors_return_before_any_launch():
 def test_oracle_library_builds():
     from oracle import kda_oracle
     assert os.path.exists(kda_oracle.build())
+
+
+def test_pipeline_wait_limit_is_bounded():
+    """The watchdog bound of the tensor-core prefill's waits: 0 restores the 2 s default, more
+    than 2 s is refused (host only; the GPU test makes the waits run out)."""
+    from linear_attention_prefill_chunked_gb300 import api
+    with pytest.raises(api.KdaError):
+        api.set_pipeline_wait_limit(3_000_000_000)
+    api.set_pipeline_wait_limit(2_000_000_000)
+    api.set_pipeline_wait_limit(0)

@@ -102,3 +102,29 @@ def test_decode_bad_slot_sets_status():
     pool = w.state.cuda()
     kda.decode(q, k, v, g, beta, pool, idx.cuda())
     assert kda.read_device_status(kda.decode.last_workspace) & kda.api.KDA_DEVICE_BAD_SLOT
+
+
+@pytest.mark.parametrize("K,state_dtype", [(128, torch.float32), (64, torch.bfloat16)])
+def test_decode_transposed_state_layout(K, state_dtype):
+    """Decode on a [V][K] (transposed) pool: the key-channel reductions are shuffles within a
+    row's threads there, so the results match the [K][V] decode within the tolerance and the
+    oracle; rows no index names stay bit-identical."""
+    w = synthetic.make([1] * 300, Hk=4, Hv=8, K=K, V=128, dtype=torch.bfloat16, seed=9,
+                       state="pool", num_slots=400, state_dtype=state_dtype, last_index_pad=True)
+    q, k, v, g, beta = (t.cuda() for t in (w.q, w.k, w.v, w.g, w.beta))
+    idx = w.state_indices.cuda()
+    pool_vk = w.state.transpose(-1, -2).contiguous().cuda()
+    before = pool_vk.clone()
+    o = kda.decode(q, k, v, g, beta, pool_vk, idx, state_layout="vk")
+    assert kda.read_device_status(kda.decode.last_workspace) == 0
+    o_ref, pool_ref = kda_oracle.recurrence(w.q[:-1], w.k[:-1], w.v[:-1], w.g[:-1], w.beta[:-1],
+                                            np.arange(300), scale=w.scale, state=w.state,
+                                            state_indices=w.state_indices[:-1])
+    assert_close(o[:-1], o_ref, torch.bfloat16, "o")
+    slots = w.state_indices[:-1].long()
+    tol = torch.float32 if state_dtype == torch.float32 else torch.bfloat16
+    assert_close(pool_vk[slots.cuda()].transpose(-1, -2), pool_ref[slots.numpy()], tol, "pool rows")
+    untouched = torch.ones(400, dtype=torch.bool)
+    untouched[slots] = False
+    untouched[-1] = False  # the sentinel (padding row)
+    assert torch.equal(pool_vk[untouched.cuda()], before[untouched.cuda()])

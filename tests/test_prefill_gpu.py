@@ -31,20 +31,30 @@ def test_tiny_varlen_fp32_dense():
     assert_close(ht, ht_ref, torch.float32, "ht")
 
 
+@pytest.mark.parametrize("layout", ["kv", "vk"])
 @pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
-def test_pool_mode_matches_dense_bitwise_and_oracle(state_dtype):
+def test_pool_mode_matches_dense_bitwise_and_oracle(state_dtype, layout):
+    """Pool mode against dense gather/scatter, bit for bit, in both state layouts: [K][V] per
+    head, and the pages' transposed [V][K] pool (PR 30169 digest, 关键源码片段), which must give
+    the [K][V] run's results transposed, bit for bit."""
     w = synthetic.pool_varlen(state_dtype=state_dtype)
     d = to_dev(w)
+    if layout == "vk":
+        kv_pool = d["state"].clone()
+        o_kv, _ = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                    state=kv_pool, state_indices=d["state_indices"])
+        d["state"] = d["state"].transpose(-1, -2).contiguous()
     pool = d["state"]
     slots = torch.where(d["state_indices"] >= 0, d["state_indices"],
                         torch.full_like(d["state_indices"], pool.shape[0] - 1)).long()
     h0_dense = pool[slots].clone()
     pool_before = pool.clone()
     o_dense, ht_dense = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"],
-                                          d["cu_seqlens"], state=h0_dense.clone())
+                                          d["cu_seqlens"], state=h0_dense.clone(),
+                                          state_layout=layout)
     o_pool, ht_pool = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"],
                                         d["cu_seqlens"], state=pool,
-                                        state_indices=d["state_indices"])
+                                        state_indices=d["state_indices"], state_layout=layout)
     torch.cuda.synchronize()
     assert ht_pool is pool
     assert torch.equal(o_pool, o_dense)
@@ -52,6 +62,10 @@ def test_pool_mode_matches_dense_bitwise_and_oracle(state_dtype):
     untouched = torch.ones(pool.shape[0], dtype=torch.bool, device=pool.device)
     untouched[slots] = False
     assert torch.equal(pool[untouched], pool_before[untouched])
+    if layout == "vk":  # the transposed layout's results are the [K][V] run's, transposed
+        assert torch.equal(o_pool, o_kv)
+        assert torch.equal(pool.transpose(-1, -2), kv_pool)
+        pool = pool.transpose(-1, -2)
     # against the oracle (the -1 sequence lands in the sentinel slot 15)
     o_ref, pool_ref = _full_oracle(w)
     assert_close(o_pool, o_ref, torch.bfloat16, "o")
@@ -274,3 +288,27 @@ def test_tensor_core_path_matches_cuda_core_path_and_oracle(state_dtype):
     assert_close(pool_tc, pool_ref, torch.bfloat16, "tensor-core pool")
     assert_close(o_cc, o_ref, torch.bfloat16, "cuda-core o")
     assert_close(o_tc, o_cc.double().cpu().numpy(), torch.bfloat16, "tc vs cuda-core o")
+
+
+@pytest.mark.parametrize("K,V,dtype", [(64, 128, torch.float32), (128, 128, torch.bfloat16)])
+def test_transposed_state_layout_cuda_core_path_and_cut(K, V, dtype):
+    """The [V][K] state layout on the CUDA-core kernel (fp32 inputs, 64-wide keys) and on the
+    tensor-core kernel with a cut sequence (the combine writes the transposed final state):
+    the [K][V] run's results, transposed."""
+    w = synthetic.make([1500, 63, 130], Hk=2, Hv=4, K=K, V=V, dtype=dtype, seed=K + 7,
+                       state="pool", num_slots=6)
+    d = to_dev(w)
+    pool_kv = d["state"].clone()
+    o_kv, _ = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                state=pool_kv, state_indices=d["state_indices"])
+    pool_vk = d["state"].transpose(-1, -2).contiguous()
+    o_vk, _ = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                state=pool_vk, state_indices=d["state_indices"], state_layout="vk")
+    ws = kda.chunk_prefill.last_workspace
+    if dtype == torch.bfloat16:
+        assert int(ws[12:16].cpu().view(torch.int32)[0]) == 1  # the 1500-token sequence is cut
+    assert torch.equal(o_vk, o_kv)
+    assert torch.equal(pool_vk.transpose(-1, -2), pool_kv)
+    o_ref, pool_ref = _full_oracle(w)
+    assert_close(o_vk, o_ref, dtype, "o")
+    assert_close(pool_vk.transpose(-1, -2), pool_ref, dtype, "pool")
