@@ -136,7 +136,11 @@ struct LoaderState {
 struct Small {
   uint64_t bar[B_COUNT];
   ItemInfo ring[kRing];
+  // beta of the chunk in the intra group; read by its extraction and by the recurrence
+  // group's Tm, which is done before the next chunk writes it (that chunk's pass B waits for
+  // MMA-U/W, issued after Tm)
   alignas(16) float beta[kC];      // read as float4
+  float inv_nrm[128];              // q/k row norms of the staged chunk (KDA_FLAG_QK_L2NORM)
   alignas(16) float gamma[2][kK];  // read as float4
   // [chunk parity][sub-chunk][half][parity]: bit l = channel 64*half + 2l + parity
   uint32_t unsafe[2][4][2][2];
@@ -144,14 +148,22 @@ struct Small {
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t num_items;  // work-list entries x Hv
+  uint32_t whole[2];   // [chunk parity]: the chunk runs as one 64-token sub-chunk
 };
-constexpr uint32_t kSmemBytes = OFF_SMALL + sizeof(Small) + 1024;  // + alignment slack
+// The operand tiles need a 1024-byte aligned base.  The dynamic shared window of a CTA
+// starts 1024-byte aligned (after the 1 KB the system reserves per block), so the slack is
+// normally unused; a base that would need more than the slack is refused at run time.
+constexpr uint32_t kAlignSlack = 232448u - OFF_SMALL - (uint32_t)sizeof(Small) < 1024u
+                                     ? (232448u - OFF_SMALL - (uint32_t)sizeof(Small)) & ~15u
+                                     : 1024u;
+constexpr uint32_t kSmemBytes = OFF_SMALL + sizeof(Small) + kAlignSlack;
 static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
 static_assert(offsetof(Small, beta) % 16 == 0 && offsetof(Small, gamma) % 16 == 0,
               "vector-read arrays must be 16-byte aligned");
 
 struct TcParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_g;
+  CUtensorMap tm_o;   // o [T, Hv, V] bf16, boxes of 64 tokens x one head x 128 values (stores)
   const __nv_bfloat16 *q, *k;
   const float *g, *beta;
   GateAct act;        // act.a set: tm_g maps the gate input a (bf16) instead of g
@@ -537,6 +549,66 @@ __device__ __forceinline__ void gate_act_exp_b(const TcParams& p, uint8_t* sm, u
   }
 }
 
+// The rest of X = (I + A)^-1 from its inverted 16x16 diagonal blocks, by the four warps of
+// a group (aw = 0..3 within it, named barrier `bar` of 128 threads), with tf32 warp MMAs:
+// the two 32x32 diagonal halves X_{a+1,a} = -X_{a+1,a+1} (A_{a+1,a} X_aa) for a = 0, 2 (the
+// product staged in the unused upper block (a, a+1) of A), then the lower-left 32x32 block
+// -X2 (A21 X1): P_kj = sum_l A_kl X_lj into the upper blocks (k-2, j+2), one 16x16 block per
+// warp, and X_ij = -sum_{2<=k<=i} X_ik P_kj.  Ends with X complete (barrier).
+__device__ __forceinline__ void inverse_merges(float* As, float* Xs, int aw, int lane, uint32_t bar) {
+  if (aw < 2) {
+    const int a = aw * 2;
+    float acc[2][4] = {};
+    blk_mma(acc, As, (a + 1) * 16, a * 16, Xs, a * 16, a * 16, lane);
+    blk_store(As, a * 16, (a + 1) * 16, acc, 1.f, lane);
+    __syncwarp();
+    float acc2[2][4] = {};
+    blk_mma(acc2, Xs, (a + 1) * 16, (a + 1) * 16, As, a * 16, (a + 1) * 16, lane);
+    blk_store(Xs, (a + 1) * 16, a * 16, acc2, -1.f, lane);
+  }
+  named_bar(bar, 128);
+  {
+    const int kb = 2 + (aw >> 1), jb = aw & 1;
+    float acc[2][4] = {};
+#pragma unroll 1
+    for (int l = jb; l < 2; ++l) blk_mma(acc, As, kb * 16, l * 16, Xs, l * 16, jb * 16, lane);
+    blk_store(As, (kb - 2) * 16, (jb + 2) * 16, acc, 1.f, lane);
+  }
+  named_bar(bar, 128);
+  {
+    const int ib = 2 + (aw >> 1), jb = aw & 1;
+    float acc[2][4] = {};
+#pragma unroll 1
+    for (int kb = 2; kb <= ib; ++kb) blk_mma(acc, Xs, ib * 16, kb * 16, As, (kb - 2) * 16, (jb + 2) * 16, lane);
+    blk_store(Xs, ib * 16, jb * 16, acc, -1.f, lane);
+  }
+  named_bar(bar, 128);
+}
+
+// Tm = X Diag(beta) -> bf16, K-major rows in the TM buffer, by 128 threads (row r = i & 63,
+// columns 32 (i >> 6) ..).
+__device__ __forceinline__ void form_tm(uint8_t* sm, const float* Xs, const float* beta, int i) {
+  const int r = i & 63, qq = i >> 6;
+#pragma unroll
+  for (int u2 = 0; u2 < 4; ++u2) {
+    const int j = qq * 4 + u2;
+    const float4 xa = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8));
+    const float4 xb = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8 + 4));
+    const float4 ba = *reinterpret_cast<const float4*>(beta + j * 8);
+    const float4 bb4 = *reinterpret_cast<const float4*>(beta + j * 8 + 4);
+    const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+    const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb4.x, bb4.y, bb4.z, bb4.w};
+    uint32_t w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i0 = j * 8 + u * 2;
+      w[u] = pack_bf16x2((i0 <= r) ? xv[2 * u] * bv[2 * u] : 0.f,
+                         (i0 + 1 <= r) ? xv[2 * u + 1] * bv[2 * u + 1] : 0.f);
+    }
+    st_chunk(sm, OFF_TM + sw128_off(r, j), w[0], w[1], w[2], w[3]);
+  }
+}
+
 __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tbase) {
   const int t = threadIdx.x;  // 0..255
   const int warp = t >> 5, lane = t & 31;
@@ -544,8 +616,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
   const int L = quad * 32 + lane;  // TMEM lane of this thread
   const uint32_t taddr_q = tbase + ((uint32_t)(quad * 32) << 16);
   const uint32_t sbase = smem_u32(sm);
-  float* As = reinterpret_cast<float*>(sm + OFF_AS);
-  float* Xs = reinterpret_cast<float*>(sm + OFF_XS);
   Loader ld{&s->ld};
   uint32_t gc = 0;
   float bt_next = 0.f;  // beta of the next chunk, read one chunk ahead (threads 0-63)
@@ -651,7 +721,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         // staged rows (k 0-63, q 64-127) -> x / max(||x||, 1e-12), re-rounded to bf16 as a
         // caller's normalise-then-cast would; thread = (row, 64-channel half).  The inverse
         // norms are kept for the pairwise path, which reads q and k from global memory.
-        if (gc > 0) wait_bar(p, s, B_UW_DONE, (gc - 1) & 1);  // Tm buffer read by MMA-U/W(c-1)
         const int row = t >> 1, hf = t & 1;
         uint8_t* base = sm + OFF_QK + hf * 16384;
         float ss = 0.f;
@@ -677,7 +746,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             o4[u] = pack_bf16x2(bf_bits(u4[u] & 0xFFFFu) * inv, bf_bits(u4[u] >> 16) * inv);
           st_chunk(sm, OFF_QK + hf * 16384 + sw128_off(row, j), o4[0], o4[1], o4[2], o4[3]);
         }
-        if (hf == 0) reinterpret_cast<float*>(sm + OFF_TM + 2048)[row] = inv;
+        if (hf == 0) s->inv_nrm[row] = inv;
       }
       // QG buffer and this gamma buffer are free once MMA-1b of the previous chunk ran
       if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
@@ -693,8 +762,22 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // pi of this thread's own sub-chunk
       const float pm0 = sc == 0 ? pi0[0] : sc == 1 ? pi0[1] : sc == 2 ? pi0[2] : pi0[3];
       const float pm1 = sc == 0 ? pi1[0] : sc == 1 ? pi1[1] : sc == 2 ? pi1[2] : pi1[3];
-      // every warp holds e and the products before pass A/B overwrite CB and AM
-      named_bar(BAR_IG, kIG);
+      // Every warp holds e and the products before pass A/B overwrite CB and AM.  The same
+      // barrier takes the vote on the chunk's form: when the whole-chunk product gamma of
+      // every channel is >= 2^-100 (which puts every sub-chunk product above it too), the
+      // chunk runs as ONE 64-token sub-chunk -- the diagonal-block factorisation of the
+      // four-sub-chunk form applied to the whole chunk: A/B from [k rho; q rho] x (k/rho)^T
+      // with rho, the inclusive product from the chunk start, >= 2^-100, so that k rho and
+      // k/rho stay normal in bf16.  One CB block instead of three, no block-2 references,
+      // an N = 64 MMA-AB, and KG / QG are the MMA-AB operand itself.  Otherwise the chunk
+      // takes the four-sub-chunk form with its exact pairwise fallback.
+      const float gm0 = pi0[0] * pi0[1] * pi0[2] * pi0[3], gm1 = pi1[0] * pi1[1] * pi1[2] * pi1[3];
+      const bool whole = !named_bar_any(BAR_IG, kIG, !(gm0 >= kSafeMin) || !(gm1 >= kSafeMin));
+      if (t == 0) s->whole[gc & 1] = whole ? 1u : 0u;
+      // inverse scratch: in AM (free after MMA-AB) for the four-sub-chunk form; in the KG and
+      // QG buffers when AM is itself KG / QG
+      float* As = reinterpret_cast<float*>(sm + (whole ? OFF_KG : OFF_AS));
+      float* Xs = reinterpret_cast<float*>(sm + (whole ? OFF_QG : OFF_XS));
       const float E0 = (sc > 0 ? pi0[0] : 1.f) * (sc > 1 ? pi0[1] : 1.f) * (sc > 2 ? pi0[2] : 1.f);
       const float E1 = (sc > 0 ? pi1[0] : 1.f) * (sc > 1 ? pi1[1] : 1.f) * (sc > 2 ? pi1[2] : 1.f);
       if (sc == 3)  // warps 6-7 (no block-2 references): gamma of their 64 channels
@@ -722,6 +805,23 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             ka1 *= e1[j];
           }
           const uint32_t cj = sc * 2 + jh;
+          if (whole) {
+            // k / rho_r = (k kap_r) F_sc / gamma = (k kap_r) / (E_sc pi_sc), rounded once
+            const float fw0 = __fdividef(1.f, E0 * pm0), fw1 = __fdividef(1.f, E1 * pm1);
+            uint32_t xw[2][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              xw[0][u] = pack_bf16x2(kk[0][2 * u] * fw0, kk[0][2 * u + 1] * fw0);
+              xw[1][u] = pack_bf16x2(kk[1][2 * u] * fw1, kk[1][2 * u + 1] * fw1);
+            }
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+              const int c = c2 ^ wsel;
+              st_chunk(sm, OFF_CB + sw128_off(c0 + c, cj), c ? xw[1][0] : xw[0][0], c ? xw[1][1] : xw[0][1],
+                       c ? xw[1][2] : xw[0][2], c ? xw[1][3] : xw[0][3]);
+            }
+            continue;
+          }
           // both channels' 8 tokens as bf16 pairs: k kap, and k kap / pi rounded once from
           // fp32 (a second rounding on the diagonal blocks shows in the output); the
           // references scale the k kap pairs with one packed bf16 product each
@@ -761,6 +861,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         // pass B, ascending: rho (inclusive product from the sub-chunk start); q and k
         // rows of the MMA-AB operand in place, and KG, QG.
         const float qs0 = p.scale * E0, qs1 = p.scale * E1;
+        // one sub-chunk: the operand rows are k rho E and scale q rho E themselves (one
+        // rounding), which are KG and QG too
+        const float mk0 = whole ? E0 : 1.f, mk1 = whole ? E1 : 1.f;
+        const float mq0 = whole ? qs0 : 1.f, mq1 = whole ? qs1 : 1.f;
         float rho0 = 1.f, rho1 = 1.f;
 #pragma unroll
         for (int jh = 0; jh < 2; ++jh) {
@@ -780,8 +884,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             const int j = jh * 8 + u;
             rho0 *= e0[j];
             rho1 *= e1[j];
-            const float kr0 = bf_bits(kw[u] & 0xFFFFu) * rho0, kr1 = bf_bits(kw[u] >> 16) * rho1;
-            const float qr0 = bf_bits(qw[u] & 0xFFFFu) * rho0, qr1 = bf_bits(qw[u] >> 16) * rho1;
+            const float kr0 = bf_bits(kw[u] & 0xFFFFu) * (rho0 * mk0), kr1 = bf_bits(kw[u] >> 16) * (rho1 * mk1);
+            const float qr0 = bf_bits(qw[u] & 0xFFFFu) * (rho0 * mq0), qr1 = bf_bits(qw[u] >> 16) * (rho1 * mq1);
             if (u & 1) {
               kaw[0][u >> 1] = pack_bf16x2(pa0, kr0);
               kaw[1][u >> 1] = pack_bf16x2(pa1, kr1);
@@ -803,6 +907,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
                      c ? kaw[1][2] : kaw[0][2], c ? kaw[1][3] : kaw[0][3]);
             st_chunk(sm, OFF_AM + 16384 + sw128_off(row, cj), c ? qaw[1][0] : qaw[0][0],
                      c ? qaw[1][1] : qaw[0][1], c ? qaw[1][2] : qaw[0][2], c ? qaw[1][3] : qaw[0][3]);
+            if (whole) continue;  // the rows just written are KG and QG
             // KG = (k rho) E and QG = (q rho) scale E as packed products of the pairs above
             const uint32_t eg = c ? pack_bf16x2(E1, E1) : pack_bf16x2(E0, E0);
             st_chunk(sm, OFF_KG + sw128_off(row, cj), bmul2(c ? kaw[1][0] : kaw[0][0], eg),
@@ -822,7 +927,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         mbar_arrive(&s->bar[B_GAMMA0 + (gc & 1)]);
         if (gc > 0) wait_bar(p, s, B_W_FREE, (gc - 1) & 1);  // W of the last chunk read out
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16(128, 176, 1, 1);  // the last 16 CB columns are unused
+        // four sub-chunks: CB blocks 0-2 (the last 16 columns unused); one: block 0
+        const uint32_t idesc = whole ? idesc_bf16(128, 64, 1, 1) : idesc_bf16(128, 176, 1, 1);
 #pragma unroll 1
         for (int st = 0; st < 8; ++st) {
           const uint64_t a = sdesc_sw128(sbase + OFF_AM + st * 2048, 16384, 1024);
@@ -857,13 +963,14 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       __syncwarp();
       if (quad >= 2) {
         // KR = (k kap) F_s for sub-chunks sc-1 and sc of this thread's channel pair
-        // (F_s = product of pi after s), by the B group while the tensor core runs MMA-AB
+        // (F_s = product of pi after s), by the B group while the tensor core runs MMA-AB;
+        // one sub-chunk: KR = (k / rho) gamma
         if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
 #pragma unroll
         for (int s2 = 0; s2 < 2; ++s2) {
           const int sk = sc - 1 + s2;
-          const float fs0 = (sk < 1 ? pi0[1] : 1.f) * (sk < 2 ? pi0[2] : 1.f) * (sk < 3 ? pi0[3] : 1.f);
-          const float fs1 = (sk < 1 ? pi1[1] : 1.f) * (sk < 2 ? pi1[2] : 1.f) * (sk < 3 ? pi1[3] : 1.f);
+          const float fs0 = whole ? gm0 : (sk < 1 ? pi0[1] : 1.f) * (sk < 2 ? pi0[2] : 1.f) * (sk < 3 ? pi0[3] : 1.f);
+          const float fs1 = whole ? gm1 : (sk < 1 ? pi1[1] : 1.f) * (sk < 2 ? pi1[2] : 1.f) * (sk < 3 ? pi1[3] : 1.f);
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
             const int c = c2 ^ wsel;
@@ -897,6 +1004,16 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         const bool isB = L >= 64;
         const int a0 = (L & 32) ? 2 : 0;  // sub-chunks a0, a0+1 live in this warp
         float x[32];
+        if (whole) {  // one sub-chunk: token column i of every row is TMEM column i
+#pragma unroll
+          for (int bb = 0; bb < 2; ++bb) {
+            float v0[16];
+            tmem_ld16(taddr_q + TM_AB + 16 * (hx * 2 + bb), v0);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[bb * 16 + j] = v0[j];
+          }
+        } else {
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
           const int b = hx * 2 + bb;
@@ -921,6 +1038,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             x[bb * 16 + j] = val;
           }
         }
+        }
         tc_fence_before();
         if (any_unsafe == 0u) {
           // fast path: mask and scale straight from TMEM
@@ -939,14 +1057,15 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             }
           } else {
             if (gc > 0) wait_bar(p, s, B_M3A, (gc - 1) & 1);  // BB free
+            const float bsc = whole ? 1.f : p.scale;  // one sub-chunk: the q rows carry it
 #pragma unroll
             for (int jc = 0; jc < 4; ++jc) {
               uint32_t w[4];
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
                 const int i0 = hx * 32 + jc * 8 + u * 2;
-                w[u] = pack_bf16x2((i0 <= r) ? p.scale * x[jc * 8 + u * 2] : 0.f,
-                                   (i0 + 1 <= r) ? p.scale * x[jc * 8 + u * 2 + 1] : 0.f);
+                w[u] = pack_bf16x2((i0 <= r) ? bsc * x[jc * 8 + u * 2] : 0.f,
+                                   (i0 + 1 <= r) ? bsc * x[jc * 8 + u * 2 + 1] : 0.f);
               }
               st_chunk(sm, OFF_BB + sw128_off(r, hx * 4 + jc), w[0], w[1], w[2], w[3]);
             }
@@ -969,7 +1088,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         named_bar(BAR_IG, kIG);
         // exact pairwise terms of the diagonal sub-chunk blocks on "unsafe" channels
         if (hx == 0)
-          unsafe_diag_terms(p, s->unsafe[gc & 1], As, Xs, reinterpret_cast<const float*>(sm + OFF_TM + 2048),
+          unsafe_diag_terms(p, s->unsafe[gc & 1], As, Xs, s->inv_nrm,
                             L, t0, cv, kh, h);
         named_bar(BAR_IG, kIG);
         // A: mask + beta_r (in place, fp32); B: mask + scale -> bf16 -> BB
@@ -1007,9 +1126,9 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         named_bar(BAR_IG, kIG);
       }
       // ------------------------------------------------------------- inverse
-      // X = (I + A)^-1 by the A group: 16x16 diagonal blocks by forward substitution
-      // (one column per lane, two blocks per warp), then the two 32x32 diagonal halves
-      // and the lower-left 32x32 block from the 16x16 blocks (tf32 warp MMAs).
+      // X = (I + A)^-1: the 16x16 diagonal blocks here, by forward substitution on warps 0-1
+      // (one column per lane, two blocks per warp); the recurrence group, idle by then, forms
+      // the rest from them (inverse_merges) and Tm.
       if (agrp) {
         // gate of the next chunk into CB 1-2 (free since MMA-AB) by warp 4, idle during the
         // diagonal blocks
@@ -1064,40 +1183,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             }
           }
         }
-        named_bar(BAR_A, 128);
-        // 32x32 halves: X_{a+1,a} = -X_{a+1,a+1} (A_{a+1,a} X_aa) for a = 0, 2 (P staged
-        // in the unused upper block (a, a+1) of A) ...
-        const int aw = (warp >> 2) * 2 + (warp & 1);  // 0..3 within the A group
-        if (aw < 2) {
-          const int a = aw * 2;
-          float acc[2][4] = {};
-          blk_mma(acc, As, (a + 1) * 16, a * 16, Xs, a * 16, a * 16, lane);
-          blk_store(As, a * 16, (a + 1) * 16, acc, 1.f, lane);
-          __syncwarp();
-          float acc2[2][4] = {};
-          blk_mma(acc2, Xs, (a + 1) * 16, (a + 1) * 16, As, a * 16, (a + 1) * 16, lane);
-          blk_store(Xs, (a + 1) * 16, a * 16, acc2, -1.f, lane);
-        }
-        named_bar(BAR_A, 128);
-        // ... then the lower-left 32x32 block -X2 (A21 X1): P_kj = sum_l A_kl X_lj into the
-        // upper blocks (k-2, j+2), one 16x16 block per warp ...
-        {
-          const int kb = 2 + (aw >> 1), jb = aw & 1;
-          float acc[2][4] = {};
-#pragma unroll 1
-          for (int l = jb; l < 2; ++l) blk_mma(acc, As, kb * 16, l * 16, Xs, l * 16, jb * 16, lane);
-          blk_store(As, (kb - 2) * 16, (jb + 2) * 16, acc, 1.f, lane);
-        }
-        named_bar(BAR_A, 128);
-        // ... and X_ij = -sum_{2<=k<=i} X_ik P_kj
-        {
-          const int ib = 2 + (aw >> 1), jb = aw & 1;
-          float acc[2][4] = {};
-#pragma unroll 1
-          for (int kb = 2; kb <= ib; ++kb)
-            blk_mma(acc, Xs, ib * 16, kb * 16, As, (kb - 2) * 16, (jb + 2) * 16, lane);
-          blk_store(Xs, ib * 16, jb * 16, acc, -1.f, lane);
-        }
       } else {
         // while the A group inverts: e, products and masks of the next chunk of this item
         // (whose gate warp 4 loads: the lookahead within an item always succeeds).  CB
@@ -1113,29 +1198,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             gate_act_exp_b(p, sm, s->unsafe[(gc + 1) & 1], h, ncv, wgb, lane);
         }
       }
-      named_bar(BAR_IG, kIG);
-      // Tm = X Diag(beta) -> bf16 -> TM   (thread: row r = t & 63, columns 16*qq..16*qq+15)
-      {
-        const int r = t & 63, qq = t >> 6;
-#pragma unroll
-        for (int u2 = 0; u2 < 2; ++u2) {
-          const int j = qq * 2 + u2;
-          const float4 xa = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8));
-          const float4 xb = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8 + 4));
-          const float4 ba = *reinterpret_cast<const float4*>(&s->beta[j * 8]);
-          const float4 bb4 = *reinterpret_cast<const float4*>(&s->beta[j * 8 + 4]);
-          const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-          const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb4.x, bb4.y, bb4.z, bb4.w};
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i0 = j * 8 + u * 2;
-            w[u] = pack_bf16x2((i0 <= r) ? xv[2 * u] * bv[2 * u] : 0.f,
-                               (i0 + 1 <= r) ? xv[2 * u + 1] * bv[2 * u + 1] : 0.f);
-          }
-          st_chunk(sm, OFF_TM + sw128_off(r, j), w[0], w[1], w[2], w[3]);
-        }
-      }
+      // B rows (BB) visible to the tensor core; the diagonal blocks of X and the B group's
+      // gate of the next chunk complete
       fence_async_smem();
       named_bar(BAR_IG, kIG);
       if (t < kC && ld.st->nx[gc & 1].have) {
@@ -1143,7 +1207,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         if (t < nx.cv) bt_next = p.beta[(size_t)(nx.t0 + t) * p.Hv + nx.h];
         bt_ok = true;
       }
-      // hand the chunk to the recurrence group: it issues MMA-U/W and reads -W out itself
+      // hand the chunk to the recurrence group: it completes X and Tm, issues MMA-U/W and
+      // reads -W out itself
       if (t == 0) mbar_arrive(&s->bar[B_REC_READY]);
       __syncwarp();
     }
@@ -1263,6 +1328,9 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
 
     bool stop = false;
     for (int lc = 0; lc < info.nchunks; ++lc, ++gc) {
+      // the output staging tile (the U^T buffer) is read by the TMA store of the chunk
+      // before, if any, before this chunk writes U^T (after the vote)
+      if (rt == 0) bulk_wait_read();
       if (named_bar_any(BAR_RG, kRG, aborted(s))) { stop = true; break; }
       const int64_t t0 = info.bos + (int64_t)lc * kC;
       const int cv = (int)min((int64_t)kC, info.eos - t0);
@@ -1271,19 +1339,36 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       // takes new work only when it is about to run out (dynamic longest-first
       // scheduling); the claim's global round trips overlap this group's slack
       if (rt == 32 && lc == (info.nchunks > 3 ? info.nchunks - 3 : 0)) ld.push_one(p, s);
-      // ---- R0 (leader warp): O = S QG^T first (frees QG and gamma for the next chunk's
-      // prologue soonest), then U~^T = V^T Tm^T and W^T = KG^T Tm^T; -W^T rows -> WB
+      // ---- R0: the hand-over.  O = S QG^T first (frees QG and gamma for the next chunk's
+      // prologue soonest), then X and Tm from the diagonal blocks the intra group inverted,
+      // then U~^T = V^T Tm^T and W^T = KG^T Tm^T; -W^T rows -> WB
+      wait_bar(p, s, B_REC_READY, gc & 1);
+      // a chunk run as one sub-chunk keeps KG and QG in the MMA-AB operand buffer, and the
+      // inverse scratch in the KG / QG buffers
+      const bool whole = s->whole[gc & 1] != 0u;
+      if (rt == 0) {
+        tc_fence_after();
+        const uint32_t off_qg = whole ? OFF_AM + 16384 : OFF_QG;
+        const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
+#pragma unroll 1
+        for (int st = 0; st < 8; ++st)
+          mma_bf16_ta(tbase + TM_O, tbase + TM_SB + st * 8,
+                      sdesc_sw128(sbase + off_qg + st * 2048, 16384, 1024), id1, st > 0 ? 1u : 0u);
+        mma_commit(&s->bar[B_M1B]);
+      }
+      {
+        float* As = reinterpret_cast<float*>(sm + (whole ? OFF_KG : OFF_AS));
+        float* Xs = reinterpret_cast<float*>(sm + (whole ? OFF_QG : OFF_XS));
+        inverse_merges(As, Xs, warp - kIG / 32, lane, BAR_RG);
+        form_tm(sm, Xs, s->beta, rt);
+        fence_async_smem();
+        named_bar(BAR_RG, kRG);
+      }
       if (leader_warp) {
-        wait_bar(p, s, B_REC_READY, gc & 1);
         wait_bar(p, s, B_V_FULL, gc & 1);
         if (lane == 0) {
           tc_fence_after();
-          const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
-#pragma unroll 1
-          for (int st = 0; st < 8; ++st)
-            mma_bf16_ta(tbase + TM_O, tbase + TM_SB + st * 8,
-                        sdesc_sw128(sbase + OFF_QG + st * 2048, 16384, 1024), id1, st > 0 ? 1u : 0u);
-          mma_commit(&s->bar[B_M1B]);
+          const uint32_t off_kg = whole ? OFF_AM : OFF_KG;
           const uint32_t idu = idesc_bf16(128, 64, 1, 0), idw = idesc_bf16(128, 64, 0, 0);
 #pragma unroll 1
           for (int st = 0; st < 4; ++st) {
@@ -1291,7 +1376,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
             if (!ident)
               mma_bf16(tbase + TM_U, sdesc_sw128(sbase + OFF_VB + st * 2048, 8192, 1024), b, idu,
                        st > 0 ? 1u : 0u);
-            mma_bf16(tbase + TM_AB, sdesc_sw128(sbase + OFF_KG + st * 32, 16, 1024), b, idw,
+            mma_bf16(tbase + TM_AB, sdesc_sw128(sbase + off_kg + st * 32, 16, 1024), b, idw,
                      st > 0 ? 1u : 0u);
           }
           mma_commit(&s->bar[B_UW_DONE]);
@@ -1419,8 +1504,27 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       // 64 contiguous bytes of one output row per store
       wait_bar(p, s, B_M3A, gc & 1);
       tc_fence_after();
-      {
-        // the identity pass writes y (K = V wide rows) into the split scratch instead of o
+      if (!ident && cv == kC) {
+        // a full chunk of o: rows of the [64 tokens][128 values] tile in the U^T buffer (free:
+        // MMA-3a/3b ran), each thread writing its value channel, then one TMA store
+        __nv_bfloat16* os = reinterpret_cast<__nv_bfloat16*>(sm + OFF_UT);
+#pragma unroll 1
+        for (int cq = 0; cq < 4; ++cq) {
+          float ov[16];
+          tmem_ld16(taddr_q + TM_O + cq * 16, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 16; ++u) os[(cq * 16 + u) * kV + v] = __float2bfloat16_rn(ov[u]);
+        }
+        fence_async_smem();
+        named_bar(BAR_RG, kRG);
+        if (rt == 0) {
+          tma_store_3d(&p.tm_o, os, 0, h, (int)t0);
+          bulk_commit();
+        }
+      } else {
+        // a partial chunk (its tile would cover the next sequence's rows) or the identity
+        // pass (y into the split scratch instead of o): each thread stores its column
         __nv_bfloat16* od = ident ? p.y + ((size_t)(t0 - info.bos + info.ybase) * p.Hv + h) * kV + v
                                   : p.o + ((size_t)t0 * p.Hv + h) * kV + v;
         const size_t rs = (size_t)p.Hv * kV;
@@ -1438,6 +1542,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
     }
     if (stop) break;
   }
+  if (rt == 0) bulk_wait_all();  // the output stores this thread issued have completed
   named_bar(BAR_RG, kRG);
   if (leader_warp) {
     if (lane == 0) mma_commit(&s->bar[B_DRAIN_RG]);
@@ -1452,7 +1557,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
   // 1024-byte aligned base, formed as an offset into the shared array (not through an
   // integer round trip) so that the compiler keeps every derived pointer in the shared
   // window and emits shared loads and stores rather than generic ones
-  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad > kAlignSlack) {  // uniform: no barrier, load or TMEM has been touched yet
+    if (threadIdx.x == 0) raise_status(p.status, KDA_DEVICE_PIPE_TIMEOUT);
+    return;
+  }
+  uint8_t* sm = smem_raw + pad;
   Small* s = reinterpret_cast<Small*>(sm + OFF_SMALL);
   const int warp = threadIdx.x >> 5;
   // the combine kernel after this one may be scheduled as SMs free up (it waits for this
@@ -1468,6 +1578,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     prefetch_tensormap(&p.tm_k);
     prefetch_tensormap(&p.tm_v);
     prefetch_tensormap(&p.tm_g);
+    prefetch_tensormap(&p.tm_o);
   }
   if (warp == 0) tmem_alloc(&s->tmem_base, 512);
   // everything above overlaps the planning kernel; the work list is read only after it
@@ -1515,9 +1626,6 @@ constexpr uint32_t kCodeN = 0x0FFFFFFFu;
 __device__ __forceinline__ int64_t seq_len_checked(const int32_t* cu, int n, int64_t T) {
   const int64_t a = cu[n], b = cu[n + 1];
   return (a >= 0 && b >= a && b <= T) ? b - a : 0;  // bad bounds: reported by the prefill
-}
-__device__ __forceinline__ int64_t chunks_of(const int32_t* cu, int n, int64_t T) {
-  return (seq_len_checked(cu, n, T) + kC - 1) / kC;
 }
 __device__ __forceinline__ int order_key(int64_t chunks) {
   return (int)min(chunks, (int64_t)(kOrderKeys - 1));
@@ -2002,6 +2110,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, d.num_v_heads, kV, 64,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&p.tm_o, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, d.num_v_heads, kV, kV,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !(a.gate_k == 1
               ? (a.act.a ? make_map_2d(&p.tm_g, a.act.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T,
                                        d.num_v_heads, 8)

@@ -312,3 +312,30 @@ def test_transposed_state_layout_cuda_core_path_and_cut(K, V, dtype):
     o_ref, pool_ref = _full_oracle(w)
     assert_close(o_vk, o_ref, dtype, "o")
     assert_close(pool_vk.transpose(-1, -2), pool_ref, dtype, "pool")
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+def test_chunk_forms_alternate_within_an_item(state_dtype):
+    """Chunks whose every key channel keeps its whole-chunk decay product above 2^-100 run as
+    one 64-token sub-chunk; the others as four 16-token sub-chunks with the exact pairwise
+    fallback.  Gates 40x stronger on every other 64-token block (aligned to the sequence
+    starts) make consecutive chunks of one item alternate between the two forms, and a
+    partial last chunk end each sequence."""
+    lens = [64 * 9 + 17, 64 * 4, 64 * 7 + 1]
+    w = synthetic.make(lens, Hk=2, Hv=4, K=128, V=128, seed=61, state="pool", num_slots=5,
+                       state_dtype=state_dtype)
+    cu = w.cu_seqlens.tolist()
+    f = torch.ones(w.T)
+    for n in range(len(lens)):
+        for c0 in range(cu[n] + 64, cu[n + 1], 128):
+            f[c0:c0 + 64] = 40.0
+    w.g = (w.g * f[:, None, None]).contiguous()
+    d = to_dev(w)
+    pool_before = w.state.clone()
+    o, pool = kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                                state=d["state"], state_indices=d["state_indices"])
+    assert kda.read_device_status(kda.chunk_prefill.last_workspace) == 0
+    o_ref, pool_ref = _full_oracle(w, state=pool_before)
+    assert_items_close(o, o_ref, cu, torch.bfloat16, "o")
+    slots = w.state_indices.long()
+    assert_rows_close(pool[slots.cuda()], pool_ref[slots.numpy()], torch.bfloat16, "pool rows")
