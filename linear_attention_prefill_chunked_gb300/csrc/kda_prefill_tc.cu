@@ -34,9 +34,10 @@
 //
 // CTA = 12 warps, one CTA per SM, persistent over (sequence, head) items sorted
 // longest first and claimed from a global counter near the end of the item before:
-//   warps 0-7   intra group (S-independent work of chunk c+1; the B-group warps
-//               2, 3, 6, 7 also turn the gate of chunk c+2 into e)
-//   warps 8-11  recurrence group (Tm, state update and output of chunk c)
+//   warps 0-7   intra group (S-independent work of chunk c+1 up to the inverted 16x16
+//               diagonal blocks of (I + A))
+//   warps 8-11  recurrence group (the rest of the inverse, Tm, state update and output
+//               of chunk c)
 // Pool I/O (sglang PR 30169 digest, 实现拆解 items 1-3) is fused: the
 // recurrence group reads h0 from pool[state_indices[n]] (-1 -> last slot) and
 // writes the final state back to the same row.
@@ -481,74 +482,6 @@ __device__ __forceinline__ void gate_exp_inplace(uint8_t* sm, uint32_t (*uns)[2]
   }
 }
 
-// The same for a staged activated gate (a, bf16 [64][128]) or a staged scalar gate
-// ([64 tokens][gw heads], col = this head's column), by the four B-group warps (wg 0-3,
-// sub-chunks wg / 2 and wg / 2 + 2).  The fp32 e rows overwrite the staged input (e row r
-// covers a rows 2r and 2r+1; the scalar tile lies under the first two), so every thread
-// reads all of its inputs before the group's barrier and writes only after it.
-__device__ __forceinline__ void gate_act_exp_b(const TcParams& p, uint8_t* sm, uint32_t (*uns)[2][2], int h,
-                                               int cv, int wg, int lane) {
-  const int half = wg & 1, c0 = 2 * (half * 32 + lane), sc0 = wg >> 1;
-  const int gk = p.gate_k, col = h & (p.gw - 1);
-  float* Es = reinterpret_cast<float*>(sm + OFF_G);
-  float* pis = reinterpret_cast<float*>(sm + OFF_CB);
-  uint32_t raw[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int r = (sc0 + 2 * (i >> 4)) * 16 + (i & 15);
-    if (gk == 1)
-      raw[i] = p.act.a ? (uint32_t)reinterpret_cast<const uint16_t*>(sm + OFF_G)[r * 8 + col]
-                       : reinterpret_cast<const uint32_t*>(sm + OFF_G)[r * 4 + col];
-    else
-      raw[i] = *reinterpret_cast<const uint32_t*>(sm + OFF_G + r * 256 + c0 * 2);
-  }
-  float gA = 0.f, gdb0 = 0.f, gdb1 = 0.f;  // activation constants of head h, channels c0, c0+1
-  if (p.act.a) {
-    gA = __expf(p.act.A_log[h]);
-    if (p.act.dt_bias) {
-      gdb0 = p.act.dt_bias[(size_t)h * gk + (gk > 1 ? c0 : 0)];
-      gdb1 = p.act.dt_bias[(size_t)h * gk + (gk > 1 ? c0 + 1 : 0)];
-    }
-  }
-  named_bar(BAR_B, 128);
-#pragma unroll
-  for (int i2 = 0; i2 < 2; ++i2) {
-    const int sc = sc0 + 2 * i2;
-    float pm0 = 1.f, pm1 = 1.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int r = sc * 16 + j;
-      const uint32_t w = raw[i2 * 16 + j];
-      float g0, g1;
-      if (gk == 1) {
-        if (p.act.a) {
-          const float x = bf_bits(w) + gdb0;
-          g0 = fmaxf(-gA * (fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)))), p.act.lb);
-        } else {
-          g0 = __uint_as_float(w);
-        }
-        g1 = g0;
-      } else {
-        const float x0 = bf_bits(w & 0xFFFFu) + gdb0, x1 = bf_bits(w >> 16) + gdb1;
-        g0 = fmaxf(-gA * (fmaxf(x0, 0.f) + __logf(1.f + __expf(-fabsf(x0)))), p.act.lb);
-        g1 = fmaxf(-gA * (fmaxf(x1, 0.f) + __logf(1.f + __expf(-fabsf(x1)))), p.act.lb);
-      }
-      const float e0 = (r < cv) ? exp_ftz(g0) : 1.f;  // padded rows: decay 1
-      const float e1 = (r < cv) ? exp_ftz(g1) : 1.f;
-      *reinterpret_cast<float2*>(Es + r * kK + c0) = make_float2(e0, e1);
-      pm0 *= e0;
-      pm1 *= e1;
-    }
-    *reinterpret_cast<float2*>(pis + sc * kK + c0) = make_float2(pm0, pm1);
-    const uint32_t m0 = __ballot_sync(0xffffffffu, !(pm0 >= kSafeMin));
-    const uint32_t m1 = __ballot_sync(0xffffffffu, !(pm1 >= kSafeMin));
-    if (lane == 0) {
-      uns[sc][half][0] = m0;
-      uns[sc][half][1] = m1;
-    }
-  }
-}
-
 // The rest of X = (I + A)^-1 from its inverted 16x16 diagonal blocks, by the four warps of
 // a group (aw = 0..3 within it, named barrier `bar` of 128 threads), with tf32 warp MMAs:
 // the two 32x32 diagonal halves X_{a+1,a} = -X_{a+1,a+1} (A_{a+1,a} X_aa) for a = 0, 2 (the
@@ -635,11 +568,15 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       const int64_t t0 = info.bos + (int64_t)lc * kC;
       const int cv = (int)min((int64_t)kC, info.eos - t0);
       // q/k and the gate of this chunk were issued during the previous chunk iff its
-      // lookahead found this one; its gate was turned into e (fp32, in the staging buffer)
-      // by the B group during the previous chunk of the same item.  Otherwise thread 0
-      // issues the loads here and each thread computes its e here.  (v: during MMA-AB.)
+      // lookahead found this one; otherwise thread 0 issues them here.  A plain fp32
+      // per-channel gate was turned into e (in its staging buffer) by the B group while the
+      // A group inverted the diagonal blocks of the chunk before in the same item; an
+      // activated gate (three multi-function operations per element) or a scalar gate, and
+      // the first chunk of an item, are turned into e here by all intra threads.
+      // (v: during MMA-AB.)
       const bool ahead = gc > 0 && ld.st->nx[(gc - 1) & 1].have;
-      const bool e_ahead = lc > 0;
+      const bool plain_gate = p.gate_k > 1 && !p.act.a;
+      const bool e_ahead = plain_gate && lc > 0;
       if (t == 0) {
         if (!ahead) ld.load_qk(p, sm, s, kh, (int)t0);
         if (ld.st->n_g == gc) ld.load_g(p, sm, s, h, (int)t0);
@@ -774,6 +711,11 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       const float gm0 = pi0[0] * pi0[1] * pi0[2] * pi0[3], gm1 = pi1[0] * pi1[1] * pi1[2] * pi1[3];
       const bool whole = !named_bar_any(BAR_IG, kIG, !(gm0 >= kSafeMin) || !(gm1 >= kSafeMin));
       if (t == 0) s->whole[gc & 1] = whole ? 1u : 0u;
+      // the gate staging (CB blocks 1-2) is free from here on when this chunk is whole (every
+      // thread holds its e, and the one-sub-chunk form neither writes nor reads blocks 1-2):
+      // the next chunk of this item gets its gate now, a whole chunk ahead of its use
+      if (t == 128 && whole && !plain_gate && lc + 1 < info.nchunks && ld.st->n_g == gc + 1)
+        ld.load_g(p, sm, s, h, (int)(t0 + kC));
       // inverse scratch: in AM (free after MMA-AB) for the four-sub-chunk form; in the KG and
       // QG buffers when AM is itself KG / QG
       float* As = reinterpret_cast<float*>(sm + (whole ? OFF_KG : OFF_AS));
@@ -1132,7 +1074,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       if (agrp) {
         // gate of the next chunk into CB 1-2 (free since MMA-AB) by warp 4, idle during the
         // diagonal blocks
-        if (t == 128 && ld.st->nx[gc & 1].have) {
+        if (t == 128 && ld.st->nx[gc & 1].have && ld.st->n_g == gc + 1) {  // not issued early
           const NextChunk& nx = ld.st->nx[gc & 1];
           ld.load_g(p, sm, s, nx.h, nx.t0);
         }
@@ -1183,23 +1125,16 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             }
           }
         }
-      } else {
+      } else if (plain_gate && lc + 1 < info.nchunks) {
         // while the A group inverts: e, products and masks of the next chunk of this item
-        // (whose gate warp 4 loads: the lookahead within an item always succeeds).  CB
-        // block 0 is free once every B-group thread is past KR (the barrier).
-        named_bar(BAR_B, 128);
-        if (lc + 1 < info.nchunks) {
-          const int ncv = (int)min((int64_t)kC, info.eos - (t0 + kC));
-          const int wgb = (warp >> 2) * 2 + (warp & 1);
-          wait_bar(p, s, B_G_FULL, (gc + 1) & 1);
-          if (p.gate_k > 1 && !p.act.a)
-            gate_exp_inplace(sm, s->unsafe[(gc + 1) & 1], ncv, wgb, 4, lane);
-          else
-            gate_act_exp_b(p, sm, s->unsafe[(gc + 1) & 1], h, ncv, wgb, lane);
-        }
+        // (whose gate warp 4 loads: the lookahead within an item always succeeds)
+        named_bar(BAR_B, 128);  // CB block 0 (the products) is free once the B group is past KR
+        const int ncv = (int)min((int64_t)kC, info.eos - (t0 + kC));
+        const int wgb = (warp >> 2) * 2 + (warp & 1);
+        wait_bar(p, s, B_G_FULL, (gc + 1) & 1);
+        gate_exp_inplace(sm, s->unsafe[(gc + 1) & 1], ncv, wgb, 4, lane);
       }
-      // B rows (BB) visible to the tensor core; the diagonal blocks of X and the B group's
-      // gate of the next chunk complete
+      // B rows (BB) visible to the tensor core; the diagonal blocks of X complete
       fence_async_smem();
       named_bar(BAR_IG, kIG);
       if (t < kC && ld.st->nx[gc & 1].have) {
