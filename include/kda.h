@@ -62,6 +62,8 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype_t;
 #define KDA_DEVICE_BAD_SLOT      0x1u  /* state index < -1 or >= num_slots          */
 #define KDA_DEVICE_BAD_SEQLENS   0x2u  /* cu_seqlens not monotone / outside [0, T]  */
 #define KDA_DEVICE_PIPE_TIMEOUT  0x4u  /* an internal pipeline wait gave up         */
+#define KDA_DEVICE_DEBUG_BOUNDS  0x8u  /* debug build only: a computed index fell outside
+                                          its buffer (the access was skipped)         */
 
 /* Descriptor flags. */
 #define KDA_FLAG_CUDA_CORE_PATH  0x1u  /* prefill: run the fp32 CUDA-core kernel even where

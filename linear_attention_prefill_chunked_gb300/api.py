@@ -22,6 +22,7 @@ KDA_FLAG_SCALAR_GATE = 0x2
 KDA_FLAG_QK_L2NORM = 0x4
 KDA_FLAG_STATE_VK = 0x8
 KDA_DEVICE_BAD_SLOT, KDA_DEVICE_BAD_SEQLENS, KDA_DEVICE_PIPE_TIMEOUT = 0x1, 0x2, 0x4
+KDA_DEVICE_DEBUG_BOUNDS = 0x8
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
            3: "workspace too small", 4: "CUDA error", 5: "invalid device data"}
 
@@ -60,8 +61,13 @@ EXPORTS = ("kda_chunk_prefill_workspace_size", "kda_chunk_prefill_min_workspace_
 _lib = None
 
 
+def debug_build() -> bool:
+    """KDA_DEBUG=1 selects the bounds-checked library (libkda_gb300_debug.so)."""
+    return os.environ.get("KDA_DEBUG", "") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.LIB_DEBUG if debug_build() else _build.LIB
 
 
 def load(build_if_missing: bool = True):
@@ -69,11 +75,12 @@ def load(build_if_missing: bool = True):
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(_build.LIB) and not build_if_missing:
-        raise RuntimeError(f"{_build.LIB} is missing; run __graft_entry__.build()")
+    path = library_path()
+    if not os.path.exists(path) and not build_if_missing:
+        raise RuntimeError(f"{path} is missing; run __graft_entry__.build()")
     if build_if_missing:
-        _build.build()  # no-op unless a source is newer than the library
-    lib = ctypes.CDLL(_build.LIB)
+        _build.build(debug=debug_build())  # no-op unless a source is newer than the library
+    lib = ctypes.CDLL(path)
     P = ctypes.c_void_p
     D = ctypes.POINTER(KdaDesc)
     lib.kda_chunk_prefill_workspace_size.argtypes = [D]

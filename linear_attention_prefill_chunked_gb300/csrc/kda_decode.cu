@@ -19,6 +19,8 @@
 namespace kda {
 namespace {
 
+KDA_DEBUG_FLAG_DEFINE();
+
 constexpr int kDecThreads = 256;
 
 template <typename ST> struct Vec4;
@@ -108,7 +110,8 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
   for (int j = 0; j < RPT; ++j) Vec4<ST>::load(S + (size_t)(rg + j * RG) * V, s[j]);
 
   for (int64_t t = bos; t < eos; ++t) {
-    if (t > bos) __syncthreads();  // the previous step's readers of the shared arrays are done
+    if (t > bos) __syncthreads();
+    if (!KDA_CHECK(t >= 0 && t < T && t - bos < dr.max_steps)) break;  // uniform  // the previous step's readers of the shared arrays are done
     // k, q, exp(g) of token t into shared memory (registers stay with the state tile);
     // with l2norm the two norms are reduced over the block first
     float kv = 0.f, qv = 0.f;
@@ -202,6 +205,7 @@ kda_decode_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const QT* 
       }
     }
   }
+  if (tid == 0) KDA_DEBUG_FOLD(status);
   if (dr.update_pool) {
 #pragma unroll
     for (int j = 0; j < RPT; ++j) Vec4<ST>::store(S + (size_t)(rg + j * RG) * V, s[j]);
@@ -258,6 +262,7 @@ kda_decode_vk_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const Q
 
   for (int64_t t = bos; t < eos; ++t) {
     if (t > bos) __syncthreads();
+    if (!KDA_CHECK(t >= 0 && t < T && t - bos < dr.max_steps)) break;  // uniform
     float kv = 0.f, qv = 0.f;
     if (tid < K) {
       kv = to_f32(k[((size_t)t * Hk + kh) * K + tid]);
@@ -327,6 +332,7 @@ kda_decode_vk_kernel(const QT* __restrict__ q, const QT* __restrict__ k, const Q
       if (C) Vec4<ST>::store(C + (size_t)row * K, s[j]);
     }
   }
+  if (tid == 0) KDA_DEBUG_FOLD(status);
   if (dr.update_pool) {
 #pragma unroll
     for (int j = 0; j < RPT; ++j) Vec4<ST>::store(S + (size_t)(rg + j * RG) * K, s[j]);

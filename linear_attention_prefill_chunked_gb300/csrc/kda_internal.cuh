@@ -25,6 +25,21 @@ __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {
   atomicOr(status, bit);
 }
 
+// Bounds checks of computed indices in the debug build (compiled with -DKDA_DEBUG): a failed
+// check records itself in a per-file device flag and the access it guards is skipped (never a
+// trap); each kernel folds the flag into KDA_DEVICE_DEBUG_BOUNDS of its status word before it
+// returns.  In the normal build KDA_CHECK(c) is the constant true and costs nothing.
+#ifdef KDA_DEBUG
+#define KDA_DEBUG_FLAG_DEFINE() static __device__ unsigned int g_kda_bounds = 0
+#define KDA_CHECK(c) ((c) ? true : (atomicOr(&g_kda_bounds, 1u), false))
+#define KDA_DEBUG_FOLD(status) \
+  do { if (*(volatile unsigned int*)&g_kda_bounds) atomicOr((status), KDA_DEVICE_DEBUG_BOUNDS); } while (0)
+#else
+#define KDA_DEBUG_FLAG_DEFINE() static_assert(true, "")
+#define KDA_CHECK(c) true
+#define KDA_DEBUG_FOLD(status) do { } while (0)
+#endif
+
 // ---- element conversions ----------------------------------------------------
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }

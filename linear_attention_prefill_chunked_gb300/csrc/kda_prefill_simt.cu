@@ -23,6 +23,8 @@
 namespace kda {
 namespace {
 
+KDA_DEBUG_FLAG_DEFINE();
+
 constexpr int kC = 64;          // chunk size
 constexpr int kSimtThreads = 256;
 
@@ -210,7 +212,7 @@ kda_prefill_simt_kernel(const QT* __restrict__ q, const QT* __restrict__ k,
       float acc = 0.f;
       for (int ch = 0; ch < K; ++ch) acc = fmaf(Qb[r * KP + ch], S[ch * V + j], acc);
       for (int i = 0; i <= r; ++i) acc = fmaf(Bm[r * AP + i], Kb[i * DP + j], acc);
-      o[((size_t)(t0 + r) * Hv + h) * V + j] = from_f32<QT>(acc);
+      if (KDA_CHECK(t0 + r < T)) o[((size_t)(t0 + r) * Hv + h) * V + j] = from_f32<QT>(acc);
     }
     __syncthreads();
     // ---- S <- Diag(exp Gamma_last) S + KR^T U
@@ -225,6 +227,7 @@ kda_prefill_simt_kernel(const QT* __restrict__ q, const QT* __restrict__ k,
   if (dst)
     for (int e = tid; e < K * V; e += kSimtThreads)
       dst[state_vk ? (e % V) * K + e / V : e] = from_f32<ST>(S[e]);
+  if (tid == 0) KDA_DEBUG_FOLD(status);
 }
 
 template <typename QT, typename ST, int K, int V>

@@ -51,6 +51,7 @@
 namespace kda {
 namespace {
 
+KDA_DEBUG_FLAG_DEFINE();
 using namespace tc;
 
 constexpr int kC = 64;
@@ -185,6 +186,7 @@ struct TcParams {
   uint32_t* status;
   uint32_t* next_item;
   uint64_t wait_limit_ns;    // bound of the pipeline waits (kWaitLimitNs unless set shorter)
+  int32_t max_cuts, ytok_cap;  // capacities of the split scratch (bounds checks)
   int32_t N, Hk, Hv;
   int64_t T, num_slots, slot_stride;
   float scale;
@@ -194,14 +196,20 @@ struct TcParams {
 __device__ __forceinline__ float bf_bits(uint32_t b16) { return __uint_as_float(b16 << 16); }
 // Element (row, ch) of a K-major operand with 128 channels in two 64-wide atoms.
 __device__ __forceinline__ uint32_t kmaj_elem(uint32_t row, uint32_t ch, uint32_t rows_per_atom) {
-  return (ch >> 6) * rows_per_atom * 128u + sw128_off(row, (ch & 63u) >> 3) + (ch & 7u) * 2u;
+  const uint32_t off = (ch >> 6) * rows_per_atom * 128u + sw128_off(row, (ch & 63u) >> 3) + (ch & 7u) * 2u;
+  return KDA_CHECK(off + 4u <= 2u * rows_per_atom * 128u) ? off : 0u;  // inside its tile
 }
 __device__ __forceinline__ void st_chunk(uint8_t* sm, uint32_t off, uint32_t a, uint32_t b,
                                          uint32_t c, uint32_t d) {
-  *reinterpret_cast<uint4*>(sm + off) = make_uint4(a, b, c, d);
+  if (KDA_CHECK(off % 16u == 0u && off + 16u <= OFF_SMALL))  // inside the operand tiles
+    *reinterpret_cast<uint4*>(sm + off) = make_uint4(a, b, c, d);
 }
-// fp32 64x64 scratch index with an XOR swizzle (conflict-free row and fragment reads)
-__device__ __forceinline__ int sidx(int r, int i) { return r * 64 + (i ^ ((r & 7) << 2)); }
+// fp32 64x64 scratch index with an XOR swizzle (conflict-free row and fragment reads); the
+// debug build maps an index outside the 64x64 tile to element 0 after recording it
+__device__ __forceinline__ int sidx(int r, int i) {
+  if (!KDA_CHECK(r >= 0 && r < 64 && i >= 0 && i < 64)) return 0;
+  return r * 64 + (i ^ ((r & 7) << 2));
+}
 
 __device__ __forceinline__ void fail(const TcParams& p, Small* s) {
   if (atomicExch(&s->abort, 1u) == 0u) raise_status(p.status, KDA_DEVICE_PIPE_TIMEOUT);
@@ -239,6 +247,7 @@ __device__ ItemInfo fetch_item(const TcParams& p, Small* s) {
   for (;;) {
     const uint32_t it = aborted(s) ? s->num_items : atomicAdd(p.next_item, 1u);
     if (it >= s->num_items) { info.done = 1; return info; }
+    if (!KDA_CHECK(it / (uint32_t)p.Hv < (uint32_t)p.N + 2u * (uint32_t)p.max_cuts)) continue;
     const uint32_t code = p.work[it / p.Hv];
     const int n = (int)(code & 0x0FFFFFFFu), kind = (int)(code >> 28), h = it % p.Hv;
     int64_t bos, eos;
@@ -254,7 +263,7 @@ __device__ ItemInfo fetch_item(const TcParams& p, Small* s) {
       const int ns = (int)p.hdr->num_splits;
       for (int i = 0; i < ns; ++i)
         if (p.splits[i].n == n) info.split = i;
-      if (info.split < 0) continue;  // not reachable: every cut entry has its record
+      if (info.split < 0 || !KDA_CHECK(info.split < p.max_cuts)) continue;
       const SplitInfo sp = p.splits[info.split];
       const int64_t cut = bos + (int64_t)sp.cut * kC;
       if (kind == KIND_HEAD) {
@@ -590,7 +599,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       const int sc = warp >> 1, cp = (warp & 1) * 32 + lane, c0 = 2 * cp;
       const int wsel = (lane >> 2) & 1;  // channel this lane writes first
       float bt = 0.f;  // beta of token t, needed only after the prologue
-      if (t < kC && t < cv) bt = bt_ok ? bt_next : p.beta[(size_t)(t0 + t) * p.Hv + h];
+      if (t < kC && t < cv && KDA_CHECK(t0 + t < p.T))
+        bt = bt_ok ? bt_next : p.beta[(size_t)(t0 + t) * p.Hv + h];
       bt_ok = false;
       float e0[16], e1[16];
       if (!e_ahead) {  // e of this chunk from the staged gate, into registers
@@ -1139,7 +1149,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       named_bar(BAR_IG, kIG);
       if (t < kC && ld.st->nx[gc & 1].have) {
         const NextChunk& nx = ld.st->nx[gc & 1];
-        if (t < nx.cv) bt_next = p.beta[(size_t)(nx.t0 + t) * p.Hv + nx.h];
+        if (t < nx.cv && KDA_CHECK((int64_t)nx.t0 + t < p.T))
+          bt_next = p.beta[(size_t)(nx.t0 + t) * p.Hv + nx.h];
         bt_ok = true;
       }
       // hand the chunk to the recurrence group: it completes X and Tm, issues MMA-U/W and
@@ -1453,7 +1464,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         }
         fence_async_smem();
         named_bar(BAR_RG, kRG);
-        if (rt == 0) {
+        if (rt == 0 && KDA_CHECK(t0 + kC <= p.T)) {
           tma_store_3d(&p.tm_o, os, 0, h, (int)t0);
           bulk_commit();
         }
@@ -1470,7 +1481,10 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
           tmem_ld_wait();
 #pragma unroll
           for (int u = 0; u < 16; ++u)
-            if (cq * 16 + u < cv) od[(size_t)(cq * 16 + u) * rs] = __float2bfloat16_rn(ov[u]);
+            if (cq * 16 + u < cv &&
+                KDA_CHECK(ident ? t0 - info.bos + info.ybase + cq * 16 + u < p.ytok_cap
+                                : t0 + cq * 16 + u < p.T))
+              od[(size_t)(cq * 16 + u) * rs] = __float2bfloat16_rn(ov[u]);
         }
       }
       tc_fence_before();
@@ -1535,6 +1549,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     if (L->n_v > 0) mbar_wait(&s->bar[B_V_FULL], (L->n_v - 1) & 1);
   }
   if (warp == 0) tmem_dealloc(tbase, 512);
+  if (threadIdx.x == 0) KDA_DEBUG_FOLD(p.status);
 }
 
 // ---- planning: the work list, longest first, with the longest sequences cut in two --------
@@ -1626,7 +1641,7 @@ __global__ void __launch_bounds__(kOrderKeys) kda_plan_kernel(const int32_t* __r
   scan_keys_desc(cnt, wsum);
   for (int n = t; n < N; n += kOrderKeys) {
     const int pos = atomicAdd(&cnt[order_key(chunks(n))], 1);
-    work[pos] = (uint32_t)n;
+    if (KDA_CHECK(pos >= 0 && pos < N)) work[pos] = (uint32_t)n;
     if (pos < kPlanCache) order_s[pos] = (uint32_t)n;
   }
   __syncthreads();
@@ -1656,7 +1671,10 @@ __global__ void __launch_bounds__(kOrderKeys) kda_plan_kernel(const int32_t* __r
     hdr->num_entries = (uint32_t)(N + 2 * nc);
   }
   __syncthreads();
-  if (ncut == 0) return;  // the sequence order stands
+  if (ncut == 0) {  // the sequence order stands
+    if (t == 0) KDA_DEBUG_FOLD(&hdr->status);
+    return;
+  }
   // the list again with the cut sequences' three entries (head; tail; tail identity pass)
   cnt[t] = 0;
   __syncthreads();
@@ -1681,16 +1699,23 @@ __global__ void __launch_bounds__(kOrderKeys) kda_plan_kernel(const int32_t* __r
   for (int n = t; n < N; n += kOrderKeys) {
     const int64_t c = chunks(n);
     const int i = cut_of(n);
+    const int cap = N + 2 * nc;
     if (i < 0) {
-      work[atomicAdd(&cnt[order_key(c)], 1)] = (uint32_t)n;
+      const int pos = atomicAdd(&cnt[order_key(c)], 1);
+      if (KDA_CHECK(pos >= 0 && pos < cap)) work[pos] = (uint32_t)n;
     } else {
-      work[atomicAdd(&cnt[order_key(cut_a[i])], 1)] = (uint32_t)n | ((uint32_t)KIND_HEAD << 28);
+      const int ph = atomicAdd(&cnt[order_key(cut_a[i])], 1);
+      if (KDA_CHECK(ph >= 0 && ph < cap)) work[ph] = (uint32_t)n | ((uint32_t)KIND_HEAD << 28);
       const int k = order_key(c - cut_a[i]);
       const int pos = atomicAdd(&cnt[k], 2);
-      work[pos] = (uint32_t)n | ((uint32_t)KIND_TAIL << 28);
-      work[pos + 1] = (uint32_t)n | ((uint32_t)KIND_TAIL_ID << 28);
+      if (KDA_CHECK(pos >= 0 && pos + 1 < cap)) {
+        work[pos] = (uint32_t)n | ((uint32_t)KIND_TAIL << 28);
+        work[pos + 1] = (uint32_t)n | ((uint32_t)KIND_TAIL_ID << 28);
+      }
     }
   }
+  __syncthreads();
+  if (t == 0) KDA_DEBUG_FOLD(&hdr->status);
 }
 
 // ---- combine: completes the tails of the cut sequences --------------------------------------
@@ -1716,8 +1741,9 @@ struct CombineParams {
   __nv_bfloat16* o;
   const int32_t *cu, *idx;
   void* state_out;
-  int32_t Hv, state_vk;
-  int64_t num_slots, slot_stride;
+  uint32_t* status;
+  int32_t Hv, state_vk, ytok_cap;
+  int64_t num_slots, slot_stride, T;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
@@ -1779,9 +1805,9 @@ __global__ void __launch_bounds__(kCombThreads) kda_combine_kernel(const __grid_
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int e = tid + i * kCombThreads, row = e >> 4, c8 = (e & 15) * 8;
-          yr[i] = row < nt ? *reinterpret_cast<const uint4*>(
-                                 p.y + ((size_t)(sp.ytok0 + tb + row) * Hv + h) * 128 + c8)
-                           : make_uint4(0u, 0u, 0u, 0u);
+          yr[i] = row < nt && KDA_CHECK(sp.ytok0 + tb + row < p.ytok_cap)
+                      ? *reinterpret_cast<const uint4*>(p.y + ((size_t)(sp.ytok0 + tb + row) * Hv + h) * 128 + c8)
+                      : make_uint4(0u, 0u, 0u, 0u);
         }
       };
       uint4 yr[4];
@@ -1807,9 +1833,9 @@ __global__ void __launch_bounds__(kCombThreads) kda_combine_kernel(const __grid_
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int e = tid + i * kCombThreads, row = e >> 4, c8 = (e & 15) * 8;
-          orr[i] = row < nt ? *reinterpret_cast<const uint4*>(
-                                  p.o + ((size_t)(tail0 + tb + row) * Hv + h) * 128 + c8)
-                            : make_uint4(0u, 0u, 0u, 0u);
+          orr[i] = row < nt && KDA_CHECK(tail0 + tb + row < p.T)
+                       ? *reinterpret_cast<const uint4*>(p.o + ((size_t)(tail0 + tb + row) * Hv + h) * 128 + c8)
+                       : make_uint4(0u, 0u, 0u, 0u);
         }
         if (tb + 64 < t_end) load_y(tb + 64, yr);
         __syncthreads();
@@ -1846,7 +1872,7 @@ __global__ void __launch_bounds__(kCombThreads) kda_combine_kernel(const __grid_
 #pragma unroll
         for (int i = 0; i < 4; ++i) {  // o rows, 16 bytes at a time
           const int e = tid + i * kCombThreads, row = e >> 4, c8 = (e & 15) * 8;
-          if (row < nt) {
+          if (row < nt && KDA_CHECK(tail0 + tb + row < p.T)) {
             const float* cs = acc_s + row * kCombAccPitch + c8;
             const uint32_t in[4] = {orr[i].x, orr[i].y, orr[i].z, orr[i].w};
             uint32_t outw[4];
@@ -1901,6 +1927,7 @@ __global__ void __launch_bounds__(kCombThreads) kda_combine_kernel(const __grid_
       }
     }
   }
+  if (threadIdx.x == 0) KDA_DEBUG_FOLD(p.status);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
@@ -2095,6 +2122,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   p.slot_stride = a.slot_stride;
   p.scale = a.scale;
   p.wait_limit_ns = pipeline_wait_limit_ns();
+  p.max_cuts = can_cut ? full_cuts(d) : 0;
+  p.ytok_cap = can_cut ? (int32_t)full_ytok(d) : 0;
 
   const int max_cuts = can_cut ? full_cuts(d) : 0;
   const int64_t max_items = ((int64_t)d.num_seqs + 2 * max_cuts) * d.num_v_heads;
@@ -2118,6 +2147,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   cp.idx = p.idx;
   cp.state_out = p.state_out;
   cp.Hv = d.num_v_heads;
+  cp.status = p.status;
+  cp.ytok_cap = p.ytok_cap;
+  cp.T = T;
   cp.state_vk = a.state_vk ? 1 : 0;
   cp.num_slots = d.num_slots;
   cp.slot_stride = a.slot_stride;
