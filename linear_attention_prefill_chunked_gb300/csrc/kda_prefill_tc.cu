@@ -91,7 +91,10 @@ constexpr uint32_t TM_U = 0;     // U~ -> U (64)
 constexpr uint32_t TM_O = 64;    // O^T (64)
 constexpr uint32_t TM_SB = 128;  // S^T as bf16 pairs: A operand of MMA-1 (64)
 constexpr uint32_t TM_S = 192;   // S^T fp32 (128)
-constexpr uint32_t TM_AB = 320;  // A/B result (176 of 192), later W^T (64)
+constexpr uint32_t TM_AB = 320;  // A/B result: 176 of 192 columns, or 64 in the whole-chunk form
+constexpr uint32_t TM_W = 448;   // W^T (64): the top of the A/B region, which the A/B of a
+                                 // whole-chunk form leaves alone (only a four-sub-chunk MMA-AB
+                                 // must wait for the W^T of the chunk before to be read out)
 
 constexpr int kIG = 256;  // intra-group threads (warps 0-7)
 constexpr int kRG = 128;  // recurrence-group threads (warps 8-11)
@@ -719,12 +722,20 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // an N = 64 MMA-AB, and KG / QG are the MMA-AB operand itself.  Otherwise the chunk
       // takes the four-sub-chunk form with its exact pairwise fallback.
       const float gm0 = pi0[0] * pi0[1] * pi0[2] * pi0[3], gm1 = pi1[0] * pi1[1] * pi1[2] * pi1[3];
+      // gamma of this chunk (by warps 6-7, which hold all 128 channels), published by the
+      // vote's barrier: the recurrence group reads it at the end of the chunk before, to
+      // pre-decay the state it hands on, or at the start of the item.  The value it replaces
+      // (two chunks back) was last read before MMA-1b of the chunk before, waited for above.
+      if (sc == 3) *reinterpret_cast<float2*>(&s->gamma[gc & 1][c0]) = make_float2(gm0, gm1);
       const bool whole = !named_bar_any(BAR_IG, kIG, !(gm0 >= kSafeMin) || !(gm1 >= kSafeMin));
-      if (t == 0) s->whole[gc & 1] = whole ? 1u : 0u;
+      if (t == 0) {
+        s->whole[gc & 1] = whole ? 1u : 0u;
+        mbar_arrive(&s->bar[B_GAMMA0 + (gc & 1)]);
+      }
       // the gate staging (CB blocks 1-2) is free from here on when this chunk is whole (every
       // thread holds its e, and the one-sub-chunk form neither writes nor reads blocks 1-2):
       // the next chunk of this item gets its gate now, a whole chunk ahead of its use
-      if (t == 128 && whole && !plain_gate && lc + 1 < info.nchunks && ld.st->n_g == gc + 1)
+      if (t == 128 && whole && lc + 1 < info.nchunks && ld.st->n_g == gc + 1)
         ld.load_g(p, sm, s, h, (int)(t0 + kC));
       // inverse scratch: in AM (free after MMA-AB) for the four-sub-chunk form; in the KG and
       // QG buffers when AM is itself KG / QG
@@ -732,9 +743,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       float* Xs = reinterpret_cast<float*>(sm + (whole ? OFF_QG : OFF_XS));
       const float E0 = (sc > 0 ? pi0[0] : 1.f) * (sc > 1 ? pi0[1] : 1.f) * (sc > 2 ? pi0[2] : 1.f);
       const float E1 = (sc > 0 ? pi1[0] : 1.f) * (sc > 1 ? pi1[1] : 1.f) * (sc > 2 ? pi1[2] : 1.f);
-      if (sc == 3)  // warps 6-7 (no block-2 references): gamma of their 64 channels
-        *reinterpret_cast<float2*>(&s->gamma[gc & 1][c0]) =
-            make_float2(pi0[0] * pi0[1] * pi0[2] * pi0[3], pi1[0] * pi1[1] * pi1[2] * pi1[3]);
       {
         const float ip0 = (pm0 >= kSafeMin) ? __fdividef(1.f, pm0) : 0.f;  // pm = pi of this sub-chunk
         const float ip1 = (pm1 >= kSafeMin) ? __fdividef(1.f, pm1) : 0.f;
@@ -876,8 +884,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       fence_async_smem();
       named_bar(BAR_IG, kIG);
       if (t == 0) {
-        mbar_arrive(&s->bar[B_GAMMA0 + (gc & 1)]);
-        if (gc > 0) wait_bar(p, s, B_W_FREE, (gc - 1) & 1);  // W of the last chunk read out
+        if (gc > 0 && !whole) wait_bar(p, s, B_W_FREE, (gc - 1) & 1);  // W of the last chunk read out
         tc_fence_after();
         // four sub-chunks: CB blocks 0-2 (the last 16 columns unused); one: block 0
         const uint32_t idesc = whole ? idesc_bf16(128, 64, 1, 1) : idesc_bf16(128, 176, 1, 1);
@@ -1081,68 +1088,70 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // X = (I + A)^-1: the 16x16 diagonal blocks here, by forward substitution on warps 0-1
       // (one column per lane, two blocks per warp); the recurrence group, idle by then, forms
       // the rest from them (inverse_merges) and Tm.
-      if (agrp) {
-        // gate of the next chunk into CB 1-2 (free since MMA-AB) by warp 4, idle during the
-        // diagonal blocks
-        if (t == 128 && ld.st->nx[gc & 1].have && ld.st->n_g == gc + 1) {  // not issued early
-          const NextChunk& nx = ld.st->nx[gc & 1];
-          ld.load_g(p, sm, s, nx.h, nx.t0);
+      // While warps 0-1 invert the diagonal blocks, warps 2-5 (one per SM sub-partition, so
+      // that the exponentials spread over all four multi-function units) turn the staged gate
+      // of the next chunk of this item into e, its products and masks.  The products go to
+      // CB block 0, free once MMA-AB ran and the B group is past KR (barrier of warps 2-7).
+      // Warp 4 first issues that gate load if the vote did not (CB 1-2 are free since MMA-AB).
+      if (t == 128 && ld.st->nx[gc & 1].have && ld.st->n_g == gc + 1) {
+        const NextChunk& nx = ld.st->nx[gc & 1];
+        ld.load_g(p, sm, s, nx.h, nx.t0);
+      }
+      if (warp < 2) {
+        // lane = column j of diagonal block o (two blocks per warp).  Its 8x8 diagonal
+        // sub-blocks are inverted by forward substitution side by side (columns 0-7
+        // take rows 0-7, columns 8-15 rows 8-15; rows of A read as broadcast float4),
+        // then columns 0-7 get rows 8-15 as -X22 (A21 x), A21 the lower-left 8x8.
+        const int o = (warp * 2 + (lane >> 4)) * 16, j = lane & 15;
+        const int hb = j & 8;
+        float xv[8];
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) xv[rr] = (hb + rr == j) ? 1.f : 0.f;
+#pragma unroll
+        for (int rr = 1; rr < 8; ++rr) {
+          const float4 a0 = *reinterpret_cast<const float4*>(As + sidx(o + hb + rr, o + hb));
+          const float4 a1 = *reinterpret_cast<const float4*>(As + sidx(o + hb + rr, o + hb + 4));
+          const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          float acc[2] = {0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < rr; ++i) acc[i & 1] = fmaf(av[i], xv[i], acc[i & 1]);
+          if (hb + rr > j) xv[rr] = -(acc[0] + acc[1]);
         }
-        if (warp < 2) {
-          // lane = column j of diagonal block o (two blocks per warp).  Its 8x8 diagonal
-          // sub-blocks are inverted by forward substitution side by side (columns 0-7
-          // take rows 0-7, columns 8-15 rows 8-15; rows of A read as broadcast float4),
-          // then columns 0-7 get rows 8-15 as -X22 (A21 x), A21 the lower-left 8x8.
-          const int o = (warp * 2 + (lane >> 4)) * 16, j = lane & 15;
-          const int hb = j & 8;
-          float xv[8];
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr) xv[rr] = (hb + rr == j) ? 1.f : 0.f;
+        for (int rr = 0; rr < 8; ++rr) Xs[sidx(o + hb + rr, o + j)] = xv[rr];
+        // upper-right 8x8 is zero: one float4 per lane (row j/2, columns 8 + 4 (j&1) ..)
+        *reinterpret_cast<float4*>(Xs + sidx(o + (j >> 1), o + 8 + 4 * (j & 1))) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncwarp();
+        if (!hb) {
+          float y[8];
 #pragma unroll
-          for (int rr = 1; rr < 8; ++rr) {
-            const float4 a0 = *reinterpret_cast<const float4*>(As + sidx(o + hb + rr, o + hb));
-            const float4 a1 = *reinterpret_cast<const float4*>(As + sidx(o + hb + rr, o + hb + 4));
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            float acc[2] = {0.f, 0.f};
-#pragma unroll
-            for (int i = 0; i < rr; ++i) acc[i & 1] = fmaf(av[i], xv[i], acc[i & 1]);
-            if (hb + rr > j) xv[rr] = -(acc[0] + acc[1]);
+          for (int i = 0; i < 8; ++i) {
+            const float4 a0 = *reinterpret_cast<const float4*>(As + sidx(o + 8 + i, o));
+            const float4 a1 = *reinterpret_cast<const float4*>(As + sidx(o + 8 + i, o + 4));
+            y[i] = fmaf(a0.x, xv[0], fmaf(a0.y, xv[1], fmaf(a0.z, xv[2], a0.w * xv[3]))) +
+                   fmaf(a1.x, xv[4], fmaf(a1.y, xv[5], fmaf(a1.z, xv[6], a1.w * xv[7])));
           }
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr) Xs[sidx(o + hb + rr, o + j)] = xv[rr];
-          // upper-right 8x8 is zero: one float4 per lane (row j/2, columns 8 + 4 (j&1) ..)
-          *reinterpret_cast<float4*>(Xs + sidx(o + (j >> 1), o + 8 + 4 * (j & 1))) =
-              make_float4(0.f, 0.f, 0.f, 0.f);
-          __syncwarp();
-          if (!hb) {
-            float y[8];
+          for (int i = 0; i < 8; ++i) {
+            const float4 x0 = *reinterpret_cast<const float4*>(Xs + sidx(o + 8 + i, o + 8));
+            const float4 x1 = *reinterpret_cast<const float4*>(Xs + sidx(o + 8 + i, o + 12));
+            const float xr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            float acc[2] = {0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 a0 = *reinterpret_cast<const float4*>(As + sidx(o + 8 + i, o));
-              const float4 a1 = *reinterpret_cast<const float4*>(As + sidx(o + 8 + i, o + 4));
-              y[i] = fmaf(a0.x, xv[0], fmaf(a0.y, xv[1], fmaf(a0.z, xv[2], a0.w * xv[3]))) +
-                     fmaf(a1.x, xv[4], fmaf(a1.y, xv[5], fmaf(a1.z, xv[6], a1.w * xv[7])));
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 x0 = *reinterpret_cast<const float4*>(Xs + sidx(o + 8 + i, o + 8));
-              const float4 x1 = *reinterpret_cast<const float4*>(Xs + sidx(o + 8 + i, o + 12));
-              const float xr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-              float acc[2] = {0.f, 0.f};
-#pragma unroll
-              for (int m = 0; m <= i; ++m) acc[m & 1] = fmaf(xr[m], y[m], acc[m & 1]);
-              Xs[sidx(o + 8 + i, o + j)] = -(acc[0] + acc[1]);
-            }
+            for (int m = 0; m <= i; ++m) acc[m & 1] = fmaf(xr[m], y[m], acc[m & 1]);
+            Xs[sidx(o + 8 + i, o + j)] = -(acc[0] + acc[1]);
           }
         }
       } else if (plain_gate && lc + 1 < info.nchunks) {
-        // while the A group inverts: e, products and masks of the next chunk of this item
-        // (whose gate warp 4 loads: the lookahead within an item always succeeds)
-        named_bar(BAR_B, 128);  // CB block 0 (the products) is free once the B group is past KR
-        const int ncv = (int)min((int64_t)kC, info.eos - (t0 + kC));
-        const int wgb = (warp >> 2) * 2 + (warp & 1);
-        wait_bar(p, s, B_G_FULL, (gc + 1) & 1);
-        gate_exp_inplace(sm, s->unsafe[(gc + 1) & 1], ncv, wgb, 4, lane);
+        // (the lookahead within an item always succeeds, so the gate load was issued)
+        named_bar(BAR_B, 192);
+        if (warp < 6) {
+          const int ncv = (int)min((int64_t)kC, info.eos - (t0 + kC));
+          const int wgb = (warp ^ 4) & 3;  // warps 4, 5, 2, 3 -> 0-3
+          wait_bar(p, s, B_G_FULL, (gc + 1) & 1);
+          gate_exp_inplace(sm, s->unsafe[(gc + 1) & 1], ncv, wgb, 4, lane);
+        }
       }
       // B rows (BB) visible to the tensor core; the diagonal blocks of X complete
       fence_async_smem();
@@ -1292,7 +1301,9 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       // a chunk run as one sub-chunk keeps KG and QG in the MMA-AB operand buffer, and the
       // inverse scratch in the KG / QG buffers
       const bool whole = s->whole[gc & 1] != 0u;
-      if (rt == 0) {
+      // issued by warp 10, idle during the first step of the merges (an MMA issue holds its
+      // thread for about as long as the tensor core takes to run it)
+      if (rt == 64) {
         tc_fence_after();
         const uint32_t off_qg = whole ? OFF_AM + 16384 : OFF_QG;
         const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
@@ -1310,31 +1321,35 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         fence_async_smem();
         named_bar(BAR_RG, kRG);
       }
-      if (leader_warp) {
+      // MMA-U and MMA-W from two threads, so that their issue overlaps; each commits to
+      // UW_DONE (two arrivals per phase)
+      if (rt == 0) {
         wait_bar(p, s, B_V_FULL, gc & 1);
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t off_kg = whole ? OFF_AM : OFF_KG;
-          const uint32_t idu = idesc_bf16(128, 64, 1, 0), idw = idesc_bf16(128, 64, 0, 0);
+        tc_fence_after();
+        const uint32_t idu = idesc_bf16(128, 64, 1, 0);
 #pragma unroll 1
-          for (int st = 0; st < 4; ++st) {
-            const uint64_t b = sdesc_sw128(sbase + OFF_TM + st * 32, 16, 1024);
-            if (!ident)
-              mma_bf16(tbase + TM_U, sdesc_sw128(sbase + OFF_VB + st * 2048, 8192, 1024), b, idu,
-                       st > 0 ? 1u : 0u);
-            mma_bf16(tbase + TM_AB, sdesc_sw128(sbase + off_kg + st * 32, 16, 1024), b, idw,
-                     st > 0 ? 1u : 0u);
-          }
-          mma_commit(&s->bar[B_UW_DONE]);
-        }
-        __syncwarp();
+        for (int st = 0; st < 4; ++st)
+          if (!ident)
+            mma_bf16(tbase + TM_U, sdesc_sw128(sbase + OFF_VB + st * 2048, 8192, 1024),
+                     sdesc_sw128(sbase + OFF_TM + st * 32, 16, 1024), idu, st > 0 ? 1u : 0u);
+        mma_commit(&s->bar[B_UW_DONE]);
+      } else if (rt == 32) {
+        tc_fence_after();
+        const uint32_t off_kg = whole ? OFF_AM : OFF_KG;
+        const uint32_t idw = idesc_bf16(128, 64, 0, 0);
+#pragma unroll 1
+        for (int st = 0; st < 4; ++st)
+          mma_bf16(tbase + TM_W, sdesc_sw128(sbase + off_kg + st * 32, 16, 1024),
+                   sdesc_sw128(sbase + OFF_TM + st * 32, 16, 1024), idw, st > 0 ? 1u : 0u);
+        mma_commit(&s->bar[B_UW_DONE]);
       }
+      __syncwarp();
       wait_bar(p, s, B_UW_DONE, gc & 1);
       tc_fence_after();
 #pragma unroll 1
       for (int cq = 0; cq < 4; ++cq) {  // row = channel v, tokens 16 cq ..
         float wv[16];
-        tmem_ld16(taddr_q + TM_AB + cq * 16, wv);
+        tmem_ld16(taddr_q + TM_W + cq * 16, wv);
         tmem_ld_wait();
         uint32_t w[8];
 #pragma unroll
@@ -1360,31 +1375,6 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         }
         __syncwarp();
       }
-      // ---- pre-decay S <- Diag(gamma_c) S in TMEM (overlaps MMA-1; MMA-3b accumulates on it)
-      if (lc > 0) {
-        wait_bar(p, s, B_GAMMA0 + (gc & 1), (gc >> 1) & 1);
-        const float* gm = s->gamma[gc & 1];
-#pragma unroll 1
-        for (int kq = 0; kq < 4; ++kq) {
-          float sv[2][16];
-#pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) tmem_ld16(taddr_q + TM_S + (kq * 2 + q2) * 16, sv[q2]);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-#pragma unroll
-            for (int u4 = 0; u4 < 4; ++u4) {
-              const float4 g4 = *reinterpret_cast<const float4*>(gm + (kq * 2 + q2) * 16 + u4 * 4);
-              sv[q2][u4 * 4 + 0] *= g4.x;
-              sv[q2][u4 * 4 + 1] *= g4.y;
-              sv[q2][u4 * 4 + 2] *= g4.z;
-              sv[q2][u4 * 4 + 3] *= g4.w;
-            }
-            tmem_st16(taddr_q + TM_S + (kq * 2 + q2) * 16, sv[q2]);
-          }
-        }
-        tmem_st_wait();
-      }
       // ---- E1: U^T row v -> UT (bf16)
       wait_bar(p, s, B_M1A, gc & 1);
       tc_fence_after();
@@ -1404,6 +1394,8 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       named_bar(BAR_RG, kRG);
       if (rt == 0) {
         mbar_arrive(&s->bar[B_E1]);
+        // MMA-3a accumulates onto O, which MMA-1b (issued by another thread) wrote
+        wait_bar(p, s, B_M1B, gc & 1);
         tc_fence_after();
         const uint32_t id3 = idesc_bf16(128, 128, 0, 0), id3o = idesc_bf16(128, 64, 0, 0);
 #pragma unroll 1
@@ -1418,9 +1410,13 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         mma_commit(&s->bar[B_M3A]);
       }
       __syncwarp();
-      // ---- E2: S -> TMEM bf16 pairs for the next chunk's MMA-1, or the final state store
+      // ---- E2: S -> TMEM bf16 pairs for the next chunk's MMA-1, and back as fp32 pre-decayed
+      // by that chunk's gamma (its MMA-3b accumulates onto Diag(gamma) S); or the final state
+      // store
       wait_bar(p, s, B_M3B, gc & 1);
+      if (!last) wait_bar(p, s, B_GAMMA0 + ((gc + 1) & 1), ((gc + 1) >> 1) & 1);
       tc_fence_after();
+      const float* gn = s->gamma[(gc + 1) & 1];
 #pragma unroll 1
       for (int kq = 0; kq < 4; ++kq) {
         float sv[32];
@@ -1432,6 +1428,16 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
 #pragma unroll
           for (int u = 0; u < 16; ++u) pw[u] = __uint_as_float(pack_bf16x2(sv[2 * u], sv[2 * u + 1]));
           tmem_st16(taddr_q + TM_SB + kq * 16, pw);
+#pragma unroll
+          for (int u4 = 0; u4 < 8; ++u4) {
+            const float4 g4 = *reinterpret_cast<const float4*>(gn + kq * 32 + u4 * 4);
+            sv[u4 * 4 + 0] *= g4.x;
+            sv[u4 * 4 + 1] *= g4.y;
+            sv[u4 * 4 + 2] *= g4.z;
+            sv[u4 * 4 + 3] *= g4.w;
+          }
+          tmem_st16(taddr_q + TM_S + kq * 32, sv);
+          tmem_st16(taddr_q + TM_S + kq * 32 + 16, sv + 16);
         } else if (dst32) {
 #pragma unroll
           for (int u = 0; u < 32; ++u) dst32[(size_t)(kq * 32 + u) * kV + v] = sv[u];
@@ -1493,11 +1499,9 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   }
   if (rt == 0) bulk_wait_all();  // the output stores this thread issued have completed
   named_bar(BAR_RG, kRG);
-  if (leader_warp) {
-    if (lane == 0) mma_commit(&s->bar[B_DRAIN_RG]);
-    __syncwarp();
-    mbar_wait(&s->bar[B_DRAIN_RG], 0);  // the full limit, aborted or not
-  }
+  // the three threads that issue this group's MMAs (rt 0, 32, 64) each commit once
+  if (rt == 0 || rt == 32 || rt == 64) mma_commit(&s->bar[B_DRAIN_RG]);
+  if (leader_warp) mbar_wait(&s->bar[B_DRAIN_RG], 0);  // the full limit, aborted or not
 }
 
 template <typename ST>
@@ -1518,7 +1522,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
   // grid before reading anything)
   grid_dep_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int b = 0; b < B_COUNT; ++b) mbar_init(&s->bar[b], 1);
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(&s->bar[b], b == B_UW_DONE ? 2 : b == B_DRAIN_RG ? 3 : 1);
     for (int r = 0; r < kRing; ++r) mbar_init(&s->bar[B_ITEM_EMPTY + r], 2);
     s->abort = 0;
     s->ld = LoaderState{};
