@@ -302,7 +302,7 @@ __device__ __forceinline__ ItemInfo next_item(const TcParams& p, Small* s, int k
 __device__ __forceinline__ void blk_mma(float acc[2][4], const float* M1, int r1, int c1,
                                         const float* M2, int r2, int c2, int lane) {
   const int g = lane >> 2, t = lane & 3;
-#pragma unroll
+#pragma unroll 1
   for (int ks = 0; ks < 2; ++ks) {
     uint32_t a[4];
     a[0] = to_tf32(M1[sidx(r1 + g, c1 + 8 * ks + t)]);
@@ -534,7 +534,7 @@ __device__ __forceinline__ void inverse_merges(float* As, float* Xs, int aw, int
 // columns 32 (i >> 6) ..).
 __device__ __forceinline__ void form_tm(uint8_t* sm, const float* Xs, const float* beta, int i) {
   const int r = i & 63, qq = i >> 6;
-#pragma unroll
+#pragma unroll 1
   for (int u2 = 0; u2 < 4; ++u2) {
     const int j = qq * 4 + u2;
     const float4 xa = *reinterpret_cast<const float4*>(Xs + sidx(r, j * 8));
@@ -618,31 +618,40 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             gdb1 = p.act.dt_bias[(size_t)h * gk + (gk > 1 ? c0 + 1 : 0)];
           }
         }
-        const int col = h & (p.gw - 1);
+        // one loop per gate form, so that only the form in use sits in the executed code
+        if (p.gate_k == 1) {  // scalar gate: staged [64 tokens][gw heads], one value per token
+          const int col = h & (p.gw - 1);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = sc * 16 + j;
-          float g0, g1;
-          if (p.gate_k == 1) {  // scalar gate: staged [64 tokens][gw heads], one value per token
+          for (int j = 0; j < 16; ++j) {
+            const int r = sc * 16 + j;
+            float g0;
             if (p.act.a) {
               const float x = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(sm + OFF_G)[r * 8 + col]) + gdb0;
               g0 = fmaxf(-gA * (fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)))), p.act.lb);
             } else {
               g0 = Gs[r * 4 + col];
             }
-            g1 = g0;
-          } else if (!p.act.a) {
+            e0[j] = e1[j] = (r < cv) ? exp_ftz(g0) : 1.f;  // padded rows: decay 1
+          }
+        } else if (!p.act.a) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = sc * 16 + j;
             const float2 gv = *reinterpret_cast<const float2*>(Gs + r * kK + c0);
-            g0 = gv.x;
-            g1 = gv.y;
-          } else {  // staged tile is a ([64][128] bf16): g = max(-A softplus(a + dt_bias), lb)
+            e0[j] = (r < cv) ? exp_ftz(gv.x) : 1.f;
+            e1[j] = (r < cv) ? exp_ftz(gv.y) : 1.f;
+          }
+        } else {  // staged tile is a ([64][128] bf16): g = max(-A softplus(a + dt_bias), lb)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = sc * 16 + j;
             const uint32_t w = *reinterpret_cast<const uint32_t*>(sm + OFF_G + r * 256 + c0 * 2);
             const float x0 = bf_bits(w & 0xFFFFu) + gdb0, x1 = bf_bits(w >> 16) + gdb1;
-            g0 = fmaxf(-gA * (fmaxf(x0, 0.f) + __logf(1.f + __expf(-fabsf(x0)))), p.act.lb);
-            g1 = fmaxf(-gA * (fmaxf(x1, 0.f) + __logf(1.f + __expf(-fabsf(x1)))), p.act.lb);
+            const float g0 = fmaxf(-gA * (fmaxf(x0, 0.f) + __logf(1.f + __expf(-fabsf(x0)))), p.act.lb);
+            const float g1 = fmaxf(-gA * (fmaxf(x1, 0.f) + __logf(1.f + __expf(-fabsf(x1)))), p.act.lb);
+            e0[j] = (r < cv) ? exp_ftz(g0) : 1.f;
+            e1[j] = (r < cv) ? exp_ftz(g1) : 1.f;
           }
-          e0[j] = (r < cv) ? exp_ftz(g0) : 1.f;  // padded rows: decay 1
-          e1[j] = (r < cv) ? exp_ftz(g1) : 1.f;
         }
         float pm0 = 1.f, pm1 = 1.f;
 #pragma unroll
@@ -752,6 +761,37 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         // blocks two and three sub-chunks below the diagonal: sub-chunk 0 -> k kap pi_1
         // (chunk jh) and k kap pi_1 pi_2 (chunk 2+jh), sub-chunk 1 -> k kap pi_2 (chunk 4+jh).
         float ka0 = 1.f, ka1 = 1.f;
+        if (whole) {
+          // one sub-chunk: k / rho_r = (k kap_r) F_sc / gamma = (k kap_r) / (E_sc pi_sc),
+          // rounded once, into CB block 0
+          const float fw0 = __fdividef(1.f, E0 * pm0), fw1 = __fdividef(1.f, E1 * pm1);
+#pragma unroll
+          for (int jh = 1; jh >= 0; --jh) {
+            uint32_t xw[2][4];
+#pragma unroll
+            for (int u = 7; u >= 0; --u) {
+              const int j = jh * 8 + u, r = sc * 16 + j;
+              const uint32_t kv = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128)) : 0u;
+              const float k0 = bf_bits(kv & 0xFFFFu) * (ka0 * fw0), k1 = bf_bits(kv >> 16) * (ka1 * fw1);
+              ka0 *= e0[j];
+              ka1 *= e1[j];
+              if (u & 1) {
+                xw[0][u >> 1] = __float_as_uint(k0);  // odd token: the high half, packed below
+                xw[1][u >> 1] = __float_as_uint(k1);
+              } else {
+                xw[0][u >> 1] = pack_bf16x2(k0, __uint_as_float(xw[0][u >> 1]));
+                xw[1][u >> 1] = pack_bf16x2(k1, __uint_as_float(xw[1][u >> 1]));
+              }
+            }
+            const uint32_t cj = sc * 2 + jh;
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+              const int c = c2 ^ wsel;
+              st_chunk(sm, OFF_CB + sw128_off(c0 + c, cj), c ? xw[1][0] : xw[0][0], c ? xw[1][1] : xw[0][1],
+                       c ? xw[1][2] : xw[0][2], c ? xw[1][3] : xw[0][3]);
+            }
+          }
+        } else {
 #pragma unroll
         for (int jh = 1; jh >= 0; --jh) {
           float kk[2][8];
@@ -765,23 +805,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             ka1 *= e1[j];
           }
           const uint32_t cj = sc * 2 + jh;
-          if (whole) {
-            // k / rho_r = (k kap_r) F_sc / gamma = (k kap_r) / (E_sc pi_sc), rounded once
-            const float fw0 = __fdividef(1.f, E0 * pm0), fw1 = __fdividef(1.f, E1 * pm1);
-            uint32_t xw[2][4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              xw[0][u] = pack_bf16x2(kk[0][2 * u] * fw0, kk[0][2 * u + 1] * fw0);
-              xw[1][u] = pack_bf16x2(kk[1][2 * u] * fw1, kk[1][2 * u + 1] * fw1);
-            }
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-              const int c = c2 ^ wsel;
-              st_chunk(sm, OFF_CB + sw128_off(c0 + c, cj), c ? xw[1][0] : xw[0][0], c ? xw[1][1] : xw[0][1],
-                       c ? xw[1][2] : xw[0][2], c ? xw[1][3] : xw[0][3]);
-            }
-            continue;
-          }
           // both channels' 8 tokens as bf16 pairs: k kap, and k kap / pi rounded once from
           // fp32 (a second rounding on the diagonal blocks shows in the output); the
           // references scale the k kap pairs with one packed bf16 product each
@@ -816,18 +839,17 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             }
           }
         }
+        }
         // KG is read by MMA-W of the previous chunk, issued by the recurrence group
         if (gc > 0) wait_bar(p, s, B_UW_DONE, (gc - 1) & 1);
         // pass B, ascending: rho (inclusive product from the sub-chunk start); q and k
         // rows of the MMA-AB operand in place, and KG, QG.
         const float qs0 = p.scale * E0, qs1 = p.scale * E1;
-        // one sub-chunk: the operand rows are k rho E and scale q rho E themselves (one
-        // rounding), which are KG and QG too
-        const float mk0 = whole ? E0 : 1.f, mk1 = whole ? E1 : 1.f;
-        const float mq0 = whole ? qs0 : 1.f, mq1 = whole ? qs1 : 1.f;
         float rho0 = 1.f, rho1 = 1.f;
-#pragma unroll
-        for (int jh = 0; jh < 2; ++jh) {
+        // tokens 8 jh .. 8 jh + 7 of channels c0, c0+1: k rho mk and q rho mq, packed as token
+        // pairs while they are formed
+        auto rows = [&](int jh, float mk0, float mk1, float mq0, float mq1, uint32_t (&kaw)[2][4],
+                        uint32_t (&qaw)[2][4]) {
           uint32_t kw[8], qw[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -835,9 +857,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             kw[u] = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128)) : 0u;
             qw[u] = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(64 + r, c0, 128)) : 0u;
           }
-          // k rho, q rho (MN-major A operand of MMA-AB) and KG, QG of channels c0 and
-          // c0+1, packed as token pairs while they are formed
-          uint32_t kaw[2][4], qaw[2][4];
           float pa0 = 0.f, pa1 = 0.f, pb0 = 0.f, pb1 = 0.f;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -858,25 +877,46 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
               pb1 = qr1;
             }
           }
-          const uint32_t cj = sc * 2 + jh;
+        };
+        // the rows as the MN-major A operand of MMA-AB: k into AM, q into AM + 16 KB
+        auto store_am = [&](uint32_t cj, int c, const uint32_t (&kaw)[2][4], const uint32_t (&qaw)[2][4]) {
+          const int row = c0 + c;
+          st_chunk(sm, OFF_AM + sw128_off(row, cj), c ? kaw[1][0] : kaw[0][0], c ? kaw[1][1] : kaw[0][1],
+                   c ? kaw[1][2] : kaw[0][2], c ? kaw[1][3] : kaw[0][3]);
+          st_chunk(sm, OFF_AM + 16384 + sw128_off(row, cj), c ? qaw[1][0] : qaw[0][0], c ? qaw[1][1] : qaw[0][1],
+                   c ? qaw[1][2] : qaw[0][2], c ? qaw[1][3] : qaw[0][3]);
+        };
+        if (whole) {
+          // one sub-chunk: the operand rows are k rho E and scale q rho E themselves (one
+          // rounding), which are KG and QG too
 #pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            const int c = c2 ^ wsel;
-            const int row = c0 + c;
-            st_chunk(sm, OFF_AM + sw128_off(row, cj), c ? kaw[1][0] : kaw[0][0], c ? kaw[1][1] : kaw[0][1],
-                     c ? kaw[1][2] : kaw[0][2], c ? kaw[1][3] : kaw[0][3]);
-            st_chunk(sm, OFF_AM + 16384 + sw128_off(row, cj), c ? qaw[1][0] : qaw[0][0],
-                     c ? qaw[1][1] : qaw[0][1], c ? qaw[1][2] : qaw[0][2], c ? qaw[1][3] : qaw[0][3]);
-            if (whole) continue;  // the rows just written are KG and QG
-            // KG = (k rho) E and QG = (q rho) scale E as packed products of the pairs above
-            const uint32_t eg = c ? pack_bf16x2(E1, E1) : pack_bf16x2(E0, E0);
-            st_chunk(sm, OFF_KG + sw128_off(row, cj), bmul2(c ? kaw[1][0] : kaw[0][0], eg),
-                     bmul2(c ? kaw[1][1] : kaw[0][1], eg), bmul2(c ? kaw[1][2] : kaw[0][2], eg),
-                     bmul2(c ? kaw[1][3] : kaw[0][3], eg));
-            const uint32_t eq = c ? pack_bf16x2(qs1, qs1) : pack_bf16x2(qs0, qs0);
-            st_chunk(sm, OFF_QG + sw128_off(row, cj), bmul2(c ? qaw[1][0] : qaw[0][0], eq),
-                     bmul2(c ? qaw[1][1] : qaw[0][1], eq), bmul2(c ? qaw[1][2] : qaw[0][2], eq),
-                     bmul2(c ? qaw[1][3] : qaw[0][3], eq));
+          for (int jh = 0; jh < 2; ++jh) {
+            uint32_t kaw[2][4], qaw[2][4];
+            rows(jh, E0, E1, qs0, qs1, kaw, qaw);
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) store_am(sc * 2 + jh, c2 ^ wsel, kaw, qaw);
+          }
+        } else {
+#pragma unroll
+          for (int jh = 0; jh < 2; ++jh) {
+            uint32_t kaw[2][4], qaw[2][4];
+            rows(jh, 1.f, 1.f, 1.f, 1.f, kaw, qaw);
+            const uint32_t cj = sc * 2 + jh;
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+              const int c = c2 ^ wsel;
+              const int row = c0 + c;
+              store_am(cj, c, kaw, qaw);
+              // KG = (k rho) E and QG = (q rho) scale E as packed products of the pairs above
+              const uint32_t eg = c ? pack_bf16x2(E1, E1) : pack_bf16x2(E0, E0);
+              st_chunk(sm, OFF_KG + sw128_off(row, cj), bmul2(c ? kaw[1][0] : kaw[0][0], eg),
+                       bmul2(c ? kaw[1][1] : kaw[0][1], eg), bmul2(c ? kaw[1][2] : kaw[0][2], eg),
+                       bmul2(c ? kaw[1][3] : kaw[0][3], eg));
+              const uint32_t eq = c ? pack_bf16x2(qs1, qs1) : pack_bf16x2(qs0, qs0);
+              st_chunk(sm, OFF_QG + sw128_off(row, cj), bmul2(c ? qaw[1][0] : qaw[0][0], eq),
+                       bmul2(c ? qaw[1][1] : qaw[0][1], eq), bmul2(c ? qaw[1][2] : qaw[0][2], eq),
+                       bmul2(c ? qaw[1][3] : qaw[0][3], eq));
+            }
           }
         }
       }
@@ -925,7 +965,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         // (F_s = product of pi after s), by the B group while the tensor core runs MMA-AB;
         // one sub-chunk: KR = (k / rho) gamma
         if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
-#pragma unroll
+#pragma unroll 1
         for (int s2 = 0; s2 < 2; ++s2) {
           const int sk = sc - 1 + s2;
           const float fs0 = whole ? gm0 : (sk < 1 ? pi0[1] : 1.f) * (sk < 2 ? pi0[2] : 1.f) * (sk < 3 ? pi0[3] : 1.f);
@@ -934,7 +974,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           for (int c2 = 0; c2 < 2; ++c2) {
             const int c = c2 ^ wsel;
             const float f = c ? fs1 : fs0;
-#pragma unroll
+#pragma unroll 1
             for (int jj = 0; jj < 2; ++jj) {
               const int j = sk * 2 + jj;
               const uint4 src = *reinterpret_cast<const uint4*>(sm + OFF_CB + sw128_off(c0 + c, j));
@@ -1416,15 +1456,14 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       wait_bar(p, s, B_M3B, gc & 1);
       if (!last) wait_bar(p, s, B_GAMMA0 + ((gc + 1) & 1), ((gc + 1) >> 1) & 1);
       tc_fence_after();
-      const float* gn = s->gamma[(gc + 1) & 1];
+      if (!last) {
+        const float* gn = s->gamma[(gc + 1) & 1];
 #pragma unroll 1
-      for (int kq = 0; kq < 4; ++kq) {
-        float sv[32];
-        tmem_ld16(taddr_q + TM_S + kq * 32, sv);
-        tmem_ld16(taddr_q + TM_S + kq * 32 + 16, sv + 16);
-        tmem_ld_wait();
-        if (!last) {
-          float pw[16];
+        for (int kq = 0; kq < 4; ++kq) {
+          float sv[32], pw[16];
+          tmem_ld16(taddr_q + TM_S + kq * 32, sv);
+          tmem_ld16(taddr_q + TM_S + kq * 32 + 16, sv + 16);
+          tmem_ld_wait();
 #pragma unroll
           for (int u = 0; u < 16; ++u) pw[u] = __uint_as_float(pack_bf16x2(sv[2 * u], sv[2 * u + 1]));
           tmem_st16(taddr_q + TM_SB + kq * 16, pw);
@@ -1438,11 +1477,18 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
           }
           tmem_st16(taddr_q + TM_S + kq * 32, sv);
           tmem_st16(taddr_q + TM_S + kq * 32 + 16, sv + 16);
-        } else if (dst32) {
+        }
+      } else if (dst32 || dst) {  // the final state (a cut part's into the split scratch)
+#pragma unroll 1
+        for (int kq = 0; kq < 4; ++kq) {
+          float sv[32];
+          tmem_ld16(taddr_q + TM_S + kq * 32, sv);
+          tmem_ld16(taddr_q + TM_S + kq * 32 + 16, sv + 16);
+          tmem_ld_wait();
+          if (dst32) {
 #pragma unroll
-          for (int u = 0; u < 32; ++u) dst32[(size_t)(kq * 32 + u) * kV + v] = sv[u];
-        } else if (dst) {
-          if (p.state_vk) {
+            for (int u = 0; u < 32; ++u) dst32[(size_t)(kq * 32 + u) * kV + v] = sv[u];
+          } else if (p.state_vk) {
             row32_store(dst + (size_t)v * kK + kq * 32, sv);
           } else {
 #pragma unroll
