@@ -26,11 +26,12 @@
 //   Tm = (I + A)^-1 Diag(beta): 16x16 diagonal blocks by fp32 forward
 //   substitution, off-diagonal blocks by block forward substitution with tf32
 //   warp MMAs (tiny, latency-bound 16x16 products)
-//   U~^T = V^T Tm^T,  W^T = KG^T Tm^T                     (MMA, KG = k rho E)
-//   per chunk, sequentially (state S^T fp32 in TMEM, lanes = value channel):
-//     U^T = U~^T - S^T W^T          (MMA accumulating onto U~)
-//     O^T = S^T QG^T + U^T B^T      (QG = scale q rho E)
-//     S^T = S^T Diag(gamma) + U^T KR   (KR = k kap F, gamma = prod e)
+//   per chunk, sequentially (state S^T fp32 in TMEM, lanes = value channel;
+//   KG = k rho E, QG = scale q rho E, KR = k kap F, gamma = prod e):
+//     [-Y^T | O^T] = [-V^T | 0] + S^T [KG | QG]^T   (one N = 128 MMA; Tm-independent)
+//     U^T = Y^T Tm^T                   (U = Tm (V - KG S), the delta-rule correction)
+//     O^T += U^T B^T
+//     S^T = S^T Diag(gamma) + U^T KR
 //
 // CTA = 12 warps, one CTA per SM, persistent over (sequence, head) items sorted
 // longest first and claimed from a global counter near the end of the item before:
@@ -87,14 +88,11 @@ constexpr uint32_t OFF_XS = OFF_AM + 16384;
 constexpr uint32_t OFF_G = OFF_CB + 16384;
 
 // ---- TMEM columns ------------------------------------------------------------------
-constexpr uint32_t TM_U = 0;     // U~ -> U (64)
+constexpr uint32_t TM_U = 0;     // -V^T -> -Y^T -> U^T (64); with O, the N = 128 MMA-X result
 constexpr uint32_t TM_O = 64;    // O^T (64)
-constexpr uint32_t TM_SB = 128;  // S^T as bf16 pairs: A operand of MMA-1 (64)
+constexpr uint32_t TM_SB = 128;  // S^T as bf16 pairs: A operand of MMA-X (64)
 constexpr uint32_t TM_S = 192;   // S^T fp32 (128)
 constexpr uint32_t TM_AB = 320;  // A/B result: 176 of 192 columns, or 64 in the whole-chunk form
-constexpr uint32_t TM_W = 448;   // W^T (64): the top of the A/B region, which the A/B of a
-                                 // whole-chunk form leaves alone (only a four-sub-chunk MMA-AB
-                                 // must wait for the W^T of the chunk before to be read out)
 
 constexpr int kIG = 256;  // intra-group threads (warps 0-7)
 constexpr int kRG = 128;  // recurrence-group threads (warps 8-11)
@@ -102,7 +100,7 @@ constexpr uint32_t BAR_IG = 1, BAR_RG = 2, BAR_A = 3, BAR_B = 4;
 
 enum Bar {
   B_QK_FULL, B_V_FULL, B_G_FULL, B_AB_DONE, B_UW_DONE, B_GAMMA0, B_GAMMA1, B_REC_READY,
-  B_M1A, B_M1B, B_M3A, B_M3B, B_E1, B_DRAIN_IG, B_DRAIN_RG, B_W_FREE,
+  B_M1B, B_M3A, B_M3B, B_DRAIN_IG, B_DRAIN_RG,
   B_ITEM_FULL, B_ITEM_EMPTY = B_ITEM_FULL + kRing, B_COUNT = B_ITEM_EMPTY + kRing
 };
 
@@ -141,10 +139,10 @@ struct LoaderState {
 struct Small {
   uint64_t bar[B_COUNT];
   ItemInfo ring[kRing];
-  // beta of the chunk in the intra group; read by its extraction and by the recurrence
-  // group's Tm, which is done before the next chunk writes it (that chunk's pass B waits for
-  // MMA-U/W, issued after Tm)
-  alignas(16) float beta[kC];      // read as float4
+  // beta of the chunk, by chunk parity: written after pass B, read by the chunk's extraction
+  // and by the recurrence group's Tm, which may still be running when the next chunk writes its
+  // own (nothing orders that chunk's pass B after this chunk's Tm)
+  alignas(16) float beta[2][kC];   // read as float4
   float inv_nrm[128];              // q/k row norms of the staged chunk (KDA_FLAG_QK_L2NORM)
   alignas(16) float gamma[2][kK];  // read as float4
   // [chunk parity][sub-chunk][half][parity]: bit l = channel 64*half + 2l + parity
@@ -214,9 +212,6 @@ __device__ __forceinline__ int sidx(int r, int i) {
   return r * 64 + (i ^ ((r & 7) << 2));
 }
 
-__device__ __forceinline__ void fail(const TcParams& p, Small* s) {
-  if (atomicExch(&s->abort, 1u) == 0u) raise_status(p.status, KDA_DEVICE_PIPE_TIMEOUT);
-}
 __device__ __forceinline__ bool aborted(Small* s) {
   return *reinterpret_cast<volatile uint32_t*>(&s->abort) != 0u;
 }
@@ -227,21 +222,26 @@ __device__ __forceinline__ bool aborted(Small* s) {
 // exits keep the full limit (mbar_wait), so that no MMA or TMA is in flight when it frees
 // its tensor memory.
 // A bound shorter than the suspend hint polls with test_wait (try_wait may itself suspend
-// the thread until the phase completes, which would let a short bound never run out).
-__device__ __forceinline__ bool wait_bar(const TcParams& p, Small* s, int b, uint32_t parity) {
-  const bool poll = p.wait_limit_ns < kSleepHintNs;
-  if (poll ? mbar_test_wait(&s->bar[b], parity) : mbar_try_wait(&s->bar[b], parity)) return true;
+// the thread until the phase completes, which would let a short bound never run out).  The
+// waiting loop is out of line: every wait of the pipeline runs the same few instructions
+// rather than a copy per call site, which keeps the chunk loop's code in the SM's
+// instruction cache.
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                           uint32_t* abort_flag, uint32_t* status) {
+  const bool poll = limit_ns < kSleepHintNs;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (poll ? mbar_test_wait(&s->bar[b], parity)
-             : mbar_try_wait_sleep(&s->bar[b], parity, kSleepHintNs))
-      return true;
-    if (aborted(s)) return false;
-    if (globaltimer_ns() - t0 > p.wait_limit_ns) {
-      fail(p, s);
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (*reinterpret_cast<volatile uint32_t*>(abort_flag) != 0u) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      if (atomicExch(abort_flag, 1u) == 0u) raise_status(status, KDA_DEVICE_PIPE_TIMEOUT);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool wait_bar(const TcParams& p, Small* s, int b, uint32_t parity) {
+  if (mbar_test_wait(&s->bar[b], parity)) return true;
+  return wait_bar_slow(&s->bar[b], parity, p.wait_limit_ns, &s->abort, p.status);
 }
 
 // Fetches the next valid item (work-list entry, head) from the global counter.
@@ -302,7 +302,7 @@ __device__ __forceinline__ ItemInfo next_item(const TcParams& p, Small* s, int k
 __device__ __forceinline__ void blk_mma(float acc[2][4], const float* M1, int r1, int c1,
                                         const float* M2, int r2, int c2, int lane) {
   const int g = lane >> 2, t = lane & 3;
-#pragma unroll 1
+#pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
     uint32_t a[4];
     a[0] = to_tf32(M1[sidx(r1 + g, c1 + 8 * ks + t)]);
@@ -707,7 +707,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         }
         if (hf == 0) s->inv_nrm[row] = inv;
       }
-      // QG buffer and this gamma buffer are free once MMA-1b of the previous chunk ran
+      // the KG and QG tiles, the v buffer and this gamma buffer are free once MMA-X of the
+      // previous chunk ran
       if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
       named_bar(BAR_IG, kIG);  // the products visible
       const float* pis = reinterpret_cast<const float*>(sm + OFF_CB);
@@ -734,7 +735,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // gamma of this chunk (by warps 6-7, which hold all 128 channels), published by the
       // vote's barrier: the recurrence group reads it at the end of the chunk before, to
       // pre-decay the state it hands on, or at the start of the item.  The value it replaces
-      // (two chunks back) was last read before MMA-1b of the chunk before, waited for above.
+      // (two chunks back) was last read before MMA-X of the chunk before, waited for above.
       if (sc == 3) *reinterpret_cast<float2*>(&s->gamma[gc & 1][c0]) = make_float2(gm0, gm1);
       const bool whole = !named_bar_any(BAR_IG, kIG, !(gm0 >= kSafeMin) || !(gm1 >= kSafeMin));
       if (t == 0) {
@@ -750,6 +751,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // QG buffers when AM is itself KG / QG
       float* As = reinterpret_cast<float*>(sm + (whole ? OFF_KG : OFF_AS));
       float* Xs = reinterpret_cast<float*>(sm + (whole ? OFF_QG : OFF_XS));
+      // the chunk before ran as one sub-chunk (its inverse scratch in the KG / QG buffers)
+      const bool prev_whole = gc > 0 && s->whole[(gc - 1) & 1] != 0u;
       const float E0 = (sc > 0 ? pi0[0] : 1.f) * (sc > 1 ? pi0[1] : 1.f) * (sc > 2 ? pi0[2] : 1.f);
       const float E1 = (sc > 0 ? pi1[0] : 1.f) * (sc > 1 ? pi1[1] : 1.f) * (sc > 2 ? pi1[2] : 1.f);
       {
@@ -840,73 +843,77 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           }
         }
         }
-        // KG is read by MMA-W of the previous chunk, issued by the recurrence group
-        if (gc > 0) wait_bar(p, s, B_UW_DONE, (gc - 1) & 1);
         // pass B, ascending: rho (inclusive product from the sub-chunk start); q and k
-        // rows of the MMA-AB operand in place, and KG, QG.
+        // rows of the MMA-AB operand in place, and KG, QG.  The recurrence group reads the
+        // chunk before's KG and QG with its MMA-X (waited for in the prologue), and its inverse
+        // scratch -- the AM buffer when that chunk took the four-sub-chunk form, the KG / QG
+        // buffers otherwise -- up to its Tm (UW_DONE of that chunk).
         const float qs0 = p.scale * E0, qs1 = p.scale * E1;
-        float rho0 = 1.f, rho1 = 1.f;
-        // tokens 8 jh .. 8 jh + 7 of channels c0, c0+1: k rho mk and q rho mq, packed as token
-        // pairs while they are formed
-        auto rows = [&](int jh, float mk0, float mk1, float mq0, float mq1, uint32_t (&kaw)[2][4],
-                        uint32_t (&qaw)[2][4]) {
-          uint32_t kw[8], qw[8];
+        // tokens 8 jh .. 8 jh + 7 of channels c0, c0+1 of the staged k (row0 = 0) or q (row0 =
+        // 64) rows, times rho m (rho carried in r0, r1), packed as token pairs
+        auto rows = [&](int row0, int jh, float& r0, float& r1, float m0, float m1, uint32_t (&aw)[2][4]) {
+          uint32_t xw[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int r = sc * 16 + jh * 8 + u;
-            kw[u] = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128)) : 0u;
-            qw[u] = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(64 + r, c0, 128)) : 0u;
+            xw[u] = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(row0 + r, c0, 128)) : 0u;
           }
-          float pa0 = 0.f, pa1 = 0.f, pb0 = 0.f, pb1 = 0.f;
+          float pa0 = 0.f, pa1 = 0.f;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int j = jh * 8 + u;
-            rho0 *= e0[j];
-            rho1 *= e1[j];
-            const float kr0 = bf_bits(kw[u] & 0xFFFFu) * (rho0 * mk0), kr1 = bf_bits(kw[u] >> 16) * (rho1 * mk1);
-            const float qr0 = bf_bits(qw[u] & 0xFFFFu) * (rho0 * mq0), qr1 = bf_bits(qw[u] >> 16) * (rho1 * mq1);
+            r0 *= e0[j];
+            r1 *= e1[j];
+            const float x0 = bf_bits(xw[u] & 0xFFFFu) * (r0 * m0), x1 = bf_bits(xw[u] >> 16) * (r1 * m1);
             if (u & 1) {
-              kaw[0][u >> 1] = pack_bf16x2(pa0, kr0);
-              kaw[1][u >> 1] = pack_bf16x2(pa1, kr1);
-              qaw[0][u >> 1] = pack_bf16x2(pb0, qr0);
-              qaw[1][u >> 1] = pack_bf16x2(pb1, qr1);
+              aw[0][u >> 1] = pack_bf16x2(pa0, x0);
+              aw[1][u >> 1] = pack_bf16x2(pa1, x1);
             } else {
-              pa0 = kr0;
-              pa1 = kr1;
-              pb0 = qr0;
-              pb1 = qr1;
+              pa0 = x0;
+              pa1 = x1;
             }
           }
         };
-        // the rows as the MN-major A operand of MMA-AB: k into AM, q into AM + 16 KB
-        auto store_am = [&](uint32_t cj, int c, const uint32_t (&kaw)[2][4], const uint32_t (&qaw)[2][4]) {
-          const int row = c0 + c;
-          st_chunk(sm, OFF_AM + sw128_off(row, cj), c ? kaw[1][0] : kaw[0][0], c ? kaw[1][1] : kaw[0][1],
-                   c ? kaw[1][2] : kaw[0][2], c ? kaw[1][3] : kaw[0][3]);
-          st_chunk(sm, OFF_AM + 16384 + sw128_off(row, cj), c ? qaw[1][0] : qaw[0][0], c ? qaw[1][1] : qaw[0][1],
-                   c ? qaw[1][2] : qaw[0][2], c ? qaw[1][3] : qaw[0][3]);
+        // rows as the MN-major A operand of MMA-AB: k into AM, q into AM + 16 KB
+        auto store_rows = [&](uint32_t base, uint32_t cj, int c, const uint32_t (&aw)[2][4]) {
+          st_chunk(sm, base + sw128_off(c0 + c, cj), c ? aw[1][0] : aw[0][0], c ? aw[1][1] : aw[0][1],
+                   c ? aw[1][2] : aw[0][2], c ? aw[1][3] : aw[0][3]);
         };
         if (whole) {
           // one sub-chunk: the operand rows are k rho E and scale q rho E themselves (one
           // rounding), which are KG and QG too
+          if (gc > 0 && !prev_whole) wait_bar(p, s, B_UW_DONE, (gc - 1) & 1);
+          float r0 = 1.f, r1 = 1.f;
 #pragma unroll
           for (int jh = 0; jh < 2; ++jh) {
-            uint32_t kaw[2][4], qaw[2][4];
-            rows(jh, E0, E1, qs0, qs1, kaw, qaw);
+            uint32_t aw[2][4];
+            rows(64, jh, r0, r1, qs0, qs1, aw);
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) store_am(sc * 2 + jh, c2 ^ wsel, kaw, qaw);
+            for (int c2 = 0; c2 < 2; ++c2) store_rows(OFF_AM + 16384, sc * 2 + jh, c2 ^ wsel, aw);
+          }
+          r0 = r1 = 1.f;
+#pragma unroll
+          for (int jh = 0; jh < 2; ++jh) {
+            uint32_t aw[2][4];
+            rows(0, jh, r0, r1, E0, E1, aw);
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) store_rows(OFF_AM, sc * 2 + jh, c2 ^ wsel, aw);
           }
         } else {
+          if (gc > 0) wait_bar(p, s, B_UW_DONE, (gc - 1) & 1);
+          float rk0 = 1.f, rk1 = 1.f, rq0 = 1.f, rq1 = 1.f;
 #pragma unroll
           for (int jh = 0; jh < 2; ++jh) {
             uint32_t kaw[2][4], qaw[2][4];
-            rows(jh, 1.f, 1.f, 1.f, 1.f, kaw, qaw);
+            rows(0, jh, rk0, rk1, 1.f, 1.f, kaw);
+            rows(64, jh, rq0, rq1, 1.f, 1.f, qaw);
             const uint32_t cj = sc * 2 + jh;
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
               const int c = c2 ^ wsel;
               const int row = c0 + c;
-              store_am(cj, c, kaw, qaw);
+              store_rows(OFF_AM, cj, c, kaw);
+              store_rows(OFF_AM + 16384, cj, c, qaw);
               // KG = (k rho) E and QG = (q rho) scale E as packed products of the pairs above
               const uint32_t eg = c ? pack_bf16x2(E1, E1) : pack_bf16x2(E0, E0);
               st_chunk(sm, OFF_KG + sw128_off(row, cj), bmul2(c ? kaw[1][0] : kaw[0][0], eg),
@@ -920,11 +927,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           }
         }
       }
-      if (t < kC) s->beta[t] = bt;
+      if (t < kC) s->beta[gc & 1][t] = bt;
       fence_async_smem();
       named_bar(BAR_IG, kIG);
       if (t == 0) {
-        if (gc > 0 && !whole) wait_bar(p, s, B_W_FREE, (gc - 1) & 1);  // W of the last chunk read out
         tc_fence_after();
         // four sub-chunks: CB blocks 0-2 (the last 16 columns unused); one: block 0
         const uint32_t idesc = whole ? idesc_bf16(128, 64, 1, 1) : idesc_bf16(128, 176, 1, 1);
@@ -947,9 +953,10 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           ld.prefetch_l2(p, nx.h, nx.t0);
         }
       } else if (t == 160) {
-        // and on warp 5: v of this chunk, for MMA-U of the recurrence group (the v buffer
-        // is free since MMA-U of the previous chunk, which pass B waited for); the identity
-        // pass of a cut tail has zero values and no MMA-U, so its phase completes bare
+        // and on warp 5: v of this chunk, which the recurrence group reads into TMEM before its
+        // MMA-X (the v buffer is free since MMA-X of the previous chunk, waited for in the
+        // prologue); the identity pass of a cut tail has zero values, so its phase completes
+        // bare
         if (info.kind == KIND_TAIL_ID) {
           if (!aborted(s)) {
             mbar_arrive(&s->bar[B_V_FULL]);
@@ -990,6 +997,9 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       }
       // ------------------------------------------------------------- A / B rows
       wait_bar(p, s, B_AB_DONE, gc & 1);
+      // a whole chunk's inverse scratch is the KG / QG buffers, which hold the chunk before's
+      // scratch when that chunk was whole too: read by its recurrence up to Tm
+      if (whole && prev_whole) wait_bar(p, s, B_UW_DONE, (gc - 1) & 1);
       tc_fence_after();
 
       __syncwarp();
@@ -1042,7 +1052,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         if (any_unsafe == 0u) {
           // fast path: mask and scale straight from TMEM
           if (!isB) {
-            const float br = s->beta[r];
+            const float br = s->beta[gc & 1][r];
 #pragma unroll
             for (int jc = 0; jc < 8; ++jc) {
               float4 w4;
@@ -1094,7 +1104,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         {
           const int r = L & 63;
           if (L < 64) {
-            const float br = s->beta[r];
+            const float br = s->beta[gc & 1][r];
 #pragma unroll
             for (int jc = 0; jc < 8; ++jc) {
               const int i = hx * 32 + jc * 4;
@@ -1296,7 +1306,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         for (int c = 0; c < kK; ++c) dst[(size_t)c * kV + v] = src ? src[(size_t)c * kV + v] : ST(0.f);
       continue;
     }
-    // ---- initial state: S^T row v -> TMEM as bf16 pairs (MMA-1 operand) and as fp32
+    // ---- initial state: S^T row v -> TMEM as bf16 pairs (MMA-X operand) and as fp32
     // pre-decayed by gamma of chunk 0
     wait_bar(p, s, B_GAMMA0 + (gc & 1), (gc >> 1) & 1);
 #pragma unroll 1
@@ -1334,89 +1344,86 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       // takes new work only when it is about to run out (dynamic longest-first
       // scheduling); the claim's global round trips overlap this group's slack
       if (rt == 32 && lc == (info.nchunks > 3 ? info.nchunks - 3 : 0)) ld.push_one(p, s);
-      // ---- R0: the hand-over.  O = S QG^T first (frees QG and gamma for the next chunk's
-      // prologue soonest), then X and Tm from the diagonal blocks the intra group inverted,
-      // then U~^T = V^T Tm^T and W^T = KG^T Tm^T; -W^T rows -> WB
+      // ---- V-in, in the group's slack before the hand-over: -V^T into the U columns (lane =
+      // value channel v, column = token; zero values in the identity pass) and zeros into O,
+      // which MMA-X accumulates onto
+      wait_bar(p, s, B_V_FULL, gc & 1);
+      {
+        const uint8_t* vb = sm + OFF_VB + (v >> 6) * 8192 + (v & 7) * 2;
+        const uint32_t vc = (uint32_t)(v & 63) >> 3;
+        float z[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) z[u] = 0.f;
+#pragma unroll 1
+        for (int cq = 0; cq < 4; ++cq) {
+          float nv[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            nv[u] = ident ? 0.f : -bf_bits(*reinterpret_cast<const uint16_t*>(vb + sw128_off(cq * 16 + u, vc)));
+          tmem_st16(taddr_q + TM_U + cq * 16, nv);
+          tmem_st16(taddr_q + TM_O + cq * 16, z);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      // ---- R0: the hand-over.  MMA-X first (it frees KG, QG, v and gamma for the next
+      // chunk's prologue), then X = (I + A)^-1 and Tm from the diagonal blocks the intra group
+      // inverted, then Y^T -> WB and U^T = Y^T Tm^T
       wait_bar(p, s, B_REC_READY, gc & 1);
       // a chunk run as one sub-chunk keeps KG and QG in the MMA-AB operand buffer, and the
       // inverse scratch in the KG / QG buffers
       const bool whole = s->whole[gc & 1] != 0u;
-      // issued by warp 10, idle during the first step of the merges (an MMA issue holds its
-      // thread for about as long as the tensor core takes to run it)
+      named_bar(BAR_RG, kRG);  // every lane's V-in is in TMEM
+      // MMA-X: [U | O] (N = 128) += S^T [KG | QG]^T, B = the KG and QG tiles as two 64-token
+      // blocks LBO apart.  Issued by warp 10, idle during the first step of the merges (an MMA
+      // issue holds its thread for about as long as the tensor core takes to run it).
       if (rt == 64) {
         tc_fence_after();
-        const uint32_t off_qg = whole ? OFF_AM + 16384 : OFF_QG;
-        const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
+        const uint32_t off_b = whole ? OFF_AM : OFF_KG;
+        const uint32_t lbo = whole ? 16384u : OFF_QG - OFF_KG;
+        const uint32_t idx = idesc_bf16(128, 128, 0, 1);
 #pragma unroll 1
         for (int st = 0; st < 8; ++st)
-          mma_bf16_ta(tbase + TM_O, tbase + TM_SB + st * 8,
-                      sdesc_sw128(sbase + off_qg + st * 2048, 16384, 1024), id1, st > 0 ? 1u : 0u);
+          mma_bf16_ta(tbase + TM_U, tbase + TM_SB + st * 8, sdesc_sw128(sbase + off_b + st * 2048, lbo, 1024),
+                      idx, 1u);
         mma_commit(&s->bar[B_M1B]);
       }
       {
         float* As = reinterpret_cast<float*>(sm + (whole ? OFF_KG : OFF_AS));
         float* Xs = reinterpret_cast<float*>(sm + (whole ? OFF_QG : OFF_XS));
         inverse_merges(As, Xs, warp - kIG / 32, lane, BAR_RG);
-        form_tm(sm, Xs, s->beta, rt);
-        fence_async_smem();
-        named_bar(BAR_RG, kRG);
+        form_tm(sm, Xs, s->beta[gc & 1], rt);
       }
-      // MMA-U and MMA-W from two threads, so that their issue overlaps; each commits to
-      // UW_DONE (two arrivals per phase)
-      if (rt == 0) {
-        wait_bar(p, s, B_V_FULL, gc & 1);
-        tc_fence_after();
-        const uint32_t idu = idesc_bf16(128, 64, 1, 0);
-#pragma unroll 1
-        for (int st = 0; st < 4; ++st)
-          if (!ident)
-            mma_bf16(tbase + TM_U, sdesc_sw128(sbase + OFF_VB + st * 2048, 8192, 1024),
-                     sdesc_sw128(sbase + OFF_TM + st * 32, 16, 1024), idu, st > 0 ? 1u : 0u);
-        mma_commit(&s->bar[B_UW_DONE]);
-      } else if (rt == 32) {
-        tc_fence_after();
-        const uint32_t off_kg = whole ? OFF_AM : OFF_KG;
-        const uint32_t idw = idesc_bf16(128, 64, 0, 0);
-#pragma unroll 1
-        for (int st = 0; st < 4; ++st)
-          mma_bf16(tbase + TM_W, sdesc_sw128(sbase + off_kg + st * 32, 16, 1024),
-                   sdesc_sw128(sbase + OFF_TM + st * 32, 16, 1024), idw, st > 0 ? 1u : 0u);
-        mma_commit(&s->bar[B_UW_DONE]);
-      }
-      __syncwarp();
-      wait_bar(p, s, B_UW_DONE, gc & 1);
+      // ---- Y^T = -(the U columns) -> WB (bf16, row = channel v, K-major A of MMA-U)
+      wait_bar(p, s, B_M1B, gc & 1);
       tc_fence_after();
 #pragma unroll 1
-      for (int cq = 0; cq < 4; ++cq) {  // row = channel v, tokens 16 cq ..
-        float wv[16];
-        tmem_ld16(taddr_q + TM_W + cq * 16, wv);
+      for (int cq = 0; cq < 4; ++cq) {  // tokens 16 cq ..
+        float yv[16];
+        tmem_ld16(taddr_q + TM_U + cq * 16, yv);
         tmem_ld_wait();
         uint32_t w[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(-wv[2 * u], -wv[2 * u + 1]);
+        for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(-yv[2 * u], -yv[2 * u + 1]);
         st_chunk(sm, OFF_WB + sw128_off(v, cq * 2), w[0], w[1], w[2], w[3]);
         st_chunk(sm, OFF_WB + sw128_off(v, cq * 2 + 1), w[4], w[5], w[6], w[7]);
       }
       tc_fence_before();
       fence_async_smem();
-      named_bar(BAR_RG, kRG);
-      if (rt == 0) mbar_arrive(&s->bar[B_W_FREE]);
-      // ---- R1: U~ -= S W^T   (leader warp)
-      if (leader_warp) {
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t id1 = idesc_bf16(128, 64, 0, 1);
+      named_bar(BAR_RG, kRG);  // Tm and Y^T in shared memory, the U columns read out
+      // ---- MMA-U: U^T = Y^T Tm^T (onto the U columns)
+      if (rt == 0) {
+        tc_fence_after();
+        const uint32_t idu = idesc_bf16(128, 64, 0, 0);
 #pragma unroll 1
-          for (int st = 0; st < 8; ++st)  // onto U~ (the identity pass: U~ = 0, no MMA-U)
-            mma_bf16_ta(tbase + TM_U, tbase + TM_SB + st * 8,
-                        sdesc_sw128(sbase + OFF_WB + st * 2048, 16384, 1024), id1,
-                        (ident && st == 0) ? 0u : 1u);
-          mma_commit(&s->bar[B_M1A]);
-        }
-        __syncwarp();
+        for (int st = 0; st < 4; ++st)
+          mma_bf16(tbase + TM_U, sdesc_sw128(sbase + OFF_WB + st * 32, 16, 1024),
+                   sdesc_sw128(sbase + OFF_TM + st * 32, 16, 1024), idu, st > 0 ? 1u : 0u);
+        mma_commit(&s->bar[B_UW_DONE]);
       }
+      __syncwarp();
       // ---- E1: U^T row v -> UT (bf16)
-      wait_bar(p, s, B_M1A, gc & 1);
+      wait_bar(p, s, B_UW_DONE, gc & 1);
       tc_fence_after();
 #pragma unroll 1
       for (int cq = 0; cq < 4; ++cq) {
@@ -1432,10 +1439,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       tc_fence_before();
       fence_async_smem();
       named_bar(BAR_RG, kRG);
-      if (rt == 0) {
-        mbar_arrive(&s->bar[B_E1]);
-        // MMA-3a accumulates onto O, which MMA-1b (issued by another thread) wrote
-        wait_bar(p, s, B_M1B, gc & 1);
+      if (rt == 0) {  // (MMA-X, which wrote O, completed before Y^T was read out)
         tc_fence_after();
         const uint32_t id3 = idesc_bf16(128, 128, 0, 0), id3o = idesc_bf16(128, 64, 0, 0);
 #pragma unroll 1
@@ -1450,7 +1454,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         mma_commit(&s->bar[B_M3A]);
       }
       __syncwarp();
-      // ---- E2: S -> TMEM bf16 pairs for the next chunk's MMA-1, and back as fp32 pre-decayed
+      // ---- E2: S -> TMEM bf16 pairs for the next chunk's MMA-X, and back as fp32 pre-decayed
       // by that chunk's gamma (its MMA-3b accumulates onto Diag(gamma) S); or the final state
       // store
       wait_bar(p, s, B_M3B, gc & 1);
@@ -1545,8 +1549,8 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   }
   if (rt == 0) bulk_wait_all();  // the output stores this thread issued have completed
   named_bar(BAR_RG, kRG);
-  // the three threads that issue this group's MMAs (rt 0, 32, 64) each commit once
-  if (rt == 0 || rt == 32 || rt == 64) mma_commit(&s->bar[B_DRAIN_RG]);
+  // the two threads that issue this group's MMAs (rt 0, 64) each commit once
+  if (rt == 0 || rt == 64) mma_commit(&s->bar[B_DRAIN_RG]);
   if (leader_warp) mbar_wait(&s->bar[B_DRAIN_RG], 0);  // the full limit, aborted or not
 }
 
@@ -1568,7 +1572,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
   // grid before reading anything)
   grid_dep_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int b = 0; b < B_COUNT; ++b) mbar_init(&s->bar[b], b == B_UW_DONE ? 2 : b == B_DRAIN_RG ? 3 : 1);
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(&s->bar[b], b == B_DRAIN_RG ? 2 : 1);
     for (int r = 0; r < kRing; ++r) mbar_init(&s->bar[B_ITEM_EMPTY + r], 2);
     s->abort = 0;
     s->ld = LoaderState{};
