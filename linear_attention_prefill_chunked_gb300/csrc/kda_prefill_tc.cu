@@ -88,10 +88,11 @@ constexpr uint32_t OFF_XS = OFF_AM + 16384;
 constexpr uint32_t OFF_G = OFF_CB + 16384;
 
 // ---- TMEM columns ------------------------------------------------------------------
-constexpr uint32_t TM_U = 0;     // -V^T -> -Y^T -> U^T (64); with O, the N = 128 MMA-X result
+// U | O is the N = 128 result of MMA-X, O | S the N = 192 result of MMA-3
+constexpr uint32_t TM_U = 0;     // -V^T -> -Y^T -> U^T (64)
 constexpr uint32_t TM_O = 64;    // O^T (64)
-constexpr uint32_t TM_SB = 128;  // S^T as bf16 pairs: A operand of MMA-X (64)
-constexpr uint32_t TM_S = 192;   // S^T fp32 (128)
+constexpr uint32_t TM_S = 128;   // S^T fp32 (128)
+constexpr uint32_t TM_SB = 256;  // S^T as bf16 pairs: A operand of MMA-X (64)
 constexpr uint32_t TM_AB = 320;  // A/B result: 176 of 192 columns, or 64 in the whole-chunk form
 
 constexpr int kIG = 256;  // intra-group threads (warps 0-7)
@@ -100,7 +101,7 @@ constexpr uint32_t BAR_IG = 1, BAR_RG = 2, BAR_A = 3, BAR_B = 4;
 
 enum Bar {
   B_QK_FULL, B_V_FULL, B_G_FULL, B_AB_DONE, B_UW_DONE, B_GAMMA0, B_GAMMA1, B_REC_READY,
-  B_M1B, B_M3A, B_M3B, B_DRAIN_IG, B_DRAIN_RG,
+  B_M1B, B_M3, B_DRAIN_IG, B_DRAIN_RG,
   B_ITEM_FULL, B_ITEM_EMPTY = B_ITEM_FULL + kRing, B_COUNT = B_ITEM_EMPTY + kRing
 };
 
@@ -554,6 +555,10 @@ __device__ __forceinline__ void form_tm(uint8_t* sm, const float* Xs, const floa
   }
 }
 
+// GEN: any gate form and KDA_FLAG_QK_L2NORM; otherwise the kernel is compiled for the plain
+// fp32 per-channel gate without normalisation only (the common case, whose chunk loop is then
+// free of the other forms' code).
+template <bool GEN>
 __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tbase) {
   const int t = threadIdx.x;  // 0..255
   const int warp = t >> 5, lane = t & 31;
@@ -587,7 +592,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // the first chunk of an item, are turned into e here by all intra threads.
       // (v: during MMA-AB.)
       const bool ahead = gc > 0 && ld.st->nx[(gc - 1) & 1].have;
-      const bool plain_gate = p.gate_k > 1 && !p.act.a;
+      const bool plain_gate = !GEN || (p.gate_k > 1 && !p.act.a);
       const bool e_ahead = plain_gate && lc > 0;
       if (t == 0) {
         if (!ahead) ld.load_qk(p, sm, s, kh, (int)t0);
@@ -610,7 +615,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         wait_bar(p, s, B_G_FULL, gc & 1);
         const float* Gs = reinterpret_cast<const float*>(sm + OFF_G);
         float gA = 0.f, gdb0 = 0.f, gdb1 = 0.f;  // activation constants of head h, channels c0, c0+1
-        if (p.act.a) {
+        if (GEN && p.act.a) {
           gA = __expf(p.act.A_log[h]);
           if (p.act.dt_bias) {
             const int gk = p.gate_k;
@@ -619,7 +624,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           }
         }
         // one loop per gate form, so that only the form in use sits in the executed code
-        if (p.gate_k == 1) {  // scalar gate: staged [64 tokens][gw heads], one value per token
+        if (GEN && p.gate_k == 1) {  // scalar gate: staged [64 tokens][gw heads], one value per token
           const int col = h & (p.gw - 1);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -633,7 +638,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             }
             e0[j] = e1[j] = (r < cv) ? exp_ftz(g0) : 1.f;  // padded rows: decay 1
           }
-        } else if (!p.act.a) {
+        } else if (!GEN || !p.act.a) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int r = sc * 16 + j;
@@ -676,7 +681,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         }
       }
       wait_bar(p, s, B_QK_FULL, gc & 1);
-      if (p.l2norm) {
+      if (GEN && p.l2norm) {
         // staged rows (k 0-63, q 64-127) -> x / max(||x||, 1e-12), re-rounded to bf16 as a
         // caller's normalise-then-cast would; thread = (row, 64-channel half).  The inverse
         // norms are kept for the pairwise path, which reads q and k from global memory.
@@ -971,7 +976,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         // KR = (k kap) F_s for sub-chunks sc-1 and sc of this thread's channel pair
         // (F_s = product of pi after s), by the B group while the tensor core runs MMA-AB;
         // one sub-chunk: KR = (k / rho) gamma
-        if (gc > 0) wait_bar(p, s, B_M3B, (gc - 1) & 1);
+        if (gc > 0) wait_bar(p, s, B_M3, (gc - 1) & 1);
 #pragma unroll 1
         for (int s2 = 0; s2 < 2; ++s2) {
           const int sk = sc - 1 + s2;
@@ -1065,7 +1070,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
               *reinterpret_cast<float4*>(As + sidx(r, i)) = w4;
             }
           } else {
-            if (gc > 0) wait_bar(p, s, B_M3A, (gc - 1) & 1);  // BB free
+            if (gc > 0) wait_bar(p, s, B_M3, (gc - 1) & 1);  // BB free
             const float bsc = whole ? 1.f : p.scale;  // one sub-chunk: the q rows carry it
 #pragma unroll
             for (int jc = 0; jc < 4; ++jc) {
@@ -1116,7 +1121,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
               *reinterpret_cast<float4*>(As + sidx(r, i)) = w4;
             }
           } else {
-            if (gc > 0) wait_bar(p, s, B_M3A, (gc - 1) & 1);  // BB free
+            if (gc > 0) wait_bar(p, s, B_M3, (gc - 1) & 1);  // BB free
 #pragma unroll
             for (int jc = 0; jc < 4; ++jc) {
               const int i = hx * 32 + jc * 8;
@@ -1439,25 +1444,23 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       tc_fence_before();
       fence_async_smem();
       named_bar(BAR_RG, kRG);
-      if (rt == 0) {  // (MMA-X, which wrote O, completed before Y^T was read out)
+      // ---- MMA-3: [O | S] (N = 192) += U^T [B | KR]^T, B = the BB rows (64 tokens) and the
+      // KR rows (128 channels) right after them, K-major.  (MMA-X, which wrote O, completed
+      // before Y^T was read out.)
+      if (rt == 0) {
         tc_fence_after();
-        const uint32_t id3 = idesc_bf16(128, 128, 0, 0), id3o = idesc_bf16(128, 64, 0, 0);
-#pragma unroll 1
-        for (int st = 0; st < 4; ++st)
-          mma_bf16(tbase + TM_S, sdesc_sw128(sbase + OFF_UT + st * 32, 16, 1024),
-                   sdesc_sw128(sbase + OFF_KR + st * 32, 16, 1024), id3, 1u);
-        mma_commit(&s->bar[B_M3B]);
+        const uint32_t id3 = idesc_bf16(128, 192, 0, 0);
 #pragma unroll 1
         for (int st = 0; st < 4; ++st)
           mma_bf16(tbase + TM_O, sdesc_sw128(sbase + OFF_UT + st * 32, 16, 1024),
-                   sdesc_sw128(sbase + OFF_BB + st * 32, 16, 1024), id3o, 1u);
-        mma_commit(&s->bar[B_M3A]);
+                   sdesc_sw128(sbase + OFF_BB + st * 32, 16, 1024), id3, 1u);
+        mma_commit(&s->bar[B_M3]);
       }
       __syncwarp();
       // ---- E2: S -> TMEM bf16 pairs for the next chunk's MMA-X, and back as fp32 pre-decayed
       // by that chunk's gamma (its MMA-3b accumulates onto Diag(gamma) S); or the final state
       // store
-      wait_bar(p, s, B_M3B, gc & 1);
+      wait_bar(p, s, B_M3, gc & 1);
       if (!last) wait_bar(p, s, B_GAMMA0 + ((gc + 1) & 1), ((gc + 1) >> 1) & 1);
       tc_fence_after();
       if (!last) {
@@ -1504,8 +1507,6 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       // ---- output of this chunk, complete once MMA-3a ran; each thread (value channel
       // v) writes its column straight to global memory, the 32 lanes of a warp covering
       // 64 contiguous bytes of one output row per store
-      wait_bar(p, s, B_M3A, gc & 1);
-      tc_fence_after();
       if (!ident && cv == kC) {
         // a full chunk of o: rows of the [64 tokens][128 values] tile in the U^T buffer (free:
         // MMA-3a/3b ran), each thread writing its value channel, then one TMA store
@@ -1554,7 +1555,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   if (leader_warp) mbar_wait(&s->bar[B_DRAIN_RG], 0);  // the full limit, aborted or not
 }
 
-template <typename ST>
+template <typename ST, bool GEN>
 __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, formed as an offset into the shared array (not through an
@@ -1591,7 +1592,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s->tmem_base;
-  if (threadIdx.x < kIG) run_intra(p, sm, s, tbase);
+  if (threadIdx.x < kIG) run_intra<GEN>(p, sm, s, tbase);
   else run_recurrence<ST>(p, sm, s, tbase);
   tc_fence_before();
   __syncthreads();
@@ -2208,10 +2209,16 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   cp.num_slots = d.num_slots;
   cp.slot_stride = a.slot_stride;
   const int cgrid = 2 * sm_count();
-  return d.state_dtype == KDA_BF16
-             ? launch_pair(kda_prefill_tc_kernel<__nv_bfloat16>, kda_combine_kernel<__nv_bfloat16>, p, cp,
-                           grid, cgrid, max_cuts > 0, st)
-             : launch_pair(kda_prefill_tc_kernel<float>, kda_combine_kernel<float>, p, cp, grid, cgrid,
+  // the plain fp32 per-channel gate without normalisation runs the kernel compiled for it alone
+  const bool gen = p.gate_k == 1 || p.act.a != nullptr || p.l2norm;
+  if (d.state_dtype == KDA_BF16)
+    return gen ? launch_pair(kda_prefill_tc_kernel<__nv_bfloat16, true>, kda_combine_kernel<__nv_bfloat16>, p, cp,
+                             grid, cgrid, max_cuts > 0, st)
+               : launch_pair(kda_prefill_tc_kernel<__nv_bfloat16, false>, kda_combine_kernel<__nv_bfloat16>, p,
+                             cp, grid, cgrid, max_cuts > 0, st);
+  return gen ? launch_pair(kda_prefill_tc_kernel<float, true>, kda_combine_kernel<float>, p, cp, grid, cgrid,
+                           max_cuts > 0, st)
+             : launch_pair(kda_prefill_tc_kernel<float, false>, kda_combine_kernel<float>, p, cp, grid, cgrid,
                            max_cuts > 0, st);
 }
 
