@@ -555,10 +555,12 @@ __device__ __forceinline__ void form_tm(uint8_t* sm, const float* Xs, const floa
   }
 }
 
-// GEN: any gate form and KDA_FLAG_QK_L2NORM; otherwise the kernel is compiled for the plain
-// fp32 per-channel gate without normalisation only (the common case, whose chunk loop is then
-// free of the other forms' code).
-template <bool GEN>
+// MODE: the gate forms the kernel is compiled for, so that a common case's chunk loop carries
+// none of the other forms' code:
+//   0  the plain fp32 per-channel gate, no q/k normalisation;
+//   1  the activated per-channel gate (bf16 or fp32 pre-activation), no q/k normalisation;
+//   2  any gate form, with or without KDA_FLAG_QK_L2NORM.
+template <int MODE>
 __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tbase) {
   const int t = threadIdx.x;  // 0..255
   const int warp = t >> 5, lane = t & 31;
@@ -592,7 +594,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // the first chunk of an item, are turned into e here by all intra threads.
       // (v: during MMA-AB.)
       const bool ahead = gc > 0 && ld.st->nx[(gc - 1) & 1].have;
-      const bool plain_gate = !GEN || (p.gate_k > 1 && !p.act.a);
+      const bool plain_gate = MODE == 0 || (MODE == 2 && p.gate_k > 1 && !p.act.a);
       const bool e_ahead = plain_gate && lc > 0;
       if (t == 0) {
         if (!ahead) ld.load_qk(p, sm, s, kh, (int)t0);
@@ -615,7 +617,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         wait_bar(p, s, B_G_FULL, gc & 1);
         const float* Gs = reinterpret_cast<const float*>(sm + OFF_G);
         float gA = 0.f, gdb0 = 0.f, gdb1 = 0.f;  // activation constants of head h, channels c0, c0+1
-        if (GEN && p.act.a) {
+        if (MODE == 1 || (MODE == 2 && p.act.a)) {
           gA = __expf(p.act.A_log[h]);
           if (p.act.dt_bias) {
             const int gk = p.gate_k;
@@ -624,7 +626,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           }
         }
         // one loop per gate form, so that only the form in use sits in the executed code
-        if (GEN && p.gate_k == 1) {  // scalar gate: staged [64 tokens][gw heads], one value per token
+        if (MODE == 2 && p.gate_k == 1) {  // scalar gate: staged [64 tokens][gw heads], one value per token
           const int col = h & (p.gw - 1);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -638,7 +640,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             }
             e0[j] = e1[j] = (r < cv) ? exp_ftz(g0) : 1.f;  // padded rows: decay 1
           }
-        } else if (!GEN || !p.act.a) {
+        } else if (MODE == 0 || (MODE == 2 && !p.act.a)) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int r = sc * 16 + j;
@@ -681,7 +683,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         }
       }
       wait_bar(p, s, B_QK_FULL, gc & 1);
-      if (GEN && p.l2norm) {
+      if (MODE == 2 && p.l2norm) {
         // staged rows (k 0-63, q 64-127) -> x / max(||x||, 1e-12), re-rounded to bf16 as a
         // caller's normalise-then-cast would; thread = (row, 64-channel half).  The inverse
         // norms are kept for the pairwise path, which reads q and k from global memory.
@@ -1555,7 +1557,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   if (leader_warp) mbar_wait(&s->bar[B_DRAIN_RG], 0);  // the full limit, aborted or not
 }
 
-template <typename ST, bool GEN>
+template <typename ST, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, formed as an offset into the shared array (not through an
@@ -1592,7 +1594,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s->tmem_base;
-  if (threadIdx.x < kIG) run_intra<GEN>(p, sm, s, tbase);
+  if (threadIdx.x < kIG) run_intra<MODE>(p, sm, s, tbase);
   else run_recurrence<ST>(p, sm, s, tbase);
   tc_fence_before();
   __syncthreads();
@@ -2209,17 +2211,19 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t st) {
   cp.num_slots = d.num_slots;
   cp.slot_stride = a.slot_stride;
   const int cgrid = 2 * sm_count();
-  // the plain fp32 per-channel gate without normalisation runs the kernel compiled for it alone
-  const bool gen = p.gate_k == 1 || p.act.a != nullptr || p.l2norm;
-  if (d.state_dtype == KDA_BF16)
-    return gen ? launch_pair(kda_prefill_tc_kernel<__nv_bfloat16, true>, kda_combine_kernel<__nv_bfloat16>, p, cp,
-                             grid, cgrid, max_cuts > 0, st)
-               : launch_pair(kda_prefill_tc_kernel<__nv_bfloat16, false>, kda_combine_kernel<__nv_bfloat16>, p,
-                             cp, grid, cgrid, max_cuts > 0, st);
-  return gen ? launch_pair(kda_prefill_tc_kernel<float, true>, kda_combine_kernel<float>, p, cp, grid, cgrid,
-                           max_cuts > 0, st)
-             : launch_pair(kda_prefill_tc_kernel<float, false>, kda_combine_kernel<float>, p, cp, grid, cgrid,
-                           max_cuts > 0, st);
+  // the plain fp32 per-channel gate and the activated per-channel gate, without normalisation,
+  // each run the kernel compiled for that form alone
+  const int mode = (p.gate_k == 1 || p.l2norm) ? 2 : (p.act.a != nullptr ? 1 : 0);
+  const bool cut = max_cuts > 0;
+  if (d.state_dtype == KDA_BF16) {
+    using C = __nv_bfloat16;
+    return mode == 0 ? launch_pair(kda_prefill_tc_kernel<C, 0>, kda_combine_kernel<C>, p, cp, grid, cgrid, cut, st)
+         : mode == 1 ? launch_pair(kda_prefill_tc_kernel<C, 1>, kda_combine_kernel<C>, p, cp, grid, cgrid, cut, st)
+                     : launch_pair(kda_prefill_tc_kernel<C, 2>, kda_combine_kernel<C>, p, cp, grid, cgrid, cut, st);
+  }
+  return mode == 0 ? launch_pair(kda_prefill_tc_kernel<float, 0>, kda_combine_kernel<float>, p, cp, grid, cgrid, cut, st)
+       : mode == 1 ? launch_pair(kda_prefill_tc_kernel<float, 1>, kda_combine_kernel<float>, p, cp, grid, cgrid, cut, st)
+                   : launch_pair(kda_prefill_tc_kernel<float, 2>, kda_combine_kernel<float>, p, cp, grid, cgrid, cut, st);
 }
 
 }  // namespace kda
