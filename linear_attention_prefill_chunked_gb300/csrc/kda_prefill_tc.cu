@@ -71,18 +71,19 @@ constexpr uint32_t OFF_VB = 32768;    // [2 v-blocks][64 tokens][128 B]        (
 constexpr uint32_t OFF_CB = 49152;    // [3 blocks][128 ch][128 B]             (MN-major B)
 constexpr uint32_t OFF_KG = 98304;    // [128 ch][64 tokens]                   (K-major A)
 constexpr uint32_t OFF_TM = 114688;   // [64 r][64 i]                          (K-major B)
-constexpr uint32_t OFF_WB = 122880;   // [128 ch][64 tokens]  -W              (MN-major B)
+constexpr uint32_t OFF_WB = 122880;   // [128 v][64 tokens]   Y^T, then U^T   (K-major A)
 constexpr uint32_t OFF_QG = 139264;   // [128 ch][64 tokens]  QG              (MN-major B)
 constexpr uint32_t OFF_BB = 155648;   // [64 r][64 i]         B               (K-major B)
 constexpr uint32_t OFF_KR = 163840;   // [128 ch][64 tokens]  KR              (K-major B)
 constexpr uint32_t OFF_AM = 180224;   // [k | q][128 ch][128 B]  k rho, q rho (MN-major A)
-constexpr uint32_t OFF_UT = 212992;   // [128 v][64 tokens]   U^T bf16        (K-major A)
+constexpr uint32_t OFF_PI = 212992;   // [4 sub-chunks][128 ch] fp32 gate products
 constexpr uint32_t OFF_SMALL = 229376;
 // After MMA-AB completes, the AM buffer holds the fp32 scratch of the inverse (A and B
 // rows, then X = (I + A)^-1) until Tm is written, the q/k buffer q and k of the next
 // chunk, and CB blocks 1-2 the TMA-staged gate of the next chunk, which the B group turns
 // into e = exp(g) ([64][128] fp32) in the same buffer when that chunk is in the same item
-// (otherwise each prologue thread forms its e in registers).
+// (otherwise each prologue thread forms its e in registers).  The WB buffer holds Y^T (the A
+// operand of MMA-U), then U^T (of MMA-3), then the chunk's output tile for its TMA store.
 constexpr uint32_t OFF_AS = OFF_AM;
 constexpr uint32_t OFF_XS = OFF_AM + 16384;
 constexpr uint32_t OFF_G = OFF_CB + 16384;
@@ -460,19 +461,19 @@ __device__ __forceinline__ float exp_ftz(float x) {
   return y;
 }
 
-// e = exp(g) of one chunk in place over its staged fp32 gate g ([64 tokens][128
-// channels]; each element read and written by the same thread; rows >= cv: 1), the
-// sub-chunk products pi into CB block 0 ([4][128] fp32) and the masks of "unsafe"
-// channels (pi below 2^-100, or not finite) into `uns`.  Run by nw warps (wg = index
-// among them): warp wg covers channels 64 (wg & 1) .. 64 (wg & 1) + 63 of sub-chunks
-// wg / 2 + i nw / 2, so its reads and writes are full rows.  The products are taken
+// e = exp(g) of sub-chunks sc0 .. sc1-1 of one chunk in place over its staged fp32 gate g
+// ([64 tokens][128 channels]; each element read and written by the same thread; rows >= cv:
+// 1), their products pi into the PI buffer ([4][128] fp32) and the masks of "unsafe"
+// channels (pi below 2^-100, or not finite) into `uns`.  Run by nw warps (wg = index among
+// them): warp wg covers channels 64 (wg & 1) .. 64 (wg & 1) + 63 of sub-chunks
+// sc0 + wg / 2 + i nw / 2, so its reads and writes are full rows.  The products are taken
 // token by token in order, as the prologue forms them.
 __device__ __forceinline__ void gate_exp_inplace(uint8_t* sm, uint32_t (*uns)[2][2], int cv, int wg, int nw,
-                                                 int lane) {
+                                                 int lane, int sc0, int sc1) {
   const int half = wg & 1, c0 = 2 * (half * 32 + lane);
   float* Es = reinterpret_cast<float*>(sm + OFF_G);
-  float* pis = reinterpret_cast<float*>(sm + OFF_CB);
-  for (int sc = wg >> 1; sc < 4; sc += nw >> 1) {
+  float* pis = reinterpret_cast<float*>(sm + OFF_PI);
+  for (int sc = sc0 + (wg >> 1); sc < sc1; sc += nw >> 1) {
     float pm0 = 1.f, pm1 = 1.f;
 #pragma unroll 4
     for (int j = 0; j < 16; ++j) {
@@ -666,7 +667,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           pm0 *= e0[j];
           pm1 *= e1[j];
         }
-        *reinterpret_cast<float2*>(reinterpret_cast<float*>(sm + OFF_CB) + sc * kK + c0) = make_float2(pm0, pm1);
+        *reinterpret_cast<float2*>(reinterpret_cast<float*>(sm + OFF_PI) + sc * kK + c0) = make_float2(pm0, pm1);
         const uint32_t m0 = __ballot_sync(0xffffffffu, !(pm0 >= kSafeMin));
         const uint32_t m1 = __ballot_sync(0xffffffffu, !(pm1 >= kSafeMin));
         if (lane == 0) {
@@ -718,7 +719,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // previous chunk ran
       if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
       named_bar(BAR_IG, kIG);  // the products visible
-      const float* pis = reinterpret_cast<const float*>(sm + OFF_CB);
+      const float* pis = reinterpret_cast<const float*>(sm + OFF_PI);
       float pi0[4], pi1[4];
 #pragma unroll
       for (int q2 = 0; q2 < 4; ++q2) {
@@ -974,6 +975,15 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         }
       }
       __syncwarp();
+      // a whole chunk followed by one in the same item has that chunk's gate in flight since the
+      // vote: the A group, idle during MMA-AB, turns its sub-chunks 0-1 into e (warps 0, 1, 4, 5
+      // -> units 0-3), warps 2-5 the rest while warps 0-1 invert
+      const bool e_split = plain_gate && whole && lc + 1 < info.nchunks;
+      if (quad < 2 && e_split) {
+        const int ncv = (int)min((int64_t)kC, info.eos - (t0 + kC));
+        wait_bar(p, s, B_G_FULL, (gc + 1) & 1);
+        gate_exp_inplace(sm, s->unsafe[(gc + 1) & 1], ncv, (warp & 1) | (hx << 1), 4, lane, 0, 2);
+      }
       if (quad >= 2) {
         // KR = (k kap) F_s for sub-chunks sc-1 and sc of this thread's channel pair
         // (F_s = product of pi after s), by the B group while the tensor core runs MMA-AB;
@@ -1147,8 +1157,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // the rest from them (inverse_merges) and Tm.
       // While warps 0-1 invert the diagonal blocks, warps 2-5 (one per SM sub-partition, so
       // that the exponentials spread over all four multi-function units) turn the staged gate
-      // of the next chunk of this item into e, its products and masks.  The products go to
-      // CB block 0, free once MMA-AB ran and the B group is past KR (barrier of warps 2-7).
+      // of the next chunk of this item into e, its products and masks (sub-chunks 2-3 when the
+      // A group did 0-1 during MMA-AB), after the B group's rows (barrier of warps 2-7).
       // Warp 4 first issues that gate load if the vote did not (CB 1-2 are free since MMA-AB).
       if (t == 128 && ld.st->nx[gc & 1].have && ld.st->n_g == gc + 1) {
         const NextChunk& nx = ld.st->nx[gc & 1];
@@ -1207,7 +1217,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           const int ncv = (int)min((int64_t)kC, info.eos - (t0 + kC));
           const int wgb = (warp ^ 4) & 3;  // warps 4, 5, 2, 3 -> 0-3
           wait_bar(p, s, B_G_FULL, (gc + 1) & 1);
-          gate_exp_inplace(sm, s->unsafe[(gc + 1) & 1], ncv, wgb, 4, lane);
+          gate_exp_inplace(sm, s->unsafe[(gc + 1) & 1], ncv, wgb, 4, lane, e_split ? 2 : 0, 4);
         }
       }
       // B rows (BB) visible to the tensor core; the diagonal blocks of X complete
@@ -1340,8 +1350,8 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
 
     bool stop = false;
     for (int lc = 0; lc < info.nchunks; ++lc, ++gc) {
-      // the output staging tile (the U^T buffer) is read by the TMA store of the chunk
-      // before, if any, before this chunk writes U^T (after the vote)
+      // the output staging tile (the WB buffer) is read by the TMA store of the chunk
+      // before, if any, before this chunk writes Y^T there
       if (rt == 0) bulk_wait_read();
       if (named_bar_any(BAR_RG, kRG, aborted(s))) { stop = true; break; }
       const int64_t t0 = info.bos + (int64_t)lc * kC;
@@ -1429,7 +1439,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         mma_commit(&s->bar[B_UW_DONE]);
       }
       __syncwarp();
-      // ---- E1: U^T row v -> UT (bf16)
+      // ---- E1: U^T row v -> WB (bf16; MMA-U has read Y^T)
       wait_bar(p, s, B_UW_DONE, gc & 1);
       tc_fence_after();
 #pragma unroll 1
@@ -1440,8 +1450,8 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         uint32_t w[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(uv[2 * u], uv[2 * u + 1]);
-        st_chunk(sm, OFF_UT + sw128_off(v, cq * 2), w[0], w[1], w[2], w[3]);
-        st_chunk(sm, OFF_UT + sw128_off(v, cq * 2 + 1), w[4], w[5], w[6], w[7]);
+        st_chunk(sm, OFF_WB + sw128_off(v, cq * 2), w[0], w[1], w[2], w[3]);
+        st_chunk(sm, OFF_WB + sw128_off(v, cq * 2 + 1), w[4], w[5], w[6], w[7]);
       }
       tc_fence_before();
       fence_async_smem();
@@ -1454,7 +1464,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         const uint32_t id3 = idesc_bf16(128, 192, 0, 0);
 #pragma unroll 1
         for (int st = 0; st < 4; ++st)
-          mma_bf16(tbase + TM_O, sdesc_sw128(sbase + OFF_UT + st * 32, 16, 1024),
+          mma_bf16(tbase + TM_O, sdesc_sw128(sbase + OFF_WB + st * 32, 16, 1024),
                    sdesc_sw128(sbase + OFF_BB + st * 32, 16, 1024), id3, 1u);
         mma_commit(&s->bar[B_M3]);
       }
@@ -1510,9 +1520,9 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       // v) writes its column straight to global memory, the 32 lanes of a warp covering
       // 64 contiguous bytes of one output row per store
       if (!ident && cv == kC) {
-        // a full chunk of o: rows of the [64 tokens][128 values] tile in the U^T buffer (free:
-        // MMA-3a/3b ran), each thread writing its value channel, then one TMA store
-        __nv_bfloat16* os = reinterpret_cast<__nv_bfloat16*>(sm + OFF_UT);
+        // a full chunk of o: rows of the [64 tokens][128 values] tile in the WB buffer (free:
+        // MMA-3 ran), each thread writing its value channel, then one TMA store
+        __nv_bfloat16* os = reinterpret_cast<__nv_bfloat16*>(sm + OFF_WB);
 #pragma unroll 1
         for (int cq = 0; cq < 4; ++cq) {
           float ov[16];
