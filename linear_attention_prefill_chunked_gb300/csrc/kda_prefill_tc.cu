@@ -71,7 +71,7 @@ constexpr uint32_t OFF_VB = 32768;    // [2 v-blocks][64 tokens][128 B]        (
 constexpr uint32_t OFF_CB = 49152;    // [3 blocks][128 ch][128 B]             (MN-major B)
 constexpr uint32_t OFF_KG = 98304;    // [128 ch][64 tokens]                   (K-major A)
 constexpr uint32_t OFF_TM = 114688;   // [64 r][64 i]                          (K-major B)
-constexpr uint32_t OFF_WB = 122880;   // [128 v][64 tokens]   Y^T, then U^T   (K-major A)
+constexpr uint32_t OFF_WB = 122880;   // [64 tokens][128 v]   output tile (TMA store)
 constexpr uint32_t OFF_QG = 139264;   // [128 ch][64 tokens]  QG              (MN-major B)
 constexpr uint32_t OFF_BB = 155648;   // [64 r][64 i]         B               (K-major B)
 constexpr uint32_t OFF_KR = 163840;   // [128 ch][64 tokens]  KR              (K-major B)
@@ -82,8 +82,7 @@ constexpr uint32_t OFF_SMALL = 229376;
 // rows, then X = (I + A)^-1) until Tm is written, the q/k buffer q and k of the next
 // chunk, and CB blocks 1-2 the TMA-staged gate of the next chunk, which the B group turns
 // into e = exp(g) ([64][128] fp32) in the same buffer when that chunk is in the same item
-// (otherwise each prologue thread forms its e in registers).  The WB buffer holds Y^T (the A
-// operand of MMA-U), then U^T (of MMA-3), then the chunk's output tile for its TMA store.
+// (otherwise each prologue thread forms its e in registers).
 constexpr uint32_t OFF_AS = OFF_AM;
 constexpr uint32_t OFF_XS = OFF_AM + 16384;
 constexpr uint32_t OFF_G = OFF_CB + 16384;
@@ -93,7 +92,8 @@ constexpr uint32_t OFF_G = OFF_CB + 16384;
 constexpr uint32_t TM_U = 0;     // -V^T -> -Y^T -> U^T (64)
 constexpr uint32_t TM_O = 64;    // O^T (64)
 constexpr uint32_t TM_S = 128;   // S^T fp32 (128)
-constexpr uint32_t TM_SB = 256;  // S^T as bf16 pairs: A operand of MMA-X (64)
+constexpr uint32_t TM_SB = 256;  // S^T as bf16 pairs: A operand of MMA-X (64); after MMA-X, Y^T
+                                 // (32) and U^T (32) as bf16 pairs: A of MMA-U and MMA-3
 constexpr uint32_t TM_AB = 320;  // A/B result: 176 of 192 columns, or 64 in the whole-chunk form
 
 constexpr int kIG = 256;  // intra-group threads (warps 0-7)
@@ -1351,7 +1351,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
     bool stop = false;
     for (int lc = 0; lc < info.nchunks; ++lc, ++gc) {
       // the output staging tile (the WB buffer) is read by the TMA store of the chunk
-      // before, if any, before this chunk writes Y^T there
+      // before, if any, before this chunk writes its own there
       if (rt == 0) bulk_wait_read();
       if (named_bar_any(BAR_RG, kRG, aborted(s))) { stop = true; break; }
       const int64_t t0 = info.bos + (int64_t)lc * kC;
@@ -1411,50 +1411,51 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         inverse_merges(As, Xs, warp - kIG / 32, lane, BAR_RG);
         form_tm(sm, Xs, s->beta[gc & 1], rt);
       }
-      // ---- Y^T = -(the U columns) -> WB (bf16, row = channel v, K-major A of MMA-U)
+      // ---- Y^T = -(the U columns) -> TMEM as bf16 pairs (columns 0-31 of the S^T pairs, free
+      // once MMA-X ran): the A operand of MMA-U
       wait_bar(p, s, B_M1B, gc & 1);
       tc_fence_after();
 #pragma unroll 1
-      for (int cq = 0; cq < 4; ++cq) {  // tokens 16 cq ..
-        float yv[16];
-        tmem_ld16(taddr_q + TM_U + cq * 16, yv);
+      for (int cq = 0; cq < 2; ++cq) {  // tokens 32 cq ..
+        float yv[32], pw[16];
+        tmem_ld16(taddr_q + TM_U + cq * 32, yv);
+        tmem_ld16(taddr_q + TM_U + cq * 32 + 16, yv + 16);
         tmem_ld_wait();
-        uint32_t w[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(-yv[2 * u], -yv[2 * u + 1]);
-        st_chunk(sm, OFF_WB + sw128_off(v, cq * 2), w[0], w[1], w[2], w[3]);
-        st_chunk(sm, OFF_WB + sw128_off(v, cq * 2 + 1), w[4], w[5], w[6], w[7]);
+        for (int u = 0; u < 16; ++u) pw[u] = __uint_as_float(pack_bf16x2(-yv[2 * u], -yv[2 * u + 1]));
+        tmem_st16(taddr_q + TM_SB + cq * 16, pw);
       }
+      tmem_st_wait();
       tc_fence_before();
       fence_async_smem();
-      named_bar(BAR_RG, kRG);  // Tm and Y^T in shared memory, the U columns read out
+      named_bar(BAR_RG, kRG);  // Tm in shared memory, Y^T in TMEM, the U columns read out
       // ---- MMA-U: U^T = Y^T Tm^T (onto the U columns)
       if (rt == 0) {
         tc_fence_after();
         const uint32_t idu = idesc_bf16(128, 64, 0, 0);
 #pragma unroll 1
         for (int st = 0; st < 4; ++st)
-          mma_bf16(tbase + TM_U, sdesc_sw128(sbase + OFF_WB + st * 32, 16, 1024),
-                   sdesc_sw128(sbase + OFF_TM + st * 32, 16, 1024), idu, st > 0 ? 1u : 0u);
+          mma_bf16_ta(tbase + TM_U, tbase + TM_SB + st * 8, sdesc_sw128(sbase + OFF_TM + st * 32, 16, 1024), idu,
+                      st > 0 ? 1u : 0u);
         mma_commit(&s->bar[B_UW_DONE]);
       }
       __syncwarp();
-      // ---- E1: U^T row v -> WB (bf16; MMA-U has read Y^T)
+      // ---- E1: U^T row v -> TMEM as bf16 pairs (columns 32-63 of the S^T pairs): the A operand
+      // of MMA-3
       wait_bar(p, s, B_UW_DONE, gc & 1);
       tc_fence_after();
 #pragma unroll 1
-      for (int cq = 0; cq < 4; ++cq) {
-        float uv[16];
-        tmem_ld16(taddr_q + TM_U + cq * 16, uv);
+      for (int cq = 0; cq < 2; ++cq) {
+        float uv[32], pw[16];
+        tmem_ld16(taddr_q + TM_U + cq * 32, uv);
+        tmem_ld16(taddr_q + TM_U + cq * 32 + 16, uv + 16);
         tmem_ld_wait();
-        uint32_t w[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(uv[2 * u], uv[2 * u + 1]);
-        st_chunk(sm, OFF_WB + sw128_off(v, cq * 2), w[0], w[1], w[2], w[3]);
-        st_chunk(sm, OFF_WB + sw128_off(v, cq * 2 + 1), w[4], w[5], w[6], w[7]);
+        for (int u = 0; u < 16; ++u) pw[u] = __uint_as_float(pack_bf16x2(uv[2 * u], uv[2 * u + 1]));
+        tmem_st16(taddr_q + TM_SB + 32 + cq * 16, pw);
       }
+      tmem_st_wait();
       tc_fence_before();
-      fence_async_smem();
       named_bar(BAR_RG, kRG);
       // ---- MMA-3: [O | S] (N = 192) += U^T [B | KR]^T, B = the BB rows (64 tokens) and the
       // KR rows (128 channels) right after them, K-major.  (MMA-X, which wrote O, completed
@@ -1464,8 +1465,8 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         const uint32_t id3 = idesc_bf16(128, 192, 0, 0);
 #pragma unroll 1
         for (int st = 0; st < 4; ++st)
-          mma_bf16(tbase + TM_O, sdesc_sw128(sbase + OFF_WB + st * 32, 16, 1024),
-                   sdesc_sw128(sbase + OFF_BB + st * 32, 16, 1024), id3, 1u);
+          mma_bf16_ta(tbase + TM_O, tbase + TM_SB + 32 + st * 8, sdesc_sw128(sbase + OFF_BB + st * 32, 16, 1024),
+                      id3, 1u);
         mma_commit(&s->bar[B_M3]);
       }
       __syncwarp();
@@ -1520,8 +1521,9 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       // v) writes its column straight to global memory, the 32 lanes of a warp covering
       // 64 contiguous bytes of one output row per store
       if (!ident && cv == kC) {
-        // a full chunk of o: rows of the [64 tokens][128 values] tile in the WB buffer (free:
-        // MMA-3 ran), each thread writing its value channel, then one TMA store
+        // a full chunk of o: rows of the [64 tokens][128 values] tile in the WB buffer (free: the
+        // chunk before's store has read it), each thread writing its value channel, then one TMA
+        // store
         __nv_bfloat16* os = reinterpret_cast<__nv_bfloat16*>(sm + OFF_WB);
 #pragma unroll 1
         for (int cq = 0; cq < 4; ++cq) {
