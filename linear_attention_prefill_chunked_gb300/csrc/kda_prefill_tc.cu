@@ -715,9 +715,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         }
         if (hf == 0) s->inv_nrm[row] = inv;
       }
-      // the KG and QG tiles, the v buffer and this gamma buffer are free once MMA-X of the
-      // previous chunk ran
-      if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
       named_bar(BAR_IG, kIG);  // the products visible
       const float* pis = reinterpret_cast<const float*>(sm + OFF_PI);
       float pi0[4], pi1[4];
@@ -743,7 +740,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
       // gamma of this chunk (by warps 6-7, which hold all 128 channels), published by the
       // vote's barrier: the recurrence group reads it at the end of the chunk before, to
       // pre-decay the state it hands on, or at the start of the item.  The value it replaces
-      // (two chunks back) was last read before MMA-X of the chunk before, waited for above.
+      // (two chunks back) was last read before MMA-X of the chunk before that, which the chunk
+      // before waited for.
       if (sc == 3) *reinterpret_cast<float2*>(&s->gamma[gc & 1][c0]) = make_float2(gm0, gm1);
       const bool whole = !named_bar_any(BAR_IG, kIG, !(gm0 >= kSafeMin) || !(gm1 >= kSafeMin));
       if (t == 0) {
@@ -857,6 +855,9 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         // scratch -- the AM buffer when that chunk took the four-sub-chunk form, the KG / QG
         // buffers otherwise -- up to its Tm (UW_DONE of that chunk).
         const float qs0 = p.scale * E0, qs1 = p.scale * E1;
+        // the KG and QG tiles (the operand buffer AM of a whole chunk) and the v buffer are free
+        // once MMA-X of the previous chunk ran
+        if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
         // tokens 8 jh .. 8 jh + 7 of channels c0, c0+1 of the staged k (row0 = 0) or q (row0 =
         // 64) rows, times rho m (rho carried in r0, r1), packed as token pairs
         auto rows = [&](int row0, int jh, float& r0, float& r1, float m0, float m1, uint32_t (&aw)[2][4]) {
