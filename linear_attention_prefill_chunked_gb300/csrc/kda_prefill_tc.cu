@@ -773,7 +773,12 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         if (whole) {
           // one sub-chunk: k / rho_r = (k kap_r) F_sc / gamma = (k kap_r) / (E_sc pi_sc),
           // rounded once, into CB block 0
+          // (plain-gate build: the running product starts at fw and takes kap_r on the way)
           const float fw0 = __fdividef(1.f, E0 * pm0), fw1 = __fdividef(1.f, E1 * pm1);
+          if (MODE == 0) {
+            ka0 = fw0;
+            ka1 = fw1;
+          }
 #pragma unroll
           for (int jh = 1; jh >= 0; --jh) {
             uint32_t xw[2][4];
@@ -781,7 +786,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             for (int u = 7; u >= 0; --u) {
               const int j = jh * 8 + u, r = sc * 16 + j;
               const uint32_t kv = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128)) : 0u;
-              const float k0 = bf_bits(kv & 0xFFFFu) * (ka0 * fw0), k1 = bf_bits(kv >> 16) * (ka1 * fw1);
+              const float k0 = bf_bits(kv & 0xFFFFu) * (MODE == 0 ? ka0 : ka0 * fw0);
+              const float k1 = bf_bits(kv >> 16) * (MODE == 0 ? ka1 : ka1 * fw1);
               ka0 *= e0[j];
               ka1 *= e1[j];
               if (u & 1) {
@@ -859,7 +865,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
         // once MMA-X of the previous chunk ran
         if (gc > 0) wait_bar(p, s, B_M1B, (gc - 1) & 1);
         // tokens 8 jh .. 8 jh + 7 of channels c0, c0+1 of the staged k (row0 = 0) or q (row0 =
-        // 64) rows, times rho m (rho carried in r0, r1), packed as token pairs
+        // 64) rows, times m rho, packed as token pairs; rho is carried in r0, r1 (in the
+        // plain-gate build they start at m and carry m rho, and m is not applied again)
         auto rows = [&](int row0, int jh, float& r0, float& r1, float m0, float m1, uint32_t (&aw)[2][4]) {
           uint32_t xw[8];
 #pragma unroll
@@ -873,7 +880,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             const int j = jh * 8 + u;
             r0 *= e0[j];
             r1 *= e1[j];
-            const float x0 = bf_bits(xw[u] & 0xFFFFu) * (r0 * m0), x1 = bf_bits(xw[u] >> 16) * (r1 * m1);
+            const float x0 = bf_bits(xw[u] & 0xFFFFu) * (MODE == 0 ? r0 : r0 * m0);
+            const float x1 = bf_bits(xw[u] >> 16) * (MODE == 0 ? r1 : r1 * m1);
             if (u & 1) {
               aw[0][u >> 1] = pack_bf16x2(pa0, x0);
               aw[1][u >> 1] = pack_bf16x2(pa1, x1);
@@ -892,7 +900,7 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           // one sub-chunk: the operand rows are k rho E and scale q rho E themselves (one
           // rounding), which are KG and QG too
           if (gc > 0 && !prev_whole) wait_bar(p, s, B_UW_DONE, (gc - 1) & 1);
-          float r0 = 1.f, r1 = 1.f;
+          float r0 = MODE == 0 ? qs0 : 1.f, r1 = MODE == 0 ? qs1 : 1.f;
 #pragma unroll
           for (int jh = 0; jh < 2; ++jh) {
             uint32_t aw[2][4];
@@ -900,7 +908,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) store_rows(OFF_AM + 16384, sc * 2 + jh, c2 ^ wsel, aw);
           }
-          r0 = r1 = 1.f;
+          r0 = MODE == 0 ? E0 : 1.f;
+          r1 = MODE == 0 ? E1 : 1.f;
 #pragma unroll
           for (int jh = 0; jh < 2; ++jh) {
             uint32_t aw[2][4];
