@@ -1715,7 +1715,10 @@ __global__ void __launch_bounds__(kOrderKeys) kda_plan_kernel(const int32_t* __r
     mine += (unsigned long long)c;
     atomicAdd(&cnt[order_key(c)], 1);
   }
-  atomicAdd(&total, mine);
+  // one shared atomic per warp (1024 on one address would serialise)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if ((t & 31) == 0) atomicAdd(&total, mine);
   __syncthreads();
   scan_keys_desc(cnt, wsum);
   for (int n = t; n < N; n += kOrderKeys) {
@@ -1726,16 +1729,19 @@ __global__ void __launch_bounds__(kOrderKeys) kda_plan_kernel(const int32_t* __r
   __syncthreads();
   if (t == 0) {  // the cuts, longest sequence first
     int nc = 0, ytok = 0;
-    const double L = (double)Hv * (double)total / (double)grid;
+    // L = Hv total / grid; c > 1.05 L and ceil(L) in exact 64-bit integer arithmetic (the
+    // double-precision unit is slow on this part)
+    const int64_t hvt = (int64_t)Hv * (int64_t)total;
+    const int64_t ceil_l = (hvt + grid - 1) / grid;
     for (int i = 0; i < N && nc < max_cuts; ++i) {
       const int n = (int)(i < kPlanCache ? order_s[i] : work[i]);
       const int64_t c = chunks(n);
       if (c < kCutMinChunks) break;
-      if ((double)c <= 1.05 * L) {
+      if (100 * c * (int64_t)grid <= 105 * hvt) {
         if (order_key(c) < kOrderKeys - 1) break;  // sorted exactly below the top key
         continue;
       }
-      const int64_t a = max((c + 1) / 2, (int64_t)ceil(L));
+      const int64_t a = max((c + 1) / 2, ceil_l);
       if (a >= c) continue;
       const int64_t tail = len_of(n) - a * kC;
       if ((int64_t)ytok + tail > (int64_t)ytok_max) continue;
