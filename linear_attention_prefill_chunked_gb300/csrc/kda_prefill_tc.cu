@@ -77,6 +77,7 @@ constexpr uint32_t OFF_BB = 155648;   // [64 r][64 i]         B               (K
 constexpr uint32_t OFF_KR = 163840;   // [128 ch][64 tokens]  KR              (K-major B)
 constexpr uint32_t OFF_AM = 180224;   // [k | q][128 ch][128 B]  k rho, q rho (MN-major A)
 constexpr uint32_t OFF_PI = 212992;   // [4 sub-chunks][128 ch] fp32 gate products
+constexpr uint32_t OFF_NI = 215040;   // [64 n][64 k] -I (K-major B; builds other than the plain gate)
 constexpr uint32_t OFF_SMALL = 229376;
 // After MMA-AB completes, the AM buffer holds the fp32 scratch of the inverse (A and B
 // rows, then X = (I + A)^-1) until Tm is written, the q/k buffer q and k of the next
@@ -971,10 +972,9 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           ld.prefetch_l2(p, nx.h, nx.t0);
         }
       } else if (t == 160) {
-        // and on warp 5: v of this chunk, which the recurrence group reads into TMEM before its
-        // MMA-X (the v buffer is free since MMA-X of the previous chunk, waited for in the
-        // prologue); the identity pass of a cut tail has zero values, so its phase completes
-        // bare
+        // and on warp 5: v of this chunk, which the recurrence group turns into -V^T in TMEM
+        // before its MMA-X (the v buffer is free once MMA-X of the previous chunk ran); the
+        // identity pass of a cut tail has zero values, so its phase completes bare
         if (info.kind == KIND_TAIL_ID) {
           if (!aborted(s)) {
             mbar_arrive(&s->bar[B_V_FULL]);
@@ -1292,7 +1292,7 @@ __device__ __forceinline__ void row32_store(__nv_bfloat16* p, const float* r) {
 // ======================================================================================
 // Recurrence group (warps 8-11): state update and output, chunk by chunk.
 // ======================================================================================
-template <typename ST>
+template <typename ST, int MODE>
 __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_t tbase) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
@@ -1303,6 +1303,18 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
   const uint32_t sbase = smem_u32(sm);
   Loader ld{&s->ld};
   uint32_t gc = 0;
+  if (MODE != 0) {
+    // the -I tile of V-in (B operand, K-major, 128-byte swizzle): row n holds -1 at column n;
+    // visible to the tensor core after the first barrier of the item loop
+    for (int c = rt; c < 64 * 8; c += kRG) {
+      const int n = c >> 3, j = c & 7;
+      const uint32_t m1 = (n >> 3) == j ? (0xBF80u << (16 * (n & 1))) : 0u;  // bf16 -1 at column n
+      const int w = (n & 7) >> 1;
+      st_chunk(sm, OFF_NI + sw128_off(n, j), w == 0 ? m1 : 0u, w == 1 ? m1 : 0u, w == 2 ? m1 : 0u,
+               w == 3 ? m1 : 0u);
+    }
+    fence_async_smem();
+  }
 
   for (int k = 0;; ++k) {
     const ItemInfo info = next_item(p, s, k, rt == 0, BAR_RG, kRG);
@@ -1373,9 +1385,12 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       if (rt == 32 && lc == (info.nchunks > 3 ? info.nchunks - 3 : 0)) ld.push_one(p, s);
       // ---- V-in, in the group's slack before the hand-over: -V^T into the U columns (lane =
       // value channel v, column = token; zero values in the identity pass) and zeros into O,
-      // which MMA-X accumulates onto
-      wait_bar(p, s, B_V_FULL, gc & 1);
-      {
+      // which MMA-X accumulates onto.  The plain-gate build reads v with per-thread loads; the
+      // other builds form -V^T as V^T (-I), four MMAs with the staged v tile as the A operand
+      // (MN-major: value channels contiguous, the two 64-value halves 8 KB apart), issued by the
+      // thread that issues MMA-X after them (on their workloads the group has more slack).
+      if (MODE == 0) {
+        wait_bar(p, s, B_V_FULL, gc & 1);
         const uint8_t* vb = sm + OFF_VB + (v >> 6) * 8192 + (v & 7) * 2;
         const uint32_t vc = (uint32_t)(v & 63) >> 3;
         float z[16];
@@ -1391,6 +1406,27 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
           tmem_st16(taddr_q + TM_O + cq * 16, z);
         }
         tmem_st_wait();
+      } else {
+        float z[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) z[u] = 0.f;
+#pragma unroll 1
+        for (int cq = 0; cq < 4; ++cq) {
+          tmem_st16(taddr_q + TM_O + cq * 16, z);
+          if (ident) tmem_st16(taddr_q + TM_U + cq * 16, z);
+        }
+        tmem_st_wait();
+        if (rt == 64) {
+          wait_bar(p, s, B_V_FULL, gc & 1);
+          if (!ident) {
+            tc_fence_after();
+            const uint32_t idv = idesc_bf16(128, 64, 1, 0);
+#pragma unroll 1
+            for (int st = 0; st < 4; ++st)
+              mma_bf16(tbase + TM_U, sdesc_sw128(sbase + OFF_VB + st * 2048, 8192, 1024),
+                       sdesc_sw128(sbase + OFF_NI + st * 32, 16, 1024), idv, st > 0 ? 1u : 0u);
+          }
+        }
       }
       tc_fence_before();
       // ---- R0: the hand-over.  MMA-X first (it frees KG, QG, v and gamma for the next
@@ -1617,7 +1653,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
   tc_fence_after();
   const uint32_t tbase = s->tmem_base;
   if (threadIdx.x < kIG) run_intra<MODE>(p, sm, s, tbase);
-  else run_recurrence<ST>(p, sm, s, tbase);
+  else run_recurrence<ST, MODE>(p, sm, s, tbase);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -10,7 +10,7 @@ SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
 # bytes of each buffer (tile shapes as the source's layout comments state them)
 SMEM_SIZES = {"QK": 2 * 128 * 128, "VB": 2 * 64 * 128, "CB": 3 * 128 * 128, "KG": 128 * 64 * 2,
               "TM": 64 * 64 * 2, "WB": 128 * 64 * 2, "QG": 128 * 64 * 2, "BB": 64 * 64 * 2,
-              "KR": 128 * 64 * 2, "AM": 2 * 128 * 128, "PI": 4 * 128 * 4}
+              "KR": 128 * 64 * 2, "AM": 2 * 128 * 128, "PI": 4 * 128 * 4, "NI": 64 * 64 * 2}
 TMEM_COLS = {"U": 64, "O": 64, "SB": 64, "S": 128, "AB": 192}
 
 
