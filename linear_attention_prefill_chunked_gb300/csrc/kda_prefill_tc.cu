@@ -1239,8 +1239,8 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
           bt_next = p.beta[(size_t)(nx.t0 + t) * p.Hv + nx.h];
         bt_ok = true;
       }
-      // hand the chunk to the recurrence group: it completes X and Tm, issues MMA-U/W and
-      // reads -W out itself
+      // hand the chunk to the recurrence group: it issues MMA-X, completes X and Tm, and runs
+      // MMA-U and MMA-3
       if (t == 0) mbar_arrive(&s->bar[B_REC_READY]);
       __syncwarp();
     }
@@ -1431,7 +1431,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       tc_fence_before();
       // ---- R0: the hand-over.  MMA-X first (it frees KG, QG, v and gamma for the next
       // chunk's prologue), then X = (I + A)^-1 and Tm from the diagonal blocks the intra group
-      // inverted, then Y^T -> WB and U^T = Y^T Tm^T
+      // inverted, then Y^T -> TMEM (bf16 pairs) and U^T = Y^T Tm^T
       wait_bar(p, s, B_REC_READY, gc & 1);
       // a chunk run as one sub-chunk keeps KG and QG in the MMA-AB operand buffer, and the
       // inverse scratch in the KG / QG buffers
@@ -1517,7 +1517,7 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
       }
       __syncwarp();
       // ---- E2: S -> TMEM bf16 pairs for the next chunk's MMA-X, and back as fp32 pre-decayed
-      // by that chunk's gamma (its MMA-3b accumulates onto Diag(gamma) S); or the final state
+      // by that chunk's gamma (its MMA-3 accumulates onto Diag(gamma) S); or the final state
       // store
       wait_bar(p, s, B_M3, gc & 1);
       if (!last) wait_bar(p, s, B_GAMMA0 + ((gc + 1) & 1), ((gc + 1) >> 1) & 1);
@@ -1563,9 +1563,8 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
         }
       }
       tmem_st_wait();
-      // ---- output of this chunk, complete once MMA-3a ran; each thread (value channel
-      // v) writes its column straight to global memory, the 32 lanes of a warp covering
-      // 64 contiguous bytes of one output row per store
+      // ---- output of this chunk, complete once MMA-3 ran: a full chunk through a shared-memory
+      // tile and one TMA store; a partial chunk or the identity pass by per-thread stores
       if (!ident && cv == kC) {
         // a full chunk of o: rows of the [64 tokens][128 values] tile in the WB buffer (free: the
         // chunk before's store has read it), each thread writing its value channel, then one TMA
