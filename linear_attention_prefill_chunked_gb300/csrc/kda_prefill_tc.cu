@@ -1255,6 +1255,15 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
   }
 }
 
+// (a, b) *= (x, y) as one packed fp32 multiply (round to nearest each)
+__device__ __forceinline__ void mul2(float& a, float& b, float x, float y) {
+  unsigned long long ab, xy;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ab) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(xy) : "f"(x), "f"(y));
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(ab) : "l"(xy));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(ab));
+}
+
 // 32 consecutive key channels of row v of a transposed ([V][K]) state, as fp32, with
 // 16-byte loads and stores (each thread owns its row).
 __device__ __forceinline__ void row32_load(const float* p, float* r) {
@@ -1536,10 +1545,8 @@ __device__ void run_recurrence(const TcParams& p, uint8_t* sm, Small* s, uint32_
 #pragma unroll
           for (int u4 = 0; u4 < 8; ++u4) {
             const float4 g4 = *reinterpret_cast<const float4*>(gn + kq * 32 + u4 * 4);
-            sv[u4 * 4 + 0] *= g4.x;
-            sv[u4 * 4 + 1] *= g4.y;
-            sv[u4 * 4 + 2] *= g4.z;
-            sv[u4 * 4 + 3] *= g4.w;
+            mul2(sv[u4 * 4 + 0], sv[u4 * 4 + 1], g4.x, g4.y);
+            mul2(sv[u4 * 4 + 2], sv[u4 * 4 + 3], g4.z, g4.w);
           }
           tmem_st16(taddr_q + TM_S + kq * 32, sv);
           tmem_st16(taddr_q + TM_S + kq * 32 + 16, sv + 16);
