@@ -198,6 +198,14 @@ struct TcParams {
 
 // ---- small helpers -----------------------------------------------------------------
 __device__ __forceinline__ float bf_bits(uint32_t b16) { return __uint_as_float(b16 << 16); }
+// (a, b) *= (x, y) as one packed fp32 multiply (round to nearest each)
+__device__ __forceinline__ void mul2(float& a, float& b, float x, float y) {
+  unsigned long long ab, xy;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ab) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(xy) : "f"(x), "f"(y));
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(ab) : "l"(xy));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(ab));
+}
 // Element (row, ch) of a K-major operand with 128 channels in two 64-wide atoms.
 __device__ __forceinline__ uint32_t kmaj_elem(uint32_t row, uint32_t ch, uint32_t rows_per_atom) {
   const uint32_t off = (ch >> 6) * rows_per_atom * 128u + sw128_off(row, (ch & 63u) >> 3) + (ch & 7u) * 2u;
@@ -456,6 +464,11 @@ __device__ __noinline__ void unsafe_diag_terms(const TcParams& p, const uint32_t
 // exp(x) as one ex2 on the multi-function unit, results below 2^-126 flushed to zero:
 // an e that low puts its channel's sub-chunk product below 2^-100, so the channel takes
 // the pairwise path, and products formed from it differ from exact by under 2^-126.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float exp_ftz(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));  // log2(e)
@@ -481,11 +494,12 @@ __device__ __forceinline__ void gate_exp_inplace(uint8_t* sm, uint32_t (*uns)[2]
       const int r = sc * 16 + j;
       float2* ep = reinterpret_cast<float2*>(Es + r * kK + c0);
       const float2 gv = *ep;
-      const float e0 = (r < cv) ? exp_ftz(gv.x) : 1.f;  // padded rows: decay 1
-      const float e1 = (r < cv) ? exp_ftz(gv.y) : 1.f;
+      float e0 = gv.x, e1 = gv.y;
+      mul2(e0, e1, 1.4426950408889634f, 1.4426950408889634f);  // log2(e)
+      e0 = (r < cv) ? ex2_ftz(e0) : 1.f;  // padded rows: decay 1
+      e1 = (r < cv) ? ex2_ftz(e1) : 1.f;
       *ep = make_float2(e0, e1);
-      pm0 *= e0;
-      pm1 *= e1;
+      mul2(pm0, pm1, e0, e1);
     }
     *reinterpret_cast<float2*>(pis + sc * kK + c0) = make_float2(pm0, pm1);
     const uint32_t m0 = __ballot_sync(0xffffffffu, !(pm0 >= kSafeMin));
@@ -787,10 +801,18 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
             for (int u = 7; u >= 0; --u) {
               const int j = jh * 8 + u, r = sc * 16 + j;
               const uint32_t kv = (r < cv) ? *reinterpret_cast<const uint32_t*>(sm + OFF_QK + kmaj_elem(r, c0, 128)) : 0u;
-              const float k0 = bf_bits(kv & 0xFFFFu) * (MODE == 0 ? ka0 : ka0 * fw0);
-              const float k1 = bf_bits(kv >> 16) * (MODE == 0 ? ka1 : ka1 * fw1);
-              ka0 *= e0[j];
-              ka1 *= e1[j];
+              float k0, k1;
+              if (MODE == 0) {
+                k0 = bf_bits(kv & 0xFFFFu);
+                k1 = bf_bits(kv >> 16);
+                mul2(k0, k1, ka0, ka1);
+                mul2(ka0, ka1, e0[j], e1[j]);
+              } else {
+                k0 = bf_bits(kv & 0xFFFFu) * (ka0 * fw0);
+                k1 = bf_bits(kv >> 16) * (ka1 * fw1);
+                ka0 *= e0[j];
+                ka1 *= e1[j];
+              }
               if (u & 1) {
                 xw[0][u >> 1] = __float_as_uint(k0);  // odd token: the high half, packed below
                 xw[1][u >> 1] = __float_as_uint(k1);
@@ -879,10 +901,18 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int j = jh * 8 + u;
-            r0 *= e0[j];
-            r1 *= e1[j];
-            const float x0 = bf_bits(xw[u] & 0xFFFFu) * (MODE == 0 ? r0 : r0 * m0);
-            const float x1 = bf_bits(xw[u] >> 16) * (MODE == 0 ? r1 : r1 * m1);
+            float x0, x1;
+            if (MODE == 0) {
+              mul2(r0, r1, e0[j], e1[j]);
+              x0 = bf_bits(xw[u] & 0xFFFFu);
+              x1 = bf_bits(xw[u] >> 16);
+              mul2(x0, x1, r0, r1);
+            } else {
+              r0 *= e0[j];
+              r1 *= e1[j];
+              x0 = bf_bits(xw[u] & 0xFFFFu) * (r0 * m0);
+              x1 = bf_bits(xw[u] >> 16) * (r1 * m1);
+            }
             if (u & 1) {
               aw[0][u >> 1] = pack_bf16x2(pa0, x0);
               aw[1][u >> 1] = pack_bf16x2(pa1, x1);
@@ -1253,15 +1283,6 @@ __device__ void run_intra(const TcParams& p, uint8_t* sm, Small* s, uint32_t tba
     __syncwarp();
     mbar_wait(&s->bar[B_DRAIN_IG], 0);  // the full limit, aborted or not
   }
-}
-
-// (a, b) *= (x, y) as one packed fp32 multiply (round to nearest each)
-__device__ __forceinline__ void mul2(float& a, float& b, float x, float y) {
-  unsigned long long ab, xy;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ab) : "f"(a), "f"(b));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(xy) : "f"(x), "f"(y));
-  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(ab) : "l"(xy));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(ab));
 }
 
 // 32 consecutive key channels of row v of a transposed ([V][K]) state, as fp32, with
